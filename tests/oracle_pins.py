@@ -1,0 +1,409 @@
+"""Pins for the fp64 oracle: checks against facts that do not come from the
+oracle itself (brute force written separately, closed forms, invariants, an
+independent library routine).  Each ``pin_*`` returns True when it holds, so
+that ``test_oracle_pins.py`` can also plant mistakes in the oracle and show
+that some pin catches each of them.
+
+All pins look the oracle up through the module at call time (``O.xxx``),
+so a monkeypatched oracle function is what they exercise.
+"""
+from __future__ import annotations
+
+import math
+import struct
+
+import numpy as np
+
+import oracle.dsa_oracle as O
+from synth import normal_bf16, f32_to_bf16_bits
+
+TOL = 1e-12
+
+
+# ----------------------------------------------------------------------------
+# a separately written decoder and brute-force dense attention (pure Python)
+# ----------------------------------------------------------------------------
+def _bf16_bits_to_float(b: int) -> float:
+    return struct.unpack("<f", struct.pack("<I", (int(b) & 0xFFFF) << 16))[0]
+
+
+def brute_dense_attention(q_bits, kv_bits, idx, k, scale, d_qk, d_v):
+    """Full N-length scores with -inf where the key is not selected, then a
+    dense softmax.  Plain Python floats and loops."""
+    T, H, _ = q_bits.shape
+    N = kv_bits.shape[0]
+    kvf = [[_bf16_bits_to_float(kv_bits[n, d]) for d in range(kv_bits.shape[1])] for n in range(N)]
+    out = np.zeros((T, H, d_v))
+    lse = np.zeros((T, H))
+    for t in range(T):
+        chosen = set(int(x) for x in idx[t][:k] if 0 <= int(x) < N)
+        for h in range(H):
+            qv = [_bf16_bits_to_float(q_bits[t, h, d]) for d in range(d_qk)]
+            scores = []
+            for n in range(N):
+                if n in chosen:
+                    scores.append(scale * math.fsum(qv[d] * kvf[n][d] for d in range(d_qk)))
+                else:
+                    scores.append(-math.inf)
+            mx = max(scores)
+            if mx == -math.inf:
+                lse[t, h] = -math.inf
+                continue
+            w = [math.exp(s - mx) if s != -math.inf else 0.0 for s in scores]
+            z = math.fsum(w)
+            lse[t, h] = mx + math.log(z)
+            for d in range(d_v):
+                out[t, h, d] = math.fsum(w[n] * kvf[n][d] for n in range(N)) / z
+    return out, lse
+
+
+def _close(a, b, tol=TOL):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    if a.shape != b.shape:
+        return False
+    if not np.array_equal(np.isinf(a), np.isinf(b)):
+        return False
+    f = np.isfinite(b)
+    return bool(np.all(np.abs(a[f] - b[f]) <= tol * (1.0 + np.abs(b[f]))))
+
+
+def _random_rows(rng, T, N, k, ld, p_dense=0.0):
+    """Index rows with -1 anywhere in the first k columns, junk-free beyond."""
+    idx = np.full((T, ld), -1, dtype=np.int32)
+    for t in range(T):
+        n = int(rng.integers(0, min(k, N) + 1))
+        sel = rng.choice(N, size=n, replace=False)
+        row = np.full(k, -1, dtype=np.int64)
+        pos = rng.choice(k, size=n, replace=False)
+        row[pos] = sel
+        idx[t, :k] = row
+        if ld > k:  # columns beyond k may hold anything valid; they must be ignored
+            idx[t, k:] = rng.integers(-1, N, size=ld - k)
+    return idx
+
+
+# ----------------------------------------------------------------------------
+# per-token pins
+# ----------------------------------------------------------------------------
+def pin_bruteforce(seed=0) -> bool:
+    """Oracle == brute-force dense attention with a -inf mask (tiny sizes,
+    RoPE-like extra K columns so d_qk > d_v, -1 anywhere, ld > k)."""
+    rng = np.random.default_rng(seed)
+    ok = True
+    for (T, N, H, d_qk, d_v, k, ld) in [(6, 20, 3, 24, 16, 7, 9), (5, 33, 2, 32, 32, 40, 40),
+                                        (4, 9, 4, 12, 8, 3, 5)]:
+        q = normal_bf16(rng, (T, H, d_qk))
+        kv = normal_bf16(rng, (N, d_qk))
+        idx = _random_rows(rng, T, N, k, ld)
+        scale = 1.0 / math.sqrt(float(d_qk) * 0.75)
+        o_ref, l_ref = brute_dense_attention(q, kv, idx, k, scale, d_qk, d_v)
+        o, l = O.sparse_prefill(q, kv, idx, k, scale, d_qk, d_v)
+        ok &= _close(o, o_ref) and _close(l, l_ref)
+    return ok
+
+
+def pin_single_key(seed=1) -> bool:
+    """|S_t| = 1: out = that row's V, lse = its scaled score."""
+    rng = np.random.default_rng(seed)
+    T, N, H, d_qk, d_v = 4, 10, 3, 16, 8
+    q = normal_bf16(rng, (T, H, d_qk))
+    kv = normal_bf16(rng, (N, d_qk))
+    idx = np.full((T, 5), -1, dtype=np.int32)
+    rows = [3, 0, 9, 5]
+    for t, r in enumerate(rows):
+        idx[t, t % 5] = r
+    scale = 0.37
+    o, l = O.sparse_prefill(q, kv, idx, 5, scale, d_qk, d_v)
+    ok = True
+    for t, r in enumerate(rows):
+        v = [_bf16_bits_to_float(kv[r, d]) for d in range(d_v)]
+        for h in range(H):
+            s = scale * math.fsum(_bf16_bits_to_float(q[t, h, d]) * _bf16_bits_to_float(kv[r, d])
+                                  for d in range(d_qk))
+            ok &= abs(l[t, h] - s) <= TOL * (1 + abs(s))
+            ok &= bool(np.all(np.abs(o[t, h] - np.asarray(v)) <= TOL))
+    return ok
+
+
+def pin_zero_query(seed=2) -> bool:
+    """q = 0: uniform weights, out = mean of the selected V rows, lse = ln n."""
+    rng = np.random.default_rng(seed)
+    T, N, H, d_qk, d_v, k = 3, 30, 2, 16, 12, 11
+    q = np.zeros((T, H, d_qk), dtype=np.uint16)
+    kv = normal_bf16(rng, (N, d_qk))
+    idx = _random_rows(rng, T, N, k, k)
+    idx[0, :] = -1
+    idx[0, 2] = 7
+    o, l = O.sparse_prefill(q, kv, idx, k, 0.5, d_qk, d_v)
+    ok = True
+    for t in range(T):
+        sel = [int(x) for x in idx[t] if x >= 0]
+        if not sel:
+            ok &= bool(np.all(o[t] == 0)) and bool(np.all(np.isneginf(l[t])))
+            continue
+        mean = [math.fsum(_bf16_bits_to_float(kv[n, d]) for n in sel) / len(sel) for d in range(d_v)]
+        for h in range(H):
+            ok &= abs(l[t, h] - math.log(len(sel))) <= TOL
+            ok &= bool(np.all(np.abs(o[t, h] - np.asarray(mean)) <= TOL))
+    return ok
+
+
+def pin_equal_keys(seed=3) -> bool:
+    """All selected K rows equal (V rows differ): uniform weights; lse = s + ln n."""
+    rng = np.random.default_rng(seed)
+    N, H, d_qk, d_v, k = 12, 3, 20, 8, 6
+    kv = normal_bf16(rng, (N, d_qk))
+    shared = normal_bf16(rng, (d_qk - d_v,))
+    kv[:, d_v:] = shared[None, :]
+    kv[:, :d_v] = normal_bf16(rng, (N, d_v))
+    q = normal_bf16(rng, (1, H, d_qk))
+    q[0, :, :d_v] = 0  # score depends only on the shared (RoPE-like) columns
+    idx = np.array([[1, 4, -1, 9, 10, 2]], dtype=np.int32)
+    sel = [1, 4, 9, 10, 2]
+    o, l = O.sparse_prefill(q, kv, idx, k, 0.25, d_qk, d_v)
+    ok = True
+    for h in range(H):
+        s = 0.25 * math.fsum(_bf16_bits_to_float(q[0, h, d]) * _bf16_bits_to_float(shared[d - d_v])
+                             for d in range(d_v, d_qk))
+        ok &= abs(l[0, h] - (s + math.log(len(sel)))) <= TOL * (1 + abs(s))
+        mean = [math.fsum(_bf16_bits_to_float(kv[n, d]) for n in sel) / len(sel) for d in range(d_v)]
+        ok &= bool(np.all(np.abs(o[0, h] - np.asarray(mean)) <= TOL))
+    return ok
+
+
+def pin_two_keys_closed_form() -> bool:
+    """Hand-worked case: q = (1, 0), rows r0 = (0, 0), r1 = (1, 1), scale 1,
+    D_QK = D_V = 2.  Scores 0 and 1, so weights 1/(1+e), e/(1+e);
+    out = (e/(1+e)) * (1, 1); lse = ln(1 + e)."""
+    one = f32_to_bf16_bits(np.array([1.0], np.float32))[0]
+    q = np.array([[[one, 0]]], dtype=np.uint16)
+    kv = np.array([[0, 0], [one, one]], dtype=np.uint16)
+    idx = np.array([[1, -1, 0]], dtype=np.int32)
+    o, l = O.sparse_prefill(q, kv, idx, 3, 1.0, 2, 2)
+    w1 = math.e / (1.0 + math.e)
+    return abs(l[0, 0] - math.log(1.0 + math.e)) <= TOL and \
+        bool(np.all(np.abs(o[0, 0] - w1) <= TOL))
+
+
+def pin_order_and_padding_invariance(seed=4) -> bool:
+    """Permuting a row's first k entries, moving -1s around and changing the
+    columns beyond k leave the result unchanged (to rounding)."""
+    rng = np.random.default_rng(seed)
+    T, N, H, d_qk, d_v, k, ld = 5, 40, 2, 24, 16, 12, 16
+    q = normal_bf16(rng, (T, H, d_qk))
+    kv = normal_bf16(rng, (N, d_qk))
+    idx = _random_rows(rng, T, N, k, ld)
+    o1, l1 = O.sparse_prefill(q, kv, idx, k, 0.3, d_qk, d_v)
+    idx2 = idx.copy()
+    for t in range(T):
+        idx2[t, :k] = rng.permutation(idx2[t, :k])
+        idx2[t, k:] = rng.integers(-1, N, size=ld - k)
+    o2, l2 = O.sparse_prefill(q, kv, idx2, k, 0.3, d_qk, d_v)
+    return _close(o1, o2, 1e-13) and _close(l1, l2, 1e-13)
+
+
+def pin_dense_causal_sdpa(seed=5) -> bool:
+    """k >= t+1 with every position selected equals dense causal attention,
+    checked against torch's scaled_dot_product_attention in float64 (CPU)."""
+    import torch
+    import torch.nn.functional as F
+    rng = np.random.default_rng(seed)
+    T, H, d_qk, d_v = 23, 4, 40, 32
+    q = normal_bf16(rng, (T, H, d_qk))
+    kv = normal_bf16(rng, (T, d_qk))
+    k = T + 3
+    idx = np.full((T, k), -1, dtype=np.int32)
+    for t in range(T):
+        idx[t, :t + 1] = rng.permutation(t + 1)
+    scale = 1.0 / math.sqrt(17.0)
+    o, _ = O.sparse_prefill(q, kv, idx, k, scale, d_qk, d_v)
+
+    def dec(b):
+        return torch.from_numpy((b.astype(np.uint32) << 16).view(np.float32).astype(np.float64))
+    qt = dec(q).permute(1, 0, 2).unsqueeze(0)                 # [1, H, T, D]
+    kt = dec(kv).unsqueeze(0).unsqueeze(0).expand(1, H, T, d_qk)
+    vt = dec(kv[:, :d_v]).unsqueeze(0).unsqueeze(0).expand(1, H, T, d_v)
+    ref = F.scaled_dot_product_attention(qt, kt, vt, is_causal=True, scale=scale)
+    ref = ref[0].permute(1, 0, 2).numpy()
+    return bool(np.max(np.abs(o - ref)) <= 1e-12)
+
+
+# ----------------------------------------------------------------------------
+# union / mask pins
+# ----------------------------------------------------------------------------
+def brute_union(idx, k, G, N, cu):
+    """Union and mask from Python sets (independent of np.unique/searchsorted)."""
+    res = []
+    cu = [int(x) for x in cu]
+    for r in range(len(cu) - 1):
+        for s in range(cu[r], cu[r + 1], G):
+            n = min(G, cu[r + 1] - s)
+            sets = [set(int(x) for x in idx[s + j][:k] if 0 <= int(x) < N) for j in range(n)]
+            u = sorted(set().union(*sets))
+            m = [sum((1 << j) for j in range(n) if x in sets[j]) for x in u]
+            res.append((u, m))
+    return res
+
+
+def pin_union_worked_example() -> bool:
+    """Hand-worked: G = 2, k = 4; token 0 selects {5, 2, 9}, token 1 {9, 3, 5}.
+    Union (ascending) = [2, 3, 5, 9]; membership bits = [01, 10, 11, 11];
+    union_pad = ceil(2*4 / 4) * 4 = 8 with a union block of 4."""
+    idx = np.array([[5, 2, -1, 9], [9, 3, 5, -1]], dtype=np.int32)
+    upad = O.union_pad(2, 4, 4)
+    u, ul, m = O.union_build(idx, 4, 2, 16, [0, 2], upad)
+    return upad == 8 and ul.tolist() == [4] and \
+        u.tolist() == [[2, 3, 5, 9, -1, -1, -1, -1]] and m.tolist() == [[1, 2, 3, 3, 0, 0, 0, 0]]
+
+
+def pin_union_bruteforce(seed=6) -> bool:
+    """Union/mask equal the Python-set construction over ragged requests and
+    every G in 1..8, and satisfy the structural invariants."""
+    rng = np.random.default_rng(seed)
+    ok = True
+    for G in range(1, 9):
+        q_lens = [int(x) for x in rng.integers(1, 3 * G + 2, size=3)]
+        T = sum(q_lens)
+        N, k, ld = 70, 9, 11
+        idx = _random_rows(rng, T, N, k, ld)
+        cu = np.concatenate([[0], np.cumsum(q_lens)])
+        upad = O.union_pad(G, k, 8)
+        u, ul, m = O.union_build(idx, k, G, N, cu, upad)
+        ref = brute_union(idx, k, G, N, cu)
+        ok &= len(ref) == u.shape[0]
+        for g, (ru, rm) in enumerate(ref):
+            U = int(ul[g])
+            ok &= U == len(ru)
+            ok &= u[g, :U].tolist() == ru and m[g, :U].tolist() == rm
+            ok &= bool(np.all(u[g, U:] == -1)) and bool(np.all(m[g, U:] == 0))
+            ok &= bool(np.all(np.diff(u[g, :U]) > 0))
+    return ok
+
+
+def pin_union_popcounts(seed=7) -> bool:
+    """For every token j of a group, the number of union slots with bit j set
+    equals the size of its own valid top-k set."""
+    rng = np.random.default_rng(seed)
+    T, N, k, G = 37, 200, 25, 8
+    idx = _random_rows(rng, T, N, k, k)
+    cu = [0, 20, 37]
+    upad = O.union_pad(G, k, 16)
+    u, ul, m = O.union_build(idx, k, G, N, cu, upad)
+    ok = True
+    for g, (t0, n) in enumerate(O.groups(cu, G)):
+        for j in range(n):
+            cnt = int(((m[g].astype(np.int64) >> j) & 1).sum())
+            ok &= cnt == int(((idx[t0 + j][:k] >= 0)).sum())
+        ok &= int(ul[g]) <= min(n * k, N)
+    return ok
+
+
+def pin_grouped_equals_per_token(seed=8) -> bool:
+    """Grouped attention over (union, mask) equals per-token attention for
+    ragged requests, several H / G and empty tokens."""
+    rng = np.random.default_rng(seed)
+    ok = True
+    for (H, G, q_lens) in [(4, 2, [5, 3]), (2, 8, [13]), (1, 8, [9, 1, 8]), (8, 1, [4])]:
+        T = sum(q_lens)
+        N, d_qk, d_v, k = 50, 24, 16, 10
+        q = normal_bf16(rng, (T, H, d_qk))
+        kv = normal_bf16(rng, (N, d_qk))
+        idx = _random_rows(rng, T, N, k, k)
+        idx[0, :] = -1  # one token with no selection at all
+        cu = np.concatenate([[0], np.cumsum(q_lens)])
+        o1, l1 = O.sparse_prefill(q, kv, idx, k, 0.2, d_qk, d_v)
+        upad = O.union_pad(G, k, 8)
+        u, ul, m = O.union_build(idx, k, G, N, cu, upad)
+        o2, l2 = O.grouped_prefill(q, kv, u, ul, m, G, cu, 0.2, d_qk, d_v)
+        ok &= _close(o1, o2, 1e-12) and _close(l1, l2, 1e-12)
+    return ok
+
+
+def pin_key_mask_bruteforce(seed=9) -> bool:
+    """Key-mask bits equal the request-local positions of the valid top-k."""
+    rng = np.random.default_rng(seed)
+    kv_lens = [40, 70]
+    q_lens = [6, 5]
+    cq = np.concatenate([[0], np.cumsum(q_lens)])
+    ck = np.concatenate([[0], np.cumsum(kv_lens)])
+    k = 9
+    idx = np.full((sum(q_lens), k), -1, dtype=np.int32)
+    for r in range(2):
+        for t in range(cq[r], cq[r + 1]):
+            n = int(rng.integers(0, k + 1))
+            sel = rng.choice(kv_lens[r], size=n, replace=False) + ck[r]
+            idx[t, rng.choice(k, size=n, replace=False)] = sel
+    words = 3
+    km = O.topk_to_key_mask(idx, k, cq, ck, words)
+    ok = True
+    for r in range(2):
+        for t in range(cq[r], cq[r + 1]):
+            want = set(int(x) - int(ck[r]) for x in idx[t] if x >= 0)
+            got = set(n for n in range(32 * words) if (int(km[t, n // 32]) >> (n % 32)) & 1)
+            ok &= want == got
+    return ok
+
+
+def pin_masked_equals_sparse(seed=10) -> bool:
+    """Masked MHA over per-head K/V equals sparse attention when every head's
+    K/V is the shared latent row (k[n, h] = kv[n, :d_qk], v[n, h] = kv[n, :d_v]),
+    across two requests (key offsets matter)."""
+    rng = np.random.default_rng(seed)
+    kv_lens, q_lens = [17, 23], [6, 9]
+    H, d_qk, d_v, k = 3, 24, 16, 8
+    cq = np.concatenate([[0], np.cumsum(q_lens)])
+    ck = np.concatenate([[0], np.cumsum(kv_lens)])
+    N, T = sum(kv_lens), sum(q_lens)
+    kv = normal_bf16(rng, (N, d_qk))
+    q = normal_bf16(rng, (T, H, d_qk))
+    idx = np.full((T, k), -1, dtype=np.int32)
+    for r in range(2):
+        for t in range(cq[r], cq[r + 1]):
+            n = int(rng.integers(0, k + 1))
+            idx[t, :n] = rng.choice(kv_lens[r], size=n, replace=False) + ck[r]
+    km = O.topk_to_key_mask(idx, k, cq, ck, 1)
+    kh = np.repeat(kv[:, None, :], H, axis=1)
+    vh = np.repeat(kv[:, None, :d_v], H, axis=1)
+    o1, l1 = O.masked_mha_prefill(q, kh, vh, km, cq, ck, 0.3)
+    o2, l2 = O.sparse_prefill(q, kv, idx, k, 0.3, d_qk, d_v)
+    return _close(o1, o2, 1e-12) and _close(l1, l2, 1e-12)
+
+
+def pin_masked_dense_causal_sdpa(seed=11) -> bool:
+    """A causal full mask makes masked MHA equal to dense causal SDPA (float64,
+    per-head K/V, one request)."""
+    import torch
+    import torch.nn.functional as F
+    rng = np.random.default_rng(seed)
+    T, H, d_qk, d_v = 19, 3, 24, 8
+    q = normal_bf16(rng, (T, H, d_qk))
+    kh = normal_bf16(rng, (T, H, d_qk))
+    vh = normal_bf16(rng, (T, H, d_v))
+    km = np.zeros((T, 1), dtype=np.uint32)
+    for t in range(T):
+        km[t, 0] = np.uint32((1 << (t + 1)) - 1)
+    o, _ = O.masked_mha_prefill(q, kh, vh, km, [0, T], [0, T], 0.4)
+
+    def dec(b):
+        return torch.from_numpy((b.astype(np.uint32) << 16).view(np.float32).astype(np.float64))
+    ref = F.scaled_dot_product_attention(dec(q).permute(1, 0, 2)[None], dec(kh).permute(1, 0, 2)[None],
+                                         dec(vh).permute(1, 0, 2)[None], is_causal=True, scale=0.4)
+    ref = ref[0].permute(1, 0, 2).numpy()
+    return bool(np.max(np.abs(o - ref)) <= 1e-12)
+
+
+ALL_PINS = [pin_bruteforce, pin_single_key, pin_zero_query, pin_equal_keys, pin_two_keys_closed_form,
+            pin_order_and_padding_invariance, pin_dense_causal_sdpa, pin_union_worked_example,
+            pin_union_bruteforce, pin_union_popcounts, pin_grouped_equals_per_token,
+            pin_key_mask_bruteforce, pin_masked_equals_sparse, pin_masked_dense_causal_sdpa]
+
+
+def run_all_pins():
+    res = {}
+    for p in ALL_PINS:
+        try:
+            res[p.__name__] = bool(p())
+        except Exception:  # a mutated oracle may also crash: that counts as caught
+            res[p.__name__] = False
+    return res

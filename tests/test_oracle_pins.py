@@ -1,0 +1,136 @@
+"""The oracle against its pins, and planted mistakes that the pins must catch.
+
+Mistakes are planted in the oracle (on the CPU, through monkeypatch); the
+pins are the functions of ``oracle_pins.py``.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle.dsa_oracle as O
+import oracle_pins as P
+
+
+@pytest.mark.parametrize("pin", P.ALL_PINS, ids=lambda p: p.__name__)
+def test_pin_holds(pin):
+    assert pin()
+
+
+# ----------------------------------------------------------------------------
+# planted mistakes
+# ----------------------------------------------------------------------------
+_orig_sparse = O.sparse_prefill
+_orig_attend = O.attend
+_orig_union = O.union_build
+_orig_grouped = O.grouped_prefill
+_orig_keymask = O.topk_to_key_mask
+_orig_masked = O.masked_mha_prefill
+
+
+def _attend_lse_base2(qf, K, V, scale):
+    out, lse = _orig_attend(qf, K, V, scale)
+    return out, lse / math.log(2.0)
+
+
+def _attend_sign(qf, K, V, scale):
+    return _orig_attend(qf, K, V, -scale)
+
+
+def _attend_no_max_shift_wrong_norm(qf, K, V, scale):
+    out, lse = _orig_attend(qf, K, V, scale)
+    n = max(K.shape[0], 1)
+    return out * (1.0 + 1.0 / n), lse
+
+
+def _attend_transposed_values(qf, K, V, scale):
+    # weights applied to K's first D_V columns reversed: a transposed/wrong operand
+    return _orig_attend(qf, K, V[::-1].copy(), scale)
+
+
+def _sparse_drop_rope(q, kv, idx, k, scale, d_qk, d_v, tokens=None):
+    return _orig_sparse(q[..., :d_v], kv[:, :d_v], idx, k, scale, d_v, d_v, tokens)
+
+
+def _sparse_wrong_scale(q, kv, idx, k, scale, d_qk, d_v, tokens=None):
+    return _orig_sparse(q, kv, idx, k, 1.0 / math.sqrt(d_qk), d_qk, d_v, tokens)
+
+
+def _sparse_v_from_tail(q, kv, idx, k, scale, d_qk, d_v, tokens=None):
+    o, l = _orig_sparse(q, kv, idx, k, scale, d_qk, d_qk, tokens)
+    return o[..., d_qk - d_v:], l
+
+
+def _sparse_ignore_k(q, kv, idx, k, scale, d_qk, d_v, tokens=None):
+    return _orig_sparse(q, kv, idx, idx.shape[1], scale, d_qk, d_v, tokens)
+
+
+def _union_mask_shifted(idx, k, G, N, cu, upad):
+    u, ul, m = _orig_union(idx, k, G, N, cu, upad)
+    return u, ul, (m.astype(np.uint16) << 1).astype(np.uint8)
+
+
+def _union_descending(idx, k, G, N, cu, upad):
+    u, ul, m = _orig_union(idx, k, G, N, cu, upad)
+    for g in range(u.shape[0]):
+        U = int(ul[g])
+        u[g, :U] = u[g, :U][::-1]
+        m[g, :U] = m[g, :U][::-1]
+    return u, ul, m
+
+
+def _union_pad_zero(idx, k, G, N, cu, upad):
+    u, ul, m = _orig_union(idx, k, G, N, cu, upad)
+    for g in range(u.shape[0]):
+        u[g, int(ul[g]):] = 0
+    return u, ul, m
+
+
+def _grouped_head_major(q, kv, u, ul, m, G, cu, scale, d_qk, d_v, group_ids=None):
+    # pseudo-head order h*G + j instead of j*H + h
+    T, H = q.shape[:2]
+    q2 = q.copy()
+    for (t0, n) in O.groups(cu, G):
+        blk = q[t0:t0 + n].reshape(n * H, -1)
+        perm = np.array([(p % n) * H + p // n for p in range(n * H)])
+        q2[t0:t0 + n] = blk[perm].reshape(n, H, -1)
+    return _orig_grouped(q2, kv, u, ul, m, G, cu, scale, d_qk, d_v, group_ids)
+
+
+def _keymask_no_offset(idx, k, cq, ck, words):
+    km = np.zeros((int(cq[-1]), words), dtype=np.uint32)
+    for t in range(int(cq[-1])):
+        for x in idx[t][:k]:
+            if x >= 0 and x < 32 * words:
+                km[t, x >> 5] |= np.uint32(1 << (int(x) & 31))
+    return km
+
+
+def _masked_shared_head(q, k, v, km, cq, ck, scale, tokens=None):
+    return _orig_masked(q, np.repeat(k[:, :1], k.shape[1], axis=1), v, km, cq, ck, scale, tokens)
+
+
+MUTATIONS = [
+    ("attend", _attend_lse_base2),
+    ("attend", _attend_sign),
+    ("attend", _attend_no_max_shift_wrong_norm),
+    ("attend", _attend_transposed_values),
+    ("sparse_prefill", _sparse_drop_rope),
+    ("sparse_prefill", _sparse_wrong_scale),
+    ("sparse_prefill", _sparse_v_from_tail),
+    ("sparse_prefill", _sparse_ignore_k),
+    ("union_build", _union_mask_shifted),
+    ("union_build", _union_descending),
+    ("union_build", _union_pad_zero),
+    ("grouped_prefill", _grouped_head_major),
+    ("topk_to_key_mask", _keymask_no_offset),
+    ("masked_mha_prefill", _masked_shared_head),
+]
+
+
+@pytest.mark.parametrize("name,fn", MUTATIONS, ids=[f.__name__ for _, f in MUTATIONS])
+def test_planted_mistake_is_caught(monkeypatch, name, fn):
+    monkeypatch.setattr(O, name, fn)
+    res = P.run_all_pins()
+    failed = [k for k, v in res.items() if not v]
+    assert failed, f"no pin caught the planted mistake {fn.__name__}"
