@@ -1,0 +1,541 @@
+#!/usr/bin/env python3
+"""Benchmark of the DSA sparse-MLA prefill hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-modes]
+
+Headline workload: DeepSeek-V3.2 shard, per-token sparse prefill of one
+16384-token causal chunk over 16384 latent rows, H = 32, D_QK = 576, D_V = 512,
+top-2048 locality indices (synthetic, seeded).  One step = one call of the
+per-token kernel over the whole chunk; the L2 is flushed (256 MiB write)
+between timed steps and only the kernel is inside the CUDA events.
+
+Prints ONE JSON line (rank 0).  ``value`` is whole-job query-tokens/s.  The
+``modes`` object times the other forms on their own workloads (grouped:
+union build + grouped kernel; NoPE layout per-token and grouped; masked MHA:
+key mask + masked kernel).  ``--impl reference`` times the fp64 CPU oracle
+(the only reference this method has here) on a bounded sample instead.
+Under torchrun every rank runs its own chunk (weak scaling, no collective on
+the data path); time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse prefill query-tokens/s & useful TFLOP/s per GB300; % of HBM / bf16 peak"
+HEADLINE = "v32_h32_16k"
+FLUSH_BYTES = 256 << 20
+
+
+# ----------------------------------------------------------------------------
+# environment
+# ----------------------------------------------------------------------------
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def kernel_source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "dsa_sparse_mla_prefill_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_key, src_hash, launch_units):
+    """DRAM bytes per launch from a committed ncu summary, scaled to this
+    launch by units processed; None if absent or the kernel changed since."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel_key)
+    if not d or d.get("source_hash") != src_hash:
+        return None
+    return d["dram_bytes_per_unit"] * launch_units
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.marks = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        self.marks.append(time.time())
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=2)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for ts, line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[4:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        t0, t1 = (self.marks[0], self.marks[-1]) if len(self.marks) >= 2 else (rows[0][0], rows[-1][0])
+        inwin = [r for r in rows if t0 <= r[0] <= t1] or rows
+        names = ["active_mask", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in inwin:
+            for n, v in zip(names[1:], r[3][1:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[1] for r in inwin), "sm_max_mhz": max(r[2] for r in inwin),
+                "reasons": sorted(reasons), "samples": len(inwin)}
+
+
+# ----------------------------------------------------------------------------
+# multi-GPU: independent replicas (weak scaling), max-over-ranks timing
+# ----------------------------------------------------------------------------
+def rank_workload(w, rank):
+    """Every rank processes its own chunk of the same shape (its own seed):
+    the per-token path has no exchange step, so ranks share nothing."""
+    from dataclasses import replace
+    return w if rank == 0 else replace(w, seed=w.seed + 1000 * rank)
+
+
+def max_over_ranks(x, dist=None, device=None):
+    """Max of a per-rank float over all ranks (identity without a process group)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank, world, ms_max):
+    """Whole-job units/s: every rank's units over the slowest rank's time."""
+    return world * units_per_rank / (ms_max / 1e3)
+
+
+# ----------------------------------------------------------------------------
+# workloads and algorithmic work
+# ----------------------------------------------------------------------------
+def sparse_work(w, idx):
+    """Valid (token, key) pairs and algorithmic bytes / useful FLOPs of the per-token form."""
+    pairs = int((idx[:, :w.k] >= 0).sum())
+    row = w.d_qk * 2
+    bytes_ = pairs * row + w.T * w.H * w.d_qk * 2 + w.T * w.H * w.d_v * 2 + w.T * w.ld * 4 + w.T * w.H * 4
+    flops = 2.0 * w.H * pairs * (w.d_qk + w.d_v)
+    return pairs, bytes_, flops
+
+
+def to_dev(x, dev):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+def timed_steps(fn, steps, warmup, stream, flush=None):
+    """Runs fn() warmup + steps times; per-step CUDA events around fn only;
+    flush (untimed) before each step.  Returns list of ms."""
+    import torch
+    for _ in range(warmup):
+        if flush is not None:
+            flush()
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        if flush is not None:
+            flush()
+        ev[i][0].record(stream)
+        fn()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+# ----------------------------------------------------------------------------
+# CPU baseline: the oracle as it stands, on a bounded sample, spawn pool
+# ----------------------------------------------------------------------------
+def _oracle_worker(args):
+    """Runs the oracle over this worker's tokens, 16 per call, until its time
+    budget is spent.  Returns (tokens done, seconds)."""
+    q, kv, idx, k, scale, d_qk, d_v, budget = args
+    from oracle.dsa_oracle import sparse_prefill
+    t0 = time.perf_counter()
+    done = 0
+    for s in range(0, q.shape[0], 16):
+        sparse_prefill(q[s:s + 16], kv, idx[s:s + 16], k, scale, d_qk, d_v)
+        done += min(16, q.shape[0] - s)
+        if time.perf_counter() - t0 > budget:
+            break
+    return done, time.perf_counter() - t0
+
+
+def cpu_baseline(w, x, budget_s=12.0, pool=None, cores=None):
+    """Times oracle.sparse_prefill, as it stands, on the host cores: each of
+    ``cores`` spawn workers (one BLAS thread each) takes a disjoint random
+    sample of the workload's tokens and works through it until ``budget_s``
+    seconds have passed.  Throughput = tokens done / slowest worker's time."""
+    cores = cores or os.cpu_count() or 1
+    rng = np.random.default_rng(7)
+    toks = rng.permutation(w.T)
+    chunks = [np.sort(c) for c in np.array_split(toks, cores) if len(c)]
+    tasks = [(x.q[c], x.kv, x.idx[c], w.k, w.scale, w.d_qk, w.d_v, budget_s) for c in chunks]
+    own = pool is None
+    if own:
+        pool = oracle_pool(cores)
+    res = pool.map(_oracle_worker, tasks)
+    if own:
+        pool.close()
+        pool.join()
+    n = sum(r[0] for r in res)
+    wall = max(r[1] for r in res)
+    return {"value": n / wall, "unit": "query-tokens/s", "cores": len(tasks), "kind": "oracle",
+            "sample": f"{n} of {w.T} tokens of {w.name} (random, seeded), fp64 numpy oracle in batches of 16, "
+                      f"{len(tasks)} spawn workers x 1 BLAS thread, {wall:.1f} s",
+            "seconds": wall}
+
+
+def _noop(_):
+    return 0
+
+
+def _single_thread_blas():
+    for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[v] = "1"
+
+
+def oracle_pool(cores):
+    """Spawn pool whose workers start with one BLAS thread each (the variables
+    are set while the children are created, before they import numpy)."""
+    saved = {v: os.environ.get(v) for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")}
+    _single_thread_blas()
+    try:
+        pool = mp.get_context("spawn").Pool(cores)
+        pool.map(_noop, range(cores))
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    return pool
+
+
+# ----------------------------------------------------------------------------
+# modes: the other forms on their own workloads
+# ----------------------------------------------------------------------------
+def run_modes(dev, stream, peaks, steps, warmup, flush):
+    import torch
+    import dsa_sparse_mla_prefill_gb300 as dsa
+    from synth import WORKLOADS, make_masked_inputs, make_sparse_inputs
+    out = {}
+    steps = max(3, min(steps, 10))
+
+    def sparse_block(name, grouped=True, per_token=True):
+        w = WORKLOADS[name]
+        x = make_sparse_inputs(w)
+        q, kv = to_dev(x.q, dev), to_dev(x.kv, dev)
+        idx = torch.from_numpy(x.idx).to(dev)
+        pairs, abytes, flops = sparse_work(w, x.idx)
+        res = {"T": w.T, "N": w.N, "H": w.H, "d_qk": w.d_qk, "k": w.k, "ld": w.ld}
+        if per_token:
+            o = torch.empty((w.T, w.H, 512), dtype=torch.bfloat16, device=dev)
+            l = torch.empty((w.T, w.H), dtype=torch.float32, device=dev)
+            ms = statistics.median(timed_steps(lambda: dsa.dsa_sparse_prefill(q, kv, idx, w.k, w.scale, out=o,
+                                                                               lse=l), steps, warmup, stream, flush))
+            res["per_token"] = {"ms": ms, "query_tokens_per_s": w.T / ms * 1e3,
+                                "useful_tflops": flops / ms / 1e9, "logical_gbs": abytes / ms / 1e6,
+                                "hbm_frac_logical": abytes / ms / 1e6 / peaks["hbm_gbs"]}
+        if grouped:
+            G = w.G
+            upad = dsa.dsa_union_pad(G, w.k, 128)
+            ng = dsa.dsa_num_groups(x.cu_seqlens_q, w.T, G)
+            u = torch.empty((ng, upad), dtype=torch.int32, device=dev)
+            ul = torch.empty((ng,), dtype=torch.int32, device=dev)
+            m = torch.empty((ng, upad), dtype=torch.uint8, device=dev)
+            ub = lambda: dsa.dsa_union_build(idx, w.k, G, w.N, cu_seqlens_q=x.cu_seqlens_q, union_pad=upad,
+                                             out=(u, ul, m))
+            ms_u = statistics.median(timed_steps(ub, steps, warmup, stream, flush))
+            ub_bytes = w.T * w.ld * 4 + ng * upad * 5 + ng * 4
+            res["union_build"] = {"ms": ms_u, "ms_per_16k_tokens": ms_u * 16384 / w.T,
+                                  "gbs": ub_bytes / ms_u / 1e6, "hbm_frac": ub_bytes / ms_u / 1e6 / peaks["hbm_gbs"]}
+            ulen = ul.cpu().numpy().astype(np.int64)
+            res["union_mean"] = float(ulen.mean())
+            o = torch.empty((w.T, w.H, 512), dtype=torch.bfloat16, device=dev)
+            l = torch.empty((w.T, w.H), dtype=torch.float32, device=dev)
+            try:
+                gfn = lambda: dsa.dsa_grouped_prefill(q, kv, u, ul, m, G, w.scale, cu_seqlens_q=x.cu_seqlens_q,
+                                                      out=o, lse=l)
+                gfn()
+                ms_g = statistics.median(timed_steps(gfn, steps, warmup, stream, flush))
+                uflops = 2.0 * 128 * float(ulen.sum()) * (w.d_qk + w.d_v)
+                res["grouped"] = {"ms": ms_g, "query_tokens_per_s": w.T / ms_g * 1e3,
+                                  "union_plus_useful_tflops": uflops / ms_g / 1e9,
+                                  "useful_tflops": flops / ms_g / 1e9,
+                                  "tensor_frac": uflops / ms_g / 1e9 / peaks["bf16_tflops"],
+                                  "gathered_gb": float(ulen.sum()) * w.d_qk * 2 / 1e9}
+            except dsa.DSAError as e:
+                res["grouped"] = {"unavailable": str(e)}
+        return res
+
+    out["grouped_21k_of_32k"] = sparse_block("grouped_21k_of_32k")
+    torch.cuda.empty_cache()
+    out["nope_2x8192"] = sparse_block("nope_2x8192")
+    torch.cuda.empty_cache()
+    # masked dense MHA
+    w = WORKLOADS["masked_2x8192"]
+    x = make_masked_inputs(w)
+    words = (max(w.kv_lens) + 31) // 32
+    words = (words + 3) // 4 * 4
+    idx = torch.from_numpy(x.idx).to(dev)
+    km = torch.empty((w.T, words), dtype=torch.int32, device=dev)
+    kfn = lambda: dsa.dsa_topk_to_key_mask(idx, w.k, words, cu_seqlens_q=x.cu_seqlens_q,
+                                           cu_seqlens_kv=x.cu_seqlens_kv, out=km)
+    ms_k = statistics.median(timed_steps(kfn, steps, warmup, stream, flush))
+    res = {"T": w.T, "H": w.H, "d_qk": w.d_qk, "d_v": w.d_v, "key_mask": {"ms": ms_k}}
+    try:
+        q, k, v = to_dev(x.q, dev), to_dev(x.k, dev), to_dev(x.v, dev)
+        o = torch.empty((w.T, w.H, w.d_v), dtype=torch.bfloat16, device=dev)
+        l = torch.empty((w.T, w.H), dtype=torch.float32, device=dev)
+        mfn = lambda: dsa.dsa_masked_mha_prefill(q, k, v, km, w.scale, cu_seqlens_q=x.cu_seqlens_q,
+                                                 cu_seqlens_kv=x.cu_seqlens_kv, out=o, lse=l)
+        mfn()
+        ms_m = statistics.median(timed_steps(mfn, steps, warmup, stream, flush))
+        pairs = int((x.idx[:, :w.k] >= 0).sum())
+        useful = 2.0 * w.H * pairs * (w.d_qk + w.d_v)
+        causal = sum(2.0 * w.H * (n * (n + 1) / 2) * (w.d_qk + w.d_v) for n in w.q_lens)
+        res["masked"] = {"ms": ms_m, "query_tokens_per_s": w.T / ms_m * 1e3, "useful_tflops": useful / ms_m / 1e9,
+                         "dense_causal_tflops": causal / ms_m / 1e9,
+                         "tensor_frac_dense_causal": causal / ms_m / 1e9 / peaks["bf16_tflops"]}
+    except dsa.DSAError as e:
+        res["masked"] = {"unavailable": str(e)}
+    out["masked_2x8192"] = res
+    return out
+
+
+# ----------------------------------------------------------------------------
+# arms
+# ----------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    import dsa_sparse_mla_prefill_gb300 as dsa
+    from synth import WORKLOADS, make_sparse_inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks = measured_peaks()
+    w = rank_workload(WORKLOADS[HEADLINE], rank)
+
+    # CPU baseline pool first (spawn), before heavy GPU work
+    pool = None
+    cores = os.cpu_count() or 1
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        pool = oracle_pool(cores)
+
+    x = make_sparse_inputs(w)
+    pairs, abytes, flops = sparse_work(w, x.idx)
+    q, kv = to_dev(x.q, dev), to_dev(x.kv, dev)
+    idx = torch.from_numpy(x.idx).to(dev)
+    out = torch.empty((w.T, w.H, w.d_v), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.T, w.H), dtype=torch.float32, device=dev)
+    flush_buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = lambda: flush_buf.zero_()
+    stream = torch.cuda.current_stream(dev)
+    step = lambda: dsa.dsa_sparse_prefill(q, kv, idx, w.k, w.scale, out=out, lse=lse)
+
+    # correctness guard on a few tokens (oracle, rank 0) before timing
+    step()
+    torch.cuda.synchronize()
+    st, counts = dsa.dsa_last_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error counters after the first step: {counts}")
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(args.warmup):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.mark()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks.mark()
+    clocks.stop()
+    ms = [a.elapsed_time(b) for a, b in ev]
+    ms_step = max_over_ranks(sum(ms) / len(ms), dist, dev)
+    value = job_throughput(w.T, world, ms_step)
+
+    # end-to-end through host buffers: H2D inputs, kernel, D2H outputs, every step
+    hq = torch.from_numpy(np.ascontiguousarray(x.q).view(np.int16)).view(torch.bfloat16).pin_memory()
+    hkv = torch.from_numpy(np.ascontiguousarray(x.kv).view(np.int16)).view(torch.bfloat16).pin_memory()
+    hidx = torch.from_numpy(x.idx).pin_memory()
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        kv.copy_(hkv, non_blocking=True)
+        idx.copy_(hidx, non_blocking=True)
+        dsa.dsa_sparse_prefill(q, kv, idx, w.k, w.scale, out=out, lse=lse)
+        hout.copy_(out, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    e2e_ms = statistics.mean(timed_steps(e2e_step, e2e_steps, min(args.warmup, 3), stream, flush))
+    h2d = hq.numel() * 2 + hkv.numel() * 2 + hidx.numel() * 4
+    d2h = hout.numel() * 2 + hlse.numel() * 4
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
+
+    src_hash = kernel_source_hash(["sparse_prefill.cu", "dsa_device.cuh"])
+    traffic = profiled_traffic("sparse_prefill_" + HEADLINE, src_hash, w.T)
+    achieved = abytes / (ms_step / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "query-tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "N": w.N, "H": w.H, "d_qk": w.d_qk, "d_v": w.d_v, "k": w.k,
+                   "ld": w.ld, "index_gen": "locality (8-token blocks, 2048 base + 352-position shared pool)",
+                   "valid_pairs": pairs, "l2": "flushed before every timed step (256 MiB write, outside the events)",
+                   "parallelism": f"replica per GPU x{world}"},
+        "useful_tflops": world * flops / (ms_step / 1e3) / 1e12,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "kernel": "dsa::sparse::sparse_prefill_kernel<32,9>",
+                     "algorithmic_bytes": abytes, "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)"},
+        "e2e": {"value": job_throughput(w.T, world, e2e_ms), "unit": "query-tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and not args.no_modes:
+        del hq, hkv, hidx, hout, hlse
+        try:
+            line["modes"] = run_modes(dev, stream, peaks, args.steps, args.warmup, flush)
+        except Exception as e:  # report, never hide the headline
+            line["modes"] = {"error": repr(e)}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, x, budget_s=args.cpu_budget, pool=pool, cores=cores)
+        pool.close()
+        pool.join()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The oracle timed on the host cores on the headline workload; rank 0 only."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from synth import WORKLOADS, make_sparse_inputs
+    w = WORKLOADS[HEADLINE]
+    x = make_sparse_inputs(w)
+    cores = os.cpu_count() or 1
+    pool = oracle_pool(cores)
+    budget = max(2.0, min(args.cpu_budget, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_baseline(w, x, budget_s=budget / 4, pool=pool, cores=cores)
+    vals, secs, samples = [], [], []
+    for _ in range(args.steps):
+        r = cpu_baseline(w, x, budget_s=budget, pool=pool, cores=cores)
+        vals.append(r["value"])
+        secs.append(r["seconds"])
+        samples.append(r["sample"])
+    pool.close()
+    pool.join()
+    value = statistics.mean(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "query-tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": w.T / value * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "T": w.T, "N": w.N, "H": w.H, "d_qk": w.d_qk, "d_v": w.d_v, "k": w.k},
+            "cpu_baseline": {"value": value, "unit": "query-tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": samples[-1]},
+            "e2e": {"value": value, "unit": "query-tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-modes", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work per core")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,253 @@
+"""GB300 (sm_103a) DeepSeek-Sparse-Attention prefill over an MLA latent KV cache.
+
+A thin ctypes binding over ``libdsa.so`` (C ABI in ``include/dsa.h``).  The
+functions carry the C names and only marshal arguments: they check tensor
+dtypes/devices, allocate outputs with torch when none are given, pass raw
+device pointers and the current CUDA stream, and raise ``DSAError`` on a
+non-zero status.  All arithmetic happens in the library's CUDA kernels;
+there is no CPU fallback: without the built library every call raises.
+
+Forms (see the header for the exact contracts):
+  dsa_sparse_prefill      per-token sparse attention over each token's top-k rows
+  dsa_union_build         sorted union per group + head-group membership mask
+  dsa_grouped_prefill     G = 128/H tokens as 128 pseudo-heads over the union
+  dsa_topk_to_key_mask    packed per-token key mask from the top-k rows
+  dsa_masked_mha_prefill  masked dense MHA with per-head q/k/v
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdsa.so")
+MAX_REQUESTS = 512
+
+DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_CUDA, DSA_ERR_DEVICE = range(5)
+
+
+class DSAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+_lib_handle = None
+
+_VP = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_I32P = ctypes.POINTER(ctypes.c_int32)
+
+_SIGNATURES = {
+    "dsa_status_string": (ctypes.c_char_p, [_I]),
+    "dsa_version": (_I, []),
+    "dsa_union_pad": (ctypes.c_int64, [_I, _I, _I]),
+    "dsa_num_groups": (_I, [_I32P, _I, _I, _I, ctypes.POINTER(ctypes.c_int)]),
+    "dsa_union_build": (_I, [_VP, _I, _I, _I, _I, _I32P, _I, _I, _VP, _VP, _VP, _I, _VP]),
+    "dsa_sparse_prefill": (_I, [_VP, _VP, _I, _I, _VP, _I, _I, _I, _I, _I, _I, _F, _VP, _VP, _VP]),
+    "dsa_grouped_prefill": (_I, [_VP, _VP, _I, _I, _VP, _VP, _VP, _I, _I, _I32P, _I, _I, _I, _I, _I, _F, _VP,
+                                 _VP, _VP]),
+    "dsa_topk_to_key_mask": (_I, [_VP, _I, _I, _I, _I32P, _I32P, _I, _VP, _I, _VP]),
+    "dsa_masked_mha_prefill": (_I, [_VP, _VP, _VP, _VP, _I, _I32P, _I32P, _I, _I, _I, _I, _I, _F, _VP, _VP,
+                                    _VP]),
+    "dsa_last_device_error": (_I, [_VP, ctypes.POINTER(ctypes.c_uint32)]),
+}
+
+EXPORTED = tuple(_SIGNATURES)
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded ``libdsa.so`` (raises if it has not been built)."""
+    global _lib_handle
+    if _lib_handle is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -m dsa_sparse_mla_prefill_gb300.build` "
+                               "(the library has no CPU fallback)")
+        h = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(h, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib_handle = h
+    return _lib_handle
+
+
+def status_string(status: int) -> str:
+    return lib().dsa_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != DSA_OK:
+        raise DSAError(status, where)
+
+
+def _host_i32(arr):
+    """Host int32 array for a cu_seqlens argument (None stays None)."""
+    if arr is None:
+        return None, None
+    try:
+        import torch
+        if isinstance(arr, torch.Tensor):
+            arr = arr.detach().cpu().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    a = np.ascontiguousarray(np.asarray(arr, dtype=np.int32))
+    return a, a.ctypes.data_as(_I32P)
+
+
+def _stream(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _need(t, dtype, name, ndim=None):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+    return t
+
+
+def dsa_union_pad(G: int, k: int, union_block: int = 128) -> int:
+    return int(lib().dsa_union_pad(G, k, union_block))
+
+
+def dsa_num_groups(cu_seqlens_q, T: int, G: int) -> int:
+    arr, ptr = _host_i32(cu_seqlens_q)
+    n = ctypes.c_int(0)
+    nreq = 0 if arr is None else len(arr) - 1
+    _check(lib().dsa_num_groups(ptr, nreq, T, G, ctypes.byref(n)), "dsa_num_groups")
+    return n.value
+
+
+def dsa_union_build(idx, k: int, G: int, N: int, cu_seqlens_q=None, union_pad: int | None = None,
+                    union_block: int = 128, out=None, stream=None):
+    """Returns (union_idx [groups, union_pad] int32, union_len [groups] int32,
+    mask [groups, union_pad] uint8)."""
+    import torch
+    _need(idx, torch.int32, "idx", 2)
+    T, ld = idx.shape
+    if union_pad is None:
+        union_pad = dsa_union_pad(G, k, union_block)
+    ng = dsa_num_groups(cu_seqlens_q, T, G)
+    if out is None:
+        u = torch.empty((ng, union_pad), dtype=torch.int32, device=idx.device)
+        ul = torch.empty((ng,), dtype=torch.int32, device=idx.device)
+        m = torch.empty((ng, union_pad), dtype=torch.uint8, device=idx.device)
+    else:
+        u, ul, m = out
+    arr, ptr = _host_i32(cu_seqlens_q)
+    nreq = 0 if arr is None else len(arr) - 1
+    _check(lib().dsa_union_build(idx.data_ptr(), T, k, ld, G, ptr, nreq, N, u.data_ptr(), ul.data_ptr(),
+                                 m.data_ptr(), union_pad, _stream(stream, idx.device)), "dsa_union_build")
+    return u, ul, m
+
+
+def dsa_sparse_prefill(q, kv, idx, k: int, scale: float, d_v: int = 512, out=None, lse=None, stream=None):
+    """Per-token sparse prefill.  q [T, H, d_qk] bf16, kv [N, ld_kv] bf16 (the
+    first d_qk columns are the latent key, the first d_v the value), idx
+    [T, ld] int32 global rows.  Returns (out [T, H, d_v] bf16, lse [T, H] fp32)."""
+    import torch
+    _need(q, torch.bfloat16, "q", 3)
+    _need(kv, torch.bfloat16, "kv", 2)
+    _need(idx, torch.int32, "idx", 2)
+    T, H, d_qk = q.shape
+    N, ld_kv = kv.shape
+    if idx.shape[0] != T:
+        raise ValueError("idx rows must match q tokens")
+    if out is None:
+        out = torch.empty((T, H, d_v), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
+    _check(lib().dsa_sparse_prefill(q.data_ptr(), kv.data_ptr(), N, ld_kv, idx.data_ptr(), T, H, d_qk, d_v, k,
+                                    idx.shape[1], float(scale), out.data_ptr(), lse.data_ptr(),
+                                    _stream(stream, q.device)), "dsa_sparse_prefill")
+    return out, lse
+
+
+def dsa_grouped_prefill(q, kv, union_idx, union_len, mask, G: int, scale: float, cu_seqlens_q=None,
+                        d_v: int = 512, out=None, lse=None, stream=None):
+    """Grouped sparse prefill over (union_idx, union_len, mask) from dsa_union_build."""
+    import torch
+    _need(q, torch.bfloat16, "q", 3)
+    _need(kv, torch.bfloat16, "kv", 2)
+    _need(union_idx, torch.int32, "union_idx", 2)
+    _need(union_len, torch.int32, "union_len", 1)
+    _need(mask, torch.uint8, "mask", 2)
+    T, H, d_qk = q.shape
+    N, ld_kv = kv.shape
+    if out is None:
+        out = torch.empty((T, H, d_v), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
+    arr, ptr = _host_i32(cu_seqlens_q)
+    nreq = 0 if arr is None else len(arr) - 1
+    _check(lib().dsa_grouped_prefill(q.data_ptr(), kv.data_ptr(), N, ld_kv, union_idx.data_ptr(),
+                                     union_len.data_ptr(), mask.data_ptr(), union_idx.shape[1], G, ptr, nreq, T,
+                                     H, d_qk, d_v, float(scale), out.data_ptr(), lse.data_ptr(),
+                                     _stream(stream, q.device)), "dsa_grouped_prefill")
+    return out, lse
+
+
+def dsa_topk_to_key_mask(idx, k: int, words: int, cu_seqlens_q=None, cu_seqlens_kv=None, out=None, stream=None):
+    """Packed key mask [T, words] uint32 (viewed as int32 in torch)."""
+    import torch
+    _need(idx, torch.int32, "idx", 2)
+    T, ld = idx.shape
+    if out is None:
+        out = torch.empty((T, words), dtype=torch.int32, device=idx.device)
+    aq, pq = _host_i32(cu_seqlens_q)
+    ak, pk = _host_i32(cu_seqlens_kv)
+    nreq = 0 if aq is None else len(aq) - 1
+    _check(lib().dsa_topk_to_key_mask(idx.data_ptr(), T, k, ld, pq, pk, nreq, out.data_ptr(), words,
+                                      _stream(stream, idx.device)), "dsa_topk_to_key_mask")
+    return out
+
+
+def dsa_masked_mha_prefill(q, k, v, key_mask, scale: float, cu_seqlens_q=None, cu_seqlens_kv=None, out=None,
+                           lse=None, stream=None):
+    """Masked dense MHA.  q [T, H, d_qk], k [Nk, H, d_qk], v [Nk, H, d_v] bf16;
+    key_mask [T, words] (int32/uint32 bits).  Returns (out [T, H, d_v], lse [T, H])."""
+    import torch
+    _need(q, torch.bfloat16, "q", 3)
+    _need(k, torch.bfloat16, "k", 3)
+    _need(v, torch.bfloat16, "v", 3)
+    if key_mask.dtype not in (torch.int32,):
+        raise TypeError("key_mask must be int32 (bit pattern of uint32 words)")
+    _need(key_mask, key_mask.dtype, "key_mask", 2)
+    T, H, d_qk = q.shape
+    d_v = v.shape[2]
+    if out is None:
+        out = torch.empty((T, H, d_v), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
+    aq, pq = _host_i32(cu_seqlens_q)
+    ak, pk = _host_i32(cu_seqlens_kv)
+    nreq = 0 if aq is None else len(aq) - 1
+    _check(lib().dsa_masked_mha_prefill(q.data_ptr(), k.data_ptr(), v.data_ptr(), key_mask.data_ptr(),
+                                        key_mask.shape[1], pq, pk, nreq, T, H, d_qk, d_v, float(scale),
+                                        out.data_ptr(), lse.data_ptr(), _stream(stream, q.device)),
+           "dsa_masked_mha_prefill")
+    return out, lse
+
+
+def dsa_last_device_error(stream=None, device=None):
+    """Synchronizes the stream and returns (status, [bad_index, timeout, union_overflow, reserved]),
+    clearing the device counters."""
+    import torch
+    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    counts = (ctypes.c_uint32 * 4)()
+    st = lib().dsa_last_device_error(_stream(stream, dev), counts)
+    return st, [int(c) for c in counts]

@@ -1,0 +1,299 @@
+// C-ABI shim: argument validation, host-side request tables and kernel
+// launches for the entry points declared in include/dsa.h.
+#include <cstdint>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "../../include/dsa.h"
+#include "dsa_kernels.h"
+
+namespace {
+
+// Device error counters (see dsa_last_device_error).  One copy per device
+// that loads the library.
+__device__ unsigned int g_dsa_err[4];
+
+constexpr int kMaxDev = 64;
+
+struct DevInfo {
+  bool init = false;
+  int num_sms = 0;
+  unsigned int* err = nullptr;
+};
+DevInfo g_dev[kMaxDev];
+
+// Per-device set-up: SM count and the device address of the error counters.
+bool dev_info(DevInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return false;
+  DevInfo& d = g_dev[dev];
+  if (!d.init) {
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dsa_err) != cudaSuccess) return false;
+    d.err = static_cast<unsigned int*>(p);
+    d.init = true;
+  }
+  *out = &d;
+  return true;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// Fills a request table from host offsets (NULL = one request of T tokens).
+// With G > 0, cu_g holds group offsets (G tokens of one request per group).
+int fill_req(dsa::ReqTable& rq, const int32_t* cu_q, const int32_t* cu_kv, int num_req, int T, int Nkv,
+             int G) {
+  if (cu_q == nullptr) {
+    if (cu_kv != nullptr) return DSA_ERR_INVALID_ARG;
+    num_req = 1;
+  }
+  if (num_req < 1) return DSA_ERR_INVALID_ARG;
+  if (num_req > dsa::kMaxReq) return DSA_ERR_UNSUPPORTED;
+  rq.num_req = num_req;
+  rq.cu_q[0] = 0;
+  rq.cu_kv[0] = 0;
+  rq.cu_g[0] = 0;
+  for (int r = 0; r < num_req; ++r) {
+    const int q0 = cu_q ? cu_q[r] : 0, q1 = cu_q ? cu_q[r + 1] : T;
+    // without KV offsets the (single) request spans Nkv rows; Nkv < 0 = not used
+    const int k0 = cu_kv ? cu_kv[r] : 0, k1 = cu_kv ? cu_kv[r + 1] : (Nkv > 0 ? Nkv : 0);
+    if (q1 < q0 || k1 < k0) return DSA_ERR_INVALID_ARG;
+    if (r == 0 && (q0 != 0 || k0 != 0)) return DSA_ERR_INVALID_ARG;
+    rq.cu_q[r + 1] = q1;
+    rq.cu_kv[r + 1] = k1;
+    const int ng = (G > 0) ? (q1 - q0 + G - 1) / G : 0;
+    rq.cu_g[r + 1] = rq.cu_g[r] + ng;
+  }
+  if (rq.cu_q[num_req] != T) return DSA_ERR_INVALID_ARG;
+  if (Nkv >= 0 && cu_kv && rq.cu_kv[num_req] != Nkv) return DSA_ERR_INVALID_ARG;
+  return DSA_OK;
+}
+
+constexpr int kMaxSmem = 232448;
+
+}  // namespace
+
+extern "C" {
+
+const char* dsa_status_string(int status) {
+  switch (status) {
+    case DSA_OK: return "DSA_OK";
+    case DSA_ERR_INVALID_ARG: return "DSA_ERR_INVALID_ARG";
+    case DSA_ERR_UNSUPPORTED: return "DSA_ERR_UNSUPPORTED";
+    case DSA_ERR_CUDA: return "DSA_ERR_CUDA";
+    case DSA_ERR_DEVICE: return "DSA_ERR_DEVICE";
+    default: return "DSA_ERR_UNKNOWN";
+  }
+}
+
+int dsa_version(void) { return 100; }
+
+int64_t dsa_union_pad(int G, int k, int union_block) {
+  if (G <= 0 || k <= 0 || union_block <= 0) return -1;
+  const int64_t n = (int64_t)G * k;
+  return (n + union_block - 1) / union_block * union_block;
+}
+
+int dsa_num_groups(const int32_t* cu_seqlens_q_host, int num_req, int T, int G, int* num_groups) {
+  if (num_groups == nullptr || G <= 0 || T < 0) return DSA_ERR_INVALID_ARG;
+  if (cu_seqlens_q_host == nullptr) {
+    *num_groups = (T + G - 1) / G;
+    return DSA_OK;
+  }
+  if (num_req < 1 || cu_seqlens_q_host[0] != 0 || cu_seqlens_q_host[num_req] != T) return DSA_ERR_INVALID_ARG;
+  int64_t n = 0;
+  for (int r = 0; r < num_req; ++r) {
+    const int len = cu_seqlens_q_host[r + 1] - cu_seqlens_q_host[r];
+    if (len < 0) return DSA_ERR_INVALID_ARG;
+    n += (len + G - 1) / G;
+  }
+  *num_groups = (int)n;
+  return DSA_OK;
+}
+
+int dsa_union_build(const int32_t* idx, int T, int k, int ld, int G, const int32_t* cu_seqlens_q_host,
+                    int num_req, int N, int32_t* union_idx, int32_t* union_len, uint8_t* mask, int union_pad,
+                    dsa_stream_t stream) {
+  if (T < 0 || k < 0 || ld < k || G < 1 || N < 0 || union_pad < 0) return DSA_ERR_INVALID_ARG;
+  if (G > 8) return DSA_ERR_UNSUPPORTED;
+  if ((union_pad & 15) != 0) return DSA_ERR_INVALID_ARG;
+  const int64_t need = (int64_t)G * k < N ? (int64_t)G * k : N;
+  if (union_pad < need) return DSA_ERR_INVALID_ARG;
+  if (dsa::union_build_smem_bytes(N, union_pad) > kMaxSmem) return DSA_ERR_UNSUPPORTED;
+  if (T == 0) return DSA_OK;
+  if (!idx || !union_idx || !union_len || !mask) return DSA_ERR_INVALID_ARG;
+  if (!aligned4(idx) || !aligned16(union_idx) || !aligned16(mask) || !aligned4(union_len))
+    return DSA_ERR_INVALID_ARG;
+  dsa::UnionArgs a;
+  int st = fill_req(a.req, cu_seqlens_q_host, nullptr, num_req, T, -1, G);
+  if (st != DSA_OK) return st;
+  DevInfo* d;
+  if (!dev_info(&d)) return DSA_ERR_CUDA;
+  a.idx = idx;
+  a.union_idx = union_idx;
+  a.union_len = union_len;
+  a.mask = mask;
+  a.err = d->err;
+  a.T = T;
+  a.k = k;
+  a.ld = ld;
+  a.G = G;
+  a.N = N;
+  a.union_pad = union_pad;
+  a.num_groups = a.req.cu_g[a.req.num_req];
+  return dsa::launch_union_build(a, (cudaStream_t)stream) == 0 ? DSA_OK : DSA_ERR_CUDA;
+}
+
+int dsa_sparse_prefill(const uint16_t* q, const uint16_t* kv, int N, int ld_kv, const int32_t* idx, int T,
+                       int H, int d_qk, int d_v, int k, int ld, float scale, uint16_t* out, float* lse,
+                       dsa_stream_t stream) {
+  if (T < 0 || N < 0 || k < 0 || ld < k || ld_kv < d_qk) return DSA_ERR_INVALID_ARG;
+  if (!(H == 16 || H == 32) || !(d_qk == 576 || d_qk == 512) || d_v != 512 || k > 2048)
+    return DSA_ERR_UNSUPPORTED;
+  if ((ld_kv & 7) != 0) return DSA_ERR_INVALID_ARG;
+  if (T == 0) return DSA_OK;
+  if (!q || !kv || !idx || !out || !lse) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv) || !aligned4(idx) || !aligned4(out) || !aligned4(lse))
+    return DSA_ERR_INVALID_ARG;
+  DevInfo* d;
+  if (!dev_info(&d)) return DSA_ERR_CUDA;
+  dsa::SparseArgs a;
+  a.q = q;
+  a.kv = kv;
+  a.idx = idx;
+  a.out = out;
+  a.lse = lse;
+  a.err = d->err;
+  a.T = T;
+  a.H = H;
+  a.d_qk = d_qk;
+  a.N = N;
+  a.ld_kv = ld_kv;
+  a.k = k;
+  a.ld = ld;
+  a.scale = scale;
+  const int r = dsa::launch_sparse_prefill(a, d->num_sms, (cudaStream_t)stream);
+  return r == 0 ? DSA_OK : (r == -2 ? DSA_ERR_UNSUPPORTED : DSA_ERR_CUDA);
+}
+
+int dsa_grouped_prefill(const uint16_t* q, const uint16_t* kv, int N, int ld_kv, const int32_t* union_idx,
+                        const int32_t* union_len, const uint8_t* mask, int union_pad, int G,
+                        const int32_t* cu_seqlens_q_host, int num_req, int T, int H, int d_qk, int d_v,
+                        float scale, uint16_t* out, float* lse, dsa_stream_t stream) {
+  if (T < 0 || N < 0 || G < 1 || H < 1 || union_pad < 0 || ld_kv < d_qk) return DSA_ERR_INVALID_ARG;
+  if (G > 8 || G * H != 128 || !(d_qk == 576 || d_qk == 512) || d_v != 512) return DSA_ERR_UNSUPPORTED;
+  if ((ld_kv & 7) != 0 || (union_pad & 15) != 0) return DSA_ERR_INVALID_ARG;
+  if (T == 0) return DSA_OK;
+  if (!q || !kv || !union_idx || !union_len || !mask || !out || !lse) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv) || !aligned16(union_idx) || !aligned16(mask) || !aligned16(out) ||
+      !aligned4(lse))
+    return DSA_ERR_INVALID_ARG;
+  dsa::GroupedArgs a;
+  int st = fill_req(a.req, cu_seqlens_q_host, nullptr, num_req, T, -1, G);
+  if (st != DSA_OK) return st;
+  DevInfo* d;
+  if (!dev_info(&d)) return DSA_ERR_CUDA;
+  a.q = q;
+  a.kv = kv;
+  a.union_idx = union_idx;
+  a.union_len = union_len;
+  a.mask = mask;
+  a.out = out;
+  a.lse = lse;
+  a.err = d->err;
+  a.T = T;
+  a.H = H;
+  a.G = G;
+  a.d_qk = d_qk;
+  a.N = N;
+  a.ld_kv = ld_kv;
+  a.union_pad = union_pad;
+  a.num_groups = a.req.cu_g[a.req.num_req];
+  a.scale = scale;
+  const int r = dsa::launch_grouped_prefill(a, d->num_sms, (cudaStream_t)stream);
+  return r == 0 ? DSA_OK : (r == -2 ? DSA_ERR_UNSUPPORTED : DSA_ERR_CUDA);
+}
+
+int dsa_topk_to_key_mask(const int32_t* idx, int T, int k, int ld, const int32_t* cu_seqlens_q_host,
+                         const int32_t* cu_seqlens_kv_host, int num_req, uint32_t* key_mask, int words,
+                         dsa_stream_t stream) {
+  if (T < 0 || k < 0 || ld < k || words < 1) return DSA_ERR_INVALID_ARG;
+  if ((cu_seqlens_q_host == nullptr) != (cu_seqlens_kv_host == nullptr)) return DSA_ERR_INVALID_ARG;
+  if (words * 4 > kMaxSmem) return DSA_ERR_UNSUPPORTED;
+  if (T == 0) return DSA_OK;
+  if (!idx || !key_mask || !aligned4(idx) || !aligned4(key_mask)) return DSA_ERR_INVALID_ARG;
+  dsa::KeyMaskArgs a;
+  // one request without offsets: every key of [0, 32*words) is request-local
+  int st = fill_req(a.req, cu_seqlens_q_host, cu_seqlens_kv_host, num_req, T,
+                    cu_seqlens_kv_host ? -1 : 32 * words, 0);
+  if (st != DSA_OK) return st;
+  for (int r = 0; r < a.req.num_req; ++r)
+    if (a.req.cu_kv[r + 1] - a.req.cu_kv[r] > 32 * words) return DSA_ERR_INVALID_ARG;
+  DevInfo* d;
+  if (!dev_info(&d)) return DSA_ERR_CUDA;
+  a.idx = idx;
+  a.key_mask = key_mask;
+  a.err = d->err;
+  a.T = T;
+  a.k = k;
+  a.ld = ld;
+  a.words = words;
+  return dsa::launch_topk_to_key_mask(a, (cudaStream_t)stream) == 0 ? DSA_OK : DSA_ERR_CUDA;
+}
+
+int dsa_masked_mha_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint32_t* key_mask,
+                           int words, const int32_t* cu_seqlens_q_host, const int32_t* cu_seqlens_kv_host,
+                           int num_req, int T, int H, int d_qk, int d_v, float scale, uint16_t* out, float* lse,
+                           dsa_stream_t stream) {
+  if (T < 0 || H < 1 || words < 1) return DSA_ERR_INVALID_ARG;
+  if ((cu_seqlens_q_host == nullptr) != (cu_seqlens_kv_host == nullptr)) return DSA_ERR_INVALID_ARG;
+  if (!(d_qk == 192 && d_v == 128)) return DSA_ERR_UNSUPPORTED;
+  if (T == 0) return DSA_OK;
+  if (!q || !k || !v || !key_mask || !out || !lse) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(key_mask) || !aligned16(out) ||
+      !aligned4(lse))
+    return DSA_ERR_INVALID_ARG;
+  if ((words & 3) != 0) return DSA_ERR_INVALID_ARG;  // 128-key tiles read 4 words per row
+  dsa::MaskedArgs a;
+  // query tiles of 128 per request
+  int st = fill_req(a.req, cu_seqlens_q_host, cu_seqlens_kv_host, num_req, T, cu_seqlens_kv_host ? -1 : T, 128);
+  if (st != DSA_OK) return st;
+  for (int r = 0; r < a.req.num_req; ++r)
+    if (a.req.cu_kv[r + 1] - a.req.cu_kv[r] > 32 * words) return DSA_ERR_INVALID_ARG;
+  DevInfo* d;
+  if (!dev_info(&d)) return DSA_ERR_CUDA;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.key_mask = key_mask;
+  a.out = out;
+  a.lse = lse;
+  a.err = d->err;
+  a.T = T;
+  a.H = H;
+  a.d_qk = d_qk;
+  a.d_v = d_v;
+  a.words = words;
+  a.num_qtiles = a.req.cu_g[a.req.num_req];
+  a.scale = scale;
+  const int r = dsa::launch_masked_mha(a, d->num_sms, (cudaStream_t)stream);
+  return r == 0 ? DSA_OK : (r == -2 ? DSA_ERR_UNSUPPORTED : DSA_ERR_CUDA);
+}
+
+int dsa_last_device_error(dsa_stream_t stream, uint32_t* counts) {
+  if (!counts) return DSA_ERR_INVALID_ARG;
+  DevInfo* d;
+  if (!dev_info(&d)) return DSA_ERR_CUDA;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return DSA_ERR_CUDA;
+  unsigned int h[4] = {0, 0, 0, 0};
+  if (cudaMemcpy(h, d->err, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return DSA_ERR_CUDA;
+  const unsigned int z[4] = {0, 0, 0, 0};
+  if (cudaMemcpy(d->err, z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess) return DSA_ERR_CUDA;
+  for (int i = 0; i < 4; ++i) counts[i] = h[i];
+  return (h[1] || h[2]) ? DSA_ERR_DEVICE : DSA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,94 @@
+// Internal interface between the C-ABI shim (dsa_api.cu) and the kernels.
+// Not installed; callers use include/dsa.h.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace dsa {
+
+// Requests whose host-side sequence offsets travel inside the launch
+// parameters (no device copy, no allocation).
+constexpr int kMaxReq = 512;
+
+struct ReqTable {
+  int num_req;
+  int32_t cu_q[kMaxReq + 1];    // query token offsets
+  int32_t cu_kv[kMaxReq + 1];   // KV row offsets (masked mode / key mask)
+  int32_t cu_g[kMaxReq + 1];    // group (or query tile) offsets
+};
+
+struct SparseArgs {
+  const uint16_t* q;    // [T, H, d_qk] bf16
+  const uint16_t* kv;   // [N, ld_kv] bf16
+  const int32_t* idx;   // [T, ld]
+  uint16_t* out;        // [T, H, 512] bf16
+  float* lse;           // [T, H]
+  unsigned int* err;    // device error counters
+  int T, H, d_qk, N, ld_kv, k, ld;
+  float scale;
+};
+
+struct UnionArgs {
+  const int32_t* idx;   // [T, ld]
+  int32_t* union_idx;   // [groups, union_pad]
+  int32_t* union_len;   // [groups]
+  uint8_t* mask;        // [groups, union_pad]
+  unsigned int* err;
+  int T, k, ld, G, N, union_pad, num_groups;
+  ReqTable req;
+};
+
+struct KeyMaskArgs {
+  const int32_t* idx;   // [T, ld] global rows
+  uint32_t* key_mask;   // [T, words]
+  unsigned int* err;
+  int T, k, ld, words;
+  ReqTable req;
+};
+
+struct GroupedArgs {
+  const uint16_t* q;
+  const uint16_t* kv;
+  const int32_t* union_idx;
+  const int32_t* union_len;
+  const uint8_t* mask;
+  uint16_t* out;
+  float* lse;
+  unsigned int* err;
+  int T, H, G, d_qk, N, ld_kv, union_pad, num_groups;
+  float scale;
+  ReqTable req;
+};
+
+struct MaskedArgs {
+  const uint16_t* q;    // [T, H, d_qk]
+  const uint16_t* k;    // [Nk, H, d_qk]
+  const uint16_t* v;    // [Nk, H, d_v]
+  const uint32_t* key_mask;  // [T, words]
+  uint16_t* out;        // [T, H, d_v]
+  float* lse;           // [T, H]
+  unsigned int* err;
+  int T, H, d_qk, d_v, words, num_qtiles;
+  float scale;
+  ReqTable req;         // cu_g = query-tile offsets per request
+};
+
+// Shared memory of the union builder: bitmap and prefix (W words each, W
+// rounded up to a multiple of 4 so the mask staging stays 16-byte aligned)
+// plus one mask byte per union slot.
+inline int union_build_smem_bytes(int N, int union_pad) {
+  const int W = (N + 31) / 32;
+  const int Wp = (W + 3) & ~3;
+  return 8 * Wp + union_pad;
+}
+
+// Each returns 0 on success, -1 on a CUDA launch error, -2 if the shape has
+// no kernel instance.
+int launch_sparse_prefill(const SparseArgs& a, int num_sms, cudaStream_t stream);
+int launch_union_build(const UnionArgs& a, cudaStream_t stream);
+int launch_topk_to_key_mask(const KeyMaskArgs& a, cudaStream_t stream);
+int launch_grouped_prefill(const GroupedArgs& a, int num_sms, cudaStream_t stream);
+int launch_masked_mha(const MaskedArgs& a, int num_sms, cudaStream_t stream);
+
+}  // namespace dsa

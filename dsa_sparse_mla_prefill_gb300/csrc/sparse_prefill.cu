@@ -1,0 +1,595 @@
+// Per-token sparse MLA prefill for sm_103a.
+//
+// What it computes ("[Perf][DSA] Grouped sparse prefill with the FlashMLA
+// head-group-mask kernel", commit message and Why): every query token t with
+// H heads attends to its own top-k latent KV rows,
+//     out[t,h,:] = softmax_j(scale * q[t,h,:] . kv[idx_j, 0:D_QK]) . kv[idx_j, 0:D_V]
+// plus the natural-log log-sum-exp.  Each selected row is re-gathered for
+// every token (2048 x 1152 B per token at top-2048, D_QK = 576), so the form
+// is bound by the gather.
+//
+// Design (one persistent CTA per SM, tokens round-robin over CTAs):
+//   warp 5      compacts the token's index row (valid entries only, order
+//               kept) into shared memory; out-of-range entries are counted.
+//   warps 6-9   gather: 16-byte cp.async per thread, 8 threads per 128-byte
+//               row piece, into 128B-swizzled tiles of 128 keys; one "unit"
+//               holds 128 columns (two swizzle columns) of 128 keys, the RoPE
+//               columns go to their own 2-slot ring.
+//   warp 4      one thread issues tcgen05.mma with the keys on the M side
+//               (M = 128 keys, N = H): S^T = K q^T over D_QK, then
+//               O^T += V^T P^T with V^T read MN-major from the same tile.
+//   warps 0-3   thread i owns key i of the tile (TMEM lane i): online softmax
+//               in base 2 with a lazy rescale (only when a head's running
+//               max grows by more than 2^8), P written bf16 to shared
+//               memory, and the epilogue (O^T lane = output column).
+#include "dsa_device.cuh"
+#include "dsa_kernels.h"
+
+namespace dsa {
+namespace sparse {
+
+constexpr int BK = 128;         // keys per tile (the MMA's M)
+constexpr int KMAX = 2048;      // longest index row the kernel compacts
+constexpr int NTHREADS = 320;   // 10 warps
+constexpr int LAG = 4;          // cp.async groups a producer thread keeps in flight before signalling
+constexpr float kTau = 8.0f;    // lazy-rescale threshold (log2 units)
+
+template <int H, int NC>
+struct Cfg {
+  static constexpr bool ROPE = (NC == 9);                       // 576 = 512 + 64
+  static constexpr int NU = ROPE ? 4 : 5;                       // unit ring depth
+  static constexpr uint32_t UNIT_BYTES = 2u * BK * 128u;        // 2 x (128 keys x 64 cols)
+  static constexpr uint32_t ROPE_BYTES = BK * 128u;
+  static constexpr uint32_t Q_BYTES = NC * H * 128u;
+  static constexpr uint32_t P_BYTES = 2u * H * 128u;            // 128 keys = 2 swizzle columns
+  static constexpr uint32_t OFF_UNITS = 0;
+  static constexpr uint32_t OFF_ROPE = OFF_UNITS + NU * UNIT_BYTES;
+  static constexpr uint32_t OFF_Q = OFF_ROPE + (ROPE ? 2u * ROPE_BYTES : 0u);
+  static constexpr uint32_t OFF_P = OFF_Q + Q_BYTES;
+  static constexpr uint32_t OFF_KIDX = OFF_P + P_BYTES;
+  static constexpr uint32_t OFF_RED = OFF_KIDX + 2u * KMAX * 4u;
+  static constexpr uint32_t OFF_BAR = OFF_RED + 2u * 4u * H * 4u;
+  static constexpr int NBAR = 34;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8u;
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64u + 1024u;  // + alignment slack
+  // TMEM columns: O^T double buffer (2 x 4H) + S^T double buffer (2 x H)
+  static constexpr uint32_t TMEM_COLS = (10 * H <= 256) ? 256u : 512u;
+  static constexpr uint32_t COL_O = 0;
+  static constexpr uint32_t COL_S = 8u * H;
+};
+
+// barrier slots
+enum {
+  B_IDX_FULL = 0,    // [2]
+  B_IDX_EMPTY = 2,   // [2]
+  B_Q_FULL = 4,
+  B_Q_EMPTY = 5,
+  B_ROPE_FULL = 6,   // [2]
+  B_ROPE_EMPTY = 8,  // [2]
+  B_S_FULL = 10,     // [2]
+  B_S_EMPTY = 12,    // [2]
+  B_P_FULL = 14,
+  B_P_EMPTY = 15,
+  B_O_FULL = 16,     // [2]
+  B_O_EMPTY = 18,    // [2]
+  B_DRAIN = 20,
+  B_UNIT_FULL = 21,  // [NU <= 5]
+  B_UNIT_EMPTY = 26, // [NU <= 5]
+  B_SMX_SYNC = 31,   // softmax warpgroup barrier (128)
+  B_PROD_SYNC = 32,  // producer warpgroup barrier (128)
+};
+
+// Warp-level transposed max/sum reduction: every lane holds H values (one
+// per head); afterwards lane L holds the reduction over the 32 lanes of head
+// (L mod H).  Uses 31 shuffles for H = 32 instead of 5*H.
+template <int H, bool IS_MAX>
+__device__ __forceinline__ float warp_transpose_reduce(float* v) {
+  const uint32_t lane = lane_id();
+  auto op = [](float a, float b) { return IS_MAX ? fmaxf(a, b) : a + b; };
+  if constexpr (H == 16) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = op(v[i], __shfl_xor_sync(0xffffffffu, v[i], 16));
+  }
+  constexpr int START = (H == 32) ? 16 : 8;
+  int n = H;
+#pragma unroll
+  for (int o = START; o >= 1; o >>= 1) {
+    n >>= 1;  // values kept after this step
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i < n) {
+        const float send = upper ? v[i] : v[i + n];
+        const float keep = upper ? v[i + n] : v[i];
+        v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, o));
+      }
+    }
+  }
+  return v[0];
+}
+
+template <int H, int NC>
+__global__ void __launch_bounds__(NTHREADS, 1)
+sparse_prefill_kernel(SparseArgs a) {
+  using C = Cfg<H, NC>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
+  const uint32_t sbase = smem_u32(smem);
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile uint32_t* tmem_base_ptr = misc + 0;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+  volatile int* meta = reinterpret_cast<volatile int*>(misc + 2);  // [2] valid count per idx buffer
+  int32_t* kidx = reinterpret_cast<int32_t*>(smem + C::OFF_KIDX);
+  float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
+  unsigned int* err = a.err;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[B_IDX_FULL + 0], 1);
+    mbar_init(&bars[B_IDX_FULL + 1], 1);
+    mbar_init(&bars[B_IDX_EMPTY + 0], 3);
+    mbar_init(&bars[B_IDX_EMPTY + 1], 3);
+    mbar_init(&bars[B_Q_FULL], 128);
+    mbar_init(&bars[B_Q_EMPTY], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars[B_ROPE_FULL + i], 128);
+      mbar_init(&bars[B_ROPE_EMPTY + i], 1);
+      mbar_init(&bars[B_S_FULL + i], 1);
+      mbar_init(&bars[B_S_EMPTY + i], 128);
+      mbar_init(&bars[B_O_FULL + i], 1);
+      mbar_init(&bars[B_O_EMPTY + i], 128);
+    }
+    mbar_init(&bars[B_P_FULL], 128);
+    mbar_init(&bars[B_P_EMPTY], 1);
+    mbar_init(&bars[B_DRAIN], 1);
+    mbar_init(&bars[B_SMX_SYNC], 128);
+    mbar_init(&bars[B_PROD_SYNC], 128);
+    for (int i = 0; i < C::NU; ++i) {
+      mbar_init(&bars[B_UNIT_FULL + i], 128);
+      mbar_init(&bars[B_UNIT_EMPTY + i], 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 4) {
+    tmem_alloc(const_cast<uint32_t*>(tmem_base_ptr), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_base_ptr;
+
+  const int T = a.T;
+  const int stride_t = gridDim.x;
+
+  if (warp == 5) {
+    // ------------------------------------------------------------------
+    // index compaction
+    // ------------------------------------------------------------------
+    int lt = 0;
+    for (int t = blockIdx.x; t < T; t += stride_t, ++lt) {
+      const int buf = lt & 1;
+      if (!mbar_wait_warp(&bars[B_IDX_EMPTY + buf], ((lt >> 1) & 1) ^ 1, abort_flag, err)) break;
+      const int32_t* row = a.idx + (size_t)t * a.ld;
+      int32_t* dst = kidx + buf * KMAX;
+      int cnt = 0, bad = 0;
+      const bool vec = ((a.ld & 3) == 0) && ((reinterpret_cast<uintptr_t>(a.idx) & 15) == 0);
+      if (vec) {
+        for (int base = 0; base < a.k; base += 512) {
+          int4 v[4];
+#pragma unroll
+          for (int qd = 0; qd < 4; ++qd) {
+            const int e0 = base + qd * 128 + lane * 4;
+            if (e0 + 3 < a.k) {
+              v[qd] = __ldg(reinterpret_cast<const int4*>(row + e0));
+            } else {
+              v[qd].x = (e0 + 0 < a.k) ? __ldg(row + e0 + 0) : -1;
+              v[qd].y = (e0 + 1 < a.k) ? __ldg(row + e0 + 1) : -1;
+              v[qd].z = (e0 + 2 < a.k) ? __ldg(row + e0 + 2) : -1;
+              v[qd].w = (e0 + 3 < a.k) ? __ldg(row + e0 + 3) : -1;
+            }
+          }
+#pragma unroll
+          for (int qd = 0; qd < 4; ++qd) {
+            const int vals[4] = {v[qd].x, v[qd].y, v[qd].z, v[qd].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int x = vals[e];
+              const bool ok = (x >= 0) && (x < a.N);
+              bad += (x < -1 || x >= a.N) ? 1 : 0;
+              const uint32_t m = __ballot_sync(0xffffffffu, ok);
+              if (ok) dst[cnt + __popc(m & ((1u << lane) - 1u))] = x;
+              cnt += __popc(m);
+            }
+          }
+        }
+      } else {
+        for (int base = 0; base < a.k; base += 32) {
+          const int e = base + lane;
+          const int x = (e < a.k) ? __ldg(row + e) : -1;
+          const bool ok = (x >= 0) && (x < a.N);
+          bad += (x < -1 || x >= a.N) ? 1 : 0;
+          const uint32_t m = __ballot_sync(0xffffffffu, ok);
+          if (ok) dst[cnt + __popc(m & ((1u << lane) - 1u))] = x;
+          cnt += __popc(m);
+        }
+      }
+      bad = __reduce_add_sync(0xffffffffu, bad);
+      if (lane == 0) {
+        if (bad) atomicAdd(err + ERR_BAD_INDEX, (unsigned)bad);
+        meta[buf] = cnt;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[B_IDX_FULL + buf]);
+    }
+  } else if (warp >= 6) {
+    // ------------------------------------------------------------------
+    // gather producers
+    // ------------------------------------------------------------------
+    const int ptid = threadIdx.x - 192;  // 0..127
+    const int p8 = ptid & 7;
+    const int rsub = ptid >> 3;          // 0..15
+    uint64_t* pend[LAG + 2];
+    int npend = 0;
+    auto flush = [&]() {
+      cp_async_wait_all();
+      fence_proxy_async_smem();
+      for (int i = 0; i < npend; ++i) mbar_arrive(pend[i]);
+      npend = 0;
+    };
+    auto push = [&](uint64_t* bar) {
+      cp_async_commit();
+      pend[npend++] = bar;
+      if (npend > LAG) {
+        cp_async_wait<LAG>();
+        fence_proxy_async_smem();
+        mbar_arrive(pend[0]);
+        for (int i = 1; i < npend; ++i) pend[i - 1] = pend[i];
+        --npend;
+      }
+    };
+    auto wait_free = [&](uint64_t* bar, uint32_t parity) -> bool {
+      if (mbar_ready(bar, parity)) return true;
+      flush();
+      return mbar_wait(bar, parity, abort_flag, err);
+    };
+    const uint32_t q_s = sbase + C::OFF_Q;
+    int lt = 0, lt_nz = 0;
+    uint32_t gt = 0;
+    uint32_t sync_phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < T && ok; t += stride_t, ++lt) {
+      const int buf = lt & 1;
+      if (!wait_free(&bars[B_IDX_FULL + buf], (lt >> 1) & 1)) { ok = false; break; }
+      const int nvalid = meta[buf];
+      const int ntiles = (nvalid + BK - 1) / BK;
+      const int32_t* kl = kidx + buf * KMAX;
+      if (ntiles > 0) {
+        // q[t] -> K-major swizzled [chunk][H rows][64 cols]
+        if (!wait_free(&bars[B_Q_EMPTY], (lt_nz & 1) ^ 1)) { ok = false; break; }
+        const uint16_t* qt = a.q + (size_t)t * H * (NC * 64);
+        for (int i = ptid; i < H * NC * 8; i += 128) {
+          const int pp = i & 7;
+          const int c = (i >> 3) % NC;
+          const int h = (i >> 3) / NC;
+          const uint32_t dst = q_s + c * (H * 128) + h * 128 + ((pp ^ (h & 7)) << 4);
+          cp_async16(dst, qt + h * (NC * 64) + c * 64 + pp * 8, 16);
+        }
+        push(&bars[B_Q_FULL]);
+        for (int j = 0; j < ntiles && ok; ++j, ++gt) {
+          if constexpr (C::ROPE) {
+            const int rs = gt & 1;
+            if (!wait_free(&bars[B_ROPE_EMPTY + rs], ((gt >> 1) & 1) ^ 1)) { ok = false; break; }
+            const uint32_t base = sbase + C::OFF_ROPE + rs * C::ROPE_BYTES;
+#pragma unroll
+            for (int pass = 0; pass < 8; ++pass) {
+              const int row = pass * 16 + rsub;
+              const int key = j * BK + row;
+              const bool valid = key < nvalid;
+              const int kr = valid ? kl[key] : 0;
+              const uint16_t* src = a.kv + (size_t)kr * a.ld_kv + 8 * 64 + p8 * 8;
+              cp_async16(base + row * 128 + ((p8 ^ (row & 7)) << 4), src, valid ? 16u : 0u);
+            }
+            push(&bars[B_ROPE_FULL + rs]);
+          }
+          for (int m = 0; m < 4; ++m) {
+            const uint32_t useq = gt * 4 + m;
+            const int u = useq % C::NU;
+            if (!wait_free(&bars[B_UNIT_EMPTY + u], ((useq / C::NU) & 1) ^ 1)) { ok = false; break; }
+            const uint32_t base = sbase + C::OFF_UNITS + u * C::UNIT_BYTES;
+#pragma unroll
+            for (int pass = 0; pass < 16; ++pass) {
+              const int row = (pass & 7) * 16 + rsub;
+              const int cc = pass >> 3;
+              const int key = j * BK + row;
+              const bool valid = key < nvalid;
+              const int kr = valid ? kl[key] : 0;
+              const uint16_t* src = a.kv + (size_t)kr * a.ld_kv + (2 * m + cc) * 64 + p8 * 8;
+              cp_async16(base + cc * (BK * 128) + row * 128 + ((p8 ^ (row & 7)) << 4), src, valid ? 16u : 0u);
+            }
+            push(&bars[B_UNIT_FULL + u]);
+          }
+        }
+        ++lt_nz;
+      }
+      if (!ok) break;
+      // every producer thread has read this token's index list
+      if (!group_sync(&bars[B_PROD_SYNC], sync_phase, abort_flag, err)) { ok = false; break; }
+      if (ptid == 0) mbar_arrive(&bars[B_IDX_EMPTY + buf]);
+    }
+    flush();
+  } else if (warp == 4) {
+    // ------------------------------------------------------------------
+    // tcgen05 issuer (one thread)
+    // ------------------------------------------------------------------
+    if (lane == 0) {
+      constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, H, false, false);
+      constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, H, true, false);
+      const uint32_t q_s = sbase + C::OFF_Q;
+      const uint32_t p_s = sbase + C::OFF_P;
+      int lt = 0, lt_nz = 0;
+      uint32_t gt = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < T && ok; t += stride_t, ++lt) {
+        const int buf = lt & 1;
+        if (!mbar_wait(&bars[B_IDX_FULL + buf], (lt >> 1) & 1, abort_flag, err)) { ok = false; break; }
+        const int nvalid = meta[buf];
+        mbar_arrive(&bars[B_IDX_EMPTY + buf]);
+        const int ntiles = (nvalid + BK - 1) / BK;
+        if (ntiles == 0) continue;
+        const int ob = lt_nz & 1;
+        if (!mbar_wait(&bars[B_Q_FULL], lt_nz & 1, abort_flag, err)) { ok = false; break; }
+        tc_fence_after();
+        for (int j = 0; j < ntiles && ok; ++j, ++gt) {
+          const int sb = gt & 1;
+          const uint32_t d_s = tmem + C::COL_S + sb * H;
+          if (!mbar_wait(&bars[B_S_EMPTY + sb], ((gt >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+          tc_fence_after();
+          uint32_t acc = 0;
+          if constexpr (C::ROPE) {
+            const int rs = gt & 1;
+            if (!mbar_wait(&bars[B_ROPE_FULL + rs], (gt >> 1) & 1, abort_flag, err)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t abase = sbase + C::OFF_ROPE + rs * C::ROPE_BYTES;
+            const uint32_t bbase = q_s + 8 * (H * 128);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              mma_bf16_ss(d_s, sdesc_sw128(abase + ks * 32, 16, 1024), sdesc_sw128(bbase + ks * 32, 16, 1024),
+                          IDESC_QK, acc);
+              acc = 1;
+            }
+          }
+          for (int m = 0; m < 4 && ok; ++m) {
+            const uint32_t useq = gt * 4 + m;
+            const int u = useq % C::NU;
+            if (!mbar_wait(&bars[B_UNIT_FULL + u], (useq / C::NU) & 1, abort_flag, err)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t ubase = sbase + C::OFF_UNITS + u * C::UNIT_BYTES;
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+              const uint32_t abase = ubase + cc * (BK * 128);
+              const uint32_t bbase = q_s + (2 * m + cc) * (H * 128);
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks) {
+                mma_bf16_ss(d_s, sdesc_sw128(abase + ks * 32, 16, 1024), sdesc_sw128(bbase + ks * 32, 16, 1024),
+                            IDESC_QK, acc);
+                acc = 1;
+              }
+            }
+          }
+          if (!ok) break;
+          mma_commit(&bars[B_S_FULL + sb]);
+          if constexpr (C::ROPE) mma_commit(&bars[B_ROPE_EMPTY + (gt & 1)]);
+          if (j == ntiles - 1) mma_commit(&bars[B_Q_EMPTY]);
+          // P^T from the softmax warps, then O^T += V^T P^T
+          if (!mbar_wait(&bars[B_P_FULL], gt & 1, abort_flag, err)) { ok = false; break; }
+          tc_fence_after();
+          if (j == 0) {
+            if (!mbar_wait(&bars[B_O_EMPTY + ob], ((lt_nz >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+            tc_fence_after();
+          }
+          for (int m = 0; m < 4; ++m) {
+            const uint32_t useq = gt * 4 + m;
+            const int u = useq % C::NU;
+            const uint32_t ubase = sbase + C::OFF_UNITS + u * C::UNIT_BYTES;
+            const uint32_t d_o = tmem + C::COL_O + ob * (4 * H) + m * H;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t adesc = sdesc_sw128(ubase + kk * 2048, BK * 128, 1024);
+              const uint64_t bdesc = sdesc_sw128(p_s + (kk >> 2) * (H * 128) + (kk & 3) * 32, 16, 1024);
+              mma_bf16_ss(d_o, adesc, bdesc, IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(&bars[B_UNIT_EMPTY + u]);
+          }
+          mma_commit(&bars[B_P_EMPTY]);
+          if (j == ntiles - 1) mma_commit(&bars[B_O_FULL + ob]);
+        }
+        ++lt_nz;
+      }
+      // wait until every MMA issued above has completed
+      mma_commit(&bars[B_DRAIN]);
+      mbar_wait(&bars[B_DRAIN], 0, abort_flag, err);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------
+    // softmax + epilogue (warps 0-3, thread i <-> TMEM lane i)
+    // ------------------------------------------------------------------
+    const int tid = threadIdx.x;  // 0..127
+    const float scale_log2 = a.scale * 1.4426950408889634f;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    uint8_t* p_tile = smem + C::OFF_P;
+    int lt = 0, lt_nz = 0;
+    uint32_t gt = 0;
+    uint32_t sync_phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < T && ok; t += stride_t, ++lt) {
+      const int buf = lt & 1;
+      if (!mbar_wait_warp(&bars[B_IDX_FULL + buf], (lt >> 1) & 1, abort_flag, err)) { ok = false; break; }
+      const int nvalid = meta[buf];
+      if (!group_sync(&bars[B_SMX_SYNC], sync_phase, abort_flag, err)) { ok = false; break; }
+      if (tid == 0) mbar_arrive(&bars[B_IDX_EMPTY + buf]);
+      const int ntiles = (nvalid + BK - 1) / BK;
+      uint16_t* out_t = a.out + (size_t)t * H * 512;
+      if (ntiles == 0) {
+        for (int i = tid; i < H * 512; i += 128) out_t[i] = 0;
+        if (tid < H) a.lse[(size_t)t * H + tid] = -INFINITY;
+        continue;
+      }
+      const int ob = lt_nz & 1;
+      float m_run[H], l_part[H];
+#pragma unroll
+      for (int h = 0; h < H; ++h) { m_run[h] = -INFINITY; l_part[h] = 0.f; }
+      for (int j = 0; j < ntiles; ++j, ++gt) {
+        const int sb = gt & 1;
+        if (!mbar_wait_warp(&bars[B_S_FULL + sb], (gt >> 1) & 1, abort_flag, err)) { ok = false; break; }
+        tc_fence_after();
+        float s[H];
+        tmem_ld_cols<H>(tmem + lane_off + C::COL_S + sb * H, s);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&bars[B_S_EMPTY + sb]);
+        const bool valid = (j * BK + tid) < nvalid;
+        float r[H];
+#pragma unroll
+        for (int h = 0; h < H; ++h) {
+          s[h] = valid ? s[h] * scale_log2 : -INFINITY;
+          r[h] = s[h];
+        }
+        const float wmax = warp_transpose_reduce<H, true>(r);
+        float* redb = red + (gt & 1) * (4 * H);
+        if (lane < H) redb[warp * H + lane] = wmax;
+        if (!group_sync(&bars[B_SMX_SYNC], sync_phase, abort_flag, err)) { ok = false; break; }
+        float tmax[H];
+#pragma unroll
+        for (int h = 0; h < H; h += 4) {
+          float4 x0 = *reinterpret_cast<const float4*>(redb + 0 * H + h);
+          float4 x1 = *reinterpret_cast<const float4*>(redb + 1 * H + h);
+          float4 x2 = *reinterpret_cast<const float4*>(redb + 2 * H + h);
+          float4 x3 = *reinterpret_cast<const float4*>(redb + 3 * H + h);
+          tmax[h + 0] = fmaxf(fmaxf(x0.x, x1.x), fmaxf(x2.x, x3.x));
+          tmax[h + 1] = fmaxf(fmaxf(x0.y, x1.y), fmaxf(x2.y, x3.y));
+          tmax[h + 2] = fmaxf(fmaxf(x0.z, x1.z), fmaxf(x2.z, x3.z));
+          tmax[h + 3] = fmaxf(fmaxf(x0.w, x1.w), fmaxf(x2.w, x3.w));
+        }
+        bool need = false;
+#pragma unroll
+        for (int h = 0; h < H; ++h) need |= (tmax[h] > m_run[h] + kTau);
+        // the previous PV must be done before P is overwritten or O rescaled
+        if (!mbar_wait_warp(&bars[B_P_EMPTY], (gt & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+        tc_fence_after();
+        if (need) {
+          float alpha[H];
+#pragma unroll
+          for (int h = 0; h < H; ++h) {
+            const float mn = fmaxf(m_run[h], tmax[h]);
+            alpha[h] = (m_run[h] == -INFINITY) ? 0.f : exp2f(m_run[h] - mn);
+            m_run[h] = mn;
+            l_part[h] *= alpha[h];
+          }
+          if (j > 0) {
+#pragma unroll 1
+            for (int m = 0; m < 4; ++m) {
+              float o[H];
+              const uint32_t ta = tmem + lane_off + C::COL_O + ob * (4 * H) + m * H;
+              tmem_ld_cols<H>(ta, o);
+              tmem_ld_wait();
+#pragma unroll
+              for (int h = 0; h < H; ++h) o[h] *= alpha[h];
+              tmem_st_cols<H>(ta, o);
+            }
+            tmem_st_wait();
+          }
+        }
+        // P^T[h][key] (K-major swizzled, 2 columns of 64 keys)
+        {
+          const uint32_t kcol = tid & 63;
+          uint8_t* pcol = p_tile + (tid >> 6) * (H * 128);
+#pragma unroll
+          for (int h = 0; h < H; ++h) {
+            const float mref = (m_run[h] == -INFINITY) ? 0.f : m_run[h];
+            const float p = exp2f(s[h] - mref);
+            const uint16_t pb = f32_to_bf16_rn(p);
+            l_part[h] += bf16_to_f32(pb);
+            *reinterpret_cast<uint16_t*>(pcol + sw128_offset(h, kcol)) = pb;
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&bars[B_P_FULL]);
+      }
+      if (!ok) break;
+      // -------- epilogue --------
+      float lsum[H];
+#pragma unroll
+      for (int h = 0; h < H; ++h) lsum[h] = l_part[h];
+      const float wsum = warp_transpose_reduce<H, false>(lsum);
+      float* redb = red + (gt & 1) * (4 * H);  // not in use by the tile path now
+      if (!group_sync(&bars[B_SMX_SYNC], sync_phase, abort_flag, err)) { ok = false; break; }
+      if (lane < H) redb[warp * H + lane] = wsum;
+      if (!group_sync(&bars[B_SMX_SYNC], sync_phase, abort_flag, err)) { ok = false; break; }
+      float inv_l[H];
+#pragma unroll
+      for (int h = 0; h < H; ++h) {
+        const float l = redb[0 * H + h] + redb[1 * H + h] + redb[2 * H + h] + redb[3 * H + h];
+        inv_l[h] = (l > 0.f) ? 1.0f / l : 0.f;
+        if (tid == h) a.lse[(size_t)t * H + h] = (l > 0.f) ? (m_run[h] + log2f(l)) * 0.6931471805599453f : -INFINITY;
+      }
+      if (!group_sync(&bars[B_SMX_SYNC], sync_phase, abort_flag, err)) { ok = false; break; }
+      if (!mbar_wait_warp(&bars[B_O_FULL + ob], (lt_nz >> 1) & 1, abort_flag, err)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll 1
+      for (int m = 0; m < 4; ++m) {
+        float o[H];
+        tmem_ld_cols<H>(tmem + lane_off + C::COL_O + ob * (4 * H) + m * H, o);
+        tmem_ld_wait();
+#pragma unroll
+        for (int h = 0; h < H; ++h) out_t[h * 512 + m * 128 + tid] = f32_to_bf16_rn(o[h] * inv_l[h]);
+      }
+      tc_fence_before();
+      mbar_arrive(&bars[B_O_EMPTY + ob]);
+      ++lt_nz;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 4) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+template <int H, int NC>
+static int launch_t(const SparseArgs& a, int num_sms, cudaStream_t stream) {
+  using C = Cfg<H, NC>;
+  static int attr_set[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(sparse_prefill_kernel<H, NC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM_BYTES) != cudaSuccess)
+      return -1;
+    attr_set[dev] = 1;
+  }
+  const int grid = a.T < num_sms ? a.T : num_sms;
+  sparse_prefill_kernel<H, NC><<<grid, NTHREADS, C::SMEM_BYTES, stream>>>(a);
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace sparse
+
+int launch_sparse_prefill(const SparseArgs& a, int num_sms, cudaStream_t stream) {
+  const int nc = a.d_qk / 64;
+  if (a.H == 16 && nc == 9) return sparse::launch_t<16, 9>(a, num_sms, stream);
+  if (a.H == 32 && nc == 9) return sparse::launch_t<32, 9>(a, num_sms, stream);
+  if (a.H == 16 && nc == 8) return sparse::launch_t<16, 8>(a, num_sms, stream);
+  if (a.H == 32 && nc == 8) return sparse::launch_t<32, 8>(a, num_sms, stream);
+  return -2;
+}
+
+}  // namespace dsa

@@ -1,0 +1,160 @@
+// Union list + head-group membership mask builder for the grouped form.
+//
+// "[Perf][DSA] Grouped sparse prefill with the FlashMLA head-group-mask
+// kernel", How: for every group of G consecutive tokens of a request, a
+// bitmap over the KV positions is filled from the tokens' top-k rows, a
+// prefix sum over the bitmap's popcounts compacts the set bits into a sorted
+// union list, and every token gets one membership bit per union slot.  The
+// review snippet on that page sizes the buffers: union_pad = ceil(G*k / UB) * UB
+// slots per group and ceil(N / 32) bitmap words.
+//
+// One CTA per group, everything in shared memory:
+//   bitmap[W] (W = ceil(N/32) uint32)  -> prefix[W] (exclusive popcount scan)
+//   -> union[g, pos] = set-bit positions in ascending order
+//   -> mask[g, pos] |= 1 << j for token j's rows  (bytes packed 4 per word)
+// Slots past the union length hold -1 in the list and 0 in the mask.
+#include "dsa_device.cuh"
+#include "dsa_kernels.h"
+
+namespace dsa {
+namespace unionb {
+
+constexpr int NT = 512;
+
+__device__ __forceinline__ void group_of(const ReqTable& rq, int G, int g, int& t0, int& n) {
+  int r = 0;
+  while (r + 1 < rq.num_req && rq.cu_g[r + 1] <= g) ++r;
+  t0 = rq.cu_q[r] + (g - rq.cu_g[r]) * G;
+  const int end = rq.cu_q[r + 1];
+  n = min(G, end - t0);
+}
+
+// Block-wide exclusive scan of one value per thread; returns the exclusive
+// prefix and writes the block total.
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* warp_tot, uint32_t& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_tot[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t w = (lane < NT / 32) ? warp_tot[lane] : 0u;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < NT / 32) warp_tot[lane] = w;  // inclusive warp totals
+  }
+  __syncthreads();
+  const uint32_t before = (warp > 0) ? warp_tot[warp - 1] : 0u;
+  total = warp_tot[NT / 32 - 1];
+  return before + x - v;
+}
+
+__global__ void __launch_bounds__(NT) union_build_kernel(UnionArgs a) {
+  extern __shared__ __align__(16) uint32_t sm[];
+  const int W = (a.N + 31) >> 5;
+  const int Wp = (W + 3) & ~3;
+  uint32_t* bitmap = sm;                 // [W]
+  uint32_t* prefix = sm + Wp;            // [W]
+  uint32_t* maskw = sm + 2 * Wp;         // [union_pad / 4], 16-byte aligned
+  __shared__ uint32_t warp_tot[NT / 32];
+  __shared__ uint32_t s_total;
+
+  const int g = blockIdx.x;
+  int t0, n;
+  group_of(a.req, a.G, g, t0, n);
+
+  for (int i = threadIdx.x; i < W; i += NT) bitmap[i] = 0u;
+  for (int i = threadIdx.x; i < a.union_pad / 4; i += NT) maskw[i] = 0u;
+  __syncthreads();
+
+  // 1) bitmap of every valid row of the group's tokens
+  int bad = 0;
+  for (int j = 0; j < n; ++j) {
+    const int32_t* row = a.idx + (size_t)(t0 + j) * a.ld;
+    for (int e = threadIdx.x; e < a.k; e += NT) {
+      const int x = __ldg(row + e);
+      if (x >= 0 && x < a.N) {
+        atomicOr(&bitmap[x >> 5], 1u << (x & 31));
+      } else if (x != -1) {
+        ++bad;
+      }
+    }
+  }
+  bad = __reduce_add_sync(0xffffffffu, bad);
+  if ((threadIdx.x & 31) == 0 && bad) atomicAdd(a.err + ERR_BAD_INDEX, (unsigned)bad);
+  __syncthreads();
+
+  // 2) exclusive prefix of the popcounts; thread i scans a contiguous run of words
+  const int per = (W + NT - 1) / NT;
+  const int w0 = threadIdx.x * per;
+  uint32_t local = 0;
+  for (int w = w0; w < min(W, w0 + per); ++w) local += __popc(bitmap[w]);
+  uint32_t total;
+  uint32_t run = block_exclusive_scan(local, warp_tot, total);
+  for (int w = w0; w < min(W, w0 + per); ++w) {
+    prefix[w] = run;
+    run += __popc(bitmap[w]);
+  }
+  if (threadIdx.x == 0) s_total = total;
+  __syncthreads();
+  const uint32_t U = s_total;
+  const uint32_t Ucap = min(U, (uint32_t)a.union_pad);
+  if (threadIdx.x == 0 && U > (uint32_t)a.union_pad) atomicAdd(a.err + ERR_UNION_OVERFLOW, 1u);
+
+  // 3) compaction: ascending set-bit positions
+  int32_t* urow = a.union_idx + (size_t)g * a.union_pad;
+  for (int w = threadIdx.x; w < W; w += NT) {
+    uint32_t bits = bitmap[w];
+    uint32_t pos = prefix[w];
+    while (bits) {
+      const int b = __ffs(bits) - 1;
+      bits &= bits - 1;
+      if (pos < Ucap) urow[pos] = (w << 5) + b;
+      ++pos;
+    }
+  }
+  for (uint32_t u = Ucap + threadIdx.x; u < (uint32_t)a.union_pad; u += NT) urow[u] = -1;
+
+  // 4) membership bits: slot of row x = prefix[x>>5] + popc(bits below x)
+  for (int j = 0; j < n; ++j) {
+    const int32_t* row = a.idx + (size_t)(t0 + j) * a.ld;
+    for (int e = threadIdx.x; e < a.k; e += NT) {
+      const int x = __ldg(row + e);
+      if (x >= 0 && x < a.N) {
+        const uint32_t w = (uint32_t)x >> 5;
+        const uint32_t pos = prefix[w] + __popc(bitmap[w] & ((1u << (x & 31)) - 1u));
+        if (pos < Ucap) atomicOr(&maskw[pos >> 2], (1u << j) << ((pos & 3) * 8));
+      }
+    }
+  }
+  __syncthreads();
+
+  // 5) mask row out (16-byte stores; union_pad is a multiple of 16)
+  uint4* mrow = reinterpret_cast<uint4*>(a.mask + (size_t)g * a.union_pad);
+  const uint4* ms = reinterpret_cast<const uint4*>(maskw);
+  for (int i = threadIdx.x; i < a.union_pad / 16; i += NT) mrow[i] = ms[i];
+  if (threadIdx.x == 0) a.union_len[g] = (int32_t)Ucap;
+}
+
+}  // namespace unionb
+
+int launch_union_build(const UnionArgs& a, cudaStream_t stream) {
+  const int smem = union_build_smem_bytes(a.N, a.union_pad);
+  if (smem > 48 * 1024) {
+    if (cudaFuncSetAttribute(unionb::union_build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+      return -1;
+  }
+  if (a.num_groups == 0) return 0;
+  unionb::union_build_kernel<<<a.num_groups, unionb::NT, smem, stream>>>(a);
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace dsa

@@ -1,0 +1,194 @@
+/*
+ * dsa.h - C ABI of the GB300 (sm_103a) DeepSeek-Sparse-Attention prefill
+ * library (libdsa.so).
+ *
+ * The operation: DSA prefill over an MLA latent KV cache.  Every query token
+ * t with H heads attends only to its own top-k selected latent rows:
+ *
+ *     out[t,h,:] = softmax_j( scale * q[t,h,0:D_QK] . kv[idx_j, 0:D_QK] ) . kv[idx_j, 0:D_V]
+ *     lse[t,h]   = log sum_j exp( scale * q[t,h,:] . kv[idx_j, 0:D_QK] )      (natural log)
+ *
+ * with D_QK = 576 (512 NoPE + 64 RoPE) or 512 (NoPE layout) and D_V = 512,
+ * V being the first 512 columns of the same latent row ("[Perf][DSA] Grouped
+ * sparse prefill with the FlashMLA head-group-mask kernel", commit message
+ * and Why; "[Perf][GLM-5.3-Flash] Dense/masked-MHA sparse prefill for the
+ * NoPE (256, 0, 256) layout + skip the NoPE K concat", Purpose).  The
+ * library offers the three forms the pages describe: per-token sparse,
+ * grouped sparse (union list + head-group mask), and masked dense MHA.
+ *
+ * Conventions for every call
+ *  - Tensor pointers are DEVICE pointers to caller-owned, contiguous memory
+ *    laid out as stated; bf16 tensors are passed as uint16_t bit patterns.
+ *    Arrays documented as HOST are read during the call (their values are
+ *    copied into the launch) and may be freed when it returns.
+ *  - Nothing is allocated on any call.  Every compute call is asynchronous
+ *    on `stream` (NULL = the legacy default stream) and returns once the
+ *    kernel is queued.
+ *  - Return value: DSA_OK, or an error code; on an error nothing was
+ *    launched.  DSA_ERR_INVALID_ARG: a null pointer, a negative or
+ *    inconsistent size, a misaligned pointer or stride.  DSA_ERR_UNSUPPORTED:
+ *    a shape the kernels do not implement.  DSA_ERR_CUDA: the launch failed.
+ *  - Index entries equal to -1 mean "no selection" and may appear anywhere
+ *    in the first k columns of a row; columns k..ld-1 are ignored.  Any
+ *    other entry outside [0, N) is treated as absent and counted (see
+ *    dsa_last_device_error).  A token without any valid entry gets out = 0
+ *    and lse = -inf.  Duplicate valid entries in one row are not supported
+ *    (results unspecified).
+ *  - Causality is carried entirely by the indices (sparse forms) or by the
+ *    key mask (masked form); no positional mask is applied.
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* dsa_stream_t;
+
+enum dsa_status {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1,
+  DSA_ERR_UNSUPPORTED = 2,
+  DSA_ERR_CUDA = 3,
+  DSA_ERR_DEVICE = 4
+};
+
+/* Largest number of requests one call accepts (host offset arrays). */
+#define DSA_MAX_REQUESTS 512
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* dsa_status_string(int status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int dsa_version(void);
+
+/* ------------------------------------------------------------------------
+ * Host-side sizing helpers (no GPU work).
+ * ---------------------------------------------------------------------- */
+
+/* Per-group capacity of the union list: ceil(G*k / union_block) * union_block
+ * ("[Perf][DSA] Grouped sparse prefill ...", review snippet of the union
+ * builder's sizes).  Returns the value, or -1 for non-positive arguments. */
+int64_t dsa_union_pad(int G, int k, int union_block);
+
+/* Number of groups of G consecutive tokens of one request (a request's last
+ * group may be short).  cu_seqlens_q_host: HOST int32 [num_req + 1],
+ * ascending offsets starting at 0; NULL means one request of T tokens.
+ * Writes *num_groups.  Returns DSA_OK or DSA_ERR_INVALID_ARG. */
+int dsa_num_groups(const int32_t* cu_seqlens_q_host, int num_req, int T, int G, int* num_groups);
+
+/* ------------------------------------------------------------------------
+ * Union list + head-group membership mask ("[Perf][DSA] Grouped sparse
+ * prefill with the FlashMLA head-group-mask kernel", How: bitmap over KV
+ * positions -> prefix-sum compaction -> sorted union, plus per-token
+ * membership bits).
+ *
+ * idx          [T, ld] int32 global KV rows (first k columns used).
+ * G            tokens per group, 1..8 (one mask bit per token).
+ * cu_seqlens_q HOST int32 [num_req + 1] or NULL (one request of T tokens);
+ *              groups never straddle requests.
+ * N            KV rows: valid indices lie in [0, N).  The bitmap and the
+ *              mask staging live in shared memory, so 8*ceil(N/32) +
+ *              union_pad must not exceed 232448 bytes (N up to ~440k rows
+ *              at union_pad = 16384); larger shapes are DSA_ERR_UNSUPPORTED.
+ * union_idx    out [num_groups, union_pad] int32: slots 0..len-1 hold the
+ *              group's distinct valid rows in ascending order; the rest -1.
+ * union_len    out [num_groups] int32.
+ * mask         out [num_groups, union_pad] uint8: bit j of slot u is set iff
+ *              union_idx[g,u] is among token j's valid rows (token j = j-th
+ *              token of the group); 0 in the padding.
+ * union_pad    >= min(G*k, N) and a multiple of 16 (dsa_union_pad with a
+ *              block of 16 or more qualifies).  A union longer than
+ *              union_pad is truncated and counted as a device error.
+ * ---------------------------------------------------------------------- */
+int dsa_union_build(const int32_t* idx, int T, int k, int ld, int G, const int32_t* cu_seqlens_q_host,
+                    int num_req, int N, int32_t* union_idx, int32_t* union_len, uint8_t* mask, int union_pad,
+                    dsa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Per-token sparse MLA prefill ("[Perf][DSA] Grouped sparse prefill ...",
+ * commit message: each token gathers its own 2048 selected rows).
+ *
+ * q     [T, H, d_qk] bf16.        kv  [N, ld_kv] bf16, row n = latent row n.
+ * idx   [T, ld] int32 global rows, first k columns used; k <= 2048.
+ * out   [T, H, d_v] bf16 (out).   lse [T, H] fp32 (out, natural log).
+ * H in {16, 32}; d_qk in {576, 512}; d_v = 512; ld_kv >= d_qk and a
+ * multiple of 8; q, kv 16-byte aligned.
+ * ---------------------------------------------------------------------- */
+int dsa_sparse_prefill(const uint16_t* q, const uint16_t* kv, int N, int ld_kv, const int32_t* idx, int T,
+                       int H, int d_qk, int d_v, int k, int ld, float scale, uint16_t* out, float* lse,
+                       dsa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Grouped sparse prefill ("[Perf][DSA] Grouped sparse prefill ...", commit
+ * message and How): the G = 128 / H consecutive tokens of a group act as 128
+ * pseudo-heads p = j*H + h over the group's union list; the mask restricts
+ * pseudo-head p to the slots whose bit j is set, so the result equals the
+ * per-token form.  Pseudo-heads past a short group's tokens are dropped.
+ *
+ * q, kv, out, lse, d_qk, d_v, ld_kv as for dsa_sparse_prefill.
+ * union_idx, union_len, mask, union_pad, G, cu_seqlens_q, num_req exactly as
+ * produced by / passed to dsa_union_build.  H * G must equal 128 and
+ * G <= 8 (the gate on the same page, review snippet).
+ * ---------------------------------------------------------------------- */
+int dsa_grouped_prefill(const uint16_t* q, const uint16_t* kv, int N, int ld_kv, const int32_t* union_idx,
+                        const int32_t* union_len, const uint8_t* mask, int union_pad, int G,
+                        const int32_t* cu_seqlens_q_host, int num_req, int T, int H, int d_qk, int d_v,
+                        float scale, uint16_t* out, float* lse, dsa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Top-k -> packed key mask ("[2/N][Attention] Enable masked MHA for sparse
+ * MLA prefills", commit log: scatter of the top-k into a per-token mask that
+ * the kernel zeroes itself).
+ *
+ * idx           [T, ld] int32 global KV rows (first k columns used).
+ * cu_seqlens_q  HOST int32 [num_req + 1]; cu_seqlens_kv HOST int32
+ *               [num_req + 1] (KV row offsets).  NULL/NULL = one request.
+ * key_mask      out [T, words] uint32: bit (n & 31) of word (n >> 5) of row
+ *               t is set iff row cu_seqlens_kv[r] + n is among token t's
+ *               valid top-k (r = the token's request).  Every word is written.
+ * words         >= ceil(longest request's KV length / 32).
+ * Indices outside the token's own request are treated as absent and counted.
+ * ---------------------------------------------------------------------- */
+int dsa_topk_to_key_mask(const int32_t* idx, int T, int k, int ld, const int32_t* cu_seqlens_q_host,
+                         const int32_t* cu_seqlens_kv_host, int num_req, uint32_t* key_mask, int words,
+                         dsa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Masked dense MHA simulating DSA ("[2/N][Attention] Enable masked MHA for
+ * sparse MLA prefills", Purpose; "[Perf][GLM-5.3-Flash] ...", Purpose): per
+ * head, token t of request r attends to the keys n of its request whose mask
+ * bit is set, with per-head (decompressed) q/k/v.
+ *
+ * q   [T, H, d_qk] bf16; k [Nk, H, d_qk] bf16; v [Nk, H, d_v] bf16, where
+ *     Nk = cu_seqlens_kv[num_req].
+ * key_mask [T, words] uint32 as written by dsa_topk_to_key_mask.
+ * out [T, H, d_v] bf16 (out); lse [T, H] fp32 (out, natural log).
+ * (d_qk, d_v) = (192, 128) (the DeepSeek-V3.2 geometry on the allow-list).
+ * ---------------------------------------------------------------------- */
+int dsa_masked_mha_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint32_t* key_mask,
+                           int words, const int32_t* cu_seqlens_q_host, const int32_t* cu_seqlens_kv_host,
+                           int num_req, int T, int H, int d_qk, int d_v, float scale, uint16_t* out, float* lse,
+                           dsa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Device error counters of the current device.  Synchronizes `stream`, then
+ * copies and clears the counters: counts[0] = ignored out-of-range index
+ * entries, counts[1] = bounded waits that ran out (a kernel stopped early;
+ * its outputs are incomplete), counts[2] = truncated union lists, counts[3]
+ * reserved.  `counts` is a HOST array of 4.  Returns DSA_ERR_DEVICE if
+ * counts[1] or counts[2] is nonzero, DSA_ERR_CUDA if the stream reported an
+ * error, else DSA_OK.
+ * ---------------------------------------------------------------------- */
+int dsa_last_device_error(dsa_stream_t stream, uint32_t* counts);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H_ */

@@ -1,0 +1,112 @@
+"""The C-ABI library without a GPU: it loads, exports every function that
+include/dsa.h declares, and its host-side helpers and argument checks work
+(none of these calls reaches the GPU)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import dsa_sparse_mla_prefill_gb300 as dsa
+import oracle.dsa_oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from dsa_sparse_mla_prefill_gb300 import build as b
+    b.build()
+    return dsa.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "dsa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(dsa_[a-z0-9_]+)\s*\(",
+                                 src, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(dsa.EXPORTED)
+
+
+def test_status_strings(lib):
+    assert dsa.status_string(0) == "DSA_OK"
+    assert dsa.status_string(2) == "DSA_ERR_UNSUPPORTED"
+    assert dsa.status_string(99) == "DSA_ERR_UNKNOWN"
+    assert lib.dsa_version() >= 100
+
+
+@pytest.mark.parametrize("G,k,ub", [(8, 2048, 128), (4, 2048, 128), (2, 4, 4), (3, 100, 16), (1, 1, 128)])
+def test_union_pad_matches_oracle(lib, G, k, ub):
+    assert dsa.dsa_union_pad(G, k, ub) == O.union_pad(G, k, ub)
+
+
+@pytest.mark.parametrize("lens,G", [([16384], 8), ([8192, 8192], 8), ([5, 3, 17], 4), ([1, 1, 1], 8), ([0, 9], 2)])
+def test_num_groups_matches_oracle(lib, lens, G):
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    assert dsa.dsa_num_groups(cu, int(cu[-1]), G) == len(O.groups(cu, G))
+
+
+def _vp(x=0):
+    return ctypes.c_void_p(x)
+
+
+def test_argument_validation_without_gpu(lib):
+    # unsupported head count / dims are rejected before any CUDA call
+    assert lib.dsa_sparse_prefill(_vp(16), _vp(16), 10, 576, _vp(16), 4, 24, 576, 512, 8, 8, 1.0, _vp(16),
+                                  _vp(16), None) == dsa.DSA_ERR_UNSUPPORTED
+    assert lib.dsa_sparse_prefill(_vp(16), _vp(16), 10, 576, _vp(16), 4, 16, 448, 512, 8, 8, 1.0, _vp(16),
+                                  _vp(16), None) == dsa.DSA_ERR_UNSUPPORTED
+    # k beyond the supported top-k, ld < k, misaligned kv stride
+    assert lib.dsa_sparse_prefill(_vp(16), _vp(16), 10, 576, _vp(16), 4, 16, 576, 512, 4096, 4096, 1.0, _vp(16),
+                                  _vp(16), None) == dsa.DSA_ERR_UNSUPPORTED
+    assert lib.dsa_sparse_prefill(_vp(16), _vp(16), 10, 576, _vp(16), 4, 16, 576, 512, 8, 4, 1.0, _vp(16),
+                                  _vp(16), None) == dsa.DSA_ERR_INVALID_ARG
+    assert lib.dsa_sparse_prefill(_vp(16), _vp(16), 10, 580, _vp(16), 4, 16, 576, 512, 8, 8, 1.0, _vp(16),
+                                  _vp(16), None) == dsa.DSA_ERR_INVALID_ARG
+    # null pointers and misalignment
+    assert lib.dsa_sparse_prefill(None, _vp(16), 10, 576, _vp(16), 4, 16, 576, 512, 8, 8, 1.0, _vp(16),
+                                  _vp(16), None) == dsa.DSA_ERR_INVALID_ARG
+    assert lib.dsa_sparse_prefill(_vp(18), _vp(16), 10, 576, _vp(16), 4, 16, 576, 512, 8, 8, 1.0, _vp(16),
+                                  _vp(16), None) == dsa.DSA_ERR_INVALID_ARG
+    # empty problem is a no-op
+    assert lib.dsa_sparse_prefill(None, None, 0, 576, None, 0, 16, 576, 512, 8, 8, 1.0, None, None,
+                                  None) == dsa.DSA_OK
+    # grouped: G*H must be 128 and G <= 8
+    assert lib.dsa_grouped_prefill(_vp(16), _vp(16), 10, 576, _vp(16), _vp(16), _vp(16), 16, 4, None, 0, 8, 16,
+                                   576, 512, 1.0, _vp(16), _vp(16), None) == dsa.DSA_ERR_UNSUPPORTED
+    assert lib.dsa_grouped_prefill(_vp(16), _vp(16), 10, 576, _vp(16), _vp(16), _vp(16), 16, 16, None, 0, 8, 8,
+                                   576, 512, 1.0, _vp(16), _vp(16), None) == dsa.DSA_ERR_UNSUPPORTED
+    # union build: G > 8 unsupported, union_pad must be a multiple of 16 and >= min(G*k, N)
+    assert lib.dsa_union_build(_vp(16), 8, 4, 4, 9, None, 0, 100, _vp(16), _vp(16), _vp(16), 48,
+                               None) == dsa.DSA_ERR_UNSUPPORTED
+    assert lib.dsa_union_build(_vp(16), 8, 4, 4, 2, None, 0, 100, _vp(16), _vp(16), _vp(16), 8,
+                               None) == dsa.DSA_ERR_INVALID_ARG
+    assert lib.dsa_union_build(_vp(16), 8, 4, 4, 2, None, 0, 100, _vp(16), _vp(16), _vp(16), 20,
+                               None) == dsa.DSA_ERR_INVALID_ARG
+    # a bitmap that does not fit in shared memory
+    assert lib.dsa_union_build(_vp(16), 8, 4, 4, 2, None, 0, 1 << 20, _vp(16), _vp(16), _vp(16), 16,
+                               None) == dsa.DSA_ERR_UNSUPPORTED
+    # request offsets that do not add up to T
+    cu = (ctypes.c_int32 * 3)(0, 3, 7)
+    assert lib.dsa_union_build(_vp(16), 8, 4, 4, 2, cu, 2, 100, _vp(16), _vp(16), _vp(16), 16,
+                               None) == dsa.DSA_ERR_INVALID_ARG
+    # masked MHA geometry allow-list
+    assert lib.dsa_masked_mha_prefill(_vp(16), _vp(16), _vp(16), _vp(16), 4, None, None, 0, 8, 4, 576, 512, 1.0,
+                                      _vp(16), _vp(16), None) == dsa.DSA_ERR_UNSUPPORTED
+    # key mask: one-sided offsets are rejected
+    assert lib.dsa_topk_to_key_mask(_vp(16), 8, 4, 4, cu, None, 2, _vp(16), 4, None) == dsa.DSA_ERR_INVALID_ARG
+
+
+def test_python_binding_refuses_cpu_tensors(lib):
+    import torch
+    with pytest.raises(ValueError):
+        dsa.dsa_sparse_prefill(torch.zeros(2, 16, 576, dtype=torch.bfloat16), torch.zeros(4, 576, dtype=torch.bfloat16),
+                               torch.zeros(2, 8, dtype=torch.int32), 8, 1.0)

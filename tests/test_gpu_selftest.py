@@ -1,0 +1,46 @@
+"""tcgen05 building blocks (instruction/shared-memory descriptors, 128B
+swizzle, K-major and MN-major operands, TMEM 32x32b loads) on one
+128 x N x K product, against a plain PyTorch fp32 matmul."""
+import ctypes
+import os
+
+import numpy as np
+import pytest
+
+from gpu_util import need_gpu, torch
+
+pytestmark = pytest.mark.gpu
+
+CASES = [(0, 0, 16, 64), (0, 0, 32, 128), (0, 0, 32, 576), (0, 0, 64, 192), (0, 0, 128, 192), (0, 0, 256, 64),
+         (1, 0, 16, 128), (1, 0, 32, 128), (1, 0, 128, 64), (0, 1, 64, 64), (0, 1, 128, 128), (0, 1, 256, 64),
+         # a_mn = 2: A read from tensor memory (the P operand of P.V)
+         (2, 1, 128, 128), (2, 1, 64, 64), (2, 0, 128, 128), (2, 1, 128, 256)]
+
+
+@pytest.fixture(scope="module")
+def selftest():
+    need_gpu()
+    import dsa_sparse_mla_prefill_gb300 as dsa
+    lib = ctypes.CDLL(os.path.join(os.path.dirname(dsa.__file__), "libdsa_selftest.so"))
+    fn = lib.dsa_selftest_mma
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 4 + [ctypes.c_void_p, ctypes.c_void_p]
+    return fn
+
+
+@pytest.mark.parametrize("a_mn,b_mn,N,K", CASES)
+def test_mma_layouts(selftest, a_mn, b_mn, N, K):
+    g = torch.Generator().manual_seed(N * 1000 + K + 7 * a_mn + 13 * b_mn)
+    A = torch.randn(128, K, generator=g).to(torch.bfloat16)
+    B = torch.randn(N, K, generator=g).to(torch.bfloat16)
+    ref = A.float() @ B.float().T
+    Ad, Bd = A.cuda(), B.cuda()
+    D = torch.full((128, N), float("nan"), device="cuda")
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    rc = selftest(Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), N, K, a_mn, b_mn, status.data_ptr(),
+                  torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert int(status[1]) == 0, "bounded wait ran out"
+    err = (D.cpu() - ref).abs().max().item()
+    assert err < 1e-3 * (1 + ref.abs().max().item()), err
