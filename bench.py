@@ -44,6 +44,14 @@ FLUSH_BYTES = 256 << 20
 # ----------------------------------------------------------------------------
 # environment
 # ----------------------------------------------------------------------------
+_T0 = time.time()
+
+
+def log(msg):
+    """Progress to stderr (the JSON line is the only stdout output)."""
+    print(f"[bench {time.time() - _T0:7.1f}s] {msg}", file=sys.stderr, flush=True)
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -278,6 +286,7 @@ def run_modes(dev, stream, peaks, steps, warmup, flush):
 
     def sparse_block(name, grouped=True, per_token=True):
         w = WORKLOADS[name]
+        log(f"mode {name}")
         x = make_sparse_inputs(w)
         q, kv = to_dev(x.q, dev), to_dev(x.kv, dev)
         idx = torch.from_numpy(x.idx).to(dev)
@@ -329,6 +338,7 @@ def run_modes(dev, stream, peaks, steps, warmup, flush):
     torch.cuda.empty_cache()
     # masked dense MHA
     w = WORKLOADS["masked_2x8192"]
+    log("mode masked_2x8192")
     x = make_masked_inputs(w)
     words = (max(w.kv_lens) + 31) // 32
     words = (words + 3) // 4 * 4
@@ -383,8 +393,10 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         pool = oracle_pool(cores)
 
+    log(f"generating {w.name}")
     x = make_sparse_inputs(w)
     pairs, abytes, flops = sparse_work(w, x.idx)
+    log("inputs ready")
     q, kv = to_dev(x.q, dev), to_dev(x.kv, dev)
     idx = torch.from_numpy(x.idx).to(dev)
     out = torch.empty((w.T, w.H, w.d_v), dtype=torch.bfloat16, device=dev)
@@ -401,6 +413,7 @@ def run_ours(args):
     if st != 0:
         raise RuntimeError(f"device error counters after the first step: {counts}")
 
+    log("first step ok; timing")
     clocks = ClockSampler(local)
     clocks.start()
     for _ in range(args.warmup):
@@ -426,6 +439,7 @@ def run_ours(args):
     ms_step = max_over_ranks(sum(ms) / len(ms), dist, dev)
     value = job_throughput(w.T, world, ms_step)
 
+    log(f"timed: {ms_step:.3f} ms/step")
     # end-to-end through host buffers: H2D inputs, kernel, D2H outputs, every step
     hq = torch.from_numpy(np.ascontiguousarray(x.q).view(np.int16)).view(torch.bfloat16).pin_memory()
     hkv = torch.from_numpy(np.ascontiguousarray(x.kv).view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -447,6 +461,7 @@ def run_ours(args):
     d2h = hout.numel() * 2 + hlse.numel() * 4
     e2e_ms = max_over_ranks(e2e_ms, dist, dev)
 
+    log(f"e2e: {e2e_ms:.3f} ms/step")
     src_hash = kernel_source_hash(["sparse_prefill.cu", "dsa_device.cuh"])
     traffic = profiled_traffic("sparse_prefill_" + HEADLINE, src_hash, w.T)
     achieved = abytes / (ms_step / 1e3) / 1e9
@@ -475,6 +490,7 @@ def run_ours(args):
         except Exception as e:  # report, never hide the headline
             line["modes"] = {"error": repr(e)}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        log("cpu baseline")
         line["cpu_baseline"] = cpu_baseline(w, x, budget_s=args.cpu_budget, pool=pool, cores=cores)
         pool.close()
         pool.join()
@@ -519,6 +535,50 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_profile_case(args):
+    """A small, bounded case of one kernel for ncu captures: inputs larger than
+    the L2 but a few hundred MB at most; runs warmup + steps launches."""
+    import torch
+    import dsa_sparse_mla_prefill_gb300 as dsa
+    from synth import WORKLOADS, make_masked_inputs, make_sparse_inputs, scaled_down
+    dev = torch.device("cuda", 0)
+    n = args.profile_tokens
+    if args.profile in ("sparse", "union", "grouped"):
+        base = WORKLOADS["v32_h32_16k" if args.profile == "sparse" else "grouped_21k_of_32k"]
+        w = scaled_down(base, (n,), (base.N,), name=f"{base.name}_last{n}")
+        x = make_sparse_inputs(w)
+        q, kv = to_dev(x.q, dev), to_dev(x.kv, dev)
+        idx = torch.from_numpy(x.idx).to(dev)
+        if args.profile == "sparse":
+            fn = lambda: dsa.dsa_sparse_prefill(q, kv, idx, w.k, w.scale)
+        else:
+            upad = dsa.dsa_union_pad(w.G, w.k, 128)
+            u, ul, m = dsa.dsa_union_build(idx, w.k, w.G, w.N, cu_seqlens_q=x.cu_seqlens_q, union_pad=upad)
+            if args.profile == "union":
+                fn = lambda: dsa.dsa_union_build(idx, w.k, w.G, w.N, cu_seqlens_q=x.cu_seqlens_q, union_pad=upad,
+                                                 out=(u, ul, m))
+            else:
+                fn = lambda: dsa.dsa_grouped_prefill(q, kv, u, ul, m, w.G, w.scale, cu_seqlens_q=x.cu_seqlens_q)
+    elif args.profile == "masked":
+        base = WORKLOADS["masked_2x8192"]
+        w = scaled_down(base, (n,), (base.kv_lens[0],), name=f"masked_last{n}")
+        x = make_masked_inputs(w)
+        words = ((max(w.kv_lens) + 31) // 32 + 3) // 4 * 4
+        idx = torch.from_numpy(x.idx).to(dev)
+        km = dsa.dsa_topk_to_key_mask(idx, w.k, words, cu_seqlens_q=x.cu_seqlens_q, cu_seqlens_kv=x.cu_seqlens_kv)
+        q, k, v = to_dev(x.q, dev), to_dev(x.k, dev), to_dev(x.v, dev)
+        fn = lambda: dsa.dsa_masked_mha_prefill(q, k, v, km, w.scale, cu_seqlens_q=x.cu_seqlens_q,
+                                                cu_seqlens_kv=x.cu_seqlens_kv)
+    else:
+        raise ValueError(args.profile)
+    ms = timed_steps(fn, args.steps, args.warmup, torch.cuda.current_stream(dev))
+    st, counts = dsa.dsa_last_device_error()
+    print(json.dumps({"profile": args.profile, "workload": w.name, "T": w.T, "ms": statistics.median(ms),
+                      "device_errors": counts}), flush=True)
+    if st != 0:
+        raise SystemExit(1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -528,10 +588,15 @@ def main():
     ap.add_argument("--no-modes", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work per core")
+    ap.add_argument("--profile", choices=["sparse", "union", "grouped", "masked"], default=None,
+                    help="run a small case of one kernel (for ncu) instead of the benchmark")
+    ap.add_argument("--profile-tokens", type=int, default=2048)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.profile:
+        run_profile_case(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

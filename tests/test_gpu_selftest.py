@@ -14,7 +14,7 @@ pytestmark = pytest.mark.gpu
 CASES = [(0, 0, 16, 64), (0, 0, 32, 128), (0, 0, 32, 576), (0, 0, 64, 192), (0, 0, 128, 192), (0, 0, 256, 64),
          (1, 0, 16, 128), (1, 0, 32, 128), (1, 0, 128, 64), (0, 1, 64, 64), (0, 1, 128, 128), (0, 1, 256, 64),
          # a_mn = 2: A read from tensor memory (the P operand of P.V)
-         (2, 1, 128, 128), (2, 1, 64, 64), (2, 0, 128, 128), (2, 1, 128, 256)]
+         (2, 1, 128, 128), (2, 1, 64, 64), (2, 0, 128, 128), (2, 0, 128, 256)]
 
 
 @pytest.fixture(scope="module")
