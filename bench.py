@@ -535,6 +535,36 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def traced_launch(fn, cap, out_path=None):
+    """One launch with the diagnostic timeline on (CTAs 0 and 1, first `cap`
+    tiles, 8 clock64 stamps per tile).  Returns per-event medians in cycles
+    relative to event 2 of the same tile, and the median tile period."""
+    import torch
+    import dsa_sparse_mla_prefill_gb300 as dsa
+    buf = torch.zeros(2 * cap * 8, dtype=torch.int64, device="cuda")
+    dsa.dsa_debug_trace(buf, cap)
+    try:
+        fn()
+        torch.cuda.synchronize()
+    finally:
+        dsa.dsa_debug_trace()
+    arr = buf.cpu().numpy().reshape(2, cap, 8).astype(np.int64)
+    if out_path:
+        np.save(out_path, arr)
+    out = {}
+    for c in range(2):
+        a = arr[c]
+        ok = np.all(a[:, 1:] > 0, axis=1) if a.shape[0] else np.zeros(0, bool)
+        a = a[ok]
+        if len(a) < 3:
+            out[f"cta{c}"] = {"tiles": int(len(a))}
+            continue
+        rel = {f"ev{e}-ev2": float(np.median(a[:, e] - a[:, 2])) for e in range(8)}
+        per = float(np.median(np.diff(a[:, 2])))
+        out[f"cta{c}"] = {"tiles": int(len(a)), "period_cycles": per, **rel}
+    return out
+
+
 def run_profile_case(args):
     """A small, bounded case of one kernel for ncu captures: inputs larger than
     the L2 but a few hundred MB at most; runs warmup + steps launches."""
@@ -573,8 +603,10 @@ def run_profile_case(args):
         raise ValueError(args.profile)
     ms = timed_steps(fn, args.steps, args.warmup, torch.cuda.current_stream(dev))
     st, counts = dsa.dsa_last_device_error()
-    print(json.dumps({"profile": args.profile, "workload": w.name, "T": w.T, "ms": statistics.median(ms),
-                      "device_errors": counts}), flush=True)
+    res = {"profile": args.profile, "workload": w.name, "T": w.T, "ms": statistics.median(ms), "device_errors": counts}
+    if args.trace > 0:
+        res["trace"] = traced_launch(fn, args.trace, args.trace_out)
+    print(json.dumps(res), flush=True)
     if st != 0:
         raise SystemExit(1)
 
@@ -591,6 +623,8 @@ def main():
     ap.add_argument("--profile", choices=["sparse", "union", "grouped", "masked"], default=None,
                     help="run a small case of one kernel (for ncu) instead of the benchmark")
     ap.add_argument("--profile-tokens", type=int, default=2048)
+    ap.add_argument("--trace", type=int, default=0, help="profile mode: record a per-tile timeline of N tiles")
+    ap.add_argument("--trace-out", default=None, help="profile mode: save the raw timeline (.npy)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -54,6 +54,7 @@ _SIGNATURES = {
     "dsa_masked_mha_prefill": (_I, [_VP, _VP, _VP, _VP, _I, _I32P, _I32P, _I, _I, _I, _I, _I, _F, _VP, _VP,
                                     _VP]),
     "dsa_last_device_error": (_I, [_VP, ctypes.POINTER(ctypes.c_uint32)]),
+    "dsa_debug_trace": (_I, [_VP, _I]),
 }
 
 EXPORTED = tuple(_SIGNATURES)
@@ -251,3 +252,15 @@ def dsa_last_device_error(stream=None, device=None):
     counts = (ctypes.c_uint32 * 4)()
     st = lib().dsa_last_device_error(_stream(stream, dev), counts)
     return st, [int(c) for c in counts]
+
+
+def dsa_debug_trace(buffer=None, capacity: int = 0):
+    """Diagnostic timeline: record per-tile clock64 stamps of CTAs 0 and 1 into
+    ``buffer`` (an int64 CUDA tensor of >= 2 * capacity * 8 elements); call with
+    no buffer to switch recording off."""
+    if buffer is None:
+        _check(lib().dsa_debug_trace(None, 0), "dsa_debug_trace")
+        return
+    if buffer.numel() < 2 * capacity * 8 or not buffer.is_cuda:
+        raise ValueError("trace buffer too small or not on the GPU")
+    _check(lib().dsa_debug_trace(buffer.data_ptr(), capacity), "dsa_debug_trace")

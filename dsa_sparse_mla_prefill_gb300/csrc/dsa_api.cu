@@ -7,6 +7,7 @@
 
 #include "../../include/dsa.h"
 #include "dsa_kernels.h"
+#include "dsa_tmap.h"
 
 namespace {
 
@@ -22,6 +23,9 @@ struct DevInfo {
   unsigned int* err = nullptr;
 };
 DevInfo g_dev[kMaxDev];
+
+// diagnostic timeline buffer (dsa_debug_trace)
+dsa::TraceArgs g_trace = {nullptr, 0};
 
 // Per-device set-up: SM count and the device address of the error counters.
 bool dev_info(DevInfo** out) {
@@ -175,6 +179,9 @@ int dsa_sparse_prefill(const uint16_t* q, const uint16_t* kv, int N, int ld_kv, 
   a.k = k;
   a.ld = ld;
   a.scale = scale;
+  a.tr = g_trace;
+  if (!dsa::make_row_gather_map(&a.tmap_kv, kv, N, ld_kv, ld_kv)) return DSA_ERR_CUDA;
+  if (!dsa::make_tile_map(&a.tmap_q, q, (int64_t)T * H, d_qk, d_qk, H)) return DSA_ERR_CUDA;
   const int r = dsa::launch_sparse_prefill(a, d->num_sms, (cudaStream_t)stream);
   return r == 0 ? DSA_OK : (r == -2 ? DSA_ERR_UNSUPPORTED : DSA_ERR_CUDA);
 }
@@ -213,6 +220,7 @@ int dsa_grouped_prefill(const uint16_t* q, const uint16_t* kv, int N, int ld_kv,
   a.union_pad = union_pad;
   a.num_groups = a.req.cu_g[a.req.num_req];
   a.scale = scale;
+  a.tr = g_trace;
   const int r = dsa::launch_grouped_prefill(a, d->num_sms, (cudaStream_t)stream);
   return r == 0 ? DSA_OK : (r == -2 ? DSA_ERR_UNSUPPORTED : DSA_ERR_CUDA);
 }
@@ -279,8 +287,22 @@ int dsa_masked_mha_prefill(const uint16_t* q, const uint16_t* k, const uint16_t*
   a.words = words;
   a.num_qtiles = a.req.cu_g[a.req.num_req];
   a.scale = scale;
+  a.tr = g_trace;
   const int r = dsa::launch_masked_mha(a, d->num_sms, (cudaStream_t)stream);
   return r == 0 ? DSA_OK : (r == -2 ? DSA_ERR_UNSUPPORTED : DSA_ERR_CUDA);
+}
+
+int dsa_debug_trace(void* device_buffer, int capacity) {
+  if (capacity < 0) return DSA_ERR_INVALID_ARG;
+  if (device_buffer == nullptr || capacity == 0) {
+    g_trace.trace = nullptr;
+    g_trace.trace_cap = 0;
+    return DSA_OK;
+  }
+  if ((reinterpret_cast<uintptr_t>(device_buffer) & 7u) != 0) return DSA_ERR_INVALID_ARG;
+  g_trace.trace = static_cast<unsigned long long*>(device_buffer);
+  g_trace.trace_cap = capacity;
+  return DSA_OK;
 }
 
 int dsa_last_device_error(dsa_stream_t stream, uint32_t* counts) {

@@ -5,6 +5,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace dsa {
@@ -165,6 +166,14 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_
   asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                : "memory");
 }
+__device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
 __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
@@ -177,6 +186,66 @@ __device__ __forceinline__ void fence_proxy_async_cluster() {
 }
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Diagnostic timeline stamp (see TraceArgs): CTAs 0 and 1 only.
+#define DSA_TRACE(tr, slot, ev)                                                              \
+  do {                                                                                       \
+    if ((tr).trace != nullptr && blockIdx.x < 2 && (int)(slot) < (tr).trace_cap)             \
+      (tr).trace[((size_t)blockIdx.x * (tr).trace_cap + (slot)) * 8 + (ev)] = clock64();     \
+  } while (0)
+
+// Arrive and add `bytes` to the transaction count the phase waits for.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+// TMA row gather: rows r0..r3 (columns x .. x+63 of a 64x1-box, 128B-swizzled
+// map) into 4 consecutive 128-byte rows at `dst`; the bytes complete on `bar`.
+// x must be a multiple of 8 elements (16 bytes); rows outside the map read as
+// zeros.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int x, int r0, int r1, int r2,
+                                            int r3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// TMA tiled 2-D load of one box (columns x .. x+63, rows y .. y+box-1).
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Bounded wait that ignores the CTA abort flag: used on the way out to let
+// copies already in flight land before the CTA exits.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(a, parity)) {
+    if (globaltimer() - t0 > kWaitTimeoutNs) return false;
+  }
+  return true;
+}
+
+// Non-blocking probe of a phase with cluster-scope acquire (barriers that
+// receive arrivals and data from the peer CTA).
+__device__ __forceinline__ bool mbar_ready_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
 }
 
 // Non-blocking probe of a phase.
@@ -302,6 +371,41 @@ __device__ __forceinline__ void tmem_st16_u32(uint32_t taddr, const uint32_t* r)
       "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
       "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+// Four accumulating MMAs in one statement (one predicate setup, no per-MMA
+// descriptor rebuild): MMA e uses a + e*da and b + e*db, where da/db advance
+// the descriptors' start-address field (units of 16 bytes).  The first MMA
+// accumulates iff accumulate != 0, the other three always accumulate.
+// Issuing them together roughly halves the per-MMA issue cost.
+__device__ __forceinline__ void mma_bf16_ss_x4(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t da, uint32_t db,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 q, %4, %4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %6, %3, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %8, %3, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %9, %10, %3, q;\n\t}"
+      ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "l"(a + da), "l"(b + db), "l"(a + 2ull * da),
+      "l"(b + 2ull * db), "l"(a + 3ull * da), "l"(b + 3ull * db)
+      : "memory");
+}
+// Same with the A operand in tensor memory (A column advance ta per MMA).
+__device__ __forceinline__ void mma_bf16_ts_x4(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t ta, uint32_t db,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 q, %4, %4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %6, %3, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %8, %3, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], %10, %3, q;\n\t}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate), "r"(a_tmem + ta), "l"(b + db),
+      "r"(a_tmem + 2 * ta), "l"(b + 2ull * db), "r"(a_tmem + 3 * ta), "l"(b + 3ull * db)
       : "memory");
 }
 

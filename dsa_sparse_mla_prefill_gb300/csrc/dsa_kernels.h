@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace dsa {
@@ -18,7 +19,17 @@ struct ReqTable {
   int32_t cu_g[kMaxReq + 1];    // group (or query tile) offsets
 };
 
+// Diagnostic timeline (dsa_debug_trace): when `trace` is set, CTAs 0 and 1
+// record clock64() at up to 8 events of each of their first `trace_cap`
+// tiles into trace[(cta * trace_cap + tile) * 8 + event].
+struct TraceArgs {
+  unsigned long long* trace;
+  int trace_cap;
+};
+
 struct SparseArgs {
+  CUtensorMap tmap_kv;  // kv rows, 64-column x 1-row box (row gathers)
+  CUtensorMap tmap_q;   // q viewed [T*H, d_qk], 64-column x H-row box
   const uint16_t* q;    // [T, H, d_qk] bf16
   const uint16_t* kv;   // [N, ld_kv] bf16
   const int32_t* idx;   // [T, ld]
@@ -27,6 +38,7 @@ struct SparseArgs {
   unsigned int* err;    // device error counters
   int T, H, d_qk, N, ld_kv, k, ld;
   float scale;
+  TraceArgs tr;
 };
 
 struct UnionArgs {
@@ -59,6 +71,7 @@ struct GroupedArgs {
   int T, H, G, d_qk, N, ld_kv, union_pad, num_groups;
   float scale;
   ReqTable req;
+  TraceArgs tr;
 };
 
 struct MaskedArgs {
@@ -72,6 +85,7 @@ struct MaskedArgs {
   int T, H, d_qk, d_v, words, num_qtiles;
   float scale;
   ReqTable req;         // cu_g = query-tile offsets per request
+  TraceArgs tr;
 };
 
 // Shared memory of the union builder: bitmap and prefix (W words each, W

@@ -24,7 +24,7 @@
 //   Then each CTA issues O_own += P . V_own (N = 256) from its own V columns.
 // Warp roles per CTA: warps 0-3 softmax (thread i <-> pseudo-head i <-> TMEM
 // lane i; "owner" warps hold this CTA's rows, the others relay the peer's
-// rows), warp 4 the tcgen05 issuer, warps 5-8 cp.async gathers.
+// rows), warp 4 the tcgen05 issuer, warps 5-6 cp.async gathers.
 #include "dsa_device.cuh"
 #include "dsa_kernels.h"
 
@@ -32,7 +32,8 @@ namespace dsa {
 namespace grouped {
 
 constexpr int BK = 64;          // union slots per tile (the MMA's N for S)
-constexpr int NTHREADS = 288;
+constexpr int NTHREADS = 224;   // 7 warps (keeps the full 255-register budget)
+constexpr int NPROD = 64;       // producer threads (warps 5-6)
 constexpr int LAG = 2;
 constexpr float kTau = 8.0f;
 
@@ -112,10 +113,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) grouped
   const int ncl = (int)nclusters_x();
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars[B_Q_FULL], 128);
+    mbar_init(&bars[B_Q_FULL], NPROD);
     mbar_init(&bars[B_Q_EMPTY], 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars[B_KV_FULL + i], 128);
+      mbar_init(&bars[B_KV_FULL + i], NPROD);
       mbar_init(&bars[B_KV_EMPTY + i], 1);
       mbar_init(&bars[B_S_FULL + i], 1);
       mbar_init(&bars[B_S_EMPTY + i], 128);
@@ -184,9 +185,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) grouped
       if (!wait_free(&bars[B_Q_EMPTY], (lgq & 1) ^ 1)) { ok = false; break; }
       {
         const uint32_t qs = sbase + C::OFF_Q;
-        for (int pass = 0; pass < 8 * nown; ++pass) {
-          const int row = (pass & 7) * 16 + rsub;
-          const int c = pass >> 3;
+        for (int pass = 0; pass < 16 * nown; ++pass) {
+          const int row = (pass & 15) * 8 + rsub;
+          const int c = pass >> 4;
           const bool valid = row < nrows;
           const uint16_t* src = a.q + (size_t)(valid ? t0 * H + row : 0) * d_qk + latent_chunk(rank, c) * 64 + p8 * 8;
           cp_async16(qs + c * (128 * 128) + row * 128 + ((p8 ^ (row & 7)) << 4), src, valid ? 16u : 0u);
@@ -198,15 +199,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) grouped
       for (int j = 0; j < ntiles; ++j, ++gt) {
         const int s = gt & 1;
         if (!wait_free(&bars[B_KV_EMPTY + s], ((gt >> 1) & 1) ^ 1)) { ok = false; break; }
+        if (ptid == 0) DSA_TRACE(a.tr, gt, 0);
         if (ptid < BK) {
           const int u = j * BK + ptid;
           smem[C::OFF_MASKB + s * 64 + ptid] = (u < U) ? __ldg(mrow + u) : (uint8_t)0;
         }
-        int kr[4];
-        bool kv_ok[4];
+        int kr[8];
+        bool kv_ok[8];
 #pragma unroll
-        for (int rb = 0; rb < 4; ++rb) {
-          const int u = j * BK + rb * 16 + rsub;
+        for (int rb = 0; rb < 8; ++rb) {
+          const int u = j * BK + rb * 8 + rsub;
           const int x = (u < U) ? __ldg(urow + u) : -1;
           kv_ok[rb] = (x >= 0) && (x < a.N);
           kr[rb] = kv_ok[rb] ? x : 0;
@@ -215,8 +217,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) grouped
         for (int c = 0; c < nown; ++c) {
           const int lc = latent_chunk(rank, c);
 #pragma unroll
-          for (int rb = 0; rb < 4; ++rb) {
-            const int row = rb * 16 + rsub;
+          for (int rb = 0; rb < 8; ++rb) {
+            const int row = rb * 8 + rsub;
             const uint16_t* src = a.kv + (size_t)kr[rb] * a.ld_kv + lc * 64 + p8 * 8;
             cp_async16(kvs + c * C::KV_CHUNK + row * 128 + ((p8 ^ (row & 7)) << 4), src, kv_ok[rb] ? 16u : 0u);
           }
@@ -236,21 +238,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) grouped
       const uint32_t qs = sbase + C::OFF_Q;
       uint32_t gt = 0, lgq = 0;
       bool ok = true;
-      auto issue_qk = [&](uint32_t i, bool last) -> bool {
+      auto qk_ready = [&](uint32_t i) -> bool {
         const int s = i & 1;
-        if (!mbar_wait(&bars[B_KV_FULL + s], (i >> 1) & 1, abort_flag, err)) return false;
-        if (!mbar_wait(&bars[B_S_EMPTY + s], ((i >> 1) & 1) ^ 1, abort_flag, err)) return false;
+        return mbar_ready(&bars[B_KV_FULL + s], (i >> 1) & 1) && mbar_ready(&bars[B_S_EMPTY + s], ((i >> 1) & 1) ^ 1);
+      };
+      auto issue_qk = [&](uint32_t i, bool last) {
+        const int s = i & 1;
+        DSA_TRACE(a.tr, i, 2);
         tc_fence_after();
         const uint32_t kvs = sbase + C::OFF_KV + s * C::KV_BYTES;
-        for (int c = 0; c < nown; ++c) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_ss(tmem + C::COL_S + s * BK, sdesc_sw128(qs + c * (128 * 128) + kk * 32, 16, 1024),
-                        sdesc_sw128(kvs + c * C::KV_CHUNK + kk * 32, 16, 1024), IDESC_QK, (c | kk) ? 1u : 0u);
-        }
+        for (int c = 0; c < nown; ++c)
+          mma_bf16_ss_x4(tmem + C::COL_S + s * BK, sdesc_sw128(qs + c * (128 * 128), 16, 1024),
+                         sdesc_sw128(kvs + c * C::KV_CHUNK, 16, 1024), 2u, 2u, IDESC_QK, c > 0 ? 1u : 0u);
         mma_commit(&bars[B_S_FULL + s]);
         if (last) mma_commit(&bars[B_Q_EMPTY]);
-        return true;
+        DSA_TRACE(a.tr, i, 1);
+      };
+      auto issue_pv = [&](uint32_t i, int j) {
+        DSA_TRACE(a.tr, i, 7);
+        tc_fence_after();
+        const uint32_t ps = sbase + C::OFF_P + (i & 1) * C::P_BYTES;
+        const uint32_t kvs = sbase + C::OFF_KV + (i & 1) * C::KV_BYTES;
+        // 64 union slots = 4 MMAs of 16: P advances 32 B, V (MN-major) 2048 B
+        mma_bf16_ss_x4(tmem + C::COL_O, sdesc_sw128(ps, 16, 1024), sdesc_sw128(kvs, C::KV_CHUNK, 1024), 2u, 128u,
+                       IDESC_PV, j > 0 ? 1u : 0u);
+        mma_commit(&bars[B_PV_DONE]);
+        mma_commit(&bars[B_KV_EMPTY + (i & 1)]);
       };
       for (int g = cid; g < a.num_groups && ok; g += ncl) {
         const int U = min(__ldg(a.union_len + g), a.union_pad);
@@ -258,26 +271,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) grouped
         if (ntiles == 0) continue;
         if (!mbar_wait(&bars[B_Q_FULL], lgq & 1, abort_flag, err)) { ok = false; break; }
         tc_fence_after();
-        if (!issue_qk(gt, ntiles == 1)) { ok = false; break; }
-        for (int j = 0; j < ntiles; ++j) {
-          const uint32_t i = gt + j;
-          if (j + 1 < ntiles && !issue_qk(i + 1, j + 2 == ntiles)) { ok = false; break; }
-          // P rows arrive from both CTAs: acquire at cluster scope
-          if (!mbar_wait_cluster(&bars[B_P_FULL + (i & 1)], (i >> 1) & 1, abort_flag, err)) { ok = false; break; }
-          tc_fence_after();
-          if (j == 0) {
-            if (!mbar_wait(&bars[B_O_EMPTY], (lgq & 1) ^ 1, abort_flag, err)) { ok = false; break; }
-            tc_fence_after();
+        // issue whichever of QK(next) / PV(oldest) is ready first; QK runs at
+        // most one tile ahead, which keeps every P buffer's previous P.V ahead
+        // of the QK whose scores allow that buffer to be written again
+        int nq = 0, np = 0;
+        uint64_t t_last = globaltimer();
+        while (np < ntiles) {
+          bool progressed = false;
+          if (nq < ntiles && nq <= np + 1 && qk_ready(gt + nq)) {
+            issue_qk(gt + nq, nq == ntiles - 1);
+            ++nq;
+            progressed = true;
           }
-          const uint32_t ps = sbase + C::OFF_P + (i & 1) * C::P_BYTES;
-          const uint32_t kvs = sbase + C::OFF_KV + (i & 1) * C::KV_BYTES;
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            mma_bf16_ss(tmem + C::COL_O, sdesc_sw128(ps + kk * 32, 16, 1024),
-                        sdesc_sw128(kvs + kk * 2048, C::KV_CHUNK, 1024), IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&bars[B_PV_DONE]);
-          mma_commit(&bars[B_KV_EMPTY + (i & 1)]);
+          // P rows arrive from both CTAs: acquire at cluster scope
+          if (np < nq && mbar_ready_cluster(&bars[B_P_FULL + ((gt + np) & 1)], ((gt + np) >> 1) & 1) &&
+              (np > 0 || mbar_ready(&bars[B_O_EMPTY], (lgq & 1) ^ 1))) {
+            issue_pv(gt + np, np);
+            ++np;
+            progressed = true;
+          }
+          if (progressed) {
+            t_last = globaltimer();
+          } else if (*abort_flag) {
+            ok = false;
+            break;
+          } else if (globaltimer() - t_last > kWaitTimeoutNs) {
+            *abort_flag = 1;
+            atomicAdd(err + ERR_TIMEOUT, 1u);
+            ok = false;
+            break;
+          }
         }
+        if (!ok) break;
         gt += ntiles;
         ++lgq;
       }
@@ -325,6 +350,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) grouped
         const int sb = i & 1;
         const uint32_t ph = (i >> 1) & 1;
         if (!mbar_wait_warp(&bars[B_S_FULL + sb], ph, abort_flag, err)) { ok = false; break; }
+        if (row == 0) DSA_TRACE(a.tr, i, 3);
         tc_fence_after();
         float sv[BK];
 #pragma unroll
@@ -343,6 +369,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) grouped
           mbar_arrive_remote(peer_bar(B_SX_FULL + sb));
           // the owner's rescale factor for this row, applied to my half of O
           if (!mbar_wait_cluster_warp(&bars[B_ALPHA_FULL + sb], ph, abort_flag, err)) { ok = false; break; }
+          if (row == 0) DSA_TRACE(a.tr, i, 4);
           const float alpha = reinterpret_cast<volatile float*>(smem + C::OFF_ALPHA)[sb * 64 + lrow];
           if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
             if (!mbar_wait_warp(&bars[B_PV_DONE], (i - 1) & 1, abort_flag, err)) { ok = false; break; }
@@ -360,9 +387,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) grouped
           }
           tc_fence_before();
           mbar_arrive(&bars[B_P_FULL + sb]);
+          if (row == 0) DSA_TRACE(a.tr, i, 5);
+          if (row == 0) DSA_TRACE(a.tr, i, 6);
         } else {
           // owner: complete the scores with the peer's partial row
           if (!mbar_wait_cluster_warp(&bars[B_SX_FULL + sb], ph, abort_flag, err)) { ok = false; break; }
+          if (row == 0) DSA_TRACE(a.tr, i, 4);
           const uint8_t* sxr = smem + C::OFF_SX + sb * C::SX_BYTES + lrow * (BK * 4);
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
@@ -376,6 +406,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) grouped
           // the producers' mask bytes of this stage (the phase cannot have moved on:
           // the stage is only released after this tile's P.V)
           if (!mbar_wait_warp(&bars[B_KV_FULL + sb], ph, abort_flag, err)) { ok = false; break; }
+          if (row == 0) DSA_TRACE(a.tr, i, 5);
           const uint8_t* mb = smem + C::OFF_MASKB + sb * 64;
           float tmax = -INFINITY;
 #pragma unroll
@@ -429,6 +460,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) grouped
           tc_fence_before();
           mbar_arrive(&bars[B_P_FULL + sb]);
           mbar_arrive_remote(peer_bar(B_P_FULL + sb));
+          if (row == 0) DSA_TRACE(a.tr, i, 6);
         }
       }
       if (!ok) break;

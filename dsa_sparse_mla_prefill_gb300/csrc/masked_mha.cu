@@ -230,10 +230,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) masked_mha_kernel(MaskedArgs a) {
         const uint32_t ks = sbase + C::OFF_K + s * C::K_BYTES;
 #pragma unroll
         for (int c = 0; c < C::QC; ++c)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_ss(tmem + C::COL_S + sb * 128, sdesc_sw128(qs + c * (BQ * 128) + kk * 32, 16, 1024),
-                        sdesc_sw128(ks + c * (BKV * 128) + kk * 32, 16, 1024), IDESC_QK, (c | kk) ? 1u : 0u);
+          mma_bf16_ss_x4(tmem + C::COL_S + sb * 128, sdesc_sw128(qs + c * (BQ * 128), 16, 1024),
+                         sdesc_sw128(ks + c * (BKV * 128), 16, 1024), 2u, 2u, IDESC_QK, c > 0 ? 1u : 0u);
         mma_commit(&bars[B_S_FULL + sb]);
         return true;
       };
@@ -259,9 +257,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) masked_mha_kernel(MaskedArgs a) {
         const int s = n & 1;
         const uint32_t vs = sbase + C::OFF_V + s * C::V_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < BKV / 16; ++kk)
-          mma_bf16_ts(tmem + C::COL_O, tmem + C::COL_S + s * 128 + kk * 8,
-                      sdesc_sw128(vs + kk * 2048, BKV * 128, 1024), IDESC_PV, (n > 0 || kk > 0) ? 1u : 0u);
+        for (int half = 0; half < 2; ++half)
+          mma_bf16_ts_x4(tmem + C::COL_O, tmem + C::COL_S + s * 128 + half * 32,
+                         sdesc_sw128(vs + half * 4 * 2048, BKV * 128, 1024), 8u, 128u, IDESC_PV,
+                         (n > 0 || half > 0) ? 1u : 0u);
         mma_commit(&bars[B_PV_DONE]);
         mma_commit(&bars[B_ST_EMPTY + s]);
         mma_commit(&bars[B_S_EMPTY + s]);

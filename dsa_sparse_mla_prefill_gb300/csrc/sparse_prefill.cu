@@ -9,15 +9,21 @@
 // is bound by the gather.
 //
 // Design (one persistent CTA per SM, tokens round-robin over CTAs):
-//   warp 5      compacts the token's index row (valid entries only, order
+//   warp 6      compacts the token's index row (valid entries only, order
 //               kept) into shared memory; out-of-range entries are counted.
-//   warps 6-9   gather: 16-byte cp.async per thread, 8 threads per 128-byte
-//               row piece, into 128B-swizzled tiles of 128 keys; one "unit"
-//               holds 128 columns (two swizzle columns) of 128 keys, the RoPE
-//               columns go to their own 2-slot ring.
-//   warp 4      one thread issues tcgen05.mma with the keys on the M side
-//               (M = 128 keys, N = H): S^T = K q^T over D_QK, then
-//               O^T += V^T P^T with V^T read MN-major from the same tile.
+//   warps 7-10  issue TMA loads: q per token (tiled boxes) and the key
+//               rows as tile::gather4 (4 rows x 128 bytes per instruction)
+//               straight into 128B-swizzled tiles of 128 keys; eight lanes
+//               per warp issue, each owning 4 rows of the tile.  One "unit"
+//               holds 128 columns (two swizzle columns) of 128 keys, the
+//               RoPE columns go to their own 2-slot ring; the copies
+//               complete on the stage's mbarrier by byte count.
+//   warps 4, 5  one thread each issues tcgen05.mma with the keys on the M
+//               side (M = 128 keys, N = H): warp 4 S^T = K q^T over D_QK
+//               into a double-buffered S, warp 5 O^T += V^T P^T with V^T
+//               read MN-major from the same tile.  Issue cost is serial per
+//               warp, so the two streams overlap, and each 128-column unit
+//               returns to the producers as soon as its PV MMAs complete.
 //   warps 0-3   thread i owns key i of the tile (TMEM lane i): online softmax
 //               in base 2 with a lazy rescale (only when a head's running
 //               max grows by more than 2^8), P written bf16 to shared
@@ -30,8 +36,7 @@ namespace sparse {
 
 constexpr int BK = 128;         // keys per tile (the MMA's M)
 constexpr int KMAX = 2048;      // longest index row the kernel compacts
-constexpr int NTHREADS = 320;   // 10 warps
-constexpr int LAG = 4;          // cp.async groups a producer thread keeps in flight before signalling
+constexpr int NTHREADS = 352;   // 11 warps
 constexpr float kTau = 8.0f;    // lazy-rescale threshold (log2 units)
 
 template <int H, int NC>
@@ -72,11 +77,10 @@ enum {
   B_P_EMPTY = 15,
   B_O_FULL = 16,     // [2]
   B_O_EMPTY = 18,    // [2]
-  B_DRAIN = 20,
-  B_UNIT_FULL = 21,  // [NU <= 5]
-  B_UNIT_EMPTY = 26, // [NU <= 5]
-  B_SMX_SYNC = 31,   // softmax warpgroup barrier (128)
-  B_PROD_SYNC = 32,  // producer warpgroup barrier (128)
+  B_DRAIN = 20,      // [2] one per MMA issuer
+  B_UNIT_FULL = 22,  // [NU <= 5]
+  B_UNIT_EMPTY = 27, // [NU <= 5]
+  B_SMX_SYNC = 32,   // softmax warpgroup barrier (128)
 };
 
 // Warp-level transposed max/sum reduction: every lane holds H values (one
@@ -110,7 +114,7 @@ __device__ __forceinline__ float warp_transpose_reduce(float* v) {
 
 template <int H, int NC>
 __global__ void __launch_bounds__(NTHREADS, 1)
-sparse_prefill_kernel(SparseArgs a) {
+sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
   using C = Cfg<H, NC>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -132,12 +136,12 @@ sparse_prefill_kernel(SparseArgs a) {
   if (threadIdx.x == 0) {
     mbar_init(&bars[B_IDX_FULL + 0], 1);
     mbar_init(&bars[B_IDX_FULL + 1], 1);
-    mbar_init(&bars[B_IDX_EMPTY + 0], 3);
-    mbar_init(&bars[B_IDX_EMPTY + 1], 3);
-    mbar_init(&bars[B_Q_FULL], 128);
+    mbar_init(&bars[B_IDX_EMPTY + 0], 7);  // 2 MMA, softmax, 4 producer warps
+    mbar_init(&bars[B_IDX_EMPTY + 1], 7);
+    mbar_init(&bars[B_Q_FULL], 1);
     mbar_init(&bars[B_Q_EMPTY], 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars[B_ROPE_FULL + i], 128);
+      mbar_init(&bars[B_ROPE_FULL + i], 1);
       mbar_init(&bars[B_ROPE_EMPTY + i], 1);
       mbar_init(&bars[B_S_FULL + i], 1);
       mbar_init(&bars[B_S_EMPTY + i], 128);
@@ -146,11 +150,11 @@ sparse_prefill_kernel(SparseArgs a) {
     }
     mbar_init(&bars[B_P_FULL], 128);
     mbar_init(&bars[B_P_EMPTY], 1);
-    mbar_init(&bars[B_DRAIN], 1);
+    mbar_init(&bars[B_DRAIN + 0], 1);
+    mbar_init(&bars[B_DRAIN + 1], 1);
     mbar_init(&bars[B_SMX_SYNC], 128);
-    mbar_init(&bars[B_PROD_SYNC], 128);
     for (int i = 0; i < C::NU; ++i) {
-      mbar_init(&bars[B_UNIT_FULL + i], 128);
+      mbar_init(&bars[B_UNIT_FULL + i], 1);
       mbar_init(&bars[B_UNIT_EMPTY + i], 1);
     }
     *abort_flag = 0;
@@ -168,7 +172,7 @@ sparse_prefill_kernel(SparseArgs a) {
   const int T = a.T;
   const int stride_t = gridDim.x;
 
-  if (warp == 5) {
+  if (warp == 6) {
     // ------------------------------------------------------------------
     // index compaction
     // ------------------------------------------------------------------
@@ -228,110 +232,164 @@ sparse_prefill_kernel(SparseArgs a) {
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[B_IDX_FULL + buf]);
     }
-  } else if (warp >= 6) {
+  } else if (warp >= 7) {
     // ------------------------------------------------------------------
-    // gather producers
+    // TMA producers: warps 7-10, lanes 0-7 of each issue; issuer g owns the
+    // tile's rows 4g .. 4g+3 in every column chunk.  TMA issue cost is
+    // serial per warp, so four warps issuing side by side land a tile about
+    // four times sooner than one.  Warp 7 lane 0 (the leader) arms each
+    // stage's byte count; copies from the other issuers may complete before
+    // it does, which only drives the transaction count negative until then.
     // ------------------------------------------------------------------
-    const int ptid = threadIdx.x - 192;  // 0..127
-    const int p8 = ptid & 7;
-    const int rsub = ptid >> 3;          // 0..15
-    uint64_t* pend[LAG + 2];
-    int npend = 0;
-    auto flush = [&]() {
-      cp_async_wait_all();
-      fence_proxy_async_smem();
-      for (int i = 0; i < npend; ++i) mbar_arrive(pend[i]);
-      npend = 0;
-    };
-    auto push = [&](uint64_t* bar) {
-      cp_async_commit();
-      pend[npend++] = bar;
-      if (npend > LAG) {
-        cp_async_wait<LAG>();
-        fence_proxy_async_smem();
-        mbar_arrive(pend[0]);
-        for (int i = 1; i < npend; ++i) pend[i - 1] = pend[i];
-        --npend;
-      }
-    };
-    auto wait_free = [&](uint64_t* bar, uint32_t parity) -> bool {
-      if (mbar_ready(bar, parity)) return true;
-      flush();
-      return mbar_wait(bar, parity, abort_flag, err);
-    };
+    const int pw = warp - 7;
+    const int g = pw * 8 + lane;          // row group (valid for lane < 8)
+    const bool issuer = lane < 8;
+    const bool leader = (pw == 0) && (lane == 0);
     const uint32_t q_s = sbase + C::OFF_Q;
     int lt = 0, lt_nz = 0;
     uint32_t gt = 0;
-    uint32_t sync_phase = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < T && ok; t += stride_t, ++lt) {
       const int buf = lt & 1;
-      if (!wait_free(&bars[B_IDX_FULL + buf], (lt >> 1) & 1)) { ok = false; break; }
+      if (!mbar_wait_warp(&bars[B_IDX_FULL + buf], (lt >> 1) & 1, abort_flag, err)) { ok = false; break; }
       const int nvalid = meta[buf];
       const int ntiles = (nvalid + BK - 1) / BK;
       const int32_t* kl = kidx + buf * KMAX;
       if (ntiles > 0) {
-        // q[t] -> K-major swizzled [chunk][H rows][64 cols]
-        if (!wait_free(&bars[B_Q_EMPTY], (lt_nz & 1) ^ 1)) { ok = false; break; }
-        const uint16_t* qt = a.q + (size_t)t * H * (NC * 64);
-        for (int i = ptid; i < H * NC * 8; i += 128) {
-          const int pp = i & 7;
-          const int c = (i >> 3) % NC;
-          const int h = (i >> 3) / NC;
-          const uint32_t dst = q_s + c * (H * 128) + h * 128 + ((pp ^ (h & 7)) << 4);
-          cp_async16(dst, qt + h * (NC * 64) + c * 64 + pp * 8, 16);
+        if (pw == 0) {
+          // q[t]: rows t*H .. t*H+H-1 of q viewed [T*H, D_QK], one box per swizzle column
+          if (!mbar_wait_warp(&bars[B_Q_EMPTY], (lt_nz & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&bars[B_Q_FULL], C::Q_BYTES);
+            for (int c = 0; c < NC; ++c)
+              tma_load_2d(q_s + c * (H * 128), &a.tmap_q, c * 64, t * H, &bars[B_Q_FULL]);
+          }
         }
-        push(&bars[B_Q_FULL]);
         for (int j = 0; j < ntiles && ok; ++j, ++gt) {
+          if (leader) DSA_TRACE(a.tr, gt, 0);
+          // this issuer's 4 rows; keys past the valid count read as zeros
+          int4 r = make_int4(-1, -1, -1, -1);
+          if (issuer) {
+            const int key = j * BK + 4 * g;
+            r = *reinterpret_cast<const int4*>(kl + key);
+            if (key + 0 >= nvalid) r.x = -1;
+            if (key + 1 >= nvalid) r.y = -1;
+            if (key + 2 >= nvalid) r.z = -1;
+            if (key + 3 >= nvalid) r.w = -1;
+          }
           if constexpr (C::ROPE) {
             const int rs = gt & 1;
-            if (!wait_free(&bars[B_ROPE_EMPTY + rs], ((gt >> 1) & 1) ^ 1)) { ok = false; break; }
-            const uint32_t base = sbase + C::OFF_ROPE + rs * C::ROPE_BYTES;
-#pragma unroll
-            for (int pass = 0; pass < 8; ++pass) {
-              const int row = pass * 16 + rsub;
-              const int key = j * BK + row;
-              const bool valid = key < nvalid;
-              const int kr = valid ? kl[key] : 0;
-              const uint16_t* src = a.kv + (size_t)kr * a.ld_kv + 8 * 64 + p8 * 8;
-              cp_async16(base + row * 128 + ((p8 ^ (row & 7)) << 4), src, valid ? 16u : 0u);
-            }
-            push(&bars[B_ROPE_FULL + rs]);
+            if (!mbar_wait_warp(&bars[B_ROPE_EMPTY + rs], ((gt >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+            if (leader) mbar_arrive_expect_tx(&bars[B_ROPE_FULL + rs], C::ROPE_BYTES);
+            if (issuer)
+              tma_gather4(sbase + C::OFF_ROPE + rs * C::ROPE_BYTES + g * 512, &a.tmap_kv, 8 * 64, r.x, r.y, r.z, r.w,
+                          &bars[B_ROPE_FULL + rs]);
           }
           for (int m = 0; m < 4; ++m) {
             const uint32_t useq = gt * 4 + m;
             const int u = useq % C::NU;
-            if (!wait_free(&bars[B_UNIT_EMPTY + u], ((useq / C::NU) & 1) ^ 1)) { ok = false; break; }
-            const uint32_t base = sbase + C::OFF_UNITS + u * C::UNIT_BYTES;
+            if (!mbar_wait_warp(&bars[B_UNIT_EMPTY + u], ((useq / C::NU) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+            if (leader) mbar_arrive_expect_tx(&bars[B_UNIT_FULL + u], C::UNIT_BYTES);
+            if (issuer) {
+              const uint32_t base = sbase + C::OFF_UNITS + u * C::UNIT_BYTES + g * 512;
 #pragma unroll
-            for (int pass = 0; pass < 16; ++pass) {
-              const int row = (pass & 7) * 16 + rsub;
-              const int cc = pass >> 3;
-              const int key = j * BK + row;
-              const bool valid = key < nvalid;
-              const int kr = valid ? kl[key] : 0;
-              const uint16_t* src = a.kv + (size_t)kr * a.ld_kv + (2 * m + cc) * 64 + p8 * 8;
-              cp_async16(base + cc * (BK * 128) + row * 128 + ((p8 ^ (row & 7)) << 4), src, valid ? 16u : 0u);
+              for (int cc = 0; cc < 2; ++cc)
+                tma_gather4(base + cc * (BK * 128), &a.tmap_kv, (2 * m + cc) * 64, r.x, r.y, r.z, r.w,
+                            &bars[B_UNIT_FULL + u]);
             }
-            push(&bars[B_UNIT_FULL + u]);
           }
         }
         ++lt_nz;
       }
       if (!ok) break;
-      // every producer thread has read this token's index list
-      if (!group_sync(&bars[B_PROD_SYNC], sync_phase, abort_flag, err)) { ok = false; break; }
-      if (ptid == 0) mbar_arrive(&bars[B_IDX_EMPTY + buf]);
+      // this warp's gathers for the token are issued (row indices were read at issue)
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[B_IDX_EMPTY + buf]);
     }
-    flush();
+    // Let copies still in flight land before the CTA can exit: wait for the
+    // last phase each barrier was used in (an older phase's parity can
+    // alias).  A phase completes only once every issuer's bytes are in.
+    if (lane == 0) {
+      if (pw == 0 && lt_nz > 0) mbar_wait_drain(&bars[B_Q_FULL], (lt_nz - 1) & 1);
+      if (C::ROPE) {
+        for (uint32_t i = (gt > 2 ? gt - 2 : 0); i < gt; ++i) mbar_wait_drain(&bars[B_ROPE_FULL + (i & 1)], (i >> 1) & 1);
+      }
+      for (int u = 0; u < C::NU; ++u) {
+        const int64_t last = 4 * (int64_t)gt - 1 - ((4 * (int64_t)gt - 1 - u) % C::NU + C::NU) % C::NU;
+        if (last >= 0) mbar_wait_drain(&bars[B_UNIT_FULL + u], (uint32_t)(last / C::NU) & 1);
+      }
+    }
+    __syncwarp();
   } else if (warp == 4) {
     // ------------------------------------------------------------------
-    // tcgen05 issuer (one thread)
+    // QK issuer (one thread): S^T = K q^T into the S double buffer
     // ------------------------------------------------------------------
     if (lane == 0) {
       constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, H, false, false);
-      constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, H, true, false);
       const uint32_t q_s = sbase + C::OFF_Q;
+      int lt = 0, lt_nz = 0;
+      uint32_t gt = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < T && ok; t += stride_t, ++lt) {
+        const int buf = lt & 1;
+        if (!mbar_wait(&bars[B_IDX_FULL + buf], (lt >> 1) & 1, abort_flag, err)) { ok = false; break; }
+        const int nvalid = meta[buf];
+        mbar_arrive(&bars[B_IDX_EMPTY + buf]);
+        const int ntiles = (nvalid + BK - 1) / BK;
+        if (ntiles == 0) continue;
+        if (!mbar_wait(&bars[B_Q_FULL], lt_nz & 1, abort_flag, err)) { ok = false; break; }
+        tc_fence_after();
+        for (int j = 0; j < ntiles && ok; ++j, ++gt) {
+          const int sb = gt & 1;
+          const uint32_t d_s = tmem + C::COL_S + sb * H;
+          if (!mbar_wait(&bars[B_S_EMPTY + sb], ((gt >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+          DSA_TRACE(a.tr, gt, 2);
+          tc_fence_after();
+          uint32_t acc = 0;
+          if constexpr (C::ROPE) {
+            const int rs = gt & 1;
+            if (!mbar_wait(&bars[B_ROPE_FULL + rs], (gt >> 1) & 1, abort_flag, err)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t abase = sbase + C::OFF_ROPE + rs * C::ROPE_BYTES;
+            const uint32_t bbase = q_s + 8 * (H * 128);
+            mma_bf16_ss_x4(d_s, sdesc_sw128(abase, 16, 1024), sdesc_sw128(bbase, 16, 1024), 2u, 2u, IDESC_QK, acc);
+            acc = 1;
+          }
+          for (int m = 0; m < 4 && ok; ++m) {
+            const uint32_t useq = gt * 4 + m;
+            const int u = useq % C::NU;
+            if (!mbar_wait(&bars[B_UNIT_FULL + u], (useq / C::NU) & 1, abort_flag, err)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t ubase = sbase + C::OFF_UNITS + u * C::UNIT_BYTES;
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+              const uint32_t abase = ubase + cc * (BK * 128);
+              const uint32_t bbase = q_s + (2 * m + cc) * (H * 128);
+              mma_bf16_ss_x4(d_s, sdesc_sw128(abase, 16, 1024), sdesc_sw128(bbase, 16, 1024), 2u, 2u, IDESC_QK, acc);
+              acc = 1;
+            }
+          }
+          if (!ok) break;
+          DSA_TRACE(a.tr, gt, 1);
+          mma_commit(&bars[B_S_FULL + sb]);
+          if constexpr (C::ROPE) mma_commit(&bars[B_ROPE_EMPTY + (gt & 1)]);
+          if (j == ntiles - 1) mma_commit(&bars[B_Q_EMPTY]);
+        }
+        ++lt_nz;
+      }
+      // wait until every MMA issued above has completed
+      mma_commit(&bars[B_DRAIN + 0]);
+      mbar_wait(&bars[B_DRAIN + 0], 0, abort_flag, err);
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------------------------
+    // PV issuer (one thread): O^T += V^T P^T, unit by unit, each unit
+    // released to the producers as soon as its MMAs complete.  The unit's
+    // QK MMAs completed before the softmax saw S, hence before P_FULL.
+    // ------------------------------------------------------------------
+    if (lane == 0) {
+      constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, H, true, false);
       const uint32_t p_s = sbase + C::OFF_P;
       int lt = 0, lt_nz = 0;
       uint32_t gt = 0;
@@ -344,51 +402,9 @@ sparse_prefill_kernel(SparseArgs a) {
         const int ntiles = (nvalid + BK - 1) / BK;
         if (ntiles == 0) continue;
         const int ob = lt_nz & 1;
-        if (!mbar_wait(&bars[B_Q_FULL], lt_nz & 1, abort_flag, err)) { ok = false; break; }
-        tc_fence_after();
         for (int j = 0; j < ntiles && ok; ++j, ++gt) {
-          const int sb = gt & 1;
-          const uint32_t d_s = tmem + C::COL_S + sb * H;
-          if (!mbar_wait(&bars[B_S_EMPTY + sb], ((gt >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
-          tc_fence_after();
-          uint32_t acc = 0;
-          if constexpr (C::ROPE) {
-            const int rs = gt & 1;
-            if (!mbar_wait(&bars[B_ROPE_FULL + rs], (gt >> 1) & 1, abort_flag, err)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t abase = sbase + C::OFF_ROPE + rs * C::ROPE_BYTES;
-            const uint32_t bbase = q_s + 8 * (H * 128);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-              mma_bf16_ss(d_s, sdesc_sw128(abase + ks * 32, 16, 1024), sdesc_sw128(bbase + ks * 32, 16, 1024),
-                          IDESC_QK, acc);
-              acc = 1;
-            }
-          }
-          for (int m = 0; m < 4 && ok; ++m) {
-            const uint32_t useq = gt * 4 + m;
-            const int u = useq % C::NU;
-            if (!mbar_wait(&bars[B_UNIT_FULL + u], (useq / C::NU) & 1, abort_flag, err)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t ubase = sbase + C::OFF_UNITS + u * C::UNIT_BYTES;
-#pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-              const uint32_t abase = ubase + cc * (BK * 128);
-              const uint32_t bbase = q_s + (2 * m + cc) * (H * 128);
-#pragma unroll
-              for (int ks = 0; ks < 4; ++ks) {
-                mma_bf16_ss(d_s, sdesc_sw128(abase + ks * 32, 16, 1024), sdesc_sw128(bbase + ks * 32, 16, 1024),
-                            IDESC_QK, acc);
-                acc = 1;
-              }
-            }
-          }
-          if (!ok) break;
-          mma_commit(&bars[B_S_FULL + sb]);
-          if constexpr (C::ROPE) mma_commit(&bars[B_ROPE_EMPTY + (gt & 1)]);
-          if (j == ntiles - 1) mma_commit(&bars[B_Q_EMPTY]);
-          // P^T from the softmax warps, then O^T += V^T P^T
           if (!mbar_wait(&bars[B_P_FULL], gt & 1, abort_flag, err)) { ok = false; break; }
+          DSA_TRACE(a.tr, gt, 7);
           tc_fence_after();
           if (j == 0) {
             if (!mbar_wait(&bars[B_O_EMPTY + ob], ((lt_nz >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
@@ -400,10 +416,11 @@ sparse_prefill_kernel(SparseArgs a) {
             const uint32_t ubase = sbase + C::OFF_UNITS + u * C::UNIT_BYTES;
             const uint32_t d_o = tmem + C::COL_O + ob * (4 * H) + m * H;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t adesc = sdesc_sw128(ubase + kk * 2048, BK * 128, 1024);
-              const uint64_t bdesc = sdesc_sw128(p_s + (kk >> 2) * (H * 128) + (kk & 3) * 32, 16, 1024);
-              mma_bf16_ss(d_o, adesc, bdesc, IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+            for (int half = 0; half < 2; ++half) {
+              // 16 keys (2048 B of V^T, MN-major) per MMA; P^T one 64-key swizzle column per half
+              const uint64_t adesc = sdesc_sw128(ubase + half * 4 * 2048, BK * 128, 1024);
+              const uint64_t bdesc = sdesc_sw128(p_s + half * (H * 128), 16, 1024);
+              mma_bf16_ss_x4(d_o, adesc, bdesc, 128u, 2u, IDESC_PV, (j > 0 || half > 0) ? 1u : 0u);
             }
             mma_commit(&bars[B_UNIT_EMPTY + u]);
           }
@@ -412,9 +429,8 @@ sparse_prefill_kernel(SparseArgs a) {
         }
         ++lt_nz;
       }
-      // wait until every MMA issued above has completed
-      mma_commit(&bars[B_DRAIN]);
-      mbar_wait(&bars[B_DRAIN], 0, abort_flag, err);
+      mma_commit(&bars[B_DRAIN + 1]);
+      mbar_wait(&bars[B_DRAIN + 1], 0, abort_flag, err);
     }
     __syncwarp();
   } else {
@@ -449,6 +465,7 @@ sparse_prefill_kernel(SparseArgs a) {
       for (int j = 0; j < ntiles; ++j, ++gt) {
         const int sb = gt & 1;
         if (!mbar_wait_warp(&bars[B_S_FULL + sb], (gt >> 1) & 1, abort_flag, err)) { ok = false; break; }
+        if (tid == 0) DSA_TRACE(a.tr, gt, 3);
         tc_fence_after();
         float s[H];
         tmem_ld_cols<H>(tmem + lane_off + C::COL_S + sb * H, s);
@@ -478,11 +495,13 @@ sparse_prefill_kernel(SparseArgs a) {
           tmax[h + 2] = fmaxf(fmaxf(x0.z, x1.z), fmaxf(x2.z, x3.z));
           tmax[h + 3] = fmaxf(fmaxf(x0.w, x1.w), fmaxf(x2.w, x3.w));
         }
+        if (tid == 0) DSA_TRACE(a.tr, gt, 4);
         bool need = false;
 #pragma unroll
         for (int h = 0; h < H; ++h) need |= (tmax[h] > m_run[h] + kTau);
         // the previous PV must be done before P is overwritten or O rescaled
         if (!mbar_wait_warp(&bars[B_P_EMPTY], (gt & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+        if (tid == 0) DSA_TRACE(a.tr, gt, 5);
         tc_fence_after();
         if (need) {
           float alpha[H];
@@ -523,6 +542,7 @@ sparse_prefill_kernel(SparseArgs a) {
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&bars[B_P_FULL]);
+        if (tid == 0) DSA_TRACE(a.tr, gt, 6);
       }
       if (!ok) break;
       // -------- epilogue --------

@@ -187,6 +187,18 @@ int dsa_masked_mha_prefill(const uint16_t* q, const uint16_t* k, const uint16_t*
  * ---------------------------------------------------------------------- */
 int dsa_last_device_error(dsa_stream_t stream, uint32_t* counts);
 
+/* ------------------------------------------------------------------------
+ * Diagnostic timeline (no counterpart on the pages; a profiling aid).  While
+ * a buffer is set, the first two CTAs of every per-token, grouped and masked
+ * launch write clock64() stamps of up to 8 pipeline events for each of their
+ * first `capacity` tiles into it: u64 slot [(cta * capacity + tile) * 8 +
+ * event]; untouched slots keep their contents.  `device_buffer` is caller-owned
+ * device memory of at least 2 * capacity * 8 * 8 bytes; NULL (or capacity 0)
+ * switches recording off.  Host-only call; returns DSA_OK or
+ * DSA_ERR_INVALID_ARG.
+ * ---------------------------------------------------------------------- */
+int dsa_debug_trace(void* device_buffer, int capacity);
+
 #ifdef __cplusplus
 }
 #endif

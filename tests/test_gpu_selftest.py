@@ -44,3 +44,38 @@ def test_mma_layouts(selftest, a_mn, b_mn, N, K):
     assert int(status[1]) == 0, "bounded wait ran out"
     err = (D.cpu() - ref).abs().max().item()
     assert err < 1e-3 * (1 + ref.abs().max().item()), err
+
+
+@pytest.mark.parametrize("col", [0, 64, 512])
+def test_tma_gather4_swizzled_layout(selftest, col):
+    """TMA tile::gather4 of 128 listed latent rows (64 columns starting at
+    `col`) lands in the 128B-swizzled layout the MMA descriptors assume: row r
+    at r*128 bytes, 16-byte piece p at (p ^ (r & 7)) * 16; rows outside the
+    table read as zeros."""
+    import dsa_sparse_mla_prefill_gb300 as dsa
+    lib = ctypes.CDLL(os.path.join(os.path.dirname(dsa.__file__), "libdsa_selftest.so"))
+    fn = lib.dsa_selftest_gather4
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                   ctypes.c_void_p, ctypes.c_void_p]
+    N, ld = 700, 576
+    g = torch.Generator().manual_seed(col + 3)
+    kv = torch.randn(N, ld, generator=g).to(torch.bfloat16)
+    rows = torch.randint(0, N, (128,), generator=g, dtype=torch.int32)
+    rows[5] = -1
+    rows[77] = N          # past the end
+    rows[126] = N - 1
+    out = torch.zeros(128 * 64, dtype=torch.int16, device="cuda")
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    rc = fn(kv.cuda().data_ptr(), N, ld, rows.cuda().data_ptr(), col, out.data_ptr(), status.data_ptr(),
+            torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert int(status[1]) == 0
+    img = out.cpu().numpy().view(np.uint16).reshape(128, 8, 8)      # [row][physical piece][element]
+    bits = kv.view(torch.int16).numpy().view(np.uint16)
+    for r in range(128):
+        src = int(rows[r])
+        for p in range(8):
+            want = bits[src, col + 8 * p: col + 8 * p + 8] if 0 <= src < N else np.zeros(8, np.uint16)
+            assert np.array_equal(img[r, p ^ (r & 7)], want), (r, p)
