@@ -285,7 +285,7 @@ extern "C" int dsa_selftest_gather4(const uint16_t* kv, int N, int ld, const int
 // `warps` warps; records cycles from first issue to all bytes landed.
 // ---------------------------------------------------------------------------
 namespace {
-__global__ void __launch_bounds__(128, 1) selftest_gather4_timing_kernel(const __grid_constant__ CUtensorMap map,
+__global__ void __launch_bounds__(512, 1) selftest_gather4_timing_kernel(const __grid_constant__ CUtensorMap map,
                                                                         int N, int total, int warps, int lanes,
                                                                         long long* out, unsigned int* status) {
   extern __shared__ uint8_t smem_raw[];
@@ -323,13 +323,13 @@ __global__ void __launch_bounds__(128, 1) selftest_gather4_timing_kernel(const _
 
 extern "C" int dsa_selftest_gather4_timing(const uint16_t* kv, int N, int ld, int total, int warps, int lanes,
                                            long long* out, unsigned int* status, cudaStream_t stream) {
-  if (N < 8 || ld < 64 || (ld & 7) || warps < 1 || warps > 4 || lanes < 1 || lanes > 32 || total < 1) return 1;
+  if (N < 8 || ld < 64 || (ld & 7) || warps < 1 || warps > 16 || lanes < 1 || lanes > 32 || total < 1) return 1;
   CUtensorMap map;
   if (!dsa::make_row_gather_map(&map, kv, N, ld, ld)) return 2;
   const int smem = 65536 + 1024;
   if (cudaFuncSetAttribute(selftest_gather4_timing_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess)
     return 3;
-  selftest_gather4_timing_kernel<<<1, 128, smem, stream>>>(map, N, total, warps, lanes, out, status);
+  selftest_gather4_timing_kernel<<<1, 512, smem, stream>>>(map, N, total, warps, lanes, out, status);
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }

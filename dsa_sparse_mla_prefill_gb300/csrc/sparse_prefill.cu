@@ -11,10 +11,10 @@
 // Design (one persistent CTA per SM, tokens round-robin over CTAs):
 //   warp 6      compacts the token's index row (valid entries only, order
 //               kept) into shared memory; out-of-range entries are counted.
-//   warps 7-10  issue TMA loads: q per token (tiled boxes) and the key
+//   warps 8-15  issue TMA loads: q per token (tiled boxes) and the key
 //               rows as tile::gather4 (4 rows x 128 bytes per instruction)
 //               straight into 128B-swizzled tiles of 128 keys; eight lanes
-//               per warp issue, each owning 4 rows of the tile.  One "unit"
+//               per warp issue, each owning 4 rows of one swizzle column.  One "unit"
 //               holds 128 columns (two swizzle columns) of 128 keys, the
 //               RoPE columns go to their own 2-slot ring; the copies
 //               complete on the stage's mbarrier by byte count.
@@ -24,6 +24,8 @@
 //               read MN-major from the same tile.  Issue cost is serial per
 //               warp, so the two streams overlap, and each 128-column unit
 //               returns to the producers as soon as its PV MMAs complete.
+//   warp 7      idle (keeps the warpgroups aligned for the register split:
+//               warps 0-3 run at 200 registers, the rest at 104).
 //   warps 0-3   thread i owns key i of the tile (TMEM lane i): online softmax
 //               in base 2 with a lazy rescale (only when a head's running
 //               max grows by more than 2^8), P written bf16 to shared
@@ -36,7 +38,9 @@ namespace sparse {
 
 constexpr int BK = 128;         // keys per tile (the MMA's M)
 constexpr int KMAX = 2048;      // longest index row the kernel compacts
-constexpr int NTHREADS = 352;   // 11 warps
+constexpr int NTHREADS = 512;   // 16 warps, launched at 128 registers each
+constexpr int REGS_SOFTMAX = 200; // warpgroup 0 after rebalancing
+constexpr int REGS_OTHER = 104;   // warpgroups 1-3 (4*32*200 + 12*32*104 = 512*128)
 constexpr float kTau = 8.0f;    // lazy-rescale threshold (log2 units)
 
 template <int H, int NC>
@@ -136,8 +140,8 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
   if (threadIdx.x == 0) {
     mbar_init(&bars[B_IDX_FULL + 0], 1);
     mbar_init(&bars[B_IDX_FULL + 1], 1);
-    mbar_init(&bars[B_IDX_EMPTY + 0], 7);  // 2 MMA, softmax, 4 producer warps
-    mbar_init(&bars[B_IDX_EMPTY + 1], 7);
+    mbar_init(&bars[B_IDX_EMPTY + 0], 11);  // 2 MMA, softmax, 8 producer warps
+    mbar_init(&bars[B_IDX_EMPTY + 1], 11);
     mbar_init(&bars[B_Q_FULL], 1);
     mbar_init(&bars[B_Q_EMPTY], 1);
     for (int i = 0; i < 2; ++i) {
@@ -172,268 +176,272 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
   const int T = a.T;
   const int stride_t = gridDim.x;
 
-  if (warp == 6) {
-    // ------------------------------------------------------------------
-    // index compaction
-    // ------------------------------------------------------------------
-    int lt = 0;
-    for (int t = blockIdx.x; t < T; t += stride_t, ++lt) {
-      const int buf = lt & 1;
-      if (!mbar_wait_warp(&bars[B_IDX_EMPTY + buf], ((lt >> 1) & 1) ^ 1, abort_flag, err)) break;
-      const int32_t* row = a.idx + (size_t)t * a.ld;
-      int32_t* dst = kidx + buf * KMAX;
-      int cnt = 0, bad = 0;
-      const bool vec = ((a.ld & 3) == 0) && ((reinterpret_cast<uintptr_t>(a.idx) & 15) == 0);
-      if (vec) {
-        for (int base = 0; base < a.k; base += 512) {
-          int4 v[4];
-#pragma unroll
-          for (int qd = 0; qd < 4; ++qd) {
-            const int e0 = base + qd * 128 + lane * 4;
-            if (e0 + 3 < a.k) {
-              v[qd] = __ldg(reinterpret_cast<const int4*>(row + e0));
-            } else {
-              v[qd].x = (e0 + 0 < a.k) ? __ldg(row + e0 + 0) : -1;
-              v[qd].y = (e0 + 1 < a.k) ? __ldg(row + e0 + 1) : -1;
-              v[qd].z = (e0 + 2 < a.k) ? __ldg(row + e0 + 2) : -1;
-              v[qd].w = (e0 + 3 < a.k) ? __ldg(row + e0 + 3) : -1;
+  if (warp >= 4) {
+    // warpgroups 1-3 give registers back; warp 7 has no role
+    regs_dec<REGS_OTHER>();
+    if (warp == 6) {
+      // ------------------------------------------------------------------
+      // index compaction
+      // ------------------------------------------------------------------
+      int lt = 0;
+      for (int t = blockIdx.x; t < T; t += stride_t, ++lt) {
+        const int buf = lt & 1;
+        if (!mbar_wait_warp(&bars[B_IDX_EMPTY + buf], ((lt >> 1) & 1) ^ 1, abort_flag, err)) break;
+        const int32_t* row = a.idx + (size_t)t * a.ld;
+        int32_t* dst = kidx + buf * KMAX;
+        int cnt = 0, bad = 0;
+        const bool vec = ((a.ld & 3) == 0) && ((reinterpret_cast<uintptr_t>(a.idx) & 15) == 0);
+        if (vec) {
+          for (int base = 0; base < a.k; base += 512) {
+            int4 v[4];
+  #pragma unroll
+            for (int qd = 0; qd < 4; ++qd) {
+              const int e0 = base + qd * 128 + lane * 4;
+              if (e0 + 3 < a.k) {
+                v[qd] = __ldg(reinterpret_cast<const int4*>(row + e0));
+              } else {
+                v[qd].x = (e0 + 0 < a.k) ? __ldg(row + e0 + 0) : -1;
+                v[qd].y = (e0 + 1 < a.k) ? __ldg(row + e0 + 1) : -1;
+                v[qd].z = (e0 + 2 < a.k) ? __ldg(row + e0 + 2) : -1;
+                v[qd].w = (e0 + 3 < a.k) ? __ldg(row + e0 + 3) : -1;
+              }
+            }
+  #pragma unroll
+            for (int qd = 0; qd < 4; ++qd) {
+              const int vals[4] = {v[qd].x, v[qd].y, v[qd].z, v[qd].w};
+  #pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int x = vals[e];
+                const bool ok = (x >= 0) && (x < a.N);
+                bad += (x < -1 || x >= a.N) ? 1 : 0;
+                const uint32_t m = __ballot_sync(0xffffffffu, ok);
+                if (ok) dst[cnt + __popc(m & ((1u << lane) - 1u))] = x;
+                cnt += __popc(m);
+              }
             }
           }
-#pragma unroll
-          for (int qd = 0; qd < 4; ++qd) {
-            const int vals[4] = {v[qd].x, v[qd].y, v[qd].z, v[qd].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int x = vals[e];
-              const bool ok = (x >= 0) && (x < a.N);
-              bad += (x < -1 || x >= a.N) ? 1 : 0;
-              const uint32_t m = __ballot_sync(0xffffffffu, ok);
-              if (ok) dst[cnt + __popc(m & ((1u << lane) - 1u))] = x;
-              cnt += __popc(m);
-            }
+        } else {
+          for (int base = 0; base < a.k; base += 32) {
+            const int e = base + lane;
+            const int x = (e < a.k) ? __ldg(row + e) : -1;
+            const bool ok = (x >= 0) && (x < a.N);
+            bad += (x < -1 || x >= a.N) ? 1 : 0;
+            const uint32_t m = __ballot_sync(0xffffffffu, ok);
+            if (ok) dst[cnt + __popc(m & ((1u << lane) - 1u))] = x;
+            cnt += __popc(m);
           }
         }
-      } else {
-        for (int base = 0; base < a.k; base += 32) {
-          const int e = base + lane;
-          const int x = (e < a.k) ? __ldg(row + e) : -1;
-          const bool ok = (x >= 0) && (x < a.N);
-          bad += (x < -1 || x >= a.N) ? 1 : 0;
-          const uint32_t m = __ballot_sync(0xffffffffu, ok);
-          if (ok) dst[cnt + __popc(m & ((1u << lane) - 1u))] = x;
-          cnt += __popc(m);
+        bad = __reduce_add_sync(0xffffffffu, bad);
+        if (lane == 0) {
+          if (bad) atomicAdd(err + ERR_BAD_INDEX, (unsigned)bad);
+          meta[buf] = cnt;
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[B_IDX_FULL + buf]);
       }
-      bad = __reduce_add_sync(0xffffffffu, bad);
-      if (lane == 0) {
-        if (bad) atomicAdd(err + ERR_BAD_INDEX, (unsigned)bad);
-        meta[buf] = cnt;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[B_IDX_FULL + buf]);
-    }
-  } else if (warp >= 7) {
-    // ------------------------------------------------------------------
-    // TMA producers: warps 7-10, lanes 0-7 of each issue; issuer g owns the
-    // tile's rows 4g .. 4g+3 in every column chunk.  TMA issue cost is
-    // serial per warp, so four warps issuing side by side land a tile about
-    // four times sooner than one.  Warp 7 lane 0 (the leader) arms each
-    // stage's byte count; copies from the other issuers may complete before
-    // it does, which only drives the transaction count negative until then.
-    // ------------------------------------------------------------------
-    const int pw = warp - 7;
-    const int g = pw * 8 + lane;          // row group (valid for lane < 8)
-    const bool issuer = lane < 8;
-    const bool leader = (pw == 0) && (lane == 0);
-    const uint32_t q_s = sbase + C::OFF_Q;
-    int lt = 0, lt_nz = 0;
-    uint32_t gt = 0;
-    bool ok = true;
-    for (int t = blockIdx.x; t < T && ok; t += stride_t, ++lt) {
-      const int buf = lt & 1;
-      if (!mbar_wait_warp(&bars[B_IDX_FULL + buf], (lt >> 1) & 1, abort_flag, err)) { ok = false; break; }
-      const int nvalid = meta[buf];
-      const int ntiles = (nvalid + BK - 1) / BK;
-      const int32_t* kl = kidx + buf * KMAX;
-      if (ntiles > 0) {
-        if (pw == 0) {
-          // q[t]: rows t*H .. t*H+H-1 of q viewed [T*H, D_QK], one box per swizzle column
-          if (!mbar_wait_warp(&bars[B_Q_EMPTY], (lt_nz & 1) ^ 1, abort_flag, err)) { ok = false; break; }
-          if (lane == 0) {
-            mbar_arrive_expect_tx(&bars[B_Q_FULL], C::Q_BYTES);
-            for (int c = 0; c < NC; ++c)
-              tma_load_2d(q_s + c * (H * 128), &a.tmap_q, c * 64, t * H, &bars[B_Q_FULL]);
-          }
-        }
-        for (int j = 0; j < ntiles && ok; ++j, ++gt) {
-          if (leader) DSA_TRACE(a.tr, gt, 0);
-          // this issuer's 4 rows; keys past the valid count read as zeros
-          int4 r = make_int4(-1, -1, -1, -1);
-          if (issuer) {
-            const int key = j * BK + 4 * g;
-            r = *reinterpret_cast<const int4*>(kl + key);
-            if (key + 0 >= nvalid) r.x = -1;
-            if (key + 1 >= nvalid) r.y = -1;
-            if (key + 2 >= nvalid) r.z = -1;
-            if (key + 3 >= nvalid) r.w = -1;
-          }
-          if constexpr (C::ROPE) {
-            const int rs = gt & 1;
-            if (!mbar_wait_warp(&bars[B_ROPE_EMPTY + rs], ((gt >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
-            if (leader) mbar_arrive_expect_tx(&bars[B_ROPE_FULL + rs], C::ROPE_BYTES);
-            if (issuer)
-              tma_gather4(sbase + C::OFF_ROPE + rs * C::ROPE_BYTES + g * 512, &a.tmap_kv, 8 * 64, r.x, r.y, r.z, r.w,
-                          &bars[B_ROPE_FULL + rs]);
-          }
-          for (int m = 0; m < 4; ++m) {
-            const uint32_t useq = gt * 4 + m;
-            const int u = useq % C::NU;
-            if (!mbar_wait_warp(&bars[B_UNIT_EMPTY + u], ((useq / C::NU) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
-            if (leader) mbar_arrive_expect_tx(&bars[B_UNIT_FULL + u], C::UNIT_BYTES);
-            if (issuer) {
-              const uint32_t base = sbase + C::OFF_UNITS + u * C::UNIT_BYTES + g * 512;
-#pragma unroll
-              for (int cc = 0; cc < 2; ++cc)
-                tma_gather4(base + cc * (BK * 128), &a.tmap_kv, (2 * m + cc) * 64, r.x, r.y, r.z, r.w,
-                            &bars[B_UNIT_FULL + u]);
-            }
-          }
-        }
-        ++lt_nz;
-      }
-      if (!ok) break;
-      // this warp's gathers for the token are issued (row indices were read at issue)
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[B_IDX_EMPTY + buf]);
-    }
-    // Let copies still in flight land before the CTA can exit: wait for the
-    // last phase each barrier was used in (an older phase's parity can
-    // alias).  A phase completes only once every issuer's bytes are in.
-    if (lane == 0) {
-      if (pw == 0 && lt_nz > 0) mbar_wait_drain(&bars[B_Q_FULL], (lt_nz - 1) & 1);
-      if (C::ROPE) {
-        for (uint32_t i = (gt > 2 ? gt - 2 : 0); i < gt; ++i) mbar_wait_drain(&bars[B_ROPE_FULL + (i & 1)], (i >> 1) & 1);
-      }
-      for (int u = 0; u < C::NU; ++u) {
-        const int64_t last = 4 * (int64_t)gt - 1 - ((4 * (int64_t)gt - 1 - u) % C::NU + C::NU) % C::NU;
-        if (last >= 0) mbar_wait_drain(&bars[B_UNIT_FULL + u], (uint32_t)(last / C::NU) & 1);
-      }
-    }
-    __syncwarp();
-  } else if (warp == 4) {
-    // ------------------------------------------------------------------
-    // QK issuer (one thread): S^T = K q^T into the S double buffer
-    // ------------------------------------------------------------------
-    if (lane == 0) {
-      constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, H, false, false);
+    } else if (warp >= 8) {
+      // ------------------------------------------------------------------
+      // TMA producers: warps 8-15, lanes 0-7 of each issue; issuer i owns the
+      // tile's rows 4(i mod 32) .. +3 in swizzle column i/32 of every unit
+      // (and, for i < 32, in the RoPE chunk).  TMA issue cost is serial per
+      // warp, so eight warps issuing side by side land a unit about eight
+      // times sooner than one.  Warp 8 lane 0 (the leader) arms each
+      // stage's byte count; copies from the other issuers may complete before
+      // it does, which only drives the transaction count negative until then.
+      // ------------------------------------------------------------------
+      const int pw = warp - 8;
+      const int iss = pw * 8 + lane;        // issuer 0..63 (lane < 8)
+      const int g = iss & 31;               // row group: rows 4g .. 4g+3
+      const int cc = iss >> 5;              // swizzle column within each unit
+      const bool issuer = lane < 8;
+      const bool leader = (pw == 0) && (lane == 0);
       const uint32_t q_s = sbase + C::OFF_Q;
       int lt = 0, lt_nz = 0;
       uint32_t gt = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < T && ok; t += stride_t, ++lt) {
         const int buf = lt & 1;
-        if (!mbar_wait(&bars[B_IDX_FULL + buf], (lt >> 1) & 1, abort_flag, err)) { ok = false; break; }
+        if (!mbar_wait_warp(&bars[B_IDX_FULL + buf], (lt >> 1) & 1, abort_flag, err)) { ok = false; break; }
         const int nvalid = meta[buf];
-        mbar_arrive(&bars[B_IDX_EMPTY + buf]);
         const int ntiles = (nvalid + BK - 1) / BK;
-        if (ntiles == 0) continue;
-        if (!mbar_wait(&bars[B_Q_FULL], lt_nz & 1, abort_flag, err)) { ok = false; break; }
-        tc_fence_after();
-        for (int j = 0; j < ntiles && ok; ++j, ++gt) {
-          const int sb = gt & 1;
-          const uint32_t d_s = tmem + C::COL_S + sb * H;
-          if (!mbar_wait(&bars[B_S_EMPTY + sb], ((gt >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
-          DSA_TRACE(a.tr, gt, 2);
-          tc_fence_after();
-          uint32_t acc = 0;
-          if constexpr (C::ROPE) {
-            const int rs = gt & 1;
-            if (!mbar_wait(&bars[B_ROPE_FULL + rs], (gt >> 1) & 1, abort_flag, err)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t abase = sbase + C::OFF_ROPE + rs * C::ROPE_BYTES;
-            const uint32_t bbase = q_s + 8 * (H * 128);
-            mma_bf16_ss_x4(d_s, sdesc_sw128(abase, 16, 1024), sdesc_sw128(bbase, 16, 1024), 2u, 2u, IDESC_QK, acc);
-            acc = 1;
+        const int32_t* kl = kidx + buf * KMAX;
+        if (ntiles > 0) {
+          if (pw == 0) {
+            // q[t]: rows t*H .. t*H+H-1 of q viewed [T*H, D_QK], one box per swizzle column
+            if (!mbar_wait_warp(&bars[B_Q_EMPTY], (lt_nz & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+            if (lane == 0) {
+              mbar_arrive_expect_tx(&bars[B_Q_FULL], C::Q_BYTES);
+              for (int c = 0; c < NC; ++c)
+                tma_load_2d(q_s + c * (H * 128), &a.tmap_q, c * 64, t * H, &bars[B_Q_FULL]);
+            }
           }
-          for (int m = 0; m < 4 && ok; ++m) {
-            const uint32_t useq = gt * 4 + m;
-            const int u = useq % C::NU;
-            if (!mbar_wait(&bars[B_UNIT_FULL + u], (useq / C::NU) & 1, abort_flag, err)) { ok = false; break; }
+          for (int j = 0; j < ntiles && ok; ++j, ++gt) {
+            if (leader) DSA_TRACE(a.tr, gt, 0);
+            // this issuer's 4 rows; keys past the valid count read as zeros
+            int4 r = make_int4(-1, -1, -1, -1);
+            if (issuer) {
+              const int key = j * BK + 4 * g;
+              r = *reinterpret_cast<const int4*>(kl + key);
+              if (key + 0 >= nvalid) r.x = -1;
+              if (key + 1 >= nvalid) r.y = -1;
+              if (key + 2 >= nvalid) r.z = -1;
+              if (key + 3 >= nvalid) r.w = -1;
+            }
+            if constexpr (C::ROPE) {
+              const int rs = gt & 1;
+              if (!mbar_wait_warp(&bars[B_ROPE_EMPTY + rs], ((gt >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+              if (leader) mbar_arrive_expect_tx(&bars[B_ROPE_FULL + rs], C::ROPE_BYTES);
+              if (issuer && cc == 0)
+                tma_gather4(sbase + C::OFF_ROPE + rs * C::ROPE_BYTES + g * 512, &a.tmap_kv, 8 * 64, r.x, r.y, r.z, r.w,
+                            &bars[B_ROPE_FULL + rs]);
+            }
+            for (int m = 0; m < 4; ++m) {
+              const uint32_t useq = gt * 4 + m;
+              const int u = useq % C::NU;
+              if (!mbar_wait_warp(&bars[B_UNIT_EMPTY + u], ((useq / C::NU) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+              if (leader) mbar_arrive_expect_tx(&bars[B_UNIT_FULL + u], C::UNIT_BYTES);
+              if (issuer)
+                tma_gather4(sbase + C::OFF_UNITS + u * C::UNIT_BYTES + cc * (BK * 128) + g * 512, &a.tmap_kv,
+                            (2 * m + cc) * 64, r.x, r.y, r.z, r.w, &bars[B_UNIT_FULL + u]);
+            }
+          }
+          ++lt_nz;
+        }
+        if (!ok) break;
+        // this warp's gathers for the token are issued (row indices were read at issue)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[B_IDX_EMPTY + buf]);
+      }
+      // Let copies still in flight land before the CTA can exit: wait for the
+      // last phase each barrier was used in (an older phase's parity can
+      // alias).  A phase completes only once every issuer's bytes are in.
+      if (lane == 0) {
+        if (pw == 0 && lt_nz > 0) mbar_wait_drain(&bars[B_Q_FULL], (lt_nz - 1) & 1);
+        if (C::ROPE) {
+          for (uint32_t i = (gt > 2 ? gt - 2 : 0); i < gt; ++i) mbar_wait_drain(&bars[B_ROPE_FULL + (i & 1)], (i >> 1) & 1);
+        }
+        for (int u = 0; u < C::NU; ++u) {
+          const int64_t last = 4 * (int64_t)gt - 1 - ((4 * (int64_t)gt - 1 - u) % C::NU + C::NU) % C::NU;
+          if (last >= 0) mbar_wait_drain(&bars[B_UNIT_FULL + u], (uint32_t)(last / C::NU) & 1);
+        }
+      }
+      __syncwarp();
+    } else if (warp == 4) {
+      // ------------------------------------------------------------------
+      // QK issuer (one thread): S^T = K q^T into the S double buffer
+      // ------------------------------------------------------------------
+      if (lane == 0) {
+        constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, H, false, false);
+        const uint32_t q_s = sbase + C::OFF_Q;
+        int lt = 0, lt_nz = 0;
+        uint32_t gt = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < T && ok; t += stride_t, ++lt) {
+          const int buf = lt & 1;
+          if (!mbar_wait(&bars[B_IDX_FULL + buf], (lt >> 1) & 1, abort_flag, err)) { ok = false; break; }
+          const int nvalid = meta[buf];
+          mbar_arrive(&bars[B_IDX_EMPTY + buf]);
+          const int ntiles = (nvalid + BK - 1) / BK;
+          if (ntiles == 0) continue;
+          if (!mbar_wait(&bars[B_Q_FULL], lt_nz & 1, abort_flag, err)) { ok = false; break; }
+          tc_fence_after();
+          for (int j = 0; j < ntiles && ok; ++j, ++gt) {
+            const int sb = gt & 1;
+            const uint32_t d_s = tmem + C::COL_S + sb * H;
+            if (!mbar_wait(&bars[B_S_EMPTY + sb], ((gt >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+            DSA_TRACE(a.tr, gt, 2);
             tc_fence_after();
-            const uint32_t ubase = sbase + C::OFF_UNITS + u * C::UNIT_BYTES;
-#pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-              const uint32_t abase = ubase + cc * (BK * 128);
-              const uint32_t bbase = q_s + (2 * m + cc) * (H * 128);
+            uint32_t acc = 0;
+            if constexpr (C::ROPE) {
+              const int rs = gt & 1;
+              if (!mbar_wait(&bars[B_ROPE_FULL + rs], (gt >> 1) & 1, abort_flag, err)) { ok = false; break; }
+              tc_fence_after();
+              const uint32_t abase = sbase + C::OFF_ROPE + rs * C::ROPE_BYTES;
+              const uint32_t bbase = q_s + 8 * (H * 128);
               mma_bf16_ss_x4(d_s, sdesc_sw128(abase, 16, 1024), sdesc_sw128(bbase, 16, 1024), 2u, 2u, IDESC_QK, acc);
               acc = 1;
             }
-          }
-          if (!ok) break;
-          DSA_TRACE(a.tr, gt, 1);
-          mma_commit(&bars[B_S_FULL + sb]);
-          if constexpr (C::ROPE) mma_commit(&bars[B_ROPE_EMPTY + (gt & 1)]);
-          if (j == ntiles - 1) mma_commit(&bars[B_Q_EMPTY]);
-        }
-        ++lt_nz;
-      }
-      // wait until every MMA issued above has completed
-      mma_commit(&bars[B_DRAIN + 0]);
-      mbar_wait(&bars[B_DRAIN + 0], 0, abort_flag, err);
-    }
-    __syncwarp();
-  } else if (warp == 5) {
-    // ------------------------------------------------------------------
-    // PV issuer (one thread): O^T += V^T P^T, unit by unit, each unit
-    // released to the producers as soon as its MMAs complete.  The unit's
-    // QK MMAs completed before the softmax saw S, hence before P_FULL.
-    // ------------------------------------------------------------------
-    if (lane == 0) {
-      constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, H, true, false);
-      const uint32_t p_s = sbase + C::OFF_P;
-      int lt = 0, lt_nz = 0;
-      uint32_t gt = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; t < T && ok; t += stride_t, ++lt) {
-        const int buf = lt & 1;
-        if (!mbar_wait(&bars[B_IDX_FULL + buf], (lt >> 1) & 1, abort_flag, err)) { ok = false; break; }
-        const int nvalid = meta[buf];
-        mbar_arrive(&bars[B_IDX_EMPTY + buf]);
-        const int ntiles = (nvalid + BK - 1) / BK;
-        if (ntiles == 0) continue;
-        const int ob = lt_nz & 1;
-        for (int j = 0; j < ntiles && ok; ++j, ++gt) {
-          if (!mbar_wait(&bars[B_P_FULL], gt & 1, abort_flag, err)) { ok = false; break; }
-          DSA_TRACE(a.tr, gt, 7);
-          tc_fence_after();
-          if (j == 0) {
-            if (!mbar_wait(&bars[B_O_EMPTY + ob], ((lt_nz >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
-            tc_fence_after();
-          }
-          for (int m = 0; m < 4; ++m) {
-            const uint32_t useq = gt * 4 + m;
-            const int u = useq % C::NU;
-            const uint32_t ubase = sbase + C::OFF_UNITS + u * C::UNIT_BYTES;
-            const uint32_t d_o = tmem + C::COL_O + ob * (4 * H) + m * H;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              // 16 keys (2048 B of V^T, MN-major) per MMA; P^T one 64-key swizzle column per half
-              const uint64_t adesc = sdesc_sw128(ubase + half * 4 * 2048, BK * 128, 1024);
-              const uint64_t bdesc = sdesc_sw128(p_s + half * (H * 128), 16, 1024);
-              mma_bf16_ss_x4(d_o, adesc, bdesc, 128u, 2u, IDESC_PV, (j > 0 || half > 0) ? 1u : 0u);
+            for (int m = 0; m < 4 && ok; ++m) {
+              const uint32_t useq = gt * 4 + m;
+              const int u = useq % C::NU;
+              if (!mbar_wait(&bars[B_UNIT_FULL + u], (useq / C::NU) & 1, abort_flag, err)) { ok = false; break; }
+              tc_fence_after();
+              const uint32_t ubase = sbase + C::OFF_UNITS + u * C::UNIT_BYTES;
+  #pragma unroll
+              for (int cc = 0; cc < 2; ++cc) {
+                const uint32_t abase = ubase + cc * (BK * 128);
+                const uint32_t bbase = q_s + (2 * m + cc) * (H * 128);
+                mma_bf16_ss_x4(d_s, sdesc_sw128(abase, 16, 1024), sdesc_sw128(bbase, 16, 1024), 2u, 2u, IDESC_QK, acc);
+                acc = 1;
+              }
             }
-            mma_commit(&bars[B_UNIT_EMPTY + u]);
+            if (!ok) break;
+            DSA_TRACE(a.tr, gt, 1);
+            mma_commit(&bars[B_S_FULL + sb]);
+            if constexpr (C::ROPE) mma_commit(&bars[B_ROPE_EMPTY + (gt & 1)]);
+            if (j == ntiles - 1) mma_commit(&bars[B_Q_EMPTY]);
           }
-          mma_commit(&bars[B_P_EMPTY]);
-          if (j == ntiles - 1) mma_commit(&bars[B_O_FULL + ob]);
+          ++lt_nz;
         }
-        ++lt_nz;
+        // wait until every MMA issued above has completed
+        mma_commit(&bars[B_DRAIN + 0]);
+        mbar_wait(&bars[B_DRAIN + 0], 0, abort_flag, err);
       }
-      mma_commit(&bars[B_DRAIN + 1]);
-      mbar_wait(&bars[B_DRAIN + 1], 0, abort_flag, err);
+      __syncwarp();
+    } else if (warp == 5) {
+      // ------------------------------------------------------------------
+      // PV issuer (one thread): O^T += V^T P^T, unit by unit, each unit
+      // released to the producers as soon as its MMAs complete.  The unit's
+      // QK MMAs completed before the softmax saw S, hence before P_FULL.
+      // ------------------------------------------------------------------
+      if (lane == 0) {
+        constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, H, true, false);
+        const uint32_t p_s = sbase + C::OFF_P;
+        int lt = 0, lt_nz = 0;
+        uint32_t gt = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < T && ok; t += stride_t, ++lt) {
+          const int buf = lt & 1;
+          if (!mbar_wait(&bars[B_IDX_FULL + buf], (lt >> 1) & 1, abort_flag, err)) { ok = false; break; }
+          const int nvalid = meta[buf];
+          mbar_arrive(&bars[B_IDX_EMPTY + buf]);
+          const int ntiles = (nvalid + BK - 1) / BK;
+          if (ntiles == 0) continue;
+          const int ob = lt_nz & 1;
+          for (int j = 0; j < ntiles && ok; ++j, ++gt) {
+            if (!mbar_wait(&bars[B_P_FULL], gt & 1, abort_flag, err)) { ok = false; break; }
+            DSA_TRACE(a.tr, gt, 7);
+            tc_fence_after();
+            if (j == 0) {
+              if (!mbar_wait(&bars[B_O_EMPTY + ob], ((lt_nz >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+              tc_fence_after();
+            }
+            for (int m = 0; m < 4; ++m) {
+              const uint32_t useq = gt * 4 + m;
+              const int u = useq % C::NU;
+              const uint32_t ubase = sbase + C::OFF_UNITS + u * C::UNIT_BYTES;
+              const uint32_t d_o = tmem + C::COL_O + ob * (4 * H) + m * H;
+  #pragma unroll
+              for (int half = 0; half < 2; ++half) {
+                // 16 keys (2048 B of V^T, MN-major) per MMA; P^T one 64-key swizzle column per half
+                const uint64_t adesc = sdesc_sw128(ubase + half * 4 * 2048, BK * 128, 1024);
+                const uint64_t bdesc = sdesc_sw128(p_s + half * (H * 128), 16, 1024);
+                mma_bf16_ss_x4(d_o, adesc, bdesc, 128u, 2u, IDESC_PV, (j > 0 || half > 0) ? 1u : 0u);
+              }
+              mma_commit(&bars[B_UNIT_EMPTY + u]);
+            }
+            mma_commit(&bars[B_P_EMPTY]);
+            if (j == ntiles - 1) mma_commit(&bars[B_O_FULL + ob]);
+          }
+          ++lt_nz;
+        }
+        mma_commit(&bars[B_DRAIN + 1]);
+        mbar_wait(&bars[B_DRAIN + 1], 0, abort_flag, err);
+      }
+      __syncwarp();
     }
-    __syncwarp();
   } else {
+    regs_inc<REGS_SOFTMAX>();
     // ------------------------------------------------------------------
     // softmax + epilogue (warps 0-3, thread i <-> TMEM lane i)
     // ------------------------------------------------------------------
