@@ -18,14 +18,14 @@
 //               holds 128 columns (two swizzle columns) of 128 keys, the
 //               RoPE columns go to their own 2-slot ring; the copies
 //               complete on the stage's mbarrier by byte count.
-//   warps 4, 5  one thread each issues tcgen05.mma with the keys on the M
+//   warps 4,5,7 one thread each issues tcgen05.mma with the keys on the M
 //               side (M = 128 keys, N = H): warp 4 S^T = K q^T over D_QK
-//               into a double-buffered S, warp 5 O^T += V^T P^T with V^T
-//               read MN-major from the same tile.  Issue cost is serial per
-//               warp, so the two streams overlap, and each 128-column unit
-//               returns to the producers as soon as its PV MMAs complete.
-//   warp 7      idle (keeps the warpgroups aligned for the register split:
-//               warps 0-3 run at 200 registers, the rest at 104).
+//               into a double-buffered S, warps 5 and 7 O^T += V^T P^T for
+//               alternate 128-column units, V^T read MN-major from the same
+//               tile.  Issue cost is serial per warp, so the streams
+//               overlap, and each unit returns to the producers as soon as
+//               its PV MMAs complete.
+//   (warps 0-3 run at 200 registers, warps 4-15 at 104.)
 //   warps 0-3   thread i owns key i of the tile (TMEM lane i): online softmax
 //               in base 2 with a lazy rescale (only when a head's running
 //               max grows by more than 2^8), P written bf16 to shared
@@ -81,10 +81,10 @@ enum {
   B_P_EMPTY = 15,
   B_O_FULL = 16,     // [2]
   B_O_EMPTY = 18,    // [2]
-  B_DRAIN = 20,      // [2] one per MMA issuer
-  B_UNIT_FULL = 22,  // [NU <= 5]
-  B_UNIT_EMPTY = 27, // [NU <= 5]
-  B_SMX_SYNC = 32,   // softmax warpgroup barrier (128)
+  B_DRAIN = 20,      // [3] one per MMA issuer
+  B_UNIT_FULL = 23,  // [NU <= 5]
+  B_UNIT_EMPTY = 28, // [NU <= 5]
+  B_SMX_SYNC = 33,   // softmax warpgroup barrier (128)
 };
 
 // Warp-level transposed max/sum reduction: every lane holds H values (one
@@ -140,8 +140,8 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
   if (threadIdx.x == 0) {
     mbar_init(&bars[B_IDX_FULL + 0], 1);
     mbar_init(&bars[B_IDX_FULL + 1], 1);
-    mbar_init(&bars[B_IDX_EMPTY + 0], 11);  // 2 MMA, softmax, 8 producer warps
-    mbar_init(&bars[B_IDX_EMPTY + 1], 11);
+    mbar_init(&bars[B_IDX_EMPTY + 0], 12);  // 3 MMA, softmax, 8 producer warps
+    mbar_init(&bars[B_IDX_EMPTY + 1], 12);
     mbar_init(&bars[B_Q_FULL], 1);
     mbar_init(&bars[B_Q_EMPTY], 1);
     for (int i = 0; i < 2; ++i) {
@@ -149,13 +149,12 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
       mbar_init(&bars[B_ROPE_EMPTY + i], 1);
       mbar_init(&bars[B_S_FULL + i], 1);
       mbar_init(&bars[B_S_EMPTY + i], 128);
-      mbar_init(&bars[B_O_FULL + i], 1);
+      mbar_init(&bars[B_O_FULL + i], 2);   // one commit per PV issuer
       mbar_init(&bars[B_O_EMPTY + i], 128);
     }
     mbar_init(&bars[B_P_FULL], 128);
-    mbar_init(&bars[B_P_EMPTY], 1);
-    mbar_init(&bars[B_DRAIN + 0], 1);
-    mbar_init(&bars[B_DRAIN + 1], 1);
+    mbar_init(&bars[B_P_EMPTY], 2);
+    for (int i = 0; i < 3; ++i) mbar_init(&bars[B_DRAIN + i], 1);
     mbar_init(&bars[B_SMX_SYNC], 128);
     for (int i = 0; i < C::NU; ++i) {
       mbar_init(&bars[B_UNIT_FULL + i], 1);
@@ -177,7 +176,7 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
   const int stride_t = gridDim.x;
 
   if (warp >= 4) {
-    // warpgroups 1-3 give registers back; warp 7 has no role
+    // warpgroups 1-3 give registers back
     regs_dec<REGS_OTHER>();
     if (warp == 6) {
       // ------------------------------------------------------------------
@@ -194,7 +193,7 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
         if (vec) {
           for (int base = 0; base < a.k; base += 512) {
             int4 v[4];
-  #pragma unroll
+#pragma unroll
             for (int qd = 0; qd < 4; ++qd) {
               const int e0 = base + qd * 128 + lane * 4;
               if (e0 + 3 < a.k) {
@@ -206,10 +205,10 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
                 v[qd].w = (e0 + 3 < a.k) ? __ldg(row + e0 + 3) : -1;
               }
             }
-  #pragma unroll
+#pragma unroll
             for (int qd = 0; qd < 4; ++qd) {
               const int vals[4] = {v[qd].x, v[qd].y, v[qd].z, v[qd].w};
-  #pragma unroll
+#pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const int x = vals[e];
                 const bool ok = (x >= 0) && (x < a.N);
@@ -367,7 +366,7 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
               if (!mbar_wait(&bars[B_UNIT_FULL + u], (useq / C::NU) & 1, abort_flag, err)) { ok = false; break; }
               tc_fence_after();
               const uint32_t ubase = sbase + C::OFF_UNITS + u * C::UNIT_BYTES;
-  #pragma unroll
+#pragma unroll
               for (int cc = 0; cc < 2; ++cc) {
                 const uint32_t abase = ubase + cc * (BK * 128);
                 const uint32_t bbase = q_s + (2 * m + cc) * (H * 128);
@@ -388,12 +387,14 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
         mbar_wait(&bars[B_DRAIN + 0], 0, abort_flag, err);
       }
       __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == 5 || warp == 7) {
       // ------------------------------------------------------------------
-      // PV issuer (one thread): O^T += V^T P^T, unit by unit, each unit
+      // PV issuers (one thread in each of warps 5 and 7): O^T += V^T P^T,
+      // warp 5 for units 0 and 2, warp 7 for units 1 and 3, each unit
       // released to the producers as soon as its MMAs complete.  The unit's
       // QK MMAs completed before the softmax saw S, hence before P_FULL.
       // ------------------------------------------------------------------
+      const int pvi = (warp == 5) ? 0 : 1;
       if (lane == 0) {
         constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, H, true, false);
         const uint32_t p_s = sbase + C::OFF_P;
@@ -410,18 +411,18 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
           const int ob = lt_nz & 1;
           for (int j = 0; j < ntiles && ok; ++j, ++gt) {
             if (!mbar_wait(&bars[B_P_FULL], gt & 1, abort_flag, err)) { ok = false; break; }
-            DSA_TRACE(a.tr, gt, 7);
+            if (pvi == 0) DSA_TRACE(a.tr, gt, 7);
             tc_fence_after();
             if (j == 0) {
               if (!mbar_wait(&bars[B_O_EMPTY + ob], ((lt_nz >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
               tc_fence_after();
             }
-            for (int m = 0; m < 4; ++m) {
+            for (int m = pvi; m < 4; m += 2) {
               const uint32_t useq = gt * 4 + m;
               const int u = useq % C::NU;
               const uint32_t ubase = sbase + C::OFF_UNITS + u * C::UNIT_BYTES;
               const uint32_t d_o = tmem + C::COL_O + ob * (4 * H) + m * H;
-  #pragma unroll
+#pragma unroll
               for (int half = 0; half < 2; ++half) {
                 // 16 keys (2048 B of V^T, MN-major) per MMA; P^T one 64-key swizzle column per half
                 const uint64_t adesc = sdesc_sw128(ubase + half * 4 * 2048, BK * 128, 1024);
@@ -435,8 +436,8 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
           }
           ++lt_nz;
         }
-        mma_commit(&bars[B_DRAIN + 1]);
-        mbar_wait(&bars[B_DRAIN + 1], 0, abort_flag, err);
+        mma_commit(&bars[B_DRAIN + 1 + pvi]);
+        mbar_wait(&bars[B_DRAIN + 1 + pvi], 0, abort_flag, err);
       }
       __syncwarp();
     }
@@ -481,32 +482,53 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
         tc_fence_before();
         mbar_arrive(&bars[B_S_EMPTY + sb]);
         const bool valid = (j * BK + tid) < nvalid;
-        float r[H];
+        bool mine = false;
 #pragma unroll
         for (int h = 0; h < H; ++h) {
           s[h] = valid ? s[h] * scale_log2 : -INFINITY;
-          r[h] = s[h];
+          mine |= (s[h] > m_run[h] + kTau);
         }
-        const float wmax = warp_transpose_reduce<H, true>(r);
+        // Lazy rescale: the tile max matters only when some score exceeds
+        // the running max by more than kTau.  Each warp votes; a warp that
+        // votes yes publishes its per-head max.  The new reference is the
+        // max over those warps, which bounds every score of the tile (the
+        // others lie within kTau of the old reference) as the full tile max
+        // would.
+        const bool wneed = __any_sync(0xffffffffu, mine);
         float* redb = red + (gt & 1) * (4 * H);
-        if (lane < H) redb[warp * H + lane] = wmax;
-        if (!group_sync(&bars[B_SMX_SYNC], sync_phase, abort_flag, err)) { ok = false; break; }
-        float tmax[H];
+        volatile uint32_t* vote = misc + 4 + (gt & 1) * 4;
+        if (wneed) {
+          float r[H];
 #pragma unroll
-        for (int h = 0; h < H; h += 4) {
-          float4 x0 = *reinterpret_cast<const float4*>(redb + 0 * H + h);
-          float4 x1 = *reinterpret_cast<const float4*>(redb + 1 * H + h);
-          float4 x2 = *reinterpret_cast<const float4*>(redb + 2 * H + h);
-          float4 x3 = *reinterpret_cast<const float4*>(redb + 3 * H + h);
-          tmax[h + 0] = fmaxf(fmaxf(x0.x, x1.x), fmaxf(x2.x, x3.x));
-          tmax[h + 1] = fmaxf(fmaxf(x0.y, x1.y), fmaxf(x2.y, x3.y));
-          tmax[h + 2] = fmaxf(fmaxf(x0.z, x1.z), fmaxf(x2.z, x3.z));
-          tmax[h + 3] = fmaxf(fmaxf(x0.w, x1.w), fmaxf(x2.w, x3.w));
+          for (int h = 0; h < H; ++h) r[h] = s[h];
+          const float wmax = warp_transpose_reduce<H, true>(r);
+          if (lane < H) redb[warp * H + lane] = wmax;
+        }
+        if (lane == 0) vote[warp] = wneed ? 1u : 0u;
+        if (!group_sync(&bars[B_SMX_SYNC], sync_phase, abort_flag, err)) { ok = false; break; }
+        uint32_t vw[4];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) vw[w] = vote[w];
+        const bool need = (vw[0] | vw[1] | vw[2] | vw[3]) != 0;
+        float tmax[H];
+        if (need) {
+#pragma unroll
+          for (int h = 0; h < H; ++h) tmax[h] = -INFINITY;
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            if (vw[w]) {
+#pragma unroll
+              for (int h = 0; h < H; h += 4) {
+                const float4 x = *reinterpret_cast<const float4*>(redb + w * H + h);
+                tmax[h + 0] = fmaxf(tmax[h + 0], x.x);
+                tmax[h + 1] = fmaxf(tmax[h + 1], x.y);
+                tmax[h + 2] = fmaxf(tmax[h + 2], x.z);
+                tmax[h + 3] = fmaxf(tmax[h + 3], x.w);
+              }
+            }
+          }
         }
         if (tid == 0) DSA_TRACE(a.tr, gt, 4);
-        bool need = false;
-#pragma unroll
-        for (int h = 0; h < H; ++h) need |= (tmax[h] > m_run[h] + kTau);
         // the previous PV must be done before P is overwritten or O rescaled
         if (!mbar_wait_warp(&bars[B_P_EMPTY], (gt & 1) ^ 1, abort_flag, err)) { ok = false; break; }
         if (tid == 0) DSA_TRACE(a.tr, gt, 5);
