@@ -8,28 +8,30 @@
 // every token (2048 x 1152 B per token at top-2048, D_QK = 576), so the form
 // is bound by the gather.
 //
-// Design (one persistent CTA per SM, tokens round-robin over CTAs):
+// Design (one persistent CTA per SM, tokens round-robin over CTAs; the key
+// rows of a tile are gathered twice, once for QK and once for PV, so the
+// QK of the next tile can stream while this tile's softmax runs; the
+// second gather hits L2):
 //   warp 6      compacts the token's index row (valid entries only, order
 //               kept) into shared memory; out-of-range entries are counted.
-//   warps 8-15  issue TMA loads: q per token (tiled boxes) and the key
+//   warps 8-19  issue TMA loads: q per token (tiled boxes) and the key
 //               rows as tile::gather4 (4 rows x 128 bytes per instruction)
-//               straight into 128B-swizzled tiles of 128 keys; eight lanes
-//               per warp issue, each owning 4 rows of one swizzle column.  One "unit"
-//               holds 128 columns (two swizzle columns) of 128 keys, the
-//               RoPE columns go to their own 2-slot ring; the copies
-//               complete on the stage's mbarrier by byte count.
+//               straight into 128B-swizzled tiles of 128 keys.  Warps 8-13
+//               stream the D_QK/64 key chunks (128 keys x 64 columns) of
+//               every tile into the K ring, warps 14-19 the four 128-column
+//               V units into the V ring; copies complete on the stage's
+//               mbarrier by byte count.
 //   warps 4,5,7 one thread each issues tcgen05.mma with the keys on the M
-//               side (M = 128 keys, N = H): warp 4 S^T = K q^T over D_QK
-//               into a double-buffered S, warps 5 and 7 O^T += V^T P^T for
-//               alternate 128-column units, V^T read MN-major from the same
-//               tile.  Issue cost is serial per warp, so the streams
-//               overlap, and each unit returns to the producers as soon as
-//               its PV MMAs complete.
-//   (warps 0-3 run at 200 registers, warps 4-15 at 104.)
+//               side (M = 128 keys, N = H): warp 4 S^T = K q^T chunk by
+//               chunk into a double-buffered S, warps 5 and 7 O^T += V^T P^T
+//               for alternate V units, V^T read MN-major.  Issue cost is
+//               serial per warp, so the streams overlap; every chunk and
+//               unit returns to the producers as soon as its MMAs complete.
 //   warps 0-3   thread i owns key i of the tile (TMEM lane i): online softmax
 //               in base 2 with a lazy rescale (only when a head's running
 //               max grows by more than 2^8), P written bf16 to shared
 //               memory, and the epilogue (O^T lane = output column).
+//   Warps 0-3 run at 192 registers, warps 4-19 at 72.
 #include "dsa_device.cuh"
 #include "dsa_kernels.h"
 
@@ -38,29 +40,45 @@ namespace sparse {
 
 constexpr int BK = 128;         // keys per tile (the MMA's M)
 constexpr int KMAX = 2048;      // longest index row the kernel compacts
-constexpr int NTHREADS = 512;   // 16 warps, launched at 128 registers each
-constexpr int REGS_SOFTMAX = 200; // warpgroup 0 after rebalancing
-constexpr int REGS_OTHER = 104;   // warpgroups 1-3 (4*32*200 + 12*32*104 = 512*128)
+constexpr int NTHREADS = 640;   // 20 warps, launched at 96 registers each
+constexpr int REGS_SOFTMAX = 192; // warpgroup 0 after rebalancing
+constexpr int REGS_OTHER = 72;    // warpgroups 1-4 (4*32*192 + 16*32*72 = 640*96)
 constexpr float kTau = 8.0f;    // lazy-rescale threshold (log2 units)
 
 template <int H, int NC>
 struct Cfg {
-  static constexpr bool ROPE = (NC == 9);                       // 576 = 512 + 64
-  static constexpr int NU = ROPE ? 4 : 5;                       // unit ring depth
-  static constexpr uint32_t UNIT_BYTES = 2u * BK * 128u;        // 2 x (128 keys x 64 cols)
-  static constexpr uint32_t ROPE_BYTES = BK * 128u;
+  static constexpr uint32_t CHUNK_BYTES = BK * 128u;            // 128 keys x 64 columns: one swizzle column
+  static constexpr uint32_t UNIT_BYTES = 2u * CHUNK_BYTES;      // 128 keys x 128 columns: one PV M-block
   static constexpr uint32_t Q_BYTES = NC * H * 128u;
   static constexpr uint32_t P_BYTES = 2u * H * 128u;            // 128 keys = 2 swizzle columns
-  static constexpr uint32_t OFF_UNITS = 0;
-  static constexpr uint32_t OFF_ROPE = OFF_UNITS + NU * UNIT_BYTES;
-  static constexpr uint32_t OFF_Q = OFF_ROPE + (ROPE ? 2u * ROPE_BYTES : 0u);
+  static constexpr uint32_t KIDX_BYTES = 2u * KMAX * 4u;
+  static constexpr uint32_t RED_BYTES = 2u * 4u * H * 4u;
+  static constexpr int NBAR = 44;
+  static constexpr uint32_t TAIL = NBAR * 8u + 64u + 1024u;     // barriers, misc words, alignment slack
+  static constexpr uint32_t SMEM_LIMIT = 227u * 1024u;
+  // V ring: 128-column units for PV; K ring: 64-column chunks for QK.
+  // Every thread that waits on a ring barrier must pass through each of
+  // its phases in order (a phase two ahead has the parity of one that
+  // already completed).  With two V slots, unit m of every tile sits in
+  // slot m mod 2, filled by V producer group m mod 2 and consumed by PV
+  // issuer m mod 2; K slot s is filled by K producer warp s and consumed
+  // by the QK issuer, which takes every chunk.
+  static constexpr int NVR = 2;
+  static constexpr int NKR_FIT =
+      (int)((SMEM_LIMIT - TAIL - Q_BYTES - P_BYTES - KIDX_BYTES - RED_BYTES - NVR * UNIT_BYTES) / CHUNK_BYTES);
+  static constexpr int NKR = 6;   // one slot per K-stream warp
+  static_assert(NKR_FIT >= NKR, "shared memory budget");
+  static_assert(NVR == 2, "V slot = unit mod 2 = PV issuer");
+  static constexpr uint32_t OFF_KR = 0;
+  static constexpr uint32_t OFF_VR = OFF_KR + NKR * CHUNK_BYTES;
+  static constexpr uint32_t OFF_Q = OFF_VR + NVR * UNIT_BYTES;
   static constexpr uint32_t OFF_P = OFF_Q + Q_BYTES;
   static constexpr uint32_t OFF_KIDX = OFF_P + P_BYTES;
-  static constexpr uint32_t OFF_RED = OFF_KIDX + 2u * KMAX * 4u;
-  static constexpr uint32_t OFF_BAR = OFF_RED + 2u * 4u * H * 4u;
-  static constexpr int NBAR = 34;
+  static constexpr uint32_t OFF_RED = OFF_KIDX + KIDX_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_RED + RED_BYTES;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8u;
-  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64u + 1024u;  // + alignment slack
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64u + 1024u;
+  static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
   // TMEM columns: O^T double buffer (2 x 4H) + S^T double buffer (2 x H)
   static constexpr uint32_t TMEM_COLS = (10 * H <= 256) ? 256u : 512u;
   static constexpr uint32_t COL_O = 0;
@@ -73,18 +91,18 @@ enum {
   B_IDX_EMPTY = 2,   // [2]
   B_Q_FULL = 4,
   B_Q_EMPTY = 5,
-  B_ROPE_FULL = 6,   // [2]
-  B_ROPE_EMPTY = 8,  // [2]
-  B_S_FULL = 10,     // [2]
-  B_S_EMPTY = 12,    // [2]
-  B_P_FULL = 14,
-  B_P_EMPTY = 15,
-  B_O_FULL = 16,     // [2]
-  B_O_EMPTY = 18,    // [2]
-  B_DRAIN = 20,      // [3] one per MMA issuer
-  B_UNIT_FULL = 23,  // [NU <= 5]
-  B_UNIT_EMPTY = 28, // [NU <= 5]
-  B_SMX_SYNC = 33,   // softmax warpgroup barrier (128)
+  B_S_FULL = 6,      // [2]
+  B_S_EMPTY = 8,     // [2]
+  B_P_FULL = 10,
+  B_P_EMPTY = 11,
+  B_O_FULL = 12,     // [2]
+  B_O_EMPTY = 14,    // [2]
+  B_DRAIN = 16,      // [3] one per MMA issuer
+  B_SMX_SYNC = 19,   // softmax warpgroup barrier (128)
+  B_KR_FULL = 20,    // [NKR <= 8]
+  B_KR_EMPTY = 28,   // [NKR <= 8]
+  B_VR_FULL = 36,    // [NVR <= 4]
+  B_VR_EMPTY = 40,   // [NVR <= 4]
 };
 
 // Warp-level transposed max/sum reduction: every lane holds H values (one
@@ -140,13 +158,11 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
   if (threadIdx.x == 0) {
     mbar_init(&bars[B_IDX_FULL + 0], 1);
     mbar_init(&bars[B_IDX_FULL + 1], 1);
-    mbar_init(&bars[B_IDX_EMPTY + 0], 12);  // 3 MMA, softmax, 8 producer warps
-    mbar_init(&bars[B_IDX_EMPTY + 1], 12);
+    mbar_init(&bars[B_IDX_EMPTY + 0], 16);  // 3 MMA, softmax, 12 producer warps
+    mbar_init(&bars[B_IDX_EMPTY + 1], 16);
     mbar_init(&bars[B_Q_FULL], 1);
     mbar_init(&bars[B_Q_EMPTY], 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars[B_ROPE_FULL + i], 1);
-      mbar_init(&bars[B_ROPE_EMPTY + i], 1);
       mbar_init(&bars[B_S_FULL + i], 1);
       mbar_init(&bars[B_S_EMPTY + i], 128);
       mbar_init(&bars[B_O_FULL + i], 2);   // one commit per PV issuer
@@ -156,9 +172,13 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
     mbar_init(&bars[B_P_EMPTY], 2);
     for (int i = 0; i < 3; ++i) mbar_init(&bars[B_DRAIN + i], 1);
     mbar_init(&bars[B_SMX_SYNC], 128);
-    for (int i = 0; i < C::NU; ++i) {
-      mbar_init(&bars[B_UNIT_FULL + i], 1);
-      mbar_init(&bars[B_UNIT_EMPTY + i], 1);
+    for (int i = 0; i < C::NKR; ++i) {
+      mbar_init(&bars[B_KR_FULL + i], 1);
+      mbar_init(&bars[B_KR_EMPTY + i], 1);
+    }
+    for (int i = 0; i < C::NVR; ++i) {
+      mbar_init(&bars[B_VR_FULL + i], 1);
+      mbar_init(&bars[B_VR_EMPTY + i], 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -176,7 +196,7 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
   const int stride_t = gridDim.x;
 
   if (warp >= 4) {
-    // warpgroups 1-3 give registers back
+    // warpgroups 1-4 give registers back
     regs_dec<REGS_OTHER>();
     if (warp == 6) {
       // ------------------------------------------------------------------
@@ -239,24 +259,34 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
         if (lane == 0) mbar_arrive(&bars[B_IDX_FULL + buf]);
       }
     } else if (warp >= 8) {
-      // ------------------------------------------------------------------
-      // TMA producers: warps 8-15, lanes 0-7 of each issue; issuer i owns the
-      // tile's rows 4(i mod 32) .. +3 in swizzle column i/32 of every unit
-      // (and, for i < 32, in the RoPE chunk).  TMA issue cost is serial per
-      // warp, so eight warps issuing side by side land a unit about eight
-      // times sooner than one.  Warp 8 lane 0 (the leader) arms each
-      // stage's byte count; copies from the other issuers may complete before
-      // it does, which only drives the transaction count negative until then.
-      // ------------------------------------------------------------------
-      const int pw = warp - 8;
-      const int iss = pw * 8 + lane;        // issuer 0..63 (lane < 8)
-      const int g = iss & 31;               // row group: rows 4g .. 4g+3
-      const int cc = iss >> 5;              // swizzle column within each unit
-      const bool issuer = lane < 8;
-      const bool leader = (pw == 0) && (lane == 0);
+      // ----------------------------------------------------------------
+      // TMA producers: twelve warps in two independent streams.
+      //   warps 8-13:  q per token (warp 8), and the D_QK/64 key chunks of
+      //                every tile into the K ring; warp 8+s owns K slot s
+      //                and issues the whole chunk (lane l: rows 4l..4l+3).
+      //   warps 14-19: the four 128-column V units of every tile into the
+      //                V ring; the three warps of group u own V slot u
+      //                (units m = u, u+2), 64 gather4 shared between them.
+      // Neither stream waits on the other, so QK of the next tile streams
+      // while this tile's softmax runs and V lands ahead of PV.  TMA issue
+      // cost is serial per warp, so many issuing warps keep many copies in
+      // flight.  The leader of a stage arms its byte count; copies from
+      // other issuers may complete first, which only drives the
+      // transaction count negative until then.
+      // ----------------------------------------------------------------
+      const bool kstream = warp < 8 + C::NKR;
+      const int kw = warp - 8;                      // K slot owned (K stream)
+      const int vgroup = (warp - 14) / 3;           // V slot owned (V stream)
+      const int vsub = (warp - 14) % 3;
+      const int e = vsub * 22 + lane;               // V gather index 0..63 (valid for e < 64, lane < 22)
+      const bool v_issuer = !kstream && lane < 22 && e < 64;
+      const int g = kstream ? lane : (e & 31);       // row group
+      const int vcc = e >> 5;                       // V swizzle column
+      const bool leader = (lane == 0) && (kstream || vsub == 0);
       const uint32_t q_s = sbase + C::OFF_Q;
       int lt = 0, lt_nz = 0;
-      uint32_t gt = 0;
+      uint32_t gt = 0, pos = 0;  // tiles and stages of this stream so far
+      int64_t last_armed = -1;   // last stage this warp's leader armed
       bool ok = true;
       for (int t = blockIdx.x; t < T && ok; t += stride_t, ++lt) {
         const int buf = lt & 1;
@@ -265,7 +295,7 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
         const int ntiles = (nvalid + BK - 1) / BK;
         const int32_t* kl = kidx + buf * KMAX;
         if (ntiles > 0) {
-          if (pw == 0) {
+          if (warp == 8) {
             // q[t]: rows t*H .. t*H+H-1 of q viewed [T*H, D_QK], one box per swizzle column
             if (!mbar_wait_warp(&bars[B_Q_EMPTY], (lt_nz & 1) ^ 1, abort_flag, err)) { ok = false; break; }
             if (lane == 0) {
@@ -275,65 +305,72 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
             }
           }
           for (int j = 0; j < ntiles && ok; ++j, ++gt) {
-            if (leader) DSA_TRACE(a.tr, gt, 0);
-            // this issuer's 4 rows; keys past the valid count read as zeros
-            int4 r = make_int4(-1, -1, -1, -1);
-            if (issuer) {
-              const int key = j * BK + 4 * g;
-              r = *reinterpret_cast<const int4*>(kl + key);
-              if (key + 0 >= nvalid) r.x = -1;
-              if (key + 1 >= nvalid) r.y = -1;
-              if (key + 2 >= nvalid) r.z = -1;
-              if (key + 3 >= nvalid) r.w = -1;
-            }
-            if constexpr (C::ROPE) {
-              const int rs = gt & 1;
-              if (!mbar_wait_warp(&bars[B_ROPE_EMPTY + rs], ((gt >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
-              if (leader) mbar_arrive_expect_tx(&bars[B_ROPE_FULL + rs], C::ROPE_BYTES);
-              if (issuer && cc == 0)
-                tma_gather4(sbase + C::OFF_ROPE + rs * C::ROPE_BYTES + g * 512, &a.tmap_kv, 8 * 64, r.x, r.y, r.z, r.w,
-                            &bars[B_ROPE_FULL + rs]);
-            }
-            for (int m = 0; m < 4; ++m) {
-              const uint32_t useq = gt * 4 + m;
-              const int u = useq % C::NU;
-              if (!mbar_wait_warp(&bars[B_UNIT_EMPTY + u], ((useq / C::NU) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
-              if (leader) mbar_arrive_expect_tx(&bars[B_UNIT_FULL + u], C::UNIT_BYTES);
-              if (issuer)
-                tma_gather4(sbase + C::OFF_UNITS + u * C::UNIT_BYTES + cc * (BK * 128) + g * 512, &a.tmap_kv,
-                            (2 * m + cc) * 64, r.x, r.y, r.z, r.w, &bars[B_UNIT_FULL + u]);
+            if (warp == 8 && lane == 0) DSA_TRACE(a.tr, gt, 0);
+            // this lane's 4 rows; keys past the valid count read as zeros
+            const int key = j * BK + 4 * g;
+            int4 r = *reinterpret_cast<const int4*>(kl + key);
+            if (key + 0 >= nvalid) r.x = -1;
+            if (key + 1 >= nvalid) r.y = -1;
+            if (key + 2 >= nvalid) r.z = -1;
+            if (key + 3 >= nvalid) r.w = -1;
+            if (kstream) {
+              for (int c = 0; c < NC; ++c, ++pos) {
+                if ((int)(pos % C::NKR) != kw) continue;
+                if (!mbar_wait_warp(&bars[B_KR_EMPTY + kw], ((pos / C::NKR) & 1) ^ 1, abort_flag, err)) {
+                  ok = false;
+                  break;
+                }
+                if (leader) mbar_arrive_expect_tx(&bars[B_KR_FULL + kw], C::CHUNK_BYTES);
+                tma_gather4(sbase + C::OFF_KR + kw * C::CHUNK_BYTES + g * 512, &a.tmap_kv, c * 64, r.x, r.y, r.z, r.w,
+                            &bars[B_KR_FULL + kw]);
+                last_armed = pos;
+              }
+            } else {
+              for (int m = 0; m < 4; ++m, ++pos) {
+                if ((int)(pos % C::NVR) != vgroup) continue;
+                if (!mbar_wait_warp(&bars[B_VR_EMPTY + vgroup], ((pos / C::NVR) & 1) ^ 1, abort_flag, err)) {
+                  ok = false;
+                  break;
+                }
+                if (leader) mbar_arrive_expect_tx(&bars[B_VR_FULL + vgroup], C::UNIT_BYTES);
+                if (v_issuer)
+                  tma_gather4(sbase + C::OFF_VR + vgroup * C::UNIT_BYTES + vcc * C::CHUNK_BYTES + g * 512, &a.tmap_kv,
+                              (2 * m + vcc) * 64, r.x, r.y, r.z, r.w, &bars[B_VR_FULL + vgroup]);
+                last_armed = pos;
+              }
             }
           }
           ++lt_nz;
         }
         if (!ok) break;
-        // this warp's gathers for the token are issued (row indices were read at issue)
+        // this warp's copies of the token are issued (row indices were read at issue)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[B_IDX_EMPTY + buf]);
       }
-      // Let copies still in flight land before the CTA can exit: wait for the
-      // last phase each barrier was used in (an older phase's parity can
-      // alias).  A phase completes only once every issuer's bytes are in.
-      if (lane == 0) {
-        if (pw == 0 && lt_nz > 0) mbar_wait_drain(&bars[B_Q_FULL], (lt_nz - 1) & 1);
-        if (C::ROPE) {
-          for (uint32_t i = (gt > 2 ? gt - 2 : 0); i < gt; ++i) mbar_wait_drain(&bars[B_ROPE_FULL + (i & 1)], (i >> 1) & 1);
-        }
-        for (int u = 0; u < C::NU; ++u) {
-          const int64_t last = 4 * (int64_t)gt - 1 - ((4 * (int64_t)gt - 1 - u) % C::NU + C::NU) % C::NU;
-          if (last >= 0) mbar_wait_drain(&bars[B_UNIT_FULL + u], (uint32_t)(last / C::NU) & 1);
+      // Let copies still in flight land before the CTA can exit: the last
+      // phase of the slot this warp fills completes only once every byte
+      // of it has landed.
+      if (leader) {
+        if (warp == 8 && lt_nz > 0) mbar_wait_drain(&bars[B_Q_FULL], (lt_nz - 1) & 1);
+        if (last_armed >= 0) {
+          if (kstream)
+            mbar_wait_drain(&bars[B_KR_FULL + kw], (uint32_t)(last_armed / C::NKR) & 1);
+          else
+            mbar_wait_drain(&bars[B_VR_FULL + vgroup], (uint32_t)(last_armed / C::NVR) & 1);
         }
       }
       __syncwarp();
     } else if (warp == 4) {
-      // ------------------------------------------------------------------
-      // QK issuer (one thread): S^T = K q^T into the S double buffer
-      // ------------------------------------------------------------------
+      // ----------------------------------------------------------------
+      // QK issuer (one thread): S^T = K q^T into the S double buffer, one
+      // K-ring chunk (64 columns, four MMAs) at a time; each chunk goes
+      // back to the producers as soon as its MMAs complete.
+      // ----------------------------------------------------------------
       if (lane == 0) {
         constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, H, false, false);
         const uint32_t q_s = sbase + C::OFF_Q;
         int lt = 0, lt_nz = 0;
-        uint32_t gt = 0;
+        uint32_t gt = 0, kpos = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < T && ok; t += stride_t, ++lt) {
           const int buf = lt & 1;
@@ -350,34 +387,19 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
             if (!mbar_wait(&bars[B_S_EMPTY + sb], ((gt >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
             DSA_TRACE(a.tr, gt, 2);
             tc_fence_after();
-            uint32_t acc = 0;
-            if constexpr (C::ROPE) {
-              const int rs = gt & 1;
-              if (!mbar_wait(&bars[B_ROPE_FULL + rs], (gt >> 1) & 1, abort_flag, err)) { ok = false; break; }
+            for (int c = 0; c < NC; ++c, ++kpos) {
+              const uint32_t slot = kpos % C::NKR;
+              if (!mbar_wait(&bars[B_KR_FULL + slot], (kpos / C::NKR) & 1, abort_flag, err)) { ok = false; break; }
               tc_fence_after();
-              const uint32_t abase = sbase + C::OFF_ROPE + rs * C::ROPE_BYTES;
-              const uint32_t bbase = q_s + 8 * (H * 128);
-              mma_bf16_ss_x4(d_s, sdesc_sw128(abase, 16, 1024), sdesc_sw128(bbase, 16, 1024), 2u, 2u, IDESC_QK, acc);
-              acc = 1;
-            }
-            for (int m = 0; m < 4 && ok; ++m) {
-              const uint32_t useq = gt * 4 + m;
-              const int u = useq % C::NU;
-              if (!mbar_wait(&bars[B_UNIT_FULL + u], (useq / C::NU) & 1, abort_flag, err)) { ok = false; break; }
-              tc_fence_after();
-              const uint32_t ubase = sbase + C::OFF_UNITS + u * C::UNIT_BYTES;
-#pragma unroll
-              for (int cc = 0; cc < 2; ++cc) {
-                const uint32_t abase = ubase + cc * (BK * 128);
-                const uint32_t bbase = q_s + (2 * m + cc) * (H * 128);
-                mma_bf16_ss_x4(d_s, sdesc_sw128(abase, 16, 1024), sdesc_sw128(bbase, 16, 1024), 2u, 2u, IDESC_QK, acc);
-                acc = 1;
-              }
+              const uint32_t abase = sbase + C::OFF_KR + slot * C::CHUNK_BYTES;
+              const uint32_t bbase = q_s + c * (H * 128);
+              mma_bf16_ss_x4(d_s, sdesc_sw128(abase, 16, 1024), sdesc_sw128(bbase, 16, 1024), 2u, 2u, IDESC_QK,
+                             c > 0 ? 1u : 0u);
+              mma_commit(&bars[B_KR_EMPTY + slot]);
             }
             if (!ok) break;
             DSA_TRACE(a.tr, gt, 1);
             mma_commit(&bars[B_S_FULL + sb]);
-            if constexpr (C::ROPE) mma_commit(&bars[B_ROPE_EMPTY + (gt & 1)]);
             if (j == ntiles - 1) mma_commit(&bars[B_Q_EMPTY]);
           }
           ++lt_nz;
@@ -388,12 +410,11 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
       }
       __syncwarp();
     } else if (warp == 5 || warp == 7) {
-      // ------------------------------------------------------------------
+      // ----------------------------------------------------------------
       // PV issuers (one thread in each of warps 5 and 7): O^T += V^T P^T,
-      // warp 5 for units 0 and 2, warp 7 for units 1 and 3, each unit
-      // released to the producers as soon as its MMAs complete.  The unit's
-      // QK MMAs completed before the softmax saw S, hence before P_FULL.
-      // ------------------------------------------------------------------
+      // warp 5 for units 0 and 2, warp 7 for units 1 and 3 of every tile,
+      // each V-ring unit released as soon as its MMAs complete.
+      // ----------------------------------------------------------------
       const int pvi = (warp == 5) ? 0 : 1;
       if (lane == 0) {
         constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, H, true, false);
@@ -417,20 +438,25 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
               if (!mbar_wait(&bars[B_O_EMPTY + ob], ((lt_nz >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
               tc_fence_after();
             }
-            for (int m = pvi; m < 4; m += 2) {
-              const uint32_t useq = gt * 4 + m;
-              const int u = useq % C::NU;
-              const uint32_t ubase = sbase + C::OFF_UNITS + u * C::UNIT_BYTES;
+            for (int m = pvi; m < 4 && ok; m += 2) {
+              const uint32_t vp = gt * 4 + m;
+              const uint32_t slot = vp % C::NVR;
+              if (!mbar_wait(&bars[B_VR_FULL + slot], (vp / C::NVR) & 1, abort_flag, err)) { ok = false; break; }
+              tc_fence_after();
+              const uint32_t ubase = sbase + C::OFF_VR + slot * C::UNIT_BYTES;
               const uint32_t d_o = tmem + C::COL_O + ob * (4 * H) + m * H;
 #pragma unroll
-              for (int half = 0; half < 2; ++half) {
-                // 16 keys (2048 B of V^T, MN-major) per MMA; P^T one 64-key swizzle column per half
-                const uint64_t adesc = sdesc_sw128(ubase + half * 4 * 2048, BK * 128, 1024);
-                const uint64_t bdesc = sdesc_sw128(p_s + half * (H * 128), 16, 1024);
-                mma_bf16_ss_x4(d_o, adesc, bdesc, 128u, 2u, IDESC_PV, (j > 0 || half > 0) ? 1u : 0u);
+              for (int hf = 0; hf < 2; ++hf) {
+                // 16 keys (2048 B of V^T, MN-major; the unit's two swizzle
+                // columns CHUNK_BYTES apart) per MMA; P^T one 64-key swizzle
+                // column per half
+                const uint64_t adesc = sdesc_sw128(ubase + hf * 4 * 2048, C::CHUNK_BYTES, 1024);
+                const uint64_t bdesc = sdesc_sw128(p_s + hf * (H * 128), 16, 1024);
+                mma_bf16_ss_x4(d_o, adesc, bdesc, 128u, 2u, IDESC_PV, (j > 0 || hf > 0) ? 1u : 0u);
               }
-              mma_commit(&bars[B_UNIT_EMPTY + u]);
+              mma_commit(&bars[B_VR_EMPTY + slot]);
             }
+            if (!ok) break;
             mma_commit(&bars[B_P_EMPTY]);
             if (j == ntiles - 1) mma_commit(&bars[B_O_FULL + ob]);
           }
