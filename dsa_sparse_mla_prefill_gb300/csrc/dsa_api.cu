@@ -180,7 +180,8 @@ int dsa_sparse_prefill(const uint16_t* q, const uint16_t* kv, int N, int ld_kv, 
   a.ld = ld;
   a.scale = scale;
   a.tr = g_trace;
-  if (!dsa::make_row_gather_map(&a.tmap_kv, kv, N, ld_kv, ld_kv)) return DSA_ERR_CUDA;
+  // (with N = 0 every index is out of range and no row is ever read)
+  if (!dsa::make_row_gather_map(&a.tmap_kv, kv, N > 0 ? N : 1, ld_kv, ld_kv)) return DSA_ERR_CUDA;
   if (!dsa::make_tile_map(&a.tmap_q, q, (int64_t)T * H, d_qk, d_qk, H)) return DSA_ERR_CUDA;
   const int r = dsa::launch_sparse_prefill(a, d->num_sms, (cudaStream_t)stream);
   return r == 0 ? DSA_OK : (r == -2 ? DSA_ERR_UNSUPPORTED : DSA_ERR_CUDA);
@@ -191,6 +192,7 @@ int dsa_grouped_prefill(const uint16_t* q, const uint16_t* kv, int N, int ld_kv,
                         const int32_t* cu_seqlens_q_host, int num_req, int T, int H, int d_qk, int d_v,
                         float scale, uint16_t* out, float* lse, dsa_stream_t stream) {
   if (T < 0 || N < 0 || G < 1 || H < 1 || union_pad < 0 || ld_kv < d_qk) return DSA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !(scale < INFINITY)) return DSA_ERR_INVALID_ARG;
   if (G > 8 || G * H != 128 || !(d_qk == 576 || d_qk == 512) || d_v != 512) return DSA_ERR_UNSUPPORTED;
   if ((ld_kv & 7) != 0 || (union_pad & 15) != 0) return DSA_ERR_INVALID_ARG;
   if (T == 0) return DSA_OK;
@@ -221,6 +223,8 @@ int dsa_grouped_prefill(const uint16_t* q, const uint16_t* kv, int N, int ld_kv,
   a.num_groups = a.req.cu_g[a.req.num_req];
   a.scale = scale;
   a.tr = g_trace;
+  if (!dsa::make_row_gather_map(&a.tmap_kv, kv, N > 0 ? N : 1, ld_kv, ld_kv)) return DSA_ERR_CUDA;
+  if (!dsa::make_tile_map(&a.tmap_q, q, (int64_t)T * H, d_qk, d_qk, 128)) return DSA_ERR_CUDA;
   const int r = dsa::launch_grouped_prefill(a, d->num_sms, (cudaStream_t)stream);
   return r == 0 ? DSA_OK : (r == -2 ? DSA_ERR_UNSUPPORTED : DSA_ERR_CUDA);
 }

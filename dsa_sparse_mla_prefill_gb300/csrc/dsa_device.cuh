@@ -178,6 +178,33 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 // Arrive on an mbarrier of another CTA of the cluster (release at cluster scope).
+// Asynchronous 16-byte store into a peer CTA's shared memory that counts
+// its bytes on the peer's mbarrier (transaction count), so the receiver
+// learns of the data by waiting on its own barrier; no release fence on the
+// sender.  Both addresses come from map_peer.
+__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                            uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   remote_addr),
+               "r"(a), "r"(b), "r"(c), "r"(d), "r"(remote_bar)
+               : "memory");
+}
+
+// Arrival on a peer CTA's barrier without release semantics: for signalling
+// that values loaded earlier are no longer needed, when every one of those
+// loads has already been consumed by an instruction before the arrival (so
+// it has completed and the peer may overwrite the buffer).
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t remote_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
+}
+
+// Two floats to a bf16 pair with round-to-nearest-even: lo in bits 0-15.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
 }
@@ -211,6 +238,19 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
       "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// The same gather delivered to every CTA of the cluster named in cta_mask,
+// at the same shared-memory offset, each completing on its own barrier at
+// the offset of `bar`.
+__device__ __forceinline__ void tma_gather4_mc(uint32_t dst, const CUtensorMap* map, int x, int r0, int r1, int r2,
+                                               int r3, uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.multicast::cluster "
+      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar)),
+      "h"(cta_mask)
       : "memory");
 }
 
@@ -418,6 +458,16 @@ __device__ __forceinline__ void mma_bf16_ts_x4(uint32_t d_tmem, uint32_t a_tmem,
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], %10, %3, q;\n\t}"
       ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate), "r"(a_tmem + ta), "l"(b + db),
       "r"(a_tmem + 2 * ta), "l"(b + 2ull * db), "r"(a_tmem + 3 * ta), "l"(b + 3ull * db)
+      : "memory");
+}
+
+// One arrival on the barrier at the offset of `bar` in every CTA of
+// cta_mask once every tcgen05 op issued so far by this thread has completed.
+__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(cta_mask)
       : "memory");
 }
 

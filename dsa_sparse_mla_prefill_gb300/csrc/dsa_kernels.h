@@ -60,6 +60,8 @@ struct KeyMaskArgs {
 };
 
 struct GroupedArgs {
+  CUtensorMap tmap_kv;  // kv rows for tile::gather4 (box 64 columns x 1 row, 128B swizzle)
+  CUtensorMap tmap_q;   // q viewed [T*H, d_qk], box 64 columns x 128 rows
   const uint16_t* q;
   const uint16_t* kv;
   const int32_t* union_idx;

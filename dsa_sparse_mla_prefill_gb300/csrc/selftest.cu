@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(128, 1) selftest_mma_timing_kernel(int N, int 
     fence_mbar_init();
   }
   if (warp == 0) {
-    tmem_alloc(&tmem_slot, 256);
+    tmem_alloc(&tmem_slot, 512);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -165,6 +165,41 @@ __global__ void __launch_bounds__(128, 1) selftest_mma_timing_kernel(int N, int 
       out[0] = t1 - t0;
       out[1] = clock64() - t0;
     }
+  } else if (precomputed == 5 && warp > 0) {
+    // TMEM load traffic from warps 1-3 (columns 384..447 of their lane
+    // quarters) while warp 0 issues the MMAs below; a fixed count
+    float v[16];
+    float acc = 0.f;
+    for (int it = 0; it < reps; ++it) {
+      tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + 384 + (it & 3) * 16, v);
+      tmem_ld_wait();
+      acc += v[it & 15];
+    }
+    if (acc == 12345.f) out[1] = 0;  // keep the loads
+  } else if (precomputed == 6 && warp > 0) {
+    // warps 1-3 poll a barrier phase that does not complete (fixed count)
+    uint32_t hits = 0;
+    for (int it = 0; it < reps * 4; ++it) hits += mbar_try_wait(smem_u32(&bar), 0u) ? 0u : 1u;
+    if (hits == 0xffffffffu) out[1] = 0;
+  } else if (precomputed == 7 && warp > 0) {
+    // warps 1-3 store 16-byte pieces into the upper half of the A region
+    uint4* dst = reinterpret_cast<uint4*>(As) + 2048;
+    for (int it = 0; it < reps * 4; ++it) dst[(it * 96 + tid) & 1023] = make_uint4(it, it, it, it);
+  } else if ((precomputed >= 4 && precomputed <= 7) && tid == 0) {
+    // A from tensor memory (columns 256..383), four MMAs per asm statement
+    const uint32_t idesc = idesc_bf16_f32(128, N, false, false);
+    const uint64_t bd0 = sdesc_sw128(smem_u32(Bs), 16, 1024);
+    const long long t0 = clock64();
+    for (int r = 0; r < reps; r += 4) {
+      const int ch = (r >> 2) & 3;
+      const uint64_t bd = bd0 + (uint64_t)((ch * (N * 128)) >> 4);
+      mma_bf16_ts_x4(tmem, tmem + 256 + ch * 32, bd, 8u, 2u, idesc, r > 0 ? 1u : 0u);
+    }
+    const long long t1 = clock64();
+    mma_commit(&bar);
+    mbar_wait(&bar, 0, &abort_flag, status);
+    out[0] = t1 - t0;
+    out[1] = clock64() - t0;
   } else if (precomputed == 3 && tid == 0) {
     // four MMAs per asm statement, one predicate setup
     const uint32_t idesc = idesc_bf16_f32(128, N, false, false);
@@ -218,7 +253,7 @@ __global__ void __launch_bounds__(128, 1) selftest_mma_timing_kernel(int N, int 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 0) tmem_dealloc(tmem, 256);
+  if (warp == 0) tmem_dealloc(tmem, 512);
 }
 }  // namespace
 
@@ -276,6 +311,53 @@ extern "C" int dsa_selftest_gather4(const uint16_t* kv, int N, int ld, const int
   if (!dsa::make_row_gather_map(&map, kv, N, ld, ld)) return 2;
   const int smem = 128 * 128 + 1024;
   selftest_gather4_kernel<<<1, 128, smem, stream>>>(map, rows_dev, col, out, status);
+  return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
+
+// ---------------------------------------------------------------------------
+// Multicast gather4 into a 2-CTA cluster: CTA r gathers the 64 listed rows
+// 64r .. 64r+63 (columns col .. col+63) for both CTAs, so each CTA ends up
+// with all 128 rows; each copies its shared-memory image to out[rank].
+// ---------------------------------------------------------------------------
+namespace {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
+    selftest_gather4_mc_kernel(const __grid_constant__ CUtensorMap map, const int* rows, int col, uint16_t* out,
+                               unsigned int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* tile = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  const int tid = threadIdx.x;
+  const int rank = (int)cluster_ctarank();
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  cluster_sync();
+  if (tid == 0) {
+    mbar_arrive_expect_tx(&bar, 128 * 128);
+    for (int g = 16 * rank; g < 16 * rank + 16; ++g)
+      tma_gather4_mc(smem_u32(tile) + g * 512, &map, col, rows[4 * g], rows[4 * g + 1], rows[4 * g + 2],
+                     rows[4 * g + 3], &bar, (uint16_t)3);
+  }
+  const bool ok = mbar_wait(&bar, 0, &abort_flag, status);
+  if (ok)
+    for (int i = tid; i < 128 * 64; i += 128) out[rank * 128 * 64 + i] = reinterpret_cast<const uint16_t*>(tile)[i];
+  __syncthreads();
+  cluster_sync();
+}
+}  // namespace
+
+extern "C" int dsa_selftest_gather4_mc(const uint16_t* kv, int N, int ld, const int* rows_dev, int col,
+                                       uint16_t* out, unsigned int* status, cudaStream_t stream) {
+  if (N < 1 || ld < 64 || (ld & 7) || col < 0 || (col & 7) || col + 64 > ld) return 1;
+  CUtensorMap map;
+  if (!dsa::make_row_gather_map(&map, kv, N, ld, ld)) return 2;
+  const int smem = 128 * 128 + 1024;
+  selftest_gather4_mc_kernel<<<2, 128, smem, stream>>>(map, rows_dev, col, out, status);
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 

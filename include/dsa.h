@@ -134,7 +134,9 @@ int dsa_sparse_prefill(const uint16_t* q, const uint16_t* kv, int N, int ld_kv, 
  * q, kv, out, lse, d_qk, d_v, ld_kv as for dsa_sparse_prefill.
  * union_idx, union_len, mask, union_pad, G, cu_seqlens_q, num_req exactly as
  * produced by / passed to dsa_union_build.  H * G must equal 128 and
- * G <= 8 (the gate on the same page, review snippet).
+ * G <= 8 (the gate on the same page, review snippet).  scale must be
+ * positive and finite (the kernel takes the row max on unscaled scores);
+ * otherwise DSA_ERR_INVALID_ARG.
  * ---------------------------------------------------------------------- */
 int dsa_grouped_prefill(const uint16_t* q, const uint16_t* kv, int N, int ld_kv, const int32_t* union_idx,
                         const int32_t* union_len, const uint8_t* mask, int union_pad, int G,

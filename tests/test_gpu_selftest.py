@@ -79,3 +79,38 @@ def test_tma_gather4_swizzled_layout(selftest, col):
         for p in range(8):
             want = bits[src, col + 8 * p: col + 8 * p + 8] if 0 <= src < N else np.zeros(8, np.uint16)
             assert np.array_equal(img[r, p ^ (r & 7)], want), (r, p)
+
+
+@pytest.mark.gpu
+def test_tma_gather4_multicast_cluster(selftest):
+    """tile::gather4 with cluster multicast: each CTA of a 2-CTA cluster
+    issues half of the 128 row gathers for both; both CTAs end up with the
+    same 128B-swizzled image of all 128 rows (rows outside the table read as
+    zeros)."""
+    import dsa_sparse_mla_prefill_gb300 as dsa
+    lib = ctypes.CDLL(os.path.join(os.path.dirname(dsa.__file__), "libdsa_selftest.so"))
+    fn = lib.dsa_selftest_gather4_mc
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                   ctypes.c_void_p, ctypes.c_void_p]
+    N, ld, col = 900, 576, 512
+    g = torch.Generator().manual_seed(11)
+    kv = torch.randn(N, ld, generator=g).to(torch.bfloat16)
+    rows = torch.randint(0, N, (128,), generator=g, dtype=torch.int32)
+    rows[3] = -1
+    rows[100] = N
+    out = torch.zeros(2 * 128 * 64, dtype=torch.int16, device="cuda")
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    rc = fn(kv.cuda().data_ptr(), N, ld, rows.cuda().data_ptr(), col, out.data_ptr(), status.data_ptr(),
+            torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert int(status[1]) == 0
+    imgs = out.cpu().numpy().view(np.uint16).reshape(2, 128, 8, 8)
+    bits = kv.view(torch.int16).numpy().view(np.uint16)
+    for rank in range(2):
+        for r in range(128):
+            src = int(rows[r])
+            for p in range(8):
+                want = bits[src, col + 8 * p: col + 8 * p + 8] if 0 <= src < N else np.zeros(8, np.uint16)
+                assert np.array_equal(imgs[rank, r, p ^ (r & 7)], want), (rank, r, p)
