@@ -224,7 +224,7 @@ int dsa_grouped_prefill(const uint16_t* q, const uint16_t* kv, int N, int ld_kv,
   a.scale = scale;
   a.tr = g_trace;
   if (!dsa::make_row_gather_map(&a.tmap_kv, kv, N > 0 ? N : 1, ld_kv, ld_kv)) return DSA_ERR_CUDA;
-  if (!dsa::make_tile_map(&a.tmap_q, q, (int64_t)T * H, d_qk, d_qk, 128)) return DSA_ERR_CUDA;
+  if (!dsa::make_tile_map(&a.tmap_q, q, (int64_t)T * H, d_qk, d_qk, 64)) return DSA_ERR_CUDA;
   const int r = dsa::launch_grouped_prefill(a, d->num_sms, (cudaStream_t)stream);
   return r == 0 ? DSA_OK : (r == -2 ? DSA_ERR_UNSUPPORTED : DSA_ERR_CUDA);
 }

@@ -8,91 +8,129 @@
 // exactly its own top-k and the result equals the per-token form while each
 // union row is gathered once per group instead of once per token.
 //
-// One SM cannot hold it: q for 128 pseudo-heads is 147 KB and the 128 x 512
-// fp32 accumulator alone fills the 512 TMEM columns.  So a group is processed
-// by a cluster of two CTAs that split the latent columns:
-//   CTA 0 owns NoPE columns 0-255 (+ the 64 RoPE columns), CTA 1 owns NoPE
-//   columns 256-511.  Each gathers only its columns of every union row (no
-//   row is fetched twice), holds its q columns in tensor memory, computes a
-//   partial S_r = q_own . K_own^T (M = 128 pseudo-heads, N = 64 union slots,
-//   A read from TMEM) and keeps its half of O (128 x 256 fp32).
-// TMEM per CTA: O 256 columns, q 160 (bf16 pairs), S 64, P 32 = 512.
-// Per tile the two CTAs swap their partial scores once over distributed
-// shared memory (thread p sends row p, 256 bytes, with st.async counting the
-// bytes on the peer's barrier) and both add them in the same order, so both
-// hold the same full S and run the same online softmax (base 2, lazy
-// rescale) on all 128 rows: P, the running max and the running sum agree bit
-// for bit without further exchange.  Each CTA then issues O_own += P . V_own
-// with P (bf16) read from tensor memory (N = 256).  The softmax threads send
-// the scores of tile j+1 before finishing tile j, so the exchange latency
-// overlaps the softmax.
-// Warp roles per CTA (16 warps): warps 0-7 softmax, two threads per
-// pseudo-head: warp w holds TMEM lanes 32(w%4) .. +31 (pseudo-head p =
-// lane) and slots 32(w/4) .. +31 of each 64-slot tile; the two halves of a
-// row agree on the running max through a per-tile pair exchange (in the
-// already consumed half of the row's SX buffer).  They also load q per group into TMEM.  Warp 8 issues QK, warp 9
-// issues PV, warps 10-15 issue the TMA row gathers (tile::gather4, 4 rows x
-// 128 bytes each) into a 4-stage ring.  Warps 0-7 run at 168 registers, the
-// others at 88.
+// A group is processed by a cluster of two CTAs that split the pseudo-heads:
+// CTA r owns pseudo-heads 64r .. 64r+63 (its q rows: 64 x D_QK in shared
+// memory) and the matching 64 columns of the output.  Every union row is
+// fetched once per cluster: each CTA issues the tile::gather4 loads for half
+// of a tile's rows with cluster multicast, so both CTAs receive the whole
+// tile, and a stage is refilled only after both CTAs' MMAs released it
+// (tcgen05.commit multicast to both CTAs' barriers).  No scores cross the
+// cluster.  Within a CTA the data path is the per-token one with 64 heads:
+//   S^T = K q^T with the union slots on the M side (M = 128 slots, N = 64),
+//   streamed chunk by chunk (128 slots x 64 columns) through a K ring;
+//   O^T += V^T P^T per 128-column V unit (V re-gathered into a V ring, an L2
+//   hit), O^T = 4 x 64 TMEM columns, P^T double-buffered in shared memory;
+//   the online softmax (base 2, lazy rescale) runs with thread i <-> slot i
+//   (TMEM lane i) in eight warps, two per lane quarter, each holding 32 of
+//   the 64 pseudo-heads.
+// Warp roles (24 warps): 0-7 softmax (at REGS_SOFTMAX registers, the others
+// at REGS_OTHER), 8 QK issuer, 9 and 10 PV issuers (units 0/2 and 1/3),
+// 12-17 K-ring producers (two warps per K slot; warp 12 also loads q),
+// 18-23 V-ring producers (three warps per V slot); warp 11 is idle.
 #include "dsa_device.cuh"
 #include "dsa_kernels.h"
 
 namespace dsa {
 namespace grouped {
 
-constexpr int BK = 64;          // union slots per tile (the MMA's N for S)
-constexpr int NTHREADS = 512;   // 16 warps, launched at 128 registers each
-constexpr int REGS_SOFTMAX = 168;
-constexpr int REGS_OTHER = 88;  // 8*32*168 + 8*32*88 = 512*128
-constexpr int NSTAGE = 4;       // gather ring depth
-constexpr int NPROD_WARPS = 6;
-constexpr float kTau = 8.0f;    // lazy-rescale threshold (log2 units)
+constexpr int BK = 128;          // union slots per tile (the MMA's M)
+constexpr int HC = 64;           // pseudo-heads per CTA (the MMA's N)
+constexpr int HW = 32;           // pseudo-heads per softmax warp
+constexpr int NTHREADS = 768;    // 24 warps, launched at 80 registers each
+constexpr int REGS_SOFTMAX = 152;
+constexpr int REGS_OTHER = 40;   // 8*32*152 + 16*32*40 <= 768*80
+constexpr int NKR = 3;           // K ring slots (one producer warp each)
+constexpr int NVR = 2;           // V ring slots: unit m in slot m mod 2, PV issuer m mod 2
+constexpr uint16_t kPair = 3;    // multicast mask: both CTAs of the cluster
+constexpr float kTau = 8.0f;     // lazy-rescale threshold (log2 units)
 
 template <int NC>
 struct Cfg {
-  static constexpr int OWN0 = (NC == 9) ? 5 : 4;   // swizzle columns held by rank 0
-  static constexpr int OWNMAX = OWN0;
-  static constexpr uint32_t KV_CHUNK = BK * 128u;            // 64 keys x 64 cols
-  static constexpr uint32_t KV_BYTES = OWNMAX * KV_CHUNK;
-  static constexpr uint32_t SX_BYTES = 128u * BK * 4u;       // 128 rows x 64 fp32 (the peer's partial S)
-  static constexpr uint32_t OFF_KV = 0;                      // [NSTAGE]
-  static constexpr uint32_t OFF_SX = OFF_KV + NSTAGE * KV_BYTES;  // [2]
-  static constexpr uint32_t OFF_MASKB = OFF_SX + 2 * SX_BYTES;    // [NSTAGE][64] bytes
-  static constexpr uint32_t OFF_BAR = OFF_MASKB + NSTAGE * 64u;
-  static constexpr int NBAR = 24;
+  static constexpr uint32_t CHUNK_BYTES = BK * 128u;          // 128 slots x 64 columns
+  static constexpr uint32_t UNIT_BYTES = 2u * CHUNK_BYTES;    // 128 slots x 128 columns
+  static constexpr uint32_t Q_CHUNK = HC * 128u;              // 64 rows x 64 columns
+  static constexpr uint32_t Q_BYTES = NC * Q_CHUNK;
+  static constexpr uint32_t P_BYTES = 2u * HC * 128u;         // 128 slots = 2 swizzle columns (x2 buffers)
+  static constexpr uint32_t RED_BYTES = 2u * 2u * 4u * HW * 4u;  // [parity][half][warp][head]
+  static constexpr uint32_t OFF_KR = 0;
+  static constexpr uint32_t OFF_VR = OFF_KR + NKR * CHUNK_BYTES;
+  static constexpr uint32_t OFF_Q = OFF_VR + NVR * UNIT_BYTES;
+  static constexpr uint32_t OFF_P = OFF_Q + Q_BYTES;
+  static constexpr uint32_t OFF_RED = OFF_P + 2 * P_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_RED + RED_BYTES;
+  static constexpr int NBAR = 32;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8u;
-  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64u + 1024u;
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 128u + 1024u;
   static_assert(SMEM_BYTES <= 227u * 1024u, "shared memory budget");
-  static constexpr uint32_t COL_O = 0;       // 256 columns
-  static constexpr uint32_t COL_Q = 256;     // OWNMAX * 32 columns (bf16 pairs)
-  static constexpr uint32_t COL_S = 416;     // 64 columns
-  static constexpr uint32_t COL_P = 480;     // 32 columns (bf16 pairs)
+  static constexpr uint32_t COL_O = 0;       // O^T: 4 units x 64 columns
+  static constexpr uint32_t COL_S = 256;     // S^T: 2 x 64 columns
   static constexpr uint32_t TMEM_COLS = 512;
 };
 
 enum {
-  B_Q_FULL = 0,      // q of the group in TMEM (256 arrivals)
-  B_KV_FULL = 1,     // [NSTAGE] union rows + mask bytes of the stage landed
-  B_KV_EMPTY = 5,    // [NSTAGE] P.V of the stage's tile completed
-  B_S_FULL = 9,      // partial S in TMEM
-  B_S_EMPTY = 10,    // the softmax threads read S
-  B_SX_FULL = 11,    // [2] the peer's partial S landed in my SX buffer (byte count)
-  B_SX_FREE = 13,    // [2] the peer read what I wrote into its SX buffer
-  B_P_FULL = 15,     // P rows in TMEM (and any O rescale done)
-  B_PV_DONE = 16,    // P.V completed (P columns free, O up to date)
-  B_O_EMPTY = 17,
-  B_DRAIN = 18,      // [2] one per MMA issuer
-  B_PAIR = 20,       // [4] the two softmax warps of a TMEM lane quarter (64 arrivals)
+  B_Q_FULL = 0,
+  B_Q_EMPTY = 1,
+  B_S_FULL = 2,      // [2]
+  B_S_EMPTY = 4,     // [2]
+  B_P_FULL = 6,      // [2] 256 arrivals (softmax threads)
+  B_P_EMPTY = 8,     // [2] one commit per PV issuer
+  B_O_FULL = 10,     // one commit per PV issuer
+  B_O_EMPTY = 11,    // 256 arrivals
+  B_DRAIN = 12,      // [3] one per MMA issuer
+  B_SMX_SYNC = 15,   // [2] one per head half (4 warps)
+  B_KR_FULL = 17,    // [NKR <= 4]
+  B_KR_EMPTY = 21,   // [NKR <= 4] one QK commit from each CTA
+  B_VR_FULL = 25,    // [NVR]
+  B_VR_EMPTY = 27,   // [NVR] one PV commit from each CTA
 };
-
-// latent swizzle column held at position c by CTA `rank`
-__device__ __forceinline__ int latent_chunk(int rank, int c) { return rank == 0 ? (c < 4 ? c : 8) : 4 + c; }
 
 __device__ __forceinline__ void group_of(const ReqTable& rq, int G, int g, int& t0, int& n) {
   int r = 0;
   while (r + 1 < rq.num_req && rq.cu_g[r + 1] <= g) ++r;
   t0 = rq.cu_q[r] + (g - rq.cu_g[r]) * G;
   n = min(G, rq.cu_q[r + 1] - t0);
+}
+
+// The four union slots 4rg .. 4rg+3 of tile j (row indices; -1 past the
+// union or out of range, which TMA reads as zeros).  Nothing at or past U is
+// read: a tile may run past the padded row.
+__device__ __forceinline__ int4 union_rows4(const int32_t* urow, int U, int N, int u) {
+  int4 r = make_int4(-1, -1, -1, -1);
+  if (u + 3 < U) {
+    r = __ldg(reinterpret_cast<const int4*>(urow + u));
+  } else {
+    if (u + 0 < U) r.x = __ldg(urow + u + 0);
+    if (u + 1 < U) r.y = __ldg(urow + u + 1);
+    if (u + 2 < U) r.z = __ldg(urow + u + 2);
+  }
+  if (r.x < 0 || r.x >= N) r.x = -1;
+  if (r.y < 0 || r.y >= N) r.y = -1;
+  if (r.z < 0 || r.z >= N) r.z = -1;
+  if (r.w < 0 || r.w >= N) r.w = -1;
+  return r;
+}
+
+// Warp-level transposed max/sum reduction over 32 lanes for 32 values per
+// lane: afterwards lane L holds the reduction over the warp of value L.
+template <bool IS_MAX>
+__device__ __forceinline__ float warp_transpose_reduce32(float* v) {
+  const uint32_t lane = lane_id();
+  auto op = [](float a, float b) { return IS_MAX ? fmaxf(a, b) : a + b; };
+  int n = 32;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    n >>= 1;
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i < n) {
+        const float send = upper ? v[i] : v[i + n];
+        const float keep = upper ? v[i + n] : v[i];
+        v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, o));
+      }
+    }
+  }
+  return v[0];
 }
 
 template <int NC>
@@ -107,34 +145,39 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile uint32_t* tmem_base_ptr = misc;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+  float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
   unsigned int* err = a.err;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int rank = (int)cluster_ctarank();
-  const int peer = rank ^ 1;
-  const int nown = (rank == 0) ? C::OWN0 : 4;
   const int H = a.H;
   const int G = a.G;
   const int cid = (int)cluster_id_x();
   const int ncl = (int)nclusters_x();
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars[B_Q_FULL], 256);
-    for (int i = 0; i < NSTAGE; ++i) {
-      mbar_init(&bars[B_KV_FULL + i], 1);
-      mbar_init(&bars[B_KV_EMPTY + i], 1);
-    }
-    mbar_init(&bars[B_S_FULL], 1);
-    mbar_init(&bars[B_S_EMPTY], 256);
+    mbar_init(&bars[B_Q_FULL], 1);
+    mbar_init(&bars[B_Q_EMPTY], 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars[B_SX_FULL + i], 1);
-      mbar_init(&bars[B_SX_FREE + i], 256);
-      mbar_init(&bars[B_DRAIN + i], 1);
+      mbar_init(&bars[B_S_FULL + i], 1);
+      mbar_init(&bars[B_S_EMPTY + i], 256);
+      mbar_init(&bars[B_SMX_SYNC + i], 128);
     }
-    mbar_init(&bars[B_P_FULL], 256);
-    mbar_init(&bars[B_PV_DONE], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars[B_P_FULL + i], 256);
+      mbar_init(&bars[B_P_EMPTY + i], 2);
+    }
+    mbar_init(&bars[B_O_FULL], 2);
     mbar_init(&bars[B_O_EMPTY], 256);
-    for (int i = 0; i < 4; ++i) mbar_init(&bars[B_PAIR + i], 64);
+    for (int i = 0; i < 3; ++i) mbar_init(&bars[B_DRAIN + i], 1);
+    for (int i = 0; i < NKR; ++i) {
+      mbar_init(&bars[B_KR_FULL + i], 1);
+      mbar_init(&bars[B_KR_EMPTY + i], 2);
+    }
+    for (int i = 0; i < NVR; ++i) {
+      mbar_init(&bars[B_VR_FULL + i], 1);
+      mbar_init(&bars[B_VR_EMPTY + i], 2);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -144,98 +187,110 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // the peer's barriers exist before anyone arrives on them
+  cluster_sync();  // the peer's barriers exist before any copy or commit reaches them
   tc_fence_after();
   const uint32_t tmem = *tmem_base_ptr;
 
   if (warp >= 8) {
     regs_dec<REGS_OTHER>();
-    if (warp >= 10) {
+    if (warp >= 12) {
       // ----------------------------------------------------------------
-      // TMA producers (warps 10-15, lanes 0-7 issue: 48 issuers).  A tile's
-      // 16 * nown gather4 (rows 4g .. 4g+3 of own swizzle column c) are
-      // dealt to the issuers, rotating from tile to tile so each gets the
-      // same share; warp 10 also stores the tile's mask bytes.  Warp 10 lane 0
-      // (the leader) arms each stage's byte count after the mask bytes are
-      // stored; copies from the other issuers may complete first, which
-      // only drives the transaction count negative until then.
+      // TMA producers.  K stream (warps 12-17): the two warps 12+s and 15+s
+      // fill K slot s with chunk c (slots x columns 64c .. 64c+63) of a
+      // tile, lanes 0-7 of each gathering half of this CTA's 16 row groups
+      // (slots 64 rank .. +63) for both CTAs.  V stream (warps 18-23): the
+      // three warps of group u fill V slot u with the 128-column units
+      // m = u, u+2 of every tile, sharing this CTA's 32 gathers of a unit.
+      // A stage's leader (lane 0 of the first warp of the slot) arms the
+      // full byte count of the stage: both CTAs' halves land in both.  Warp
+      // 12 also loads q.  Every warp of a slot passes through each of its
+      // phases in order.
       // ----------------------------------------------------------------
-      constexpr int NI = NPROD_WARPS * 8;
-      const int pw = warp - 10;
-      const int iss = pw * 8 + lane;
-      const bool issuer = lane < 8;
-      const bool leader = (pw == 0) && (lane == 0);
-      const int ng = 16 * nown;
-      uint32_t gt = 0;
+      const bool kstream = warp < 18;
+      const int ks = (warp - 12) % NKR;         // K slot owned
+      const int ksub = (warp - 12) / NKR;
+      const int vg = (warp - 18) / 3;           // V slot owned
+      const int vsub = (warp - 18) % 3;
+      const int e = vsub * 11 + lane;           // V gather index 0..31 of this CTA
+      const bool issuer = kstream ? (lane < 8) : (lane < 11 && e < 32);
+      const int rg = 16 * rank + (kstream ? 8 * ksub + (lane & 7) : (e & 15));   // row group of the tile
+      const int vcc = (e >> 4) & 1;             // V swizzle column
+      const bool leader = (lane == 0) && (kstream ? ksub == 0 : vsub == 0);
+      const uint32_t q_s = sbase + C::OFF_Q;
+      uint32_t gt = 0, pos = 0, lgq = 0;
+      int64_t last_armed = -1;
       bool ok = true;
       for (int g = cid; g < a.num_groups && ok; g += ncl) {
+        int t0, n;
+        group_of(a.req, G, g, t0, n);
         const int U = min(__ldg(a.union_len + g), a.union_pad);
         const int ntiles = (U + BK - 1) / BK;
         if (ntiles == 0) continue;
-        const int32_t* urow = a.union_idx + (size_t)g * a.union_pad;
-        const uint8_t* mrow = a.mask + (size_t)g * a.union_pad;
-        for (int j = 0; j < ntiles && ok; ++j, ++gt) {
-          const int s = gt % NSTAGE;
-          if (!mbar_wait_warp(&bars[B_KV_EMPTY + s], ((gt / NSTAGE) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
-          if (leader) DSA_TRACE(a.tr, gt, 0);
-          if (pw == 0) {
-            if (lane < 16) {
-              // mask bytes of union slots j*64 .. j*64+63 (zero past the union)
-              const int u0 = j * BK + 4 * lane;
-              uint32_t w = 0;
-              if (u0 + 3 < U) {
-                w = __ldg(reinterpret_cast<const uint32_t*>(mrow + u0));
-              } else {
-                for (int e = 0; e < 4; ++e)
-                  if (u0 + e < U) w |= (uint32_t)__ldg(mrow + u0 + e) << (8 * e);
-              }
-              *reinterpret_cast<uint32_t*>(smem + C::OFF_MASKB + s * 64 + 4 * lane) = w;
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive_expect_tx(&bars[B_KV_FULL + s], (uint32_t)nown * C::KV_CHUNK);
+        if (warp == 12) {
+          // q rows t0*H + 64 rank .. +63 of q viewed [T*H, D_QK], one box per swizzle column
+          if (!mbar_wait_warp(&bars[B_Q_EMPTY], (lgq & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&bars[B_Q_FULL], C::Q_BYTES);
+            for (int c = 0; c < NC; ++c)
+              tma_load_2d(q_s + c * C::Q_CHUNK, &a.tmap_q, c * 64, t0 * H + HC * rank, &bars[B_Q_FULL]);
           }
-          if (issuer) {
-            const uint32_t kvs = sbase + C::OFF_KV + s * C::KV_BYTES;
-            const int b = (int)((iss + gt * (uint32_t)(ng % NI)) % NI);
-            for (int e = b; e < ng; e += NI) {
-              const int rg = e & 15;
-              const int c = e >> 4;
-              // union rows of the row group; nothing at or past U is read
-              // (a tile may run past the padded row)
-              const int u = j * BK + 4 * rg;
-              int4 r = make_int4(-1, -1, -1, -1);
-              if (u + 3 < U) {
-                r = __ldg(reinterpret_cast<const int4*>(urow + u));
-              } else {
-                if (u + 0 < U) r.x = __ldg(urow + u + 0);
-                if (u + 1 < U) r.y = __ldg(urow + u + 1);
-                if (u + 2 < U) r.z = __ldg(urow + u + 2);
+        }
+        const int32_t* urow = a.union_idx + (size_t)g * a.union_pad;
+        for (int j = 0; j < ntiles && ok; ++j, ++gt) {
+          if (warp == 12 && lane == 0) DSA_TRACE(a.tr, gt, 0);
+          const int4 r = union_rows4(urow, U, a.N, j * BK + 4 * rg);
+          if (kstream) {
+            for (int c = 0; c < NC; ++c, ++pos) {
+              if ((int)(pos % NKR) != ks) continue;
+              if (!mbar_wait_warp(&bars[B_KR_EMPTY + ks], ((pos / NKR) & 1) ^ 1, abort_flag, err)) {
+                ok = false;
+                break;
               }
-              if (r.x < 0 || r.x >= a.N) r.x = -1;
-              if (r.y < 0 || r.y >= a.N) r.y = -1;
-              if (r.z < 0 || r.z >= a.N) r.z = -1;
-              if (r.w < 0 || r.w >= a.N) r.w = -1;
-              tma_gather4(kvs + c * C::KV_CHUNK + rg * 512, &a.tmap_kv, latent_chunk(rank, c) * 64, r.x, r.y, r.z,
-                          r.w, &bars[B_KV_FULL + s]);
+              if (leader) mbar_arrive_expect_tx(&bars[B_KR_FULL + ks], C::CHUNK_BYTES);
+              if (issuer)
+                tma_gather4_mc(sbase + C::OFF_KR + ks * C::CHUNK_BYTES + rg * 512, &a.tmap_kv, c * 64, r.x, r.y, r.z,
+                               r.w, &bars[B_KR_FULL + ks], kPair);
+              last_armed = pos;
+            }
+          } else {
+            for (int m = 0; m < 4; ++m, ++pos) {
+              if ((int)(pos % NVR) != vg) continue;
+              if (!mbar_wait_warp(&bars[B_VR_EMPTY + vg], ((pos / NVR) & 1) ^ 1, abort_flag, err)) {
+                ok = false;
+                break;
+              }
+              if (leader) mbar_arrive_expect_tx(&bars[B_VR_FULL + vg], C::UNIT_BYTES);
+              if (issuer)
+                tma_gather4_mc(sbase + C::OFF_VR + vg * C::UNIT_BYTES + vcc * C::CHUNK_BYTES + rg * 512, &a.tmap_kv,
+                               (2 * m + vcc) * 64, r.x, r.y, r.z, r.w, &bars[B_VR_FULL + vg], kPair);
+              last_armed = pos;
             }
           }
         }
+        ++lgq;
       }
-      // Let copies still in flight land before the CTA can exit: wait for
-      // the last phase each stage was used in (an older phase's parity can
-      // alias).
+      // Let copies still in flight land before the CTA can exit: the last
+      // phase of the slot this warp arms completes only once both CTAs'
+      // bytes have landed here.
       if (leader) {
-        for (uint32_t i = (gt > NSTAGE ? gt - NSTAGE : 0); i < gt; ++i)
-          mbar_wait_drain(&bars[B_KV_FULL + (i % NSTAGE)], (i / NSTAGE) & 1);
+        if (warp == 12 && lgq > 0) mbar_wait_drain(&bars[B_Q_FULL], (lgq - 1) & 1);
+        if (last_armed >= 0) {
+          if (kstream)
+            mbar_wait_drain(&bars[B_KR_FULL + ks], (uint32_t)(last_armed / NKR) & 1);
+          else
+            mbar_wait_drain(&bars[B_VR_FULL + vg], (uint32_t)(last_armed / NVR) & 1);
+        }
       }
       __syncwarp();
     } else if (warp == 8) {
       // ----------------------------------------------------------------
-      // QK issuer: partial S = q_own . K_own^T, q (A) from TMEM
+      // QK issuer: S^T = K q^T chunk by chunk into the S double buffer; each
+      // K chunk is released to both CTAs' producers once its MMAs complete
       // ----------------------------------------------------------------
       if (lane == 0) {
-        constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, BK, false, false);
-        uint32_t gt = 0, lgq = 0;
+        constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, HC, false, false);
+        const uint32_t q_s = sbase + C::OFF_Q;
+        uint32_t gt = 0, kpos = 0, lgq = 0;
         bool ok = true;
         for (int g = cid; g < a.num_groups && ok; g += ncl) {
           const int U = min(__ldg(a.union_len + g), a.union_pad);
@@ -244,18 +299,23 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
           if (!mbar_wait(&bars[B_Q_FULL], lgq & 1, abort_flag, err)) { ok = false; break; }
           tc_fence_after();
           for (int j = 0; j < ntiles && ok; ++j, ++gt) {
-            const int s = gt % NSTAGE;
-            if (!mbar_wait(&bars[B_S_EMPTY], (gt & 1) ^ 1, abort_flag, err)) { ok = false; break; }
-            if (!mbar_wait(&bars[B_KV_FULL + s], (gt / NSTAGE) & 1, abort_flag, err)) { ok = false; break; }
+            const int sb = gt & 1;
+            const uint32_t d_s = tmem + C::COL_S + sb * HC;
+            if (!mbar_wait(&bars[B_S_EMPTY + sb], ((gt >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
             DSA_TRACE(a.tr, gt, 2);
             tc_fence_after();
-            const uint32_t kvs = sbase + C::OFF_KV + s * C::KV_BYTES;
-            // per swizzle column: 4 MMAs of K = 16, A advances 8 TMEM columns, B 32 bytes
-            for (int c = 0; c < nown; ++c)
-              mma_bf16_ts_x4(tmem + C::COL_S, tmem + C::COL_Q + 32 * c, sdesc_sw128(kvs + c * C::KV_CHUNK, 16, 1024),
-                             8u, 2u, IDESC_QK, c > 0 ? 1u : 0u);
-            mma_commit(&bars[B_S_FULL]);
+            for (int c = 0; c < NC; ++c, ++kpos) {
+              const uint32_t slot = kpos % NKR;
+              if (!mbar_wait(&bars[B_KR_FULL + slot], (kpos / NKR) & 1, abort_flag, err)) { ok = false; break; }
+              tc_fence_after();
+              mma_bf16_ss_x4(d_s, sdesc_sw128(sbase + C::OFF_KR + slot * C::CHUNK_BYTES, 16, 1024),
+                             sdesc_sw128(q_s + c * C::Q_CHUNK, 16, 1024), 2u, 2u, IDESC_QK, c > 0 ? 1u : 0u);
+              mma_commit_mc(&bars[B_KR_EMPTY + slot], kPair);
+            }
+            if (!ok) break;
             DSA_TRACE(a.tr, gt, 1);
+            mma_commit(&bars[B_S_FULL + sb]);
+            if (j == ntiles - 1) mma_commit(&bars[B_Q_EMPTY]);
           }
           ++lgq;
         }
@@ -263,12 +323,16 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
         mbar_wait(&bars[B_DRAIN + 0], 0, abort_flag, err);
       }
       __syncwarp();
-    } else if (warp == 9) {
+    } else if (warp == 9 || warp == 10) {
       // ----------------------------------------------------------------
-      // PV issuer: O_own += P . V_own, P (bf16) read from tensor memory
+      // PV issuers: O^T += V^T P^T, warp 9 for units 0 and 2, warp 10 for
+      // units 1 and 3 (V slot = unit mod 2); each unit released to both
+      // CTAs' producers once its MMAs complete
       // ----------------------------------------------------------------
+      const int pvi = warp - 9;
       if (lane == 0) {
-        constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 256, false, true);
+        constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, HC, true, false);
+        const uint32_t p_base = sbase + C::OFF_P;
         uint32_t gt = 0, lgq = 0;
         bool ok = true;
         for (int g = cid; g < a.num_groups && ok; g += ncl) {
@@ -276,256 +340,211 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
           const int ntiles = (U + BK - 1) / BK;
           if (ntiles == 0) continue;
           for (int j = 0; j < ntiles && ok; ++j, ++gt) {
-            const int s = gt % NSTAGE;
-            if (!mbar_wait(&bars[B_P_FULL], gt & 1, abort_flag, err)) { ok = false; break; }
-            if (j == 0 && !mbar_wait(&bars[B_O_EMPTY], (lgq & 1) ^ 1, abort_flag, err)) { ok = false; break; }
-            DSA_TRACE(a.tr, gt, 6);
+            const int pb = gt & 1;
+            if (!mbar_wait(&bars[B_P_FULL + pb], (gt >> 1) & 1, abort_flag, err)) { ok = false; break; }
+            if (pvi == 0) DSA_TRACE(a.tr, gt, 7);
             tc_fence_after();
-            // 64 union slots = 4 MMAs of 16: P advances 8 TMEM columns, V (MN-major) 2048 B
-            const uint32_t kvs = sbase + C::OFF_KV + s * C::KV_BYTES;
-            mma_bf16_ts_x4(tmem + C::COL_O, tmem + C::COL_P, sdesc_sw128(kvs, C::KV_CHUNK, 1024), 8u, 128u, IDESC_PV,
-                           j > 0 ? 1u : 0u);
-            mma_commit(&bars[B_PV_DONE]);
-            mma_commit(&bars[B_KV_EMPTY + s]);
+            if (j == 0) {
+              if (!mbar_wait(&bars[B_O_EMPTY], (lgq & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+              tc_fence_after();
+            }
+            for (int m = pvi; m < 4 && ok; m += 2) {
+              const uint32_t vp = gt * 4 + m;
+              if (!mbar_wait(&bars[B_VR_FULL + pvi], (vp / NVR) & 1, abort_flag, err)) { ok = false; break; }
+              tc_fence_after();
+              const uint32_t ubase = sbase + C::OFF_VR + pvi * C::UNIT_BYTES;
+              const uint32_t d_o = tmem + C::COL_O + m * HC;
+#pragma unroll
+              for (int hf = 0; hf < 2; ++hf) {
+                // 16 slots (2048 B of V^T, MN-major; the unit's two swizzle
+                // columns CHUNK_BYTES apart) per MMA; P^T one 64-slot
+                // swizzle column per half
+                const uint64_t adesc = sdesc_sw128(ubase + hf * 4 * 2048, C::CHUNK_BYTES, 1024);
+                const uint64_t bdesc = sdesc_sw128(p_base + pb * C::P_BYTES + hf * (HC * 128), 16, 1024);
+                mma_bf16_ss_x4(d_o, adesc, bdesc, 128u, 2u, IDESC_PV, (j > 0 || hf > 0) ? 1u : 0u);
+              }
+              mma_commit_mc(&bars[B_VR_EMPTY + pvi], kPair);
+            }
+            if (!ok) break;
+            mma_commit(&bars[B_P_EMPTY + pb]);
+            if (j == ntiles - 1) mma_commit(&bars[B_O_FULL]);
           }
           ++lgq;
         }
-        mma_commit(&bars[B_DRAIN + 1]);
-        mbar_wait(&bars[B_DRAIN + 1], 0, abort_flag, err);
+        mma_commit(&bars[B_DRAIN + 1 + pvi]);
+        mbar_wait(&bars[B_DRAIN + 1 + pvi], 0, abort_flag, err);
       }
       __syncwarp();
     }
   } else {
     regs_inc<REGS_SOFTMAX>();
     // ------------------------------------------------------------------
-    // softmax warps: thread (row, half) <-> pseudo-head row = TMEM lane,
-    // slots 32*half .. 32*half+31 of each tile
+    // softmax + epilogue: thread (key i = TMEM lane i, head half hh) holds
+    // the 32 local pseudo-heads 32hh .. 32hh+31 of union slot i of the tile.
+    // The running max and sum are per head and the same for every thread,
+    // so lane L keeps them for head L only and shuffles them out.
     // ------------------------------------------------------------------
-    constexpr int HK = BK / 2;               // slots per thread
-    const int half = warp >> 2;
-    const int row = (warp & 3) * 32 + lane;
+    const int hh = warp >> 2;
+    const int key = (warp & 3) * 32 + lane;  // 0..127
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const float sl2 = a.scale * 1.4426950408889634f;
-    const int tok = row / H;  // token of the group this pseudo-head belongs to
-    // my row of the SX buffers: 16-byte pieces XOR-swizzled by row; this
-    // thread moves pieces 8*half .. 8*half+7
-    const uint32_t sx_row = C::OFF_SX + row * (BK * 4);
-    const uint32_t sx_peer = map_peer(sbase + sx_row, peer);
-    const uint32_t bar_base = smem_u32(bars);
-    auto peer_bar = [&](int idx) { return map_peer(bar_base + idx * 8, peer); };
-    auto piece = [&](int c) { return (uint32_t)(((8 * half + c) ^ (row & 15)) << 4); };
-    uint64_t* pair_bar = &bars[B_PAIR + (warp & 3)];
-    uint32_t pair_phase = 0;
-    uint32_t gt = 0, lgq = 0;
+    const float scale_log2 = a.scale * 1.4426950408889634f;
+    uint64_t* smx = &bars[B_SMX_SYNC + hh];
+    // token of local pseudo-head h: t_lo for h < split, t_lo + 1 after
+    const int base = HC * rank + HW * hh;
+    const int t_lo = base / H;
+    const int split = (t_lo + 1) * H - base;
+    uint32_t gt = 0, lgq = 0, sync_phase = 0;
     bool ok = true;
-
-    // Step A of tile i: this thread's half of the partial S row from TMEM,
-    // S freed for the next QK, the half sent to the peer once it has read
-    // what we sent two tiles ago.
-    auto step_a = [&](uint32_t i, float* v) -> bool {
-      if (!mbar_wait_warp(&bars[B_S_FULL], i & 1, abort_flag, err)) return false;
-      if (row == 0 && half == 0) DSA_TRACE(a.tr, i, 3);
-      tc_fence_after();
-      tmem_ld16(tmem + lane_off + C::COL_S + HK * half, v);
-      tmem_ld16(tmem + lane_off + C::COL_S + HK * half + 16, v + 16);
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(&bars[B_S_EMPTY]);
-      const int sb = i & 1;
-      if (!mbar_wait_cluster_warp(&bars[B_SX_FREE + sb], ((i >> 1) & 1) ^ 1, abort_flag, err)) return false;
-      // (my own receive buffer for tile i: armed after tile i-2's completed)
-      if (threadIdx.x == 0) mbar_arrive_expect_tx(&bars[B_SX_FULL + sb], C::SX_BYTES);
-      const uint32_t dst = sx_peer + sb * C::SX_BYTES;
-      const uint32_t rbar = peer_bar(B_SX_FULL + sb);
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        st_async_v4(dst + piece(c), __float_as_uint(v[4 * c]), __float_as_uint(v[4 * c + 1]),
-                    __float_as_uint(v[4 * c + 2]), __float_as_uint(v[4 * c + 3]), rbar);
-      if (row == 0 && half == 0) DSA_TRACE(a.tr, i, 7);
-      return true;
-    };
-
-    // Step B of tile i (j-th of its group): add the peer's partial half row,
-    // mask, agree on the running max with the other half, P (bf16 pairs)
-    // into TMEM.
-    // For the last tile of a group the SX_FREE arrival is left to the
-    // epilogue, which still uses the buffer to add the two halves' row sums.
-    auto step_b = [&](uint32_t i, int j, bool last, float* v, float& m_run, float& l_run) -> bool {
-      const int sb = i & 1;
-      if (!mbar_wait_cluster_warp(&bars[B_SX_FULL + sb], (i >> 1) & 1, abort_flag, err)) return false;
-      if (row == 0 && half == 0) DSA_TRACE(a.tr, i, 4);
-      uint8_t* sxr = smem + sx_row + sb * C::SX_BYTES;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const float4 x = *reinterpret_cast<const float4*>(sxr + piece(c));
-        // S = S_0 + S_1 with the operands in rank order on both CTAs
-        if (rank == 0) {
-          v[4 * c] = v[4 * c] + x.x;
-          v[4 * c + 1] = v[4 * c + 1] + x.y;
-          v[4 * c + 2] = v[4 * c + 2] + x.z;
-          v[4 * c + 3] = v[4 * c + 3] + x.w;
-        } else {
-          v[4 * c] = x.x + v[4 * c];
-          v[4 * c + 1] = x.y + v[4 * c + 1];
-          v[4 * c + 2] = x.z + v[4 * c + 2];
-          v[4 * c + 3] = x.w + v[4 * c + 3];
-        }
-      }
-      // the stage's mask bytes (its phase cannot have moved on: the stage is
-      // released only after this tile's P.V); raw scores are kept, masked
-      // slots become -inf, the scale is applied in the exponent
-      const int s = i % NSTAGE;
-      if (!mbar_wait_warp(&bars[B_KV_FULL + s], (i / NSTAGE) & 1, abort_flag, err)) return false;
-      float hmax = -INFINITY;
-      {
-        const uint4* mb4 = reinterpret_cast<const uint4*>(smem + C::OFF_MASKB + s * 64 + HK * half);
-#pragma unroll
-        for (int q4 = 0; q4 < 2; ++q4) {
-          const uint4 m4 = mb4[q4];
-          const uint32_t mw[4] = {m4.x, m4.y, m4.z, m4.w};
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int c = 16 * q4 + 4 * w + e;
-              const bool on = (mw[w] >> (8 * e + tok)) & 1u;
-              v[c] = on ? v[c] : -INFINITY;
-              hmax = fmaxf(hmax, v[c]);
-            }
-          }
-        }
-      }
-      // the other half's max, through a fixed slot of the consumed half of
-      // my SX row (the peer may refill the row only after both halves
-      // arrived below)
-      reinterpret_cast<volatile float*>(sxr + piece(0))[0] = hmax;
-      if (!group_sync(pair_bar, pair_phase, abort_flag, err)) return false;
-      const float omax = reinterpret_cast<volatile float*>(smem + sx_row + sb * C::SX_BYTES +
-                                                           ((((8 * (half ^ 1)) ^ (row & 15))) << 4))[0];
-      // (every loaded value was consumed above, so the loads have completed)
-      const float tmax = (half == 0 ? fmaxf(hmax, omax) : fmaxf(omax, hmax)) * sl2;
-      if (!last) mbar_arrive_remote_relaxed(peer_bar(B_SX_FREE + sb));
-      // lazy rescale: move the reference only when the max grows by more than kTau
-      const bool need = tmax > m_run + kTau;
-      float alpha = 1.f;
-      if (need) {
-        const float mn = fmaxf(m_run, tmax);
-        alpha = (m_run == -INFINITY) ? 0.f : exp2f(m_run - mn);
-        m_run = mn;
-        l_run *= alpha;
-      }
-      // P.V of the previous tile must be complete before P is overwritten or O rescaled
-      if (!mbar_wait_warp(&bars[B_PV_DONE], (i - 1) & 1, abort_flag, err)) return false;
-      tc_fence_after();
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
-#pragma unroll 1
-        for (int c = 128 * half; c < 128 * half + 128; c += 16) {
-          float o[16];
-          tmem_ld16(tmem + lane_off + C::COL_O + c, o);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 16; ++e) o[e] *= alpha;
-          tmem_st16(tmem + lane_off + C::COL_O + c, o);
-        }
-      }
-      const float mref = (m_run == -INFINITY) ? 0.f : m_run;
-      uint32_t pk[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        pk[e] = pack_bf16x2(exp2f(fmaf(v[2 * e], sl2, -mref)), exp2f(fmaf(v[2 * e + 1], sl2, -mref)));
-        l_run += __uint_as_float(pk[e] << 16) + __uint_as_float(pk[e] & 0xffff0000u);
-      }
-      tmem_st16_u32(tmem + lane_off + C::COL_P + 16 * half, pk);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bars[B_P_FULL]);
-      if (row == 0 && half == 0) DSA_TRACE(a.tr, i, 5);
-      return true;
-    };
-
     for (int g = cid; g < a.num_groups && ok; g += ncl) {
       int t0, n;
       group_of(a.req, G, g, t0, n);
       const int U = min(__ldg(a.union_len + g), a.union_pad);
       const int ntiles = (U + BK - 1) / BK;
       const int nrows = n * H;
-      uint16_t* out_row = a.out + (size_t)(t0 * H + row) * 512 + 256 * rank + 128 * half;
+      const uint8_t* mrow = a.mask + (size_t)g * a.union_pad;
       if (ntiles == 0) {
-        if (row < nrows) {
-          for (int c = 0; c < 16; ++c) reinterpret_cast<uint4*>(out_row)[c] = make_uint4(0, 0, 0, 0);
-          if (rank == 0 && half == 0) a.lse[(size_t)t0 * H + row] = -INFINITY;
+        // no union rows: zero output, lse = -inf for this CTA's pseudo-heads
+        for (int h = 0; h < HW; ++h) {
+          const int p = base + h;
+          if (p < nrows) {
+            for (int c = key; c < 512; c += 128) a.out[(size_t)(t0 * H + p) * 512 + c] = 0;
+            if (key == 0) a.lse[(size_t)t0 * H + p] = -INFINITY;
+          }
         }
         continue;
       }
-      // q row t0*H + row, own columns, into TMEM as bf16 pairs: this thread
-      // writes the 32 columns 32*half .. +31 of every own swizzle column (the
-      // previous group's QK MMAs completed before its last scores were read)
-      {
-        const int64_t qrow = (int64_t)t0 * H + row;
-        const bool qvalid = qrow < (int64_t)a.T * H;
-        const uint16_t* src = a.q + (qvalid ? qrow : 0) * a.d_qk + HK * half;
-        uint4 qv[C::OWNMAX][4];
-#pragma unroll
-        for (int c = 0; c < C::OWNMAX; ++c)
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            qv[c][e] = (c < nown && qvalid)
-                           ? __ldg(reinterpret_cast<const uint4*>(src + latent_chunk(rank, c) * 64) + e)
-                           : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int c = 0; c < C::OWNMAX; ++c)
-          if (c < nown)
-            tmem_st16_u32(tmem + lane_off + C::COL_Q + 32 * c + 16 * half, reinterpret_cast<const uint32_t*>(qv[c]));
-        tmem_st_wait();
+      float m_l = -INFINITY;  // running max of head `lane` (base 2, scaled)
+      float l_l = 0.f;        // this warp's running sum of head `lane`
+      for (int j = 0; j < ntiles; ++j, ++gt) {
+        const int sb = gt & 1;
+        const int pb = gt & 1;
+        // this slot's membership byte (zero past the union)
+        const int u = j * BK + key;
+        const uint32_t mbyte = (u < U) ? (uint32_t)__ldg(mrow + u) : 0u;
+        const bool on_lo = (mbyte >> t_lo) & 1u;
+        const bool on_hi = (mbyte >> (t_lo + 1)) & 1u;
+        if (!mbar_wait_warp(&bars[B_S_FULL + sb], (gt >> 1) & 1, abort_flag, err)) { ok = false; break; }
+        if (key == 0 && hh == 0) DSA_TRACE(a.tr, gt, 3);
+        tc_fence_after();
+        float s[HW];
+        tmem_ld_cols<HW>(tmem + lane_off + C::COL_S + sb * HC + HW * hh, s);
+        tmem_ld_wait();
         tc_fence_before();
-        mbar_arrive(&bars[B_Q_FULL]);
-      }
-      float m_run = -INFINITY, l_run = 0.f;
-      float va[HK], vb[HK];
-      if (!step_a(gt, va)) { ok = false; break; }
-      for (int j = 0; j < ntiles;) {
-        if (j + 1 < ntiles && !step_a(gt + j + 1, vb)) { ok = false; break; }
-        if (!step_b(gt + j, j, j + 1 == ntiles, va, m_run, l_run)) { ok = false; break; }
-        if (++j == ntiles) break;
-        if (j + 1 < ntiles && !step_a(gt + j + 1, va)) { ok = false; break; }
-        if (!step_b(gt + j, j, j + 1 == ntiles, vb, m_run, l_run)) { ok = false; break; }
-        ++j;
+        mbar_arrive(&bars[B_S_EMPTY + sb]);
+        bool mine = false;
+#pragma unroll
+        for (int h = 0; h < HW; ++h) {
+          const bool on = (h < split) ? on_lo : on_hi;
+          s[h] = on ? s[h] * scale_log2 : -INFINITY;
+          mine |= (s[h] > __shfl_sync(0xffffffffu, m_l, h) + kTau);
+        }
+        // Lazy rescale: the tile max matters only when some score exceeds
+        // the running max by more than kTau.  Each warp of the head half
+        // votes; a warp that votes yes publishes its per-head max.  The new
+        // reference is the max over those warps, which bounds every score of
+        // the tile (the others lie within kTau of the old reference).
+        const bool wneed = __any_sync(0xffffffffu, mine);
+        float* redb = red + ((gt & 1) * 2 + hh) * (4 * HW);
+        volatile uint32_t* vote = misc + 4 + ((gt & 1) * 2 + hh) * 4;
+        if (wneed) {
+          float r[HW];
+#pragma unroll
+          for (int h = 0; h < HW; ++h) r[h] = s[h];
+          redb[(warp & 3) * HW + lane] = warp_transpose_reduce32<true>(r);
+        }
+        if (lane == 0) vote[warp & 3] = wneed ? 1u : 0u;
+        if (!group_sync(smx, sync_phase, abort_flag, err)) { ok = false; break; }
+        uint32_t vw[4];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) vw[w] = vote[w];
+        const bool need = (vw[0] | vw[1] | vw[2] | vw[3]) != 0;
+        if (key == 0 && hh == 0) DSA_TRACE(a.tr, gt, 4);
+        float alpha_l = 1.f;
+        if (need) {
+          float tm = -INFINITY;
+#pragma unroll
+          for (int w = 0; w < 4; ++w)
+            if (vw[w]) tm = fmaxf(tm, redb[w * HW + lane]);
+          const float mn = fmaxf(m_l, tm);
+          alpha_l = (m_l == -INFINITY) ? 0.f : exp2f(m_l - mn);
+          m_l = mn;
+          l_l *= alpha_l;
+        }
+        // P buffer pb was last read by P.V two tiles ago
+        if (!mbar_wait_warp(&bars[B_P_EMPTY + pb], ((gt >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+        // P^T[head][slot] (K-major swizzled, 2 columns of 64 slots); s[] becomes
+        // the bf16-rounded P for the row sums
+        {
+          const uint32_t kcol = key & 63;
+          uint8_t* pcol = smem + C::OFF_P + pb * C::P_BYTES + (key >> 6) * (HC * 128);
+#pragma unroll
+          for (int h = 0; h < HW; ++h) {
+            const float mh = __shfl_sync(0xffffffffu, m_l, h);
+            const float mref = (mh == -INFINITY) ? 0.f : mh;
+            const uint16_t pbits = f32_to_bf16_rn(exp2f(s[h] - mref));
+            s[h] = bf16_to_f32(pbits);
+            *reinterpret_cast<uint16_t*>(pcol + sw128_offset(HW * hh + h, kcol)) = pbits;
+          }
+        }
+        l_l += warp_transpose_reduce32<false>(s);
+        if (need && j > 0) {
+          // O must hold the previous tile's P.V before it is rescaled
+          if (!mbar_wait_warp(&bars[B_P_EMPTY + ((gt - 1) & 1)], ((gt - 1) >> 1) & 1, abort_flag, err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // O^T lane = output column 128m + key, TMEM columns = heads
+#pragma unroll 1
+          for (int m = 0; m < 4; ++m) {
+#pragma unroll
+            for (int q16 = 0; q16 < 2; ++q16) {
+              float o[16];
+              const uint32_t ta = tmem + lane_off + C::COL_O + m * HC + HW * hh + 16 * q16;
+              tmem_ld16(ta, o);
+              tmem_ld_wait();
+#pragma unroll
+              for (int h = 0; h < 16; ++h) o[h] *= __shfl_sync(0xffffffffu, alpha_l, 16 * q16 + h);
+              tmem_st16(ta, o);
+            }
+          }
+          tmem_st_wait();
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&bars[B_P_FULL + pb]);
+        if (key == 0 && hh == 0) DSA_TRACE(a.tr, gt, 6);
       }
       if (!ok) break;
-      // ---- epilogue: row sum of both halves, normalise this CTA's half of O ----
-      // (through the row's slot in the last tile's SX buffer, which the peer
-      // cannot refill before both halves' deferred SX_FREE arrivals below)
-      float lsum;
-      {
-        const int sb = (gt + ntiles - 1) & 1;
-        volatile float* slot = reinterpret_cast<volatile float*>(smem + sx_row + sb * C::SX_BYTES);
-        slot[half] = l_run;
-        if (!group_sync(pair_bar, pair_phase, abort_flag, err)) { ok = false; break; }
-        lsum = slot[0] + slot[1];  // (consumes the loads before the arrival)
-        mbar_arrive_remote_relaxed(peer_bar(B_SX_FREE + sb));
-      }
-      const float inv_l = (lsum > 0.f) ? 1.f / lsum : 0.f;
-      if (rank == 0 && half == 0 && row < nrows)
-        a.lse[(size_t)t0 * H + row] = (lsum > 0.f) ? (m_run + log2f(lsum)) * 0.6931471805599453f : -INFINITY;
-      if (!mbar_wait_warp(&bars[B_PV_DONE], (gt + ntiles - 1) & 1, abort_flag, err)) { ok = false; break; }
+      // -------- epilogue --------
+      float* redb = red + ((gt & 1) * 2 + hh) * (4 * HW);  // not in use by the tile path now
+      if (!group_sync(smx, sync_phase, abort_flag, err)) { ok = false; break; }
+      redb[(warp & 3) * HW + lane] = l_l;
+      if (!group_sync(smx, sync_phase, abort_flag, err)) { ok = false; break; }
+      const float l = redb[0 * HW + lane] + redb[1 * HW + lane] + redb[2 * HW + lane] + redb[3 * HW + lane];
+      const float inv_l_l = (l > 0.f) ? 1.0f / l : 0.f;
+      if (warp == 4 * hh && base + lane < nrows)
+        a.lse[(size_t)t0 * H + base + lane] = (l > 0.f) ? (m_l + log2f(l)) * 0.6931471805599453f : -INFINITY;
+      if (!group_sync(smx, sync_phase, abort_flag, err)) { ok = false; break; }
+      if (!mbar_wait_warp(&bars[B_O_FULL], lgq & 1, abort_flag, err)) { ok = false; break; }
       tc_fence_after();
+      uint16_t* out_g = a.out + (size_t)(t0 * H + base) * 512;
 #pragma unroll 1
-      for (int c = 0; c < 128; c += 16) {
-        float o[16];
-        tmem_ld16(tmem + lane_off + C::COL_O + 128 * half + c, o);
-        tmem_ld_wait();
-        if (row < nrows) {
-          uint32_t pk[8];
+      for (int m = 0; m < 4; ++m) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) pk[e] = pack_bf16x2(o[2 * e] * inv_l, o[2 * e + 1] * inv_l);
-          uint4* dst = reinterpret_cast<uint4*>(out_row + c);
-          dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        for (int q16 = 0; q16 < 2; ++q16) {
+          float o[16];
+          tmem_ld16(tmem + lane_off + C::COL_O + m * HC + HW * hh + 16 * q16, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int h = 0; h < 16; ++h) {
+            const float il = __shfl_sync(0xffffffffu, inv_l_l, 16 * q16 + h);
+            if (base + 16 * q16 + h < nrows) out_g[(16 * q16 + h) * 512 + m * 128 + key] = f32_to_bf16_rn(o[h] * il);
+          }
         }
       }
       tc_fence_before();
       mbar_arrive(&bars[B_O_EMPTY]);
-      gt += ntiles;
       ++lgq;
     }
   }
