@@ -159,7 +159,8 @@ int dsa_sparse_prefill(const uint16_t* q, const uint16_t* kv, int N, int ld_kv, 
     return DSA_ERR_UNSUPPORTED;
   if ((ld_kv & 7) != 0) return DSA_ERR_INVALID_ARG;
   if (T == 0) return DSA_OK;
-  if (!q || !kv || !idx || !out || !lse) return DSA_ERR_INVALID_ARG;
+  // (kv may be null only for an empty table, N = 0)
+  if (!q || (!kv && N > 0) || !idx || !out || !lse) return DSA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(kv) || !aligned4(idx) || !aligned4(out) || !aligned4(lse))
     return DSA_ERR_INVALID_ARG;
   DevInfo* d;
@@ -180,8 +181,11 @@ int dsa_sparse_prefill(const uint16_t* q, const uint16_t* kv, int N, int ld_kv, 
   a.ld = ld;
   a.scale = scale;
   a.tr = g_trace;
-  // (with N = 0 every index is out of range and no row is ever read)
-  if (!dsa::make_row_gather_map(&a.tmap_kv, kv, N > 0 ? N : 1, ld_kv, ld_kv)) return DSA_ERR_CUDA;
+  // With N = 0 every index is out of range, no tile is formed and the map is
+  // never used: it is encoded over q so that it is well formed.
+  if (!dsa::make_row_gather_map(&a.tmap_kv, N > 0 ? (const void*)kv : (const void*)q, N > 0 ? N : 1,
+                                N > 0 ? ld_kv : d_qk, N > 0 ? ld_kv : d_qk))
+    return DSA_ERR_CUDA;
   if (!dsa::make_tile_map(&a.tmap_q, q, (int64_t)T * H, d_qk, d_qk, H)) return DSA_ERR_CUDA;
   const int r = dsa::launch_sparse_prefill(a, d->num_sms, (cudaStream_t)stream);
   return r == 0 ? DSA_OK : (r == -2 ? DSA_ERR_UNSUPPORTED : DSA_ERR_CUDA);
@@ -196,7 +200,8 @@ int dsa_grouped_prefill(const uint16_t* q, const uint16_t* kv, int N, int ld_kv,
   if (G > 8 || G * H != 128 || !(d_qk == 576 || d_qk == 512) || d_v != 512) return DSA_ERR_UNSUPPORTED;
   if ((ld_kv & 7) != 0 || (union_pad & 15) != 0) return DSA_ERR_INVALID_ARG;
   if (T == 0) return DSA_OK;
-  if (!q || !kv || !union_idx || !union_len || !mask || !out || !lse) return DSA_ERR_INVALID_ARG;
+  // (kv may be null only for an empty table, N = 0)
+  if (!q || (!kv && N > 0) || !union_idx || !union_len || !mask || !out || !lse) return DSA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(kv) || !aligned16(union_idx) || !aligned16(mask) || !aligned16(out) ||
       !aligned4(lse))
     return DSA_ERR_INVALID_ARG;
@@ -223,7 +228,10 @@ int dsa_grouped_prefill(const uint16_t* q, const uint16_t* kv, int N, int ld_kv,
   a.num_groups = a.req.cu_g[a.req.num_req];
   a.scale = scale;
   a.tr = g_trace;
-  if (!dsa::make_row_gather_map(&a.tmap_kv, kv, N > 0 ? N : 1, ld_kv, ld_kv)) return DSA_ERR_CUDA;
+  // With N = 0 every union is empty and the map is never used (encoded over q).
+  if (!dsa::make_row_gather_map(&a.tmap_kv, N > 0 ? (const void*)kv : (const void*)q, N > 0 ? N : 1,
+                                N > 0 ? ld_kv : d_qk, N > 0 ? ld_kv : d_qk))
+    return DSA_ERR_CUDA;
   if (!dsa::make_tile_map(&a.tmap_q, q, (int64_t)T * H, d_qk, d_qk, 64)) return DSA_ERR_CUDA;
   const int r = dsa::launch_grouped_prefill(a, d->num_sms, (cudaStream_t)stream);
   return r == 0 ? DSA_OK : (r == -2 ? DSA_ERR_UNSUPPORTED : DSA_ERR_CUDA);

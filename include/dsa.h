@@ -114,7 +114,8 @@ int dsa_union_build(const int32_t* idx, int T, int k, int ld, int G, const int32
  * Per-token sparse MLA prefill ("[Perf][DSA] Grouped sparse prefill ...",
  * commit message: each token gathers its own 2048 selected rows).
  *
- * q     [T, H, d_qk] bf16.        kv  [N, ld_kv] bf16, row n = latent row n.
+ * q     [T, H, d_qk] bf16.        kv  [N, ld_kv] bf16, row n = latent row n
+ *       (kv may be null when N = 0: every index is then out of range).
  * idx   [T, ld] int32 global rows, first k columns used; k <= 2048.
  * out   [T, H, d_v] bf16 (out).   lse [T, H] fp32 (out, natural log).
  * H in {16, 32}; d_qk in {576, 512}; d_v = 512; ld_kv >= d_qk and a

@@ -84,6 +84,10 @@ def test_argument_validation_without_gpu(lib):
                                    576, 512, 1.0, _vp(16), _vp(16), None) == dsa.DSA_ERR_UNSUPPORTED
     assert lib.dsa_grouped_prefill(_vp(16), _vp(16), 10, 576, _vp(16), _vp(16), _vp(16), 16, 16, None, 0, 8, 8,
                                    576, 512, 1.0, _vp(16), _vp(16), None) == dsa.DSA_ERR_UNSUPPORTED
+    # grouped: the softmax scale must be positive and finite
+    for bad in (0.0, -0.5, float("inf"), float("nan")):
+        assert lib.dsa_grouped_prefill(_vp(16), _vp(16), 10, 576, _vp(16), _vp(16), _vp(16), 16, 8, None, 0, 8,
+                                       16, 576, 512, bad, _vp(16), _vp(16), None) == dsa.DSA_ERR_INVALID_ARG
     # union build: G > 8 unsupported, union_pad must be a multiple of 16 and >= min(G*k, N)
     assert lib.dsa_union_build(_vp(16), 8, 4, 4, 9, None, 0, 100, _vp(16), _vp(16), _vp(16), 48,
                                None) == dsa.DSA_ERR_UNSUPPORTED

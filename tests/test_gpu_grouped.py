@@ -104,3 +104,22 @@ def test_grouped_equals_per_token_kernel():
     torch.cuda.synchronize()
     res = O.compare(og, lg, f32(op), lp.cpu().numpy().astype(np.float64))
     assert res["ok"], res
+
+
+def test_grouped_empty_kv_table():
+    """N = 0: every union is empty; zero output and lse = -inf for every
+    pseudo-head (the kv pointer may be null)."""
+    import dsa_sparse_mla_prefill_gb300 as dsa
+    H, G, k, T = 16, 8, 8, 13
+    q = bf(normal_bf16(np.random.default_rng(5), (T, H, 576)))
+    kv = torch.empty((0, 576), dtype=torch.bfloat16, device="cuda")
+    idx = torch.full((T, k), -1, dtype=torch.int32, device="cuda")
+    upad = dsa.dsa_union_pad(G, k, 128)
+    u, ul, m = dsa.dsa_union_build(idx, k, G, 0, union_pad=upad)
+    out = torch.full((T, H, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((T, H), float("nan"), dtype=torch.float32, device="cuda")
+    out, lse = dsa.dsa_grouped_prefill(q, kv, u, ul, m, G, 0.125, out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert int(ul.sum()) == 0
+    assert torch.all(out == 0).item()
+    assert torch.all(torch.isneginf(lse)).item()

@@ -137,3 +137,19 @@ def test_full_size_sampled(name):
     ro, rl = O.sparse_prefill(x.q, x.kv, x.idx, w.k, w.scale, w.d_qk, w.d_v, tokens=toks)
     res = O.compare(o[toks], l[toks], ro, rl)
     assert res["ok"], res
+
+
+def test_empty_kv_table():
+    """N = 0: every index is out of range, so every token has no keys: zero
+    output and lse = -inf (the kv pointer may be null)."""
+    import dsa_sparse_mla_prefill_gb300 as dsa
+    T, H, k = 5, 16, 8
+    q = bf(normal_bf16(np.random.default_rng(3), (T, H, 576)))
+    kv = torch.empty((0, 576), dtype=torch.bfloat16, device="cuda")
+    idx = torch.full((T, k), -1, dtype=torch.int32, device="cuda")
+    out = torch.full((T, H, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((T, H), float("nan"), dtype=torch.float32, device="cuda")
+    out, lse = dsa.dsa_sparse_prefill(q, kv, idx, k, 0.125, out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert torch.all(out == 0).item()
+    assert torch.all(torch.isneginf(lse)).item()
