@@ -269,6 +269,7 @@ int dsa_masked_mha_prefill(const uint16_t* q, const uint16_t* k, const uint16_t*
                            int num_req, int T, int H, int d_qk, int d_v, float scale, uint16_t* out, float* lse,
                            dsa_stream_t stream) {
   if (T < 0 || H < 1 || words < 1) return DSA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !(scale < INFINITY)) return DSA_ERR_INVALID_ARG;
   if ((cu_seqlens_q_host == nullptr) != (cu_seqlens_kv_host == nullptr)) return DSA_ERR_INVALID_ARG;
   if (!(d_qk == 192 && d_v == 128)) return DSA_ERR_UNSUPPORTED;
   if (T == 0) return DSA_OK;
@@ -300,6 +301,11 @@ int dsa_masked_mha_prefill(const uint16_t* q, const uint16_t* k, const uint16_t*
   a.num_qtiles = a.req.cu_g[a.req.num_req];
   a.scale = scale;
   a.tr = g_trace;
+  // (with no keys no key tile is loaded; the maps still need one row)
+  const int64_t nk = a.req.cu_kv[a.req.num_req] > 0 ? a.req.cu_kv[a.req.num_req] : 1;
+  if (!dsa::make_head_tile_map(&a.tmap_q, q, T, H, d_qk, 128) || !dsa::make_head_tile_map(&a.tmap_k, k, nk, H, d_qk, 128) ||
+      !dsa::make_head_tile_map(&a.tmap_v, v, nk, H, d_v, 128))
+    return DSA_ERR_CUDA;
   const int r = dsa::launch_masked_mha(a, d->num_sms, (cudaStream_t)stream);
   return r == 0 ? DSA_OK : (r == -2 ? DSA_ERR_UNSUPPORTED : DSA_ERR_CUDA);
 }

@@ -241,6 +241,16 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// TMA tiled 3-D load of one box (columns x .. x+63, head y, rows z .. z+box-1).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // The same gather delivered to every CTA of the cluster named in cta_mask,
 // at the same shared-memory offset, each completing on its own barrier at
 // the offset of `bar`.
@@ -265,11 +275,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
 
 // Bounded wait that ignores the CTA abort flag: used on the way out to let
 // copies already in flight land before the CTA exits.
-__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, unsigned int* err) {
   const uint32_t a = smem_u32(bar);
   const uint64_t t0 = globaltimer();
   while (!mbar_try_wait(a, parity)) {
-    if (globaltimer() - t0 > kWaitTimeoutNs) return false;
+    if (globaltimer() - t0 > kWaitTimeoutNs) {
+      atomicAdd(err + ERR_TIMEOUT, 1u);
+      return false;
+    }
   }
   return true;
 }

@@ -77,6 +77,9 @@ struct GroupedArgs {
 };
 
 struct MaskedArgs {
+  CUtensorMap tmap_q;   // q [T, H, d_qk]: box 64 columns x 1 head x 128 rows
+  CUtensorMap tmap_k;   // k [Nk, H, d_qk]: same box
+  CUtensorMap tmap_v;   // v [Nk, H, d_v]: same box
   const uint16_t* q;    // [T, H, d_qk]
   const uint16_t* k;    // [Nk, H, d_qk]
   const uint16_t* v;    // [Nk, H, d_v]

@@ -273,12 +273,12 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
       // phase of the slot this warp arms completes only once both CTAs'
       // bytes have landed here.
       if (leader) {
-        if (warp == 12 && lgq > 0) mbar_wait_drain(&bars[B_Q_FULL], (lgq - 1) & 1);
+        if (warp == 12 && lgq > 0) mbar_wait_drain(&bars[B_Q_FULL], (lgq - 1) & 1, err);
         if (last_armed >= 0) {
           if (kstream)
-            mbar_wait_drain(&bars[B_KR_FULL + ks], (uint32_t)(last_armed / NKR) & 1);
+            mbar_wait_drain(&bars[B_KR_FULL + ks], (uint32_t)(last_armed / NKR) & 1, err);
           else
-            mbar_wait_drain(&bars[B_VR_FULL + vg], (uint32_t)(last_armed / NVR) & 1);
+            mbar_wait_drain(&bars[B_VR_FULL + vg], (uint32_t)(last_armed / NVR) & 1, err);
         }
       }
       __syncwarp();

@@ -9,15 +9,18 @@
 //
 // One CTA per (128-query tile, head), FlashAttention-style over 128-key
 // tiles of the request:
-//   warps 5-8   cp.async loads of the q tile and of each k/v tile (128B
-//               swizzled); before a key tile they read its 4 mask words per
-//               query row and skip tiles where every bit is zero (the whole
-//               upper causal triangle, and any empty tile).
-//   warp 4      one thread: S = Q K^T (M = 128 queries, N = 128 keys) into a
+//   warp 9      TMA: the q tile and each k/v tile as 3-D boxes of one head
+//               (64 columns x 1 head x 128 rows, 128B-swizzled); before a
+//               key tile it reads the tile's 4 mask words of every query
+//               row and skips tiles where every bit is zero (the whole upper
+//               causal triangle, and any empty tile).
+//   warp 8      one thread: S = Q K^T (M = 128 queries, N = 128 keys) into a
 //               double-buffered TMEM S, then O += P V with P read from TMEM.
-//   warps 0-3   thread i owns query row i: mask, online softmax (base 2, lazy
-//               rescale), P packed bf16 into the S columns it came from, and
-//               the epilogue.
+//   warps 0-7   two threads per query row (TMEM lane): warp w holds row
+//               32(w%4) + lane and keys 64(w/4) .. +63 of each tile; mask,
+//               online softmax (base 2, lazy rescale) with the row max
+//               agreed through a per-tile pair exchange, P packed bf16 into
+//               the S columns it came from, and the epilogue.
 #include "dsa_device.cuh"
 #include "dsa_kernels.h"
 
@@ -26,8 +29,8 @@ namespace masked {
 
 constexpr int BQ = 128;
 constexpr int BKV = 128;
-constexpr int NTHREADS = 288;
-constexpr int LAG = 2;
+constexpr int HK = BKV / 2;     // keys per softmax thread
+constexpr int NTHREADS = 320;   // 10 warps
 constexpr float kTau = 8.0f;
 
 template <int DQK, int DV>
@@ -41,30 +44,32 @@ struct Cfg {
   static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;             // [2]
   static constexpr uint32_t OFF_V = OFF_K + 2 * K_BYTES;         // [2]
   static constexpr uint32_t OFF_MASK = OFF_V + 2 * V_BYTES;      // [2][128] x uint4
-  static constexpr uint32_t OFF_INFO = OFF_MASK + 2 * BQ * 16u;  // tile index per stage [2], votes [2]
+  static constexpr uint32_t OFF_PAIR = OFF_MASK + 2 * BQ * 16u;  // [2][2][128] floats
+  static constexpr uint32_t OFF_INFO = OFF_PAIR + 2 * 2 * BQ * 4u;  // tile index per stage [2]
   static constexpr uint32_t OFF_BAR = OFF_INFO + 64u;
-  static constexpr int NBAR = 16;
+  static constexpr int NBAR = 20;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8u;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64u + 1024u;
-  static constexpr uint32_t COL_S = 0;      // [2] x 128 columns
+  static_assert(SMEM_BYTES <= 227u * 1024u, "shared memory budget");
+  static constexpr uint32_t COL_S = 0;      // [2] x 128 columns; P (bf16 pairs) in the first 64
   static constexpr uint32_t COL_O = 256;    // DV columns
   static constexpr uint32_t TMEM_COLS = 512;
 };
 
 enum {
   B_Q_FULL = 0,
-  B_ST_FULL = 1,   // [2]
-  B_ST_EMPTY = 3,  // [2]
+  B_ST_FULL = 1,   // [2] k/v tile + its mask words landed (or the end marker)
+  B_ST_EMPTY = 3,  // [2] P.V of the stage's tile completed
   B_S_FULL = 5,    // [2]
-  B_S_EMPTY = 7,   // [2]
-  B_P_FULL = 9,
+  B_S_EMPTY = 7,   // [2] P.V completed (P aliases S)
+  B_P_FULL = 9,    // 256 arrivals
   B_PV_DONE = 10,
-  B_PROD_SYNC = 11,
-  B_DRAIN = 12,
+  B_DRAIN = 11,
+  B_PAIR = 12,     // [4] the two softmax warps of a TMEM lane quarter (64 arrivals)
 };
 
 template <int DQK, int DV>
-__global__ void __launch_bounds__(NTHREADS, 1) masked_mha_kernel(MaskedArgs a) {
+__global__ void __launch_bounds__(NTHREADS, 1) masked_mha_kernel(const __grid_constant__ MaskedArgs a) {
   using C = Cfg<DQK, DV>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -75,7 +80,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) masked_mha_kernel(MaskedArgs a) {
   volatile uint32_t* tmem_base_ptr = misc;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
   volatile int* stage_tile = reinterpret_cast<volatile int*>(smem + C::OFF_INFO);      // [2]
-  int* votes = reinterpret_cast<int*>(smem + C::OFF_INFO + 16);                        // [4] ring
   unsigned int* err = a.err;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -91,25 +95,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) masked_mha_kernel(MaskedArgs a) {
   const int kv0 = a.req.cu_kv[r];
   const int nkv = a.req.cu_kv[r + 1] - kv0;
   const int ntk = (nkv + BKV - 1) / BKV;
-  const int H = a.H;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars[B_Q_FULL], 128);
+    mbar_init(&bars[B_Q_FULL], 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars[B_ST_FULL + i], 128);
+      mbar_init(&bars[B_ST_FULL + i], 1);
       mbar_init(&bars[B_ST_EMPTY + i], 1);
       mbar_init(&bars[B_S_FULL + i], 1);
       mbar_init(&bars[B_S_EMPTY + i], 1);
     }
-    mbar_init(&bars[B_P_FULL], 128);
+    mbar_init(&bars[B_P_FULL], 256);
     mbar_init(&bars[B_PV_DONE], 1);
-    mbar_init(&bars[B_PROD_SYNC], 128);
     mbar_init(&bars[B_DRAIN], 1);
-    votes[0] = votes[1] = votes[2] = votes[3] = 0;
+    for (int i = 0; i < 4; ++i) mbar_init(&bars[B_PAIR + i], 64);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 4) {
+  if (warp == 8) {
     tmem_alloc(const_cast<uint32_t*>(tmem_base_ptr), C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -118,101 +120,73 @@ __global__ void __launch_bounds__(NTHREADS, 1) masked_mha_kernel(MaskedArgs a) {
   tc_fence_after();
   const uint32_t tmem = *tmem_base_ptr;
 
-  if (warp >= 5) {
+  if (warp == 9) {
     // ------------------------------------------------------------------
-    // producers
+    // TMA producer: q tile, then each key tile with any mask bit set
     // ------------------------------------------------------------------
-    const int ptid = threadIdx.x - 160;
-    const int p8 = ptid & 7;
-    const int rsub = ptid >> 3;  // 0..15
-    uint64_t* pend[LAG + 2];
-    int npend = 0;
-    auto flush = [&]() {
-      cp_async_wait_all();
-      fence_proxy_async_smem();
-      for (int i = 0; i < npend; ++i) mbar_arrive(pend[i]);
-      npend = 0;
-    };
-    auto push = [&](uint64_t* bar) {
-      cp_async_commit();
-      pend[npend++] = bar;
-      if (npend > LAG) {
-        cp_async_wait<LAG>();
-        fence_proxy_async_smem();
-        mbar_arrive(pend[0]);
-        for (int i = 1; i < npend; ++i) pend[i - 1] = pend[i];
-        --npend;
-      }
-    };
-    auto wait_free = [&](uint64_t* bar, uint32_t parity) -> bool {
-      if (mbar_ready(bar, parity)) return true;
-      flush();
-      return mbar_wait(bar, parity, abort_flag, err);
-    };
-    // q tile: rows q0 .. q0+127 of head h
-    {
-      const uint32_t qs = sbase + C::OFF_Q;
-      for (int pass = 0; pass < (BQ / 16) * C::QC; ++pass) {
-        const int row = (pass % (BQ / 16)) * 16 + rsub;
-        const int c = pass / (BQ / 16);
-        const bool valid = row < nq;
-        const uint16_t* src = a.q + ((size_t)(valid ? q0 + row : 0) * H + h) * DQK + c * 64 + p8 * 8;
-        cp_async16(qs + c * (BQ * 128) + row * 128 + ((p8 ^ (row & 7)) << 4), src, valid ? 16u : 0u);
-      }
-      push(&bars[B_Q_FULL]);
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bars[B_Q_FULL], C::Q_BYTES);
+      for (int c = 0; c < C::QC; ++c)
+        tma_load_3d(sbase + C::OFF_Q + c * (BQ * 128), &a.tmap_q, c * 64, h, q0, &bars[B_Q_FULL]);
     }
-    const uint32_t* km_row = reinterpret_cast<const uint32_t*>(a.key_mask) +
-                             (size_t)(q0 + (ptid < nq ? ptid : 0)) * a.words;
-    uint32_t sync_phase = 0;
+    const uint32_t* km = a.key_mask;
     uint32_t st = 0;  // stages used
     bool ok = true;
     for (int j = 0; j < ntk && ok; ++j) {
-      uint4 w = make_uint4(0, 0, 0, 0);
-      if (ptid < nq) w = __ldg(reinterpret_cast<const uint4*>(km_row + 4 * j));
-      const bool any = (w.x | w.y | w.z | w.w) != 0u;
-      // one vote slot per key tile, 4-slot ring: slot (j-1)&3 was read by
-      // every thread before the barrier below and is next written at j+3,
-      // which no thread reaches before thread 0 has passed barrier j+1
-      if (__any_sync(0xffffffffu, any) && lane == 0) atomicOr(&votes[j & 3], 1);
-      if (!group_sync(&bars[B_PROD_SYNC], sync_phase, abort_flag, err)) { ok = false; break; }
-      const int v = *reinterpret_cast<volatile int*>(&votes[j & 3]);
-      if (ptid == 0) votes[(j + 3) & 3] = 0;
-      if (v == 0) continue;
+      // the tile's 4 mask words of query rows lane, lane+32, lane+64, lane+96
+      uint4 w[4];
+      uint32_t any = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int row = lane + 32 * i;
+        w[i] = make_uint4(0, 0, 0, 0);
+        if (row < nq) w[i] = __ldg(reinterpret_cast<const uint4*>(km + (size_t)(q0 + row) * a.words) + j);
+        any |= w[i].x | w[i].y | w[i].z | w[i].w;
+      }
+      if (!__any_sync(0xffffffffu, any != 0)) continue;
       const int s = st & 1;
-      if (!wait_free(&bars[B_ST_EMPTY + s], ((st >> 1) & 1) ^ 1)) { ok = false; break; }
-      reinterpret_cast<uint4*>(smem + C::OFF_MASK + s * BQ * 16)[ptid] = w;
-      if (ptid == 0) stage_tile[s] = j;
-      const uint32_t ks = sbase + C::OFF_K + s * C::K_BYTES;
-      const uint32_t vs = sbase + C::OFF_V + s * C::V_BYTES;
-      for (int pass = 0; pass < (BKV / 16) * C::QC; ++pass) {
-        const int row = (pass % (BKV / 16)) * 16 + rsub;
-        const int c = pass / (BKV / 16);
-        const int key = j * BKV + row;
-        const bool valid = key < nkv;
-        const uint16_t* src = a.k + ((size_t)(kv0 + (valid ? key : 0)) * H + h) * DQK + c * 64 + p8 * 8;
-        cp_async16(ks + c * (BKV * 128) + row * 128 + ((p8 ^ (row & 7)) << 4), src, valid ? 16u : 0u);
+      if (!mbar_wait_warp(&bars[B_ST_EMPTY + s], ((st >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) reinterpret_cast<uint4*>(smem + C::OFF_MASK + s * BQ * 16)[lane + 32 * i] = w[i];
+      if (lane == 0) stage_tile[s] = j;
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars[B_ST_FULL + s], C::K_BYTES + C::V_BYTES);
+        // keys past the request read the next request's rows (their mask
+        // bits are zero) or, past the table, zeros
+        for (int c = 0; c < C::QC; ++c)
+          tma_load_3d(sbase + C::OFF_K + s * C::K_BYTES + c * (BKV * 128), &a.tmap_k, c * 64, h, kv0 + j * BKV,
+                      &bars[B_ST_FULL + s]);
+        for (int c = 0; c < C::VC; ++c)
+          tma_load_3d(sbase + C::OFF_V + s * C::V_BYTES + c * (BKV * 128), &a.tmap_v, c * 64, h, kv0 + j * BKV,
+                      &bars[B_ST_FULL + s]);
       }
-      for (int pass = 0; pass < (BKV / 16) * C::VC; ++pass) {
-        const int row = (pass % (BKV / 16)) * 16 + rsub;
-        const int c = pass / (BKV / 16);
-        const int key = j * BKV + row;
-        const bool valid = key < nkv;
-        const uint16_t* src = a.v + ((size_t)(kv0 + (valid ? key : 0)) * H + h) * DV + c * 64 + p8 * 8;
-        cp_async16(vs + c * (BKV * 128) + row * 128 + ((p8 ^ (row & 7)) << 4), src, valid ? 16u : 0u);
-      }
-      push(&bars[B_ST_FULL + s]);
       ++st;
     }
+    bool marked = false;
     if (ok) {
       // end marker
       const int s = st & 1;
-      if (wait_free(&bars[B_ST_EMPTY + s], ((st >> 1) & 1) ^ 1)) {
-        if (ptid == 0) stage_tile[s] = -1;
-        push(&bars[B_ST_FULL + s]);
+      marked = mbar_wait_warp(&bars[B_ST_EMPTY + s], ((st >> 1) & 1) ^ 1, abort_flag, err);
+      if (marked && lane == 0) {
+        stage_tile[s] = -1;
+        mbar_arrive(&bars[B_ST_FULL + s]);
       }
     }
-    flush();
-  } else if (warp == 4) {
+    // Let copies still in flight land before the CTA can exit: q, and the
+    // last data phase of each stage barrier.  Once the end marker is posted
+    // on stage st, that barrier's data phase st-2 was consumed already (and
+    // its parity now names the marker's successor phase), so only stage
+    // st-1 is left.
+    if (lane == 0) {
+      mbar_wait_drain(&bars[B_Q_FULL], 0, err);
+      for (uint32_t i = (st > 2 ? st - 2 : 0); i < st; ++i) {
+        if (marked && i + 2 == st) continue;
+        mbar_wait_drain(&bars[B_ST_FULL + (i & 1)], (i >> 1) & 1, err);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 8) {
     // ------------------------------------------------------------------
     // tcgen05 issuer
     // ------------------------------------------------------------------
@@ -224,15 +198,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) masked_mha_kernel(MaskedArgs a) {
       tc_fence_after();
       uint32_t n = 0;  // tiles consumed (stage sequence)
       auto issue_qk = [&](uint32_t i) -> bool {
-        const int s = i & 1, sb = i & 1;
-        if (!mbar_wait(&bars[B_S_EMPTY + sb], ((i >> 1) & 1) ^ 1, abort_flag, err)) return false;
+        const int s = i & 1;
+        if (!mbar_wait(&bars[B_S_EMPTY + s], ((i >> 1) & 1) ^ 1, abort_flag, err)) return false;
         tc_fence_after();
         const uint32_t ks = sbase + C::OFF_K + s * C::K_BYTES;
 #pragma unroll
         for (int c = 0; c < C::QC; ++c)
-          mma_bf16_ss_x4(tmem + C::COL_S + sb * 128, sdesc_sw128(qs + c * (BQ * 128), 16, 1024),
+          mma_bf16_ss_x4(tmem + C::COL_S + s * 128, sdesc_sw128(qs + c * (BQ * 128), 16, 1024),
                          sdesc_sw128(ks + c * (BKV * 128), 16, 1024), 2u, 2u, IDESC_QK, c > 0 ? 1u : 0u);
-        mma_commit(&bars[B_S_FULL + sb]);
+        mma_commit(&bars[B_S_FULL + s]);
         return true;
       };
       int cur_tile = -1;
@@ -251,7 +225,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) masked_mha_kernel(MaskedArgs a) {
         tc_fence_after();
         const int nx_tile = stage_tile[nx & 1];
         if (nx_tile >= 0 && !issue_qk(nx)) { ok = false; break; }
-        // O += P V for the current tile
+        // O += P V for the current tile (P: 128 keys as 64 TMEM columns of bf16 pairs)
         if (!mbar_wait(&bars[B_P_FULL], n & 1, abort_flag, err)) { ok = false; break; }
         tc_fence_after();
         const int s = n & 1;
@@ -273,11 +247,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) masked_mha_kernel(MaskedArgs a) {
     __syncwarp();
   } else {
     // ------------------------------------------------------------------
-    // softmax + epilogue: thread i <-> query row i <-> TMEM lane i
+    // softmax + epilogue: two threads per query row (TMEM lane); this one
+    // holds keys 64*half .. 64*half+63 of every tile and output columns
+    // (DV/2)*half .. of the row
     // ------------------------------------------------------------------
-    const int row = threadIdx.x;
+    const int half = warp >> 2;
+    const int row = (warp & 3) * 32 + lane;
     const float sl2 = a.scale * 1.4426950408889634f;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    float* pair = reinterpret_cast<float*>(smem + C::OFF_PAIR);   // [parity][half][row]
+    uint64_t* pair_bar = &bars[B_PAIR + (warp & 3)];
+    uint32_t pair_phase = 0;
     float m_run = -INFINITY, l_run = 0.f;
     uint32_t n = 0;
     bool ok = true;
@@ -287,20 +267,25 @@ __global__ void __launch_bounds__(NTHREADS, 1) masked_mha_kernel(MaskedArgs a) {
       const int tile = stage_tile[s];
       if (tile < 0) break;
       const uint4 mw = reinterpret_cast<const uint4*>(smem + C::OFF_MASK + s * BQ * 16)[row];
+      const uint32_t mwords[2] = {half ? mw.z : mw.x, half ? mw.w : mw.y};
       if (!mbar_wait_warp(&bars[B_S_FULL + s], (n >> 1) & 1, abort_flag, err)) { ok = false; break; }
       tc_fence_after();
-      float sv[BKV];
+      float sv[HK];
 #pragma unroll
-      for (int c = 0; c < BKV; c += 16) tmem_ld16(tmem + lane_off + C::COL_S + s * 128 + c, sv + c);
+      for (int c = 0; c < HK; c += 16) tmem_ld16(tmem + lane_off + C::COL_S + s * 128 + HK * half + c, sv + c);
       tmem_ld_wait();
-      const uint32_t mwords[4] = {mw.x, mw.y, mw.z, mw.w};
-      float tmax = -INFINITY;
+      float hmax = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < BKV; ++c) {
+      for (int c = 0; c < HK; ++c) {
         const bool on = (mwords[c >> 5] >> (c & 31)) & 1u;
-        sv[c] = on ? sv[c] * sl2 : -INFINITY;
-        tmax = fmaxf(tmax, sv[c]);
+        sv[c] = on ? sv[c] : -INFINITY;
+        hmax = fmaxf(hmax, sv[c]);
       }
+      // the row max of both halves (raw scores; the scale is applied in the exponent)
+      pair[((n & 1) * 2 + half) * BQ + row] = hmax;
+      if (!group_sync(pair_bar, pair_phase, abort_flag, err)) { ok = false; break; }
+      const float omax = pair[((n & 1) * 2 + (half ^ 1)) * BQ + row];
+      const float tmax = (half == 0 ? fmaxf(hmax, omax) : fmaxf(omax, hmax)) * sl2;
       const bool need = tmax > m_run + kTau;
       float alpha = 1.f;
       if (need) {
@@ -314,7 +299,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) masked_mha_kernel(MaskedArgs a) {
         if (!mbar_wait_warp(&bars[B_PV_DONE], (n - 1) & 1, abort_flag, err)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < DV; c += 16) {
+        for (int c = (DV / 2) * half; c < (DV / 2) * (half + 1); c += 16) {
           float o[16];
           tmem_ld16(tmem + lane_off + C::COL_O + c, o);
           tmem_ld_wait();
@@ -322,20 +307,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) masked_mha_kernel(MaskedArgs a) {
           for (int i = 0; i < 16; ++i) o[i] *= alpha;
           tmem_st16(tmem + lane_off + C::COL_O + c, o);
         }
-        tmem_st_wait();
       }
       const float mref = (m_run == -INFINITY) ? 0.f : m_run;
 #pragma unroll
-      for (int c = 0; c < BKV; c += 32) {
+      for (int c = 0; c < HK; c += 32) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const uint16_t b0 = f32_to_bf16_rn(exp2f(sv[c + 2 * i] - mref));
-          const uint16_t b1 = f32_to_bf16_rn(exp2f(sv[c + 2 * i + 1] - mref));
-          l_run += bf16_to_f32(b0) + bf16_to_f32(b1);
-          pk[i] = (uint32_t)b0 | ((uint32_t)b1 << 16);
+          pk[i] = pack_bf16x2(exp2f(fmaf(sv[c + 2 * i], sl2, -mref)), exp2f(fmaf(sv[c + 2 * i + 1], sl2, -mref)));
+          l_run += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xffff0000u);
         }
-        tmem_st16_u32(tmem + lane_off + C::COL_S + s * 128 + c / 2, pk);
+        tmem_st16_u32(tmem + lane_off + C::COL_S + s * 128 + (HK * half + c) / 2, pk);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -345,41 +327,43 @@ __global__ void __launch_bounds__(NTHREADS, 1) masked_mha_kernel(MaskedArgs a) {
     // epilogue
     if (ok) {
       const int t = q0 + row;
-      if (n > 0) {
+      // the row sum of both halves (pair slot of parity n: last read before barrier n-1)
+      pair[((n & 1) * 2 + half) * BQ + row] = l_run;
+      const bool synced = group_sync(pair_bar, pair_phase, abort_flag, err);
+      const float lsum = pair[(n & 1) * 2 * BQ + row] + pair[((n & 1) * 2 + 1) * BQ + row];
+      if (synced && n > 0) {
         const bool got = mbar_wait_warp(&bars[B_PV_DONE], (n - 1) & 1, abort_flag, err);
         tc_fence_after();
         if (got) {
-          const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
+          const float inv_l = (lsum > 0.f) ? 1.f / lsum : 0.f;
 #pragma unroll 1
-          for (int c = 0; c < DV; c += 16) {
+          for (int c = (DV / 2) * half; c < (DV / 2) * (half + 1); c += 16) {
             float o[16];
             tmem_ld16(tmem + lane_off + C::COL_O + c, o);
             tmem_ld_wait();
             if (row < nq) {
               uint32_t pk[8];
 #pragma unroll
-              for (int i = 0; i < 8; ++i)
-                pk[i] = (uint32_t)f32_to_bf16_rn(o[2 * i] * inv_l) |
-                        ((uint32_t)f32_to_bf16_rn(o[2 * i + 1] * inv_l) << 16);
-              uint4* dst = reinterpret_cast<uint4*>(a.out + ((size_t)t * H + h) * DV + c);
+              for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(o[2 * i] * inv_l, o[2 * i + 1] * inv_l);
+              uint4* dst = reinterpret_cast<uint4*>(a.out + ((size_t)t * a.H + h) * DV + c);
               dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
               dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
             }
           }
         }
-      } else if (row < nq) {
-        uint4* dst = reinterpret_cast<uint4*>(a.out + ((size_t)t * H + h) * DV);
-        for (int c = 0; c < DV / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+      } else if (synced && row < nq) {
+        uint4* dst = reinterpret_cast<uint4*>(a.out + ((size_t)t * a.H + h) * DV + (DV / 2) * half);
+        for (int c = 0; c < DV / 16; ++c) dst[c] = make_uint4(0, 0, 0, 0);
       }
-      if (row < nq)
-        a.lse[(size_t)t * H + h] = (l_run > 0.f) ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
+      if (synced && half == 0 && row < nq)
+        a.lse[(size_t)t * a.H + h] = (lsum > 0.f) ? (m_run + log2f(lsum)) * 0.6931471805599453f : -INFINITY;
     }
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 4) tmem_dealloc(tmem, C::TMEM_COLS);
+  if (warp == 8) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
 template <int DQK, int DV>

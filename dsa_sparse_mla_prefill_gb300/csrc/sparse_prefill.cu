@@ -351,12 +351,12 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
       // phase of the slot this warp fills completes only once every byte
       // of it has landed.
       if (leader) {
-        if (warp == 8 && lt_nz > 0) mbar_wait_drain(&bars[B_Q_FULL], (lt_nz - 1) & 1);
+        if (warp == 8 && lt_nz > 0) mbar_wait_drain(&bars[B_Q_FULL], (lt_nz - 1) & 1, err);
         if (last_armed >= 0) {
           if (kstream)
-            mbar_wait_drain(&bars[B_KR_FULL + kw], (uint32_t)(last_armed / C::NKR) & 1);
+            mbar_wait_drain(&bars[B_KR_FULL + kw], (uint32_t)(last_armed / C::NKR) & 1, err);
           else
-            mbar_wait_drain(&bars[B_VR_FULL + vgroup], (uint32_t)(last_armed / C::NVR) & 1);
+            mbar_wait_drain(&bars[B_VR_FULL + vgroup], (uint32_t)(last_armed / C::NVR) & 1, err);
         }
       }
       __syncwarp();

@@ -173,6 +173,8 @@ int dsa_topk_to_key_mask(const int32_t* idx, int T, int k, int ld, const int32_t
  * key_mask [T, words] uint32 as written by dsa_topk_to_key_mask.
  * out [T, H, d_v] bf16 (out); lse [T, H] fp32 (out, natural log).
  * (d_qk, d_v) = (192, 128) (the DeepSeek-V3.2 geometry on the allow-list).
+ * scale must be positive and finite (the kernel takes the row max on
+ * unscaled scores); otherwise DSA_ERR_INVALID_ARG.
  * ---------------------------------------------------------------------- */
 int dsa_masked_mha_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint32_t* key_mask,
                            int words, const int32_t* cu_seqlens_q_host, const int32_t* cu_seqlens_kv_host,

@@ -105,6 +105,10 @@ def test_argument_validation_without_gpu(lib):
     # masked MHA geometry allow-list
     assert lib.dsa_masked_mha_prefill(_vp(16), _vp(16), _vp(16), _vp(16), 4, None, None, 0, 8, 4, 576, 512, 1.0,
                                       _vp(16), _vp(16), None) == dsa.DSA_ERR_UNSUPPORTED
+    # masked MHA: the softmax scale must be positive and finite
+    for bad in (0.0, -1.0, float("inf"), float("nan")):
+        assert lib.dsa_masked_mha_prefill(_vp(16), _vp(16), _vp(16), _vp(16), 4, None, None, 0, 8, 4, 192, 128,
+                                          bad, _vp(16), _vp(16), None) == dsa.DSA_ERR_INVALID_ARG
     # key mask: one-sided offsets are rejected
     assert lib.dsa_topk_to_key_mask(_vp(16), 8, 4, 4, cu, None, 2, _vp(16), 4, None) == dsa.DSA_ERR_INVALID_ARG
 
