@@ -13,7 +13,10 @@
 //               (64 columns x 1 head x 128 rows, 128B-swizzled); before a
 //               key tile it reads the tile's 4 mask words of every query
 //               row and skips tiles where every bit is zero (the whole upper
-//               causal triangle, and any empty tile).
+//               causal triangle, and any empty tile).  K and V have their
+//               own 2-stage rings: a K stage returns after its QK, a V stage
+//               after its PV, so the next tiles' K loads are not held up by
+//               this tile's softmax.
 //   warp 8      one thread: S = Q K^T (M = 128 queries, N = 128 keys) into a
 //               double-buffered TMEM S, then O += P V with P read from TMEM.
 //   warps 0-7   two threads per query row (TMEM lane): warp w holds row
@@ -43,11 +46,11 @@ struct Cfg {
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;             // [2]
   static constexpr uint32_t OFF_V = OFF_K + 2 * K_BYTES;         // [2]
-  static constexpr uint32_t OFF_MASK = OFF_V + 2 * V_BYTES;      // [2][128] x uint4
-  static constexpr uint32_t OFF_PAIR = OFF_MASK + 2 * BQ * 16u;  // [2][2][128] floats
-  static constexpr uint32_t OFF_INFO = OFF_PAIR + 2 * 2 * BQ * 4u;  // tile index per stage [2]
+  static constexpr uint32_t OFF_MASK = OFF_V + 2 * V_BYTES;      // [4][128] x uint4 (tile info ring)
+  static constexpr uint32_t OFF_PAIR = OFF_MASK + 4 * BQ * 16u;  // [2][2][128] floats
+  static constexpr uint32_t OFF_INFO = OFF_PAIR + 2 * 2 * BQ * 4u;  // key-tile index per info slot [4]
   static constexpr uint32_t OFF_BAR = OFF_INFO + 64u;
-  static constexpr int NBAR = 20;
+  static constexpr int NBAR = 24;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8u;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64u + 1024u;
   static_assert(SMEM_BYTES <= 227u * 1024u, "shared memory budget");
@@ -58,14 +61,17 @@ struct Cfg {
 
 enum {
   B_Q_FULL = 0,
-  B_ST_FULL = 1,   // [2] k/v tile + its mask words landed (or the end marker)
-  B_ST_EMPTY = 3,  // [2] P.V of the stage's tile completed
-  B_S_FULL = 5,    // [2]
-  B_S_EMPTY = 7,   // [2] P.V completed (P aliases S)
-  B_P_FULL = 9,    // 256 arrivals
-  B_PV_DONE = 10,
-  B_DRAIN = 11,
-  B_PAIR = 12,     // [4] the two softmax warps of a TMEM lane quarter (64 arrivals)
+  B_K_FULL = 1,    // [2] k tile landed (or the end marker, no bytes)
+  B_K_EMPTY = 3,   // [2] QK of the stage's tile completed
+  B_V_FULL = 5,    // [2] v tile landed
+  B_V_EMPTY = 7,   // [2] P.V of the stage's tile completed
+  B_INFO = 9,      // [4] the tile's index and mask words are written (or the end marker)
+  B_S_FULL = 13,   // [2]
+  B_S_EMPTY = 15,  // [2] P.V completed (P aliases S)
+  B_P_FULL = 17,   // 256 arrivals
+  B_PV_DONE = 18,
+  B_DRAIN = 19,
+  B_PAIR = 20,     // [4] the two softmax warps of a TMEM lane quarter (64 arrivals)
 };
 
 template <int DQK, int DV>
@@ -79,7 +85,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) masked_mha_kernel(const __grid_co
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile uint32_t* tmem_base_ptr = misc;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
-  volatile int* stage_tile = reinterpret_cast<volatile int*>(smem + C::OFF_INFO);      // [2]
+  volatile int* stage_tile = reinterpret_cast<volatile int*>(smem + C::OFF_INFO);      // [4]
   unsigned int* err = a.err;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -99,11 +105,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) masked_mha_kernel(const __grid_co
   if (threadIdx.x == 0) {
     mbar_init(&bars[B_Q_FULL], 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars[B_ST_FULL + i], 1);
-      mbar_init(&bars[B_ST_EMPTY + i], 1);
+      mbar_init(&bars[B_K_FULL + i], 1);
+      mbar_init(&bars[B_K_EMPTY + i], 1);
+      mbar_init(&bars[B_V_FULL + i], 1);
+      mbar_init(&bars[B_V_EMPTY + i], 1);
       mbar_init(&bars[B_S_FULL + i], 1);
       mbar_init(&bars[B_S_EMPTY + i], 1);
     }
+    for (int i = 0; i < 4; ++i) mbar_init(&bars[B_INFO + i], 1);
     mbar_init(&bars[B_P_FULL], 256);
     mbar_init(&bars[B_PV_DONE], 1);
     mbar_init(&bars[B_DRAIN], 1);
@@ -144,45 +153,54 @@ __global__ void __launch_bounds__(NTHREADS, 1) masked_mha_kernel(const __grid_co
         any |= w[i].x | w[i].y | w[i].z | w[i].w;
       }
       if (!__any_sync(0xffffffffu, any != 0)) continue;
+      // Info slot st % 4 is rewritten only after QK(st-2) completed, which
+      // follows P.V(st-4) and hence the softmax of tile st-4 that read it.
       const int s = st & 1;
-      if (!mbar_wait_warp(&bars[B_ST_EMPTY + s], ((st >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+      const int is = st & 3;
+      if (!mbar_wait_warp(&bars[B_K_EMPTY + s], ((st >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
 #pragma unroll
-      for (int i = 0; i < 4; ++i) reinterpret_cast<uint4*>(smem + C::OFF_MASK + s * BQ * 16)[lane + 32 * i] = w[i];
-      if (lane == 0) stage_tile[s] = j;
+      for (int i = 0; i < 4; ++i) reinterpret_cast<uint4*>(smem + C::OFF_MASK + is * BQ * 16)[lane + 32 * i] = w[i];
+      if (lane == 0) stage_tile[is] = j;
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bars[B_ST_FULL + s], C::K_BYTES + C::V_BYTES);
+        mbar_arrive(&bars[B_INFO + is]);
+        mbar_arrive_expect_tx(&bars[B_K_FULL + s], C::K_BYTES);
         // keys past the request read the next request's rows (their mask
         // bits are zero) or, past the table, zeros
         for (int c = 0; c < C::QC; ++c)
           tma_load_3d(sbase + C::OFF_K + s * C::K_BYTES + c * (BKV * 128), &a.tmap_k, c * 64, h, kv0 + j * BKV,
-                      &bars[B_ST_FULL + s]);
+                      &bars[B_K_FULL + s]);
+      }
+      if (!mbar_wait_warp(&bars[B_V_EMPTY + s], ((st >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars[B_V_FULL + s], C::V_BYTES);
         for (int c = 0; c < C::VC; ++c)
           tma_load_3d(sbase + C::OFF_V + s * C::V_BYTES + c * (BKV * 128), &a.tmap_v, c * 64, h, kv0 + j * BKV,
-                      &bars[B_ST_FULL + s]);
+                      &bars[B_V_FULL + s]);
       }
       ++st;
     }
     bool marked = false;
     if (ok) {
-      // end marker
+      // end marker (to the softmax through the info ring, to the MMA issuer
+      // through a K stage without bytes)
       const int s = st & 1;
-      marked = mbar_wait_warp(&bars[B_ST_EMPTY + s], ((st >> 1) & 1) ^ 1, abort_flag, err);
+      marked = mbar_wait_warp(&bars[B_K_EMPTY + s], ((st >> 1) & 1) ^ 1, abort_flag, err);
       if (marked && lane == 0) {
-        stage_tile[s] = -1;
-        mbar_arrive(&bars[B_ST_FULL + s]);
+        stage_tile[st & 3] = -1;
+        mbar_arrive(&bars[B_INFO + (st & 3)]);
+        mbar_arrive(&bars[B_K_FULL + s]);
       }
     }
     // Let copies still in flight land before the CTA can exit: q, and the
-    // last data phase of each stage barrier.  Once the end marker is posted
-    // on stage st, that barrier's data phase st-2 was consumed already (and
-    // its parity now names the marker's successor phase), so only stage
-    // st-1 is left.
+    // last data phase of each K and V stage barrier.  Once the end marker is
+    // posted on K stage st, that barrier's data phase st-2 was consumed
+    // already (and its parity now names the marker's successor phase).
     if (lane == 0) {
       mbar_wait_drain(&bars[B_Q_FULL], 0, err);
       for (uint32_t i = (st > 2 ? st - 2 : 0); i < st; ++i) {
-        if (marked && i + 2 == st) continue;
-        mbar_wait_drain(&bars[B_ST_FULL + (i & 1)], (i >> 1) & 1, err);
+        if (!(marked && i + 2 == st)) mbar_wait_drain(&bars[B_K_FULL + (i & 1)], (i >> 1) & 1, err);
+        mbar_wait_drain(&bars[B_V_FULL + (i & 1)], (i >> 1) & 1, err);
       }
     }
     __syncwarp();
@@ -207,11 +225,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) masked_mha_kernel(const __grid_co
           mma_bf16_ss_x4(tmem + C::COL_S + s * 128, sdesc_sw128(qs + c * (BQ * 128), 16, 1024),
                          sdesc_sw128(ks + c * (BKV * 128), 16, 1024), 2u, 2u, IDESC_QK, c > 0 ? 1u : 0u);
         mma_commit(&bars[B_S_FULL + s]);
+        mma_commit(&bars[B_K_EMPTY + s]);
         return true;
       };
       int cur_tile = -1;
       if (ok) {
-        ok = mbar_wait(&bars[B_ST_FULL + 0], 0, abort_flag, err);
+        ok = mbar_wait(&bars[B_K_FULL + 0], 0, abort_flag, err);
         if (ok) {
           tc_fence_after();
           cur_tile = stage_tile[0];
@@ -221,14 +240,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) masked_mha_kernel(const __grid_co
       while (ok && cur_tile >= 0) {
         const uint32_t nx = n + 1;
         // next stage: its QK overlaps this tile's softmax
-        if (!mbar_wait(&bars[B_ST_FULL + (nx & 1)], (nx >> 1) & 1, abort_flag, err)) { ok = false; break; }
+        if (!mbar_wait(&bars[B_K_FULL + (nx & 1)], (nx >> 1) & 1, abort_flag, err)) { ok = false; break; }
         tc_fence_after();
-        const int nx_tile = stage_tile[nx & 1];
+        const int nx_tile = stage_tile[nx & 3];
         if (nx_tile >= 0 && !issue_qk(nx)) { ok = false; break; }
         // O += P V for the current tile (P: 128 keys as 64 TMEM columns of bf16 pairs)
         if (!mbar_wait(&bars[B_P_FULL], n & 1, abort_flag, err)) { ok = false; break; }
-        tc_fence_after();
         const int s = n & 1;
+        if (!mbar_wait(&bars[B_V_FULL + s], (n >> 1) & 1, abort_flag, err)) { ok = false; break; }
+        tc_fence_after();
         const uint32_t vs = sbase + C::OFF_V + s * C::V_BYTES;
 #pragma unroll
         for (int half = 0; half < 2; ++half)
@@ -236,7 +256,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) masked_mha_kernel(const __grid_co
                          sdesc_sw128(vs + half * 4 * 2048, BKV * 128, 1024), 8u, 128u, IDESC_PV,
                          (n > 0 || half > 0) ? 1u : 0u);
         mma_commit(&bars[B_PV_DONE]);
-        mma_commit(&bars[B_ST_EMPTY + s]);
+        mma_commit(&bars[B_V_EMPTY + s]);
         mma_commit(&bars[B_S_EMPTY + s]);
         n = nx;
         cur_tile = nx_tile;
@@ -263,10 +283,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) masked_mha_kernel(const __grid_co
     bool ok = true;
     while (true) {
       const int s = n & 1;
-      if (!mbar_wait_warp(&bars[B_ST_FULL + s], (n >> 1) & 1, abort_flag, err)) { ok = false; break; }
-      const int tile = stage_tile[s];
+      const int is = n & 3;
+      if (!mbar_wait_warp(&bars[B_INFO + is], (n >> 2) & 1, abort_flag, err)) { ok = false; break; }
+      const int tile = stage_tile[is];
       if (tile < 0) break;
-      const uint4 mw = reinterpret_cast<const uint4*>(smem + C::OFF_MASK + s * BQ * 16)[row];
+      const uint4 mw = reinterpret_cast<const uint4*>(smem + C::OFF_MASK + is * BQ * 16)[row];
       const uint32_t mwords[2] = {half ? mw.z : mw.x, half ? mw.w : mw.y};
       if (!mbar_wait_warp(&bars[B_S_FULL + s], (n >> 1) & 1, abort_flag, err)) { ok = false; break; }
       tc_fence_after();
