@@ -574,7 +574,7 @@ def run_profile_case(args):
     dev = torch.device("cuda", 0)
     n = args.profile_tokens
     if args.profile in ("sparse", "union", "grouped"):
-        base = WORKLOADS["v32_h32_16k" if args.profile == "sparse" else "grouped_21k_of_32k"]
+        base = WORKLOADS[args.profile_workload or ("v32_h32_16k" if args.profile == "sparse" else "grouped_21k_of_32k")]
         w = scaled_down(base, (n,), (base.N,), name=f"{base.name}_last{n}")
         x = make_sparse_inputs(w)
         q, kv = to_dev(x.q, dev), to_dev(x.kv, dev)
@@ -623,6 +623,8 @@ def main():
     ap.add_argument("--profile", choices=["sparse", "union", "grouped", "masked"], default=None,
                     help="run a small case of one kernel (for ncu) instead of the benchmark")
     ap.add_argument("--profile-tokens", type=int, default=2048)
+    ap.add_argument("--profile-workload", default=None,
+                    help="profile mode (sparse, union, grouped): base workload, e.g. nope_2x8192")
     ap.add_argument("--trace", type=int, default=0, help="profile mode: record a per-tile timeline of N tiles")
     ap.add_argument("--trace-out", default=None, help="profile mode: save the raw timeline (.npy)")
     args = ap.parse_args()

@@ -233,6 +233,9 @@ int dsa_grouped_prefill(const uint16_t* q, const uint16_t* kv, int N, int ld_kv,
                                 N > 0 ? ld_kv : d_qk, N > 0 ? ld_kv : d_qk))
     return DSA_ERR_CUDA;
   if (!dsa::make_tile_map(&a.tmap_q, q, (int64_t)T * H, d_qk, d_qk, 64)) return DSA_ERR_CUDA;
+  if (!dsa::make_tile_map(&a.tmap_kv_blk, N > 0 ? (const void*)kv : (const void*)q, N > 0 ? N : 1,
+                          N > 0 ? ld_kv : d_qk, N > 0 ? ld_kv : d_qk, 64))
+    return DSA_ERR_CUDA;
   const int r = dsa::launch_grouped_prefill(a, d->num_sms, (cudaStream_t)stream);
   return r == 0 ? DSA_OK : (r == -2 ? DSA_ERR_UNSUPPORTED : DSA_ERR_CUDA);
 }

@@ -273,6 +273,18 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// The same tiled load delivered to every CTA of the cluster named in
+// cta_mask, at the same shared-memory offset, each completing on its own
+// barrier at the offset of `bar`.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                               uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
+      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(cta_mask)
+      : "memory");
+}
+
 // Bounded wait that ignores the CTA abort flag: used on the way out to let
 // copies already in flight land before the CTA exits.
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, unsigned int* err) {
@@ -447,13 +459,12 @@ __device__ __forceinline__ void tmem_st16_u32(uint32_t taddr, const uint32_t* r)
 __device__ __forceinline__ void mma_bf16_ss_x4(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t da, uint32_t db,
                                                uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
+      "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "setp.eq.b32 q, %4, %4;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %6, %3, q;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %8, %3, q;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %9, %10, %3, q;\n\t}"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %6, %3, 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %8, %3, 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %9, %10, %3, 1;\n\t}"
       ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "l"(a + da), "l"(b + db), "l"(a + 2ull * da),
       "l"(b + 2ull * db), "l"(a + 3ull * da), "l"(b + 3ull * db)
       : "memory");
@@ -462,13 +473,12 @@ __device__ __forceinline__ void mma_bf16_ss_x4(uint32_t d_tmem, uint64_t a, uint
 __device__ __forceinline__ void mma_bf16_ts_x4(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t ta, uint32_t db,
                                                uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
+      "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "setp.eq.b32 q, %4, %4;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %6, %3, q;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %8, %3, q;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], %10, %3, q;\n\t}"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %6, %3, 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %8, %3, 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], %10, %3, 1;\n\t}"
       ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate), "r"(a_tmem + ta), "l"(b + db),
       "r"(a_tmem + 2 * ta), "l"(b + 2ull * db), "r"(a_tmem + 3 * ta), "l"(b + 3ull * db)
       : "memory");

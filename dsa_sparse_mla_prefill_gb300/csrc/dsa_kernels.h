@@ -60,8 +60,9 @@ struct KeyMaskArgs {
 };
 
 struct GroupedArgs {
-  CUtensorMap tmap_kv;  // kv rows for tile::gather4 (box 64 columns x 1 row, 128B swizzle)
-  CUtensorMap tmap_q;   // q viewed [T*H, d_qk], box 64 columns x 128 rows
+  CUtensorMap tmap_kv;      // kv rows for tile::gather4 (box 64 columns x 1 row, 128B swizzle)
+  CUtensorMap tmap_q;       // q viewed [T*H, d_qk], box 64 columns x 64 rows
+  CUtensorMap tmap_kv_blk;  // kv rows, box 64 columns x 64 rows (contiguous runs of the union)
   const uint16_t* q;
   const uint16_t* kv;
   const int32_t* union_idx;

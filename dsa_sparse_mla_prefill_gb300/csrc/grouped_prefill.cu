@@ -9,24 +9,27 @@
 // union row is gathered once per group instead of once per token.
 //
 // A group is processed by a cluster of two CTAs that split the pseudo-heads:
-// CTA r owns pseudo-heads 64r .. 64r+63 (its q rows: 64 x D_QK in shared
-// memory) and the matching 64 columns of the output.  Every union row is
+// CTA r owns pseudo-heads 64r .. 64r+63 (its q rows: 64 x D_QK) and the
+// matching 64 columns of the output.  Every union row is
 // fetched once per cluster: each CTA issues the tile::gather4 loads for half
 // of a tile's rows with cluster multicast, so both CTAs receive the whole
 // tile, and a stage is refilled only after both CTAs' MMAs released it
 // (tcgen05.commit multicast to both CTAs' barriers).  No scores cross the
 // cluster.  Within a CTA the data path is the per-token one with 64 heads:
 //   S^T = K q^T with the union slots on the M side (M = 128 slots, N = 64),
-//   streamed chunk by chunk (128 slots x 64 columns) through a K ring;
+//   streamed chunk by chunk through a K ring whose stages hold a K chunk
+//   (128 slots x 64 columns) and the matching q chunk (64 rows x 64
+//   columns, re-read from L2 every tile: q is not kept resident, which
+//   leaves room for five stages);
 //   O^T += V^T P^T per 128-column V unit (V re-gathered into a V ring, an L2
 //   hit), O^T = 4 x 64 TMEM columns, P^T double-buffered in shared memory;
 //   the online softmax (base 2, lazy rescale) runs with thread i <-> slot i
 //   (TMEM lane i) in eight warps, two per lane quarter, each holding 32 of
 //   the 64 pseudo-heads.
 // Warp roles (24 warps): 0-7 softmax (at REGS_SOFTMAX registers, the others
-// at REGS_OTHER), 8 QK issuer, 9 and 10 PV issuers (units 0/2 and 1/3),
-// 12-17 K-ring producers (two warps per K slot; warp 12 also loads q),
-// 18-23 V-ring producers (three warps per V slot); warp 11 is idle.
+// at REGS_OTHER), 8 and 11 QK issuers (alternate K chunks, two partial S^T
+// sums; warp 11 idle for 8-chunk rows), 9 and 10 PV issuers (units 0/2 and 1/3), 12-17 K-ring producers
+// (all six on every stage), 18-23 V-ring producers (three warps per V slot).
 #include "dsa_device.cuh"
 #include "dsa_kernels.h"
 
@@ -37,25 +40,33 @@ constexpr int BK = 128;          // union slots per tile (the MMA's M)
 constexpr int HC = 64;           // pseudo-heads per CTA (the MMA's N)
 constexpr int HW = 32;           // pseudo-heads per softmax warp
 constexpr int NTHREADS = 768;    // 24 warps, launched at 80 registers each
-constexpr int REGS_SOFTMAX = 152;
-constexpr int REGS_OTHER = 40;   // 8*32*152 + 16*32*40 <= 768*80
-constexpr int NKR = 3;           // K ring slots (one producer warp each)
+constexpr int REGS_SOFTMAX = 144;
+constexpr int REGS_OTHER = 48;   // 8*32*144 + 16*32*48 <= 768*80
+constexpr int NKW = 6;           // K producer warps
+constexpr int KLANES = 3;        // issuing lanes per K producer warp: 16 gathers + 1 q load
 constexpr int NVR = 2;           // V ring slots: unit m in slot m mod 2, PV issuer m mod 2
 constexpr uint16_t kPair = 3;    // multicast mask: both CTAs of the cluster
 constexpr float kTau = 8.0f;     // lazy-rescale threshold (log2 units)
 
 template <int NC>
 struct Cfg {
+  // QK issuing threads: two for the 9-chunk (NoPE + RoPE) rows, where one
+  // thread's per-chunk wait, fence and commit set the tile period; one for
+  // 8-chunk rows, where two made the softmax the slower stage (measured)
+  static constexpr int NQ = (NC % 2) ? 2 : 1;
+  // K ring stages (K chunk + q chunk each); even with two issuers, so that
+  // stage s is issuer s & 1's
+  static constexpr int NKR = NQ == 2 ? 4 : 5;
   static constexpr uint32_t CHUNK_BYTES = BK * 128u;          // 128 slots x 64 columns
   static constexpr uint32_t UNIT_BYTES = 2u * CHUNK_BYTES;    // 128 slots x 128 columns
   static constexpr uint32_t Q_CHUNK = HC * 128u;              // 64 rows x 64 columns
-  static constexpr uint32_t Q_BYTES = NC * Q_CHUNK;
+  static constexpr uint32_t KSTAGE_BYTES = CHUNK_BYTES + Q_CHUNK;
   static constexpr uint32_t P_BYTES = 2u * HC * 128u;         // 128 slots = 2 swizzle columns (x2 buffers)
   static constexpr uint32_t RED_BYTES = 2u * 2u * 4u * HW * 4u;  // [parity][half][warp][head]
   static constexpr uint32_t OFF_KR = 0;
-  static constexpr uint32_t OFF_VR = OFF_KR + NKR * CHUNK_BYTES;
-  static constexpr uint32_t OFF_Q = OFF_VR + NVR * UNIT_BYTES;
-  static constexpr uint32_t OFF_P = OFF_Q + Q_BYTES;
+  static constexpr uint32_t OFF_VR = OFF_KR + NKR * KSTAGE_BYTES;
+  static_assert(NKR <= 6 && (NQ == 1 || NKR % 2 == 0), "K ring layout");
+  static constexpr uint32_t OFF_P = OFF_VR + NVR * UNIT_BYTES;
   static constexpr uint32_t OFF_RED = OFF_P + 2 * P_BYTES;
   static constexpr uint32_t OFF_BAR = OFF_RED + RED_BYTES;
   static constexpr int NBAR = 32;
@@ -63,26 +74,26 @@ struct Cfg {
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 128u + 1024u;
   static_assert(SMEM_BYTES <= 227u * 1024u, "shared memory budget");
   static constexpr uint32_t COL_O = 0;       // O^T: 4 units x 64 columns
-  static constexpr uint32_t COL_S = 256;     // S^T: 2 x 64 columns
+  static constexpr uint32_t COL_S = 256;     // S^T: 2 buffers x 2 partial sums x 64 columns
   static constexpr uint32_t TMEM_COLS = 512;
 };
 
 enum {
-  B_Q_FULL = 0,
-  B_Q_EMPTY = 1,
-  B_S_FULL = 2,      // [2]
-  B_S_EMPTY = 4,     // [2]
-  B_P_FULL = 6,      // [2] 256 arrivals (softmax threads)
-  B_P_EMPTY = 8,     // [2] one commit per PV issuer
-  B_O_FULL = 10,     // one commit per PV issuer
-  B_O_EMPTY = 11,    // 256 arrivals
-  B_DRAIN = 12,      // [3] one per MMA issuer
-  B_SMX_SYNC = 15,   // [2] one per head half (4 warps)
-  B_KR_FULL = 17,    // [NKR <= 4]
-  B_KR_EMPTY = 21,   // [NKR <= 4] one QK commit from each CTA
-  B_VR_FULL = 25,    // [NVR]
-  B_VR_EMPTY = 27,   // [NVR] one PV commit from each CTA
+  B_S_FULL = 0,      // [2] one commit per QK issuer
+  B_S_EMPTY = 2,     // [2]
+  B_P_FULL = 4,      // [2] 256 arrivals (softmax threads)
+  B_P_EMPTY = 6,     // [2] one commit per PV issuer
+  B_O_FULL = 8,      // one commit per PV issuer
+  B_O_EMPTY = 9,     // 256 arrivals
+  B_DRAIN = 10,      // [4] one per MMA issuer
+  B_SMX_SYNC = 14,   // [2] one per head half (4 warps)
+  B_KR_FULL = 16,    // [NKR <= 6]
+  B_KR_EMPTY = 22,   // [NKR <= 6] one QK commit from each CTA
+  B_VR_FULL = 28,    // [NVR]
+  B_VR_EMPTY = 30,   // [NVR] one PV commit from each CTA
 };
+static_assert(NVR <= 2, "barrier layout");
+static_assert(NKW * KLANES >= 17, "K stage requests");
 
 __device__ __forceinline__ void group_of(const ReqTable& rq, int G, int g, int& t0, int& n) {
   int r = 0;
@@ -156,10 +167,8 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
   const int ncl = (int)nclusters_x();
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars[B_Q_FULL], 1);
-    mbar_init(&bars[B_Q_EMPTY], 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars[B_S_FULL + i], 1);
+      mbar_init(&bars[B_S_FULL + i], C::NQ);
       mbar_init(&bars[B_S_EMPTY + i], 256);
       mbar_init(&bars[B_SMX_SYNC + i], 128);
     }
@@ -169,8 +178,8 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
     }
     mbar_init(&bars[B_O_FULL], 2);
     mbar_init(&bars[B_O_EMPTY], 256);
-    for (int i = 0; i < 3; ++i) mbar_init(&bars[B_DRAIN + i], 1);
-    for (int i = 0; i < NKR; ++i) {
+    for (int i = 0; i < 4; ++i) mbar_init(&bars[B_DRAIN + i], 1);
+    for (int i = 0; i < C::NKR; ++i) {
       mbar_init(&bars[B_KR_FULL + i], 1);
       mbar_init(&bars[B_KR_EMPTY + i], 2);
     }
@@ -195,29 +204,33 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
     regs_dec<REGS_OTHER>();
     if (warp >= 12) {
       // ----------------------------------------------------------------
-      // TMA producers.  K stream (warps 12-17): the two warps 12+s and 15+s
-      // fill K slot s with chunk c (slots x columns 64c .. 64c+63) of a
-      // tile, lanes 0-7 of each gathering half of this CTA's 16 row groups
-      // (slots 64 rank .. +63) for both CTAs.  V stream (warps 18-23): the
+      // TMA producers.  K stream (warps 12-17): every stage (K chunk c of a
+      // tile: slots x columns 64c .. 64c+63, plus q chunk c of this CTA's 64
+      // pseudo-heads) is filled by all six warps, lanes 0-2 of each: requests
+      // 0-15 gather this CTA's 16 row groups (slots 64 rank .. +63) for both
+      // CTAs, request 16 loads the local q chunk.  V stream (warps 18-23): the
       // three warps of group u fill V slot u with the 128-column units
       // m = u, u+2 of every tile, sharing this CTA's 32 gathers of a unit.
-      // A stage's leader (lane 0 of the first warp of the slot) arms the
-      // full byte count of the stage: both CTAs' halves land in both.  Warp
-      // 12 also loads q.  Every warp of a slot passes through each of its
-      // phases in order.
+      // When this CTA's 64 slots of the tile are one contiguous run of rows,
+      // each of its 64-row halves is one tiled load (box 64 columns x 64
+      // rows) instead of 16 gathers.  The union lists distinct rows in
+      // ascending order, so the run test needs only the two end slots.
+      // A stage's leader (lane 0 of warp 12 for K, of the group's first warp
+      // for V) arms the full byte count of the stage: both CTAs' halves land
+      // in both.  Every warp of a slot passes through each of its phases in
+      // order.
       // ----------------------------------------------------------------
       const bool kstream = warp < 18;
-      const int ks = (warp - 12) % NKR;         // K slot owned
-      const int ksub = (warp - 12) / NKR;
+      const int kreq = (warp - 12) * KLANES + lane;   // K request of this lane
       const int vg = (warp - 18) / 3;           // V slot owned
       const int vsub = (warp - 18) % 3;
       const int e = vsub * 11 + lane;           // V gather index 0..31 of this CTA
-      const bool issuer = kstream ? (lane < 8) : (lane < 11 && e < 32);
-      const int rg = 16 * rank + (kstream ? 8 * ksub + (lane & 7) : (e & 15));   // row group of the tile
+      const bool issuer = kstream ? (lane < KLANES && kreq < 17) : (lane < 11 && e < 32);
+      const bool kgather = kstream && lane < KLANES && kreq < 16;
+      const int rg = 16 * rank + (kstream ? (kreq & 15) : (e & 15));   // row group of the tile
       const int vcc = (e >> 4) & 1;             // V swizzle column
-      const bool leader = (lane == 0) && (kstream ? ksub == 0 : vsub == 0);
-      const uint32_t q_s = sbase + C::OFF_Q;
-      uint32_t gt = 0, pos = 0, lgq = 0;
+      const bool leader = (lane == 0) && (kstream ? warp == 12 : vsub == 0);
+      uint32_t gt = 0, pos = 0;
       int64_t last_armed = -1;
       bool ok = true;
       for (int g = cid; g < a.num_groups && ok; g += ncl) {
@@ -226,33 +239,41 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
         const int U = min(__ldg(a.union_len + g), a.union_pad);
         const int ntiles = (U + BK - 1) / BK;
         if (ntiles == 0) continue;
-        if (warp == 12) {
-          // q rows t0*H + 64 rank .. +63 of q viewed [T*H, D_QK], one box per swizzle column
-          if (!mbar_wait_warp(&bars[B_Q_EMPTY], (lgq & 1) ^ 1, abort_flag, err)) { ok = false; break; }
-          if (lane == 0) {
-            mbar_arrive_expect_tx(&bars[B_Q_FULL], C::Q_BYTES);
-            for (int c = 0; c < NC; ++c)
-              tma_load_2d(q_s + c * C::Q_CHUNK, &a.tmap_q, c * 64, t0 * H + HC * rank, &bars[B_Q_FULL]);
-          }
-        }
         const int32_t* urow = a.union_idx + (size_t)g * a.union_pad;
         for (int j = 0; j < ntiles && ok; ++j, ++gt) {
           if (warp == 12 && lane == 0) DSA_TRACE(a.tr, gt, 0);
-          const int4 r = union_rows4(urow, U, a.N, j * BK + 4 * rg);
+          const int u0 = j * BK + HC * rank;   // this CTA's 64 slots of the tile
+          int first = -1;
+          bool run = false;
+          if (u0 + HC - 1 < U) {
+            first = __ldg(urow + u0);
+            const int last = __ldg(urow + u0 + HC - 1);
+            run = first >= 0 && last < a.N && last - first == HC - 1;
+          }
+          const uint32_t half_off = (uint32_t)rank * (C::CHUNK_BYTES / 2);
           if (kstream) {
+            const int4 r = (kgather && !run) ? union_rows4(urow, U, a.N, j * BK + 4 * rg) : make_int4(-1, -1, -1, -1);
             for (int c = 0; c < NC; ++c, ++pos) {
-              if ((int)(pos % NKR) != ks) continue;
-              if (!mbar_wait_warp(&bars[B_KR_EMPTY + ks], ((pos / NKR) & 1) ^ 1, abort_flag, err)) {
+              const int ks = (int)(pos % C::NKR);
+              if (!mbar_wait_warp(&bars[B_KR_EMPTY + ks], ((pos / C::NKR) & 1) ^ 1, abort_flag, err)) {
                 ok = false;
                 break;
               }
-              if (leader) mbar_arrive_expect_tx(&bars[B_KR_FULL + ks], C::CHUNK_BYTES);
-              if (issuer)
-                tma_gather4_mc(sbase + C::OFF_KR + ks * C::CHUNK_BYTES + rg * 512, &a.tmap_kv, c * 64, r.x, r.y, r.z,
-                               r.w, &bars[B_KR_FULL + ks], kPair);
+              const uint32_t stage = sbase + C::OFF_KR + ks * C::KSTAGE_BYTES;
+              if (leader) mbar_arrive_expect_tx(&bars[B_KR_FULL + ks], C::KSTAGE_BYTES);
+              if (run) {
+                if (kreq == 0)
+                  tma_load_2d_mc(stage + half_off, &a.tmap_kv_blk, c * 64, first, &bars[B_KR_FULL + ks], kPair);
+              } else if (kgather) {
+                tma_gather4_mc(stage + rg * 512, &a.tmap_kv, c * 64, r.x, r.y, r.z, r.w, &bars[B_KR_FULL + ks], kPair);
+              }
+              if (issuer && !kgather)
+                // q rows t0*H + 64 rank .. +63 of q viewed [T*H, D_QK], columns 64c ..
+                tma_load_2d(stage + C::CHUNK_BYTES, &a.tmap_q, c * 64, t0 * H + HC * rank, &bars[B_KR_FULL + ks]);
               last_armed = pos;
             }
           } else {
+            const int4 r = (issuer && !run) ? union_rows4(urow, U, a.N, j * BK + 4 * rg) : make_int4(-1, -1, -1, -1);
             for (int m = 0; m < 4; ++m, ++pos) {
               if ((int)(pos % NVR) != vg) continue;
               if (!mbar_wait_warp(&bars[B_VR_EMPTY + vg], ((pos / NVR) & 1) ^ 1, abort_flag, err)) {
@@ -260,67 +281,77 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
                 break;
               }
               if (leader) mbar_arrive_expect_tx(&bars[B_VR_FULL + vg], C::UNIT_BYTES);
-              if (issuer)
-                tma_gather4_mc(sbase + C::OFF_VR + vg * C::UNIT_BYTES + vcc * C::CHUNK_BYTES + rg * 512, &a.tmap_kv,
-                               (2 * m + vcc) * 64, r.x, r.y, r.z, r.w, &bars[B_VR_FULL + vg], kPair);
+              const uint32_t vdst = sbase + C::OFF_VR + vg * C::UNIT_BYTES + vcc * C::CHUNK_BYTES;
+              if (run) {
+                if (issuer && (e & 15) == 0)
+                  tma_load_2d_mc(vdst + half_off, &a.tmap_kv_blk, (2 * m + vcc) * 64, first, &bars[B_VR_FULL + vg],
+                                 kPair);
+              } else if (issuer) {
+                tma_gather4_mc(vdst + rg * 512, &a.tmap_kv, (2 * m + vcc) * 64, r.x, r.y, r.z, r.w,
+                               &bars[B_VR_FULL + vg], kPair);
+              }
               last_armed = pos;
             }
           }
         }
-        ++lgq;
       }
       // Let copies still in flight land before the CTA can exit: the last
-      // phase of the slot this warp arms completes only once both CTAs'
-      // bytes have landed here.
-      if (leader) {
-        if (warp == 12 && lgq > 0) mbar_wait_drain(&bars[B_Q_FULL], (lgq - 1) & 1, err);
-        if (last_armed >= 0) {
-          if (kstream)
-            mbar_wait_drain(&bars[B_KR_FULL + ks], (uint32_t)(last_armed / NKR) & 1, err);
-          else
-            mbar_wait_drain(&bars[B_VR_FULL + vg], (uint32_t)(last_armed / NVR) & 1, err);
+      // phase of every stage this warp's leader armed completes only once
+      // both CTAs' bytes have landed here.
+      if (leader && last_armed >= 0) {
+        if (kstream) {
+          for (int64_t p = last_armed; p >= 0 && p > last_armed - C::NKR; --p)
+            mbar_wait_drain(&bars[B_KR_FULL + (int)(p % C::NKR)], (uint32_t)(p / C::NKR) & 1, err);
+        } else {
+          mbar_wait_drain(&bars[B_VR_FULL + vg], (uint32_t)(last_armed / NVR) & 1, err);
         }
       }
       __syncwarp();
-    } else if (warp == 8) {
+    } else if (warp == 8 || (warp == 11 && C::NQ == 2)) {
       // ----------------------------------------------------------------
-      // QK issuer: S^T = K q^T chunk by chunk into the S double buffer; each
-      // K chunk is released to both CTAs' producers once its MMAs complete
+      // QK issuers: S^T = K q^T chunk by chunk.  With two issuing threads
+      // the chunks alternate between them (warp 8 takes ring positions of
+      // even parity, warp 11 odd ones; with an even ring size each stage
+      // belongs to one of them), each summing into its own partial S^T; the
+      // softmax adds the two.  One thread issuing every chunk spends most of
+      // its time in the per-chunk wait, fence and commit, not in MMAs.
+      // Each K chunk is released to both CTAs' producers once its MMAs
+      // complete; S_FULL takes one commit from each issuer.
       // ----------------------------------------------------------------
+      const uint32_t qa = warp == 8 ? 0u : 1u;
       if (lane == 0) {
         constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, HC, false, false);
-        const uint32_t q_s = sbase + C::OFF_Q;
-        uint32_t gt = 0, kpos = 0, lgq = 0;
+        uint32_t gt = 0, kpos = 0;
         bool ok = true;
         for (int g = cid; g < a.num_groups && ok; g += ncl) {
           const int U = min(__ldg(a.union_len + g), a.union_pad);
           const int ntiles = (U + BK - 1) / BK;
           if (ntiles == 0) continue;
-          if (!mbar_wait(&bars[B_Q_FULL], lgq & 1, abort_flag, err)) { ok = false; break; }
-          tc_fence_after();
           for (int j = 0; j < ntiles && ok; ++j, ++gt) {
             const int sb = gt & 1;
-            const uint32_t d_s = tmem + C::COL_S + sb * HC;
+            const uint32_t d_s = tmem + C::COL_S + (2 * sb + qa) * HC;
             if (!mbar_wait(&bars[B_S_EMPTY + sb], ((gt >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
-            DSA_TRACE(a.tr, gt, 2);
+            if (qa == 0) DSA_TRACE(a.tr, gt, 2);
             tc_fence_after();
+            bool first = true;
             for (int c = 0; c < NC; ++c, ++kpos) {
-              const uint32_t slot = kpos % NKR;
-              if (!mbar_wait(&bars[B_KR_FULL + slot], (kpos / NKR) & 1, abort_flag, err)) { ok = false; break; }
+              if (C::NQ == 2 && (kpos & 1u) != qa) continue;
+              const uint32_t slot = kpos % C::NKR;
+              if (!mbar_wait(&bars[B_KR_FULL + slot], (kpos / C::NKR) & 1, abort_flag, err)) { ok = false; break; }
               tc_fence_after();
-              mma_bf16_ss_x4(d_s, sdesc_sw128(sbase + C::OFF_KR + slot * C::CHUNK_BYTES, 16, 1024),
-                             sdesc_sw128(q_s + c * C::Q_CHUNK, 16, 1024), 2u, 2u, IDESC_QK, c > 0 ? 1u : 0u);
+              const uint32_t stage = sbase + C::OFF_KR + slot * C::KSTAGE_BYTES;
+              mma_bf16_ss_x4(d_s, sdesc_sw128(stage, 16, 1024), sdesc_sw128(stage + C::CHUNK_BYTES, 16, 1024), 2u, 2u,
+                             IDESC_QK, first ? 0u : 1u);
               mma_commit_mc(&bars[B_KR_EMPTY + slot], kPair);
+              first = false;
             }
             if (!ok) break;
-            DSA_TRACE(a.tr, gt, 1);
+            if (qa == 0) DSA_TRACE(a.tr, gt, 1);
             mma_commit(&bars[B_S_FULL + sb]);
-            if (j == ntiles - 1) mma_commit(&bars[B_Q_EMPTY]);
           }
-          ++lgq;
         }
-        mma_commit(&bars[B_DRAIN + 0]);
-        mbar_wait(&bars[B_DRAIN + 0], 0, abort_flag, err);
+        mma_commit(&bars[B_DRAIN + 2 + qa]);
+        mbar_wait(&bars[B_DRAIN + 2 + qa], 0, abort_flag, err);
       }
       __syncwarp();
     } else if (warp == 9 || warp == 10) {
@@ -371,8 +402,8 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
           }
           ++lgq;
         }
-        mma_commit(&bars[B_DRAIN + 1 + pvi]);
-        mbar_wait(&bars[B_DRAIN + 1 + pvi], 0, abort_flag, err);
+        mma_commit(&bars[B_DRAIN + pvi]);
+        mbar_wait(&bars[B_DRAIN + pvi], 0, abort_flag, err);
       }
       __syncwarp();
     }
@@ -426,11 +457,27 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
         if (!mbar_wait_warp(&bars[B_S_FULL + sb], (gt >> 1) & 1, abort_flag, err)) { ok = false; break; }
         if (key == 0 && hh == 0) DSA_TRACE(a.tr, gt, 3);
         tc_fence_after();
+        // S^T = the QK issuers' partial sums
         float s[HW];
-        tmem_ld_cols<HW>(tmem + lane_off + C::COL_S + sb * HC + HW * hh, s);
-        tmem_ld_wait();
+        const uint32_t s_addr = tmem + lane_off + C::COL_S + 2 * sb * HC + HW * hh;
+        if constexpr (C::NQ == 2) {
+#pragma unroll
+          for (int q16 = 0; q16 < HW / 16; ++q16) {
+            float t[16];
+            tmem_ld16(s_addr + 16 * q16, s + 16 * q16);
+            tmem_ld16(s_addr + HC + 16 * q16, t);
+            tmem_ld_wait();
+#pragma unroll
+            for (int h = 0; h < 16; ++h) s[16 * q16 + h] += t[h];
+          }
+        } else {
+#pragma unroll
+          for (int q16 = 0; q16 < HW / 16; ++q16) tmem_ld16(s_addr + 16 * q16, s + 16 * q16);
+          tmem_ld_wait();
+        }
         tc_fence_before();
         mbar_arrive(&bars[B_S_EMPTY + sb]);
+        if (key == 0 && hh == 0) DSA_TRACE(a.tr, gt, 5);
         bool mine = false;
 #pragma unroll
         for (int h = 0; h < HW; ++h) {

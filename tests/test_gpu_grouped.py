@@ -94,6 +94,36 @@ def test_grouped_full_size_sampled(name):
     assert res["ok"], res
 
 
+@pytest.mark.parametrize("H,G", [(16, 8), (32, 4)])
+def test_grouped_contiguous_runs(H, G):
+    """Unions made of long runs of consecutive rows: dense sliding windows in
+    the first request, and in the second a run that ends at the table's last
+    row next to scattered rows.  Whole 64-slot halves of a tile are then one
+    contiguous block (fetched as one tiled load) beside gathered halves, with
+    runs that start and end inside a half and ragged union tails."""
+    rng = np.random.default_rng(5 + H)
+    k, N = 320, 700
+    q_lens = [300, 37]
+    T = sum(q_lens)
+    cu = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    q = normal_bf16(rng, (T, H, 576))
+    kv = normal_bf16(rng, (N, 576))
+    idx = np.full((T, k), -1, dtype=np.int32)
+    for t in range(q_lens[0]):
+        rows = np.arange(max(0, t - k + 1), t + 1, dtype=np.int32)
+        idx[t, :len(rows)] = rng.permutation(rows)
+    for i in range(q_lens[1]):
+        sel = np.concatenate([np.arange(N - 150, N), rng.choice(N - 150, size=100 + i, replace=False)])
+        idx[q_lens[0] + i, :len(sel)] = rng.permutation(sel).astype(np.int32)
+    (u, ul, m), o, l = run_grouped(q, kv, idx, k, G, N, cu, 0.07)
+    upad = O.union_pad(G, k, 128)
+    ru, rl, rm = O.union_build(idx, k, G, N, cu, upad)
+    assert np.array_equal(ul, rl) and np.array_equal(u, ru) and np.array_equal(m, rm)
+    po, pl = O.sparse_prefill(q, kv, idx, k, 0.07, 576, 512)
+    res = O.compare(o, l, po, pl)
+    assert res["ok"], res
+
+
 def test_grouped_equals_per_token_kernel():
     """The two GPU forms agree with each other on a mid-size workload."""
     import dsa_sparse_mla_prefill_gb300 as dsa
