@@ -22,14 +22,16 @@
 //   columns, re-read from L2 every tile: q is not kept resident, which
 //   leaves room for five stages);
 //   O^T += V^T P^T per 128-column V unit (V re-gathered into a V ring, an L2
-//   hit), O^T = 4 x 64 TMEM columns, P^T double-buffered in shared memory;
+//   hit), O^T = 4 x 64 TMEM columns, P^T in shared memory (one or two buffers);
 //   the online softmax (base 2, lazy rescale) runs with thread i <-> slot i
 //   (TMEM lane i) in eight warps, two per lane quarter, each holding 32 of
 //   the 64 pseudo-heads.
 // Warp roles (24 warps): 0-7 softmax (at REGS_SOFTMAX registers, the others
 // at REGS_OTHER), 8 and 11 QK issuers (alternate K chunks, two partial S^T
-// sums; warp 11 idle for 8-chunk rows), 9 and 10 PV issuers (units 0/2 and 1/3), 12-17 K-ring producers
-// (all six on every stage), 18-23 V-ring producers (three warps per V slot).
+// sums; warp 11 idle for 8-chunk rows), 9 and 10 PV issuers (units 0/2 and
+// 1/3), 12-17 K-ring producers (one per stage for 9-chunk rows, all six on
+// every stage for 8-chunk rows), 18-23 V-ring producers (three warps per V
+// slot).
 #include "dsa_device.cuh"
 #include "dsa_kernels.h"
 
@@ -42,8 +44,7 @@ constexpr int HW = 32;           // pseudo-heads per softmax warp
 constexpr int NTHREADS = 768;    // 24 warps, launched at 80 registers each
 constexpr int REGS_SOFTMAX = 144;
 constexpr int REGS_OTHER = 48;   // 8*32*144 + 16*32*48 <= 768*80
-constexpr int NKW = 6;           // K producer warps
-constexpr int KLANES = 3;        // issuing lanes per K producer warp: 16 gathers + 1 q load
+constexpr int NKW = 6;           // K producer warps (one per K stage)
 constexpr int NVR = 2;           // V ring slots: unit m in slot m mod 2, PV issuer m mod 2
 constexpr uint16_t kPair = 3;    // multicast mask: both CTAs of the cluster
 constexpr float kTau = 8.0f;     // lazy-rescale threshold (log2 units)
@@ -55,23 +56,33 @@ struct Cfg {
   // 8-chunk rows, where two made the softmax the slower stage (measured)
   static constexpr int NQ = (NC % 2) ? 2 : 1;
   // K ring stages (K chunk + q chunk each); even with two issuers, so that
-  // stage s is issuer s & 1's
-  static constexpr int NKR = NQ == 2 ? 4 : 5;
+  // stage s is issuer s & 1's.  With two issuers the softmax keeps ahead of
+  // P.V, so one P^T buffer serves and its 16 KB go to the K ring.
+  static constexpr int NKR = NQ == 2 ? 6 : 5;
+  static constexpr int NPB = NQ == 2 ? 1 : 2;   // P^T buffers
+  // slack for aligning the dynamic shared memory to 1024 bytes; the 6-stage
+  // layout has no room for it and requires an aligned base (checked at
+  // entry: the launch stops and counts an early stop otherwise)
+  static constexpr uint32_t ALIGN_SLACK = NQ == 2 ? 0u : 1024u;
+  // K producers: with two issuers warp 12+s owns stage s (17 lanes issue a
+  // stage); with one, all six warps take part in every stage (3 lanes each).
+  // Both measured per layout: each is the faster one where it is used.
+  static constexpr bool OWNED = NQ == 2;
   static constexpr uint32_t CHUNK_BYTES = BK * 128u;          // 128 slots x 64 columns
   static constexpr uint32_t UNIT_BYTES = 2u * CHUNK_BYTES;    // 128 slots x 128 columns
   static constexpr uint32_t Q_CHUNK = HC * 128u;              // 64 rows x 64 columns
   static constexpr uint32_t KSTAGE_BYTES = CHUNK_BYTES + Q_CHUNK;
-  static constexpr uint32_t P_BYTES = 2u * HC * 128u;         // 128 slots = 2 swizzle columns (x2 buffers)
+  static constexpr uint32_t P_BYTES = 2u * HC * 128u;         // one buffer: 128 slots = 2 swizzle columns
   static constexpr uint32_t RED_BYTES = 2u * 2u * 4u * HW * 4u;  // [parity][half][warp][head]
   static constexpr uint32_t OFF_KR = 0;
   static constexpr uint32_t OFF_VR = OFF_KR + NKR * KSTAGE_BYTES;
-  static_assert(NKR <= 6 && (NQ == 1 || NKR % 2 == 0), "K ring layout");
+  static_assert(NKR <= NKW && (NQ == 1 || NKR % 2 == 0), "K ring layout: one producer warp per stage");
   static constexpr uint32_t OFF_P = OFF_VR + NVR * UNIT_BYTES;
-  static constexpr uint32_t OFF_RED = OFF_P + 2 * P_BYTES;
+  static constexpr uint32_t OFF_RED = OFF_P + NPB * P_BYTES;
   static constexpr uint32_t OFF_BAR = OFF_RED + RED_BYTES;
   static constexpr int NBAR = 32;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8u;
-  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 128u + 1024u;
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 128u + ALIGN_SLACK;
   static_assert(SMEM_BYTES <= 227u * 1024u, "shared memory budget");
   static constexpr uint32_t COL_O = 0;       // O^T: 4 units x 64 columns
   static constexpr uint32_t COL_S = 256;     // S^T: 2 buffers x 2 partial sums x 64 columns
@@ -81,8 +92,8 @@ struct Cfg {
 enum {
   B_S_FULL = 0,      // [2] one commit per QK issuer
   B_S_EMPTY = 2,     // [2]
-  B_P_FULL = 4,      // [2] 256 arrivals (softmax threads)
-  B_P_EMPTY = 6,     // [2] one commit per PV issuer
+  B_P_FULL = 4,      // [NPB] 256 arrivals (softmax threads)
+  B_P_EMPTY = 6,     // [NPB] one commit per PV issuer
   B_O_FULL = 8,      // one commit per PV issuer
   B_O_EMPTY = 9,     // 256 arrivals
   B_DRAIN = 10,      // [4] one per MMA issuer
@@ -93,7 +104,7 @@ enum {
   B_VR_EMPTY = 30,   // [NVR] one PV commit from each CTA
 };
 static_assert(NVR <= 2, "barrier layout");
-static_assert(NKW * KLANES >= 17, "K stage requests");
+
 
 __device__ __forceinline__ void group_of(const ReqTable& rq, int G, int g, int& t0, int& n) {
   int r = 0;
@@ -150,6 +161,11 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
   using C = Cfg<NC>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
+  if (C::ALIGN_SLACK == 0 && (raw_u32 & 1023u) != 0) {
+    // same base in every CTA of the launch: the whole grid stops here
+    if (threadIdx.x == 0) atomicAdd(a.err + ERR_TIMEOUT, 1u);
+    return;
+  }
   uint8_t* smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
   const uint32_t sbase = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
@@ -172,7 +188,7 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
       mbar_init(&bars[B_S_EMPTY + i], 256);
       mbar_init(&bars[B_SMX_SYNC + i], 128);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::NPB; ++i) {
       mbar_init(&bars[B_P_FULL + i], 256);
       mbar_init(&bars[B_P_EMPTY + i], 2);
     }
@@ -204,32 +220,38 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
     regs_dec<REGS_OTHER>();
     if (warp >= 12) {
       // ----------------------------------------------------------------
-      // TMA producers.  K stream (warps 12-17): every stage (K chunk c of a
-      // tile: slots x columns 64c .. 64c+63, plus q chunk c of this CTA's 64
-      // pseudo-heads) is filled by all six warps, lanes 0-2 of each: requests
-      // 0-15 gather this CTA's 16 row groups (slots 64 rank .. +63) for both
-      // CTAs, request 16 loads the local q chunk.  V stream (warps 18-23): the
+      // TMA producers.  K stream (warps 12-17): a stage holds K chunk c of a
+      // tile (slots x columns 64c .. 64c+63) plus q chunk c of this CTA's 64
+      // pseudo-heads; requests 0-15 gather this CTA's 16 row groups (slots
+      // 64 rank .. +63) for both CTAs, request 16 loads the local q chunk.
+      // OWNED: warp 12+s fills stage s with every chunk that maps there,
+      // lanes 0-16 issuing (a warp's per-stage loop of wait, arm and issue
+      // costs several hundred cycles, so stages are filled side by side);
+      // otherwise all six warps take part in every stage, lanes 0-2 of each.
+      // V stream (warps 18-23): the
       // three warps of group u fill V slot u with the 128-column units
       // m = u, u+2 of every tile, sharing this CTA's 32 gathers of a unit.
       // When this CTA's 64 slots of the tile are one contiguous run of rows,
       // each of its 64-row halves is one tiled load (box 64 columns x 64
       // rows) instead of 16 gathers.  The union lists distinct rows in
       // ascending order, so the run test needs only the two end slots.
-      // A stage's leader (lane 0 of warp 12 for K, of the group's first warp
-      // for V) arms the full byte count of the stage: both CTAs' halves land
-      // in both.  Every warp of a slot passes through each of its phases in
+      // A stage's leader (lane 0 of its K warp, or of warp 12, and of the
+      // group's first warp for V) arms the full byte count of the stage: both CTAs' halves land in
+      // both.  Every warp of a slot passes through each of its phases in
       // order.
       // ----------------------------------------------------------------
       const bool kstream = warp < 18;
-      const int kreq = (warp - 12) * KLANES + lane;   // K request of this lane
+      const int kw = warp - 12;                 // K stage owned (OWNED; none past the ring)
+      // K request of this lane: 0-15 gathers, 16 the q chunk
+      const int kreq = C::OWNED ? lane : kw * 3 + (lane < 3 ? lane : 32);
       const int vg = (warp - 18) / 3;           // V slot owned
       const int vsub = (warp - 18) % 3;
       const int e = vsub * 11 + lane;           // V gather index 0..31 of this CTA
-      const bool issuer = kstream ? (lane < KLANES && kreq < 17) : (lane < 11 && e < 32);
-      const bool kgather = kstream && lane < KLANES && kreq < 16;
+      const bool issuer = kstream ? (kreq < 17) : (lane < 11 && e < 32);
+      const bool kgather = kstream && kreq < 16;
       const int rg = 16 * rank + (kstream ? (kreq & 15) : (e & 15));   // row group of the tile
       const int vcc = (e >> 4) & 1;             // V swizzle column
-      const bool leader = (lane == 0) && (kstream ? warp == 12 : vsub == 0);
+      const bool leader = (lane == 0) && (kstream ? (C::OWNED || kw == 0) : vsub == 0);
       uint32_t gt = 0, pos = 0;
       int64_t last_armed = -1;
       bool ok = true;
@@ -255,6 +277,7 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
             const int4 r = (kgather && !run) ? union_rows4(urow, U, a.N, j * BK + 4 * rg) : make_int4(-1, -1, -1, -1);
             for (int c = 0; c < NC; ++c, ++pos) {
               const int ks = (int)(pos % C::NKR);
+              if (C::OWNED && ks != kw) continue;
               if (!mbar_wait_warp(&bars[B_KR_EMPTY + ks], ((pos / C::NKR) & 1) ^ 1, abort_flag, err)) {
                 ok = false;
                 break;
@@ -300,8 +323,10 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
       // both CTAs' bytes have landed here.
       if (leader && last_armed >= 0) {
         if (kstream) {
+          // the last phase of every stage this leader armed
           for (int64_t p = last_armed; p >= 0 && p > last_armed - C::NKR; --p)
-            mbar_wait_drain(&bars[B_KR_FULL + (int)(p % C::NKR)], (uint32_t)(p / C::NKR) & 1, err);
+            if (!C::OWNED || (int)(p % C::NKR) == kw)
+              mbar_wait_drain(&bars[B_KR_FULL + (int)(p % C::NKR)], (uint32_t)(p / C::NKR) & 1, err);
         } else {
           mbar_wait_drain(&bars[B_VR_FULL + vg], (uint32_t)(last_armed / NVR) & 1, err);
         }
@@ -371,8 +396,9 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
           const int ntiles = (U + BK - 1) / BK;
           if (ntiles == 0) continue;
           for (int j = 0; j < ntiles && ok; ++j, ++gt) {
-            const int pb = gt & 1;
-            if (!mbar_wait(&bars[B_P_FULL + pb], (gt >> 1) & 1, abort_flag, err)) { ok = false; break; }
+            const int pb = C::NPB == 2 ? (int)(gt & 1) : 0;
+            const uint32_t pph = C::NPB == 2 ? (gt >> 1) : gt;   // phase of P buffer pb
+            if (!mbar_wait(&bars[B_P_FULL + pb], pph & 1, abort_flag, err)) { ok = false; break; }
             if (pvi == 0) DSA_TRACE(a.tr, gt, 7);
             tc_fence_after();
             if (j == 0) {
@@ -448,7 +474,8 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
       float l_l = 0.f;        // this warp's running sum of head `lane`
       for (int j = 0; j < ntiles; ++j, ++gt) {
         const int sb = gt & 1;
-        const int pb = gt & 1;
+        const int pb = C::NPB == 2 ? (int)(gt & 1) : 0;
+        const uint32_t pph = C::NPB == 2 ? (gt >> 1) : gt;   // phase of P buffer pb
         // this slot's membership byte (zero past the union)
         const int u = j * BK + key;
         const uint32_t mbyte = (u < U) ? (uint32_t)__ldg(mrow + u) : 0u;
@@ -517,8 +544,8 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
           m_l = mn;
           l_l *= alpha_l;
         }
-        // P buffer pb was last read by P.V two tiles ago
-        if (!mbar_wait_warp(&bars[B_P_EMPTY + pb], ((gt >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+        // P buffer pb was last read by the P.V NPB tiles ago
+        if (!mbar_wait_warp(&bars[B_P_EMPTY + pb], (pph & 1) ^ 1, abort_flag, err)) { ok = false; break; }
         // P^T[head][slot] (K-major swizzled, 2 columns of 64 slots); s[] becomes
         // the bf16-rounded P for the row sums
         {
@@ -536,7 +563,9 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
         l_l += warp_transpose_reduce32<false>(s);
         if (need && j > 0) {
           // O must hold the previous tile's P.V before it is rescaled
-          if (!mbar_wait_warp(&bars[B_P_EMPTY + ((gt - 1) & 1)], ((gt - 1) >> 1) & 1, abort_flag, err)) {
+          const int pbp = C::NPB == 2 ? (int)((gt - 1) & 1) : 0;
+          const uint32_t pphp = C::NPB == 2 ? ((gt - 1) >> 1) : (gt - 1);
+          if (!mbar_wait_warp(&bars[B_P_EMPTY + pbp], pphp & 1, abort_flag, err)) {
             ok = false;
             break;
           }
