@@ -544,23 +544,31 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
           m_l = mn;
           l_l *= alpha_l;
         }
-        // P buffer pb was last read by the P.V NPB tiles ago
+        // P (bf16) and its row sums first, in registers: only the stores
+        // into the P^T buffer wait for the P.V that last read it (NPB tiles
+        // ago); s[] becomes the bf16-rounded P for the row sums
+        uint32_t pk[HW / 2];
+#pragma unroll
+        for (int h = 0; h < HW; h += 2) {
+          const float m0 = __shfl_sync(0xffffffffu, m_l, h);
+          const float m1 = __shfl_sync(0xffffffffu, m_l, h + 1);
+          const uint16_t b0 = f32_to_bf16_rn(exp2f(s[h] - ((m0 == -INFINITY) ? 0.f : m0)));
+          const uint16_t b1 = f32_to_bf16_rn(exp2f(s[h + 1] - ((m1 == -INFINITY) ? 0.f : m1)));
+          s[h] = bf16_to_f32(b0);
+          s[h + 1] = bf16_to_f32(b1);
+          pk[h / 2] = (uint32_t)b0 | ((uint32_t)b1 << 16);
+        }
+        l_l += warp_transpose_reduce32<false>(s);
         if (!mbar_wait_warp(&bars[B_P_EMPTY + pb], (pph & 1) ^ 1, abort_flag, err)) { ok = false; break; }
-        // P^T[head][slot] (K-major swizzled, 2 columns of 64 slots); s[] becomes
-        // the bf16-rounded P for the row sums
+        // P^T[head][slot] (K-major swizzled, 2 columns of 64 slots)
         {
           const uint32_t kcol = key & 63;
           uint8_t* pcol = smem + C::OFF_P + pb * C::P_BYTES + (key >> 6) * (HC * 128);
 #pragma unroll
-          for (int h = 0; h < HW; ++h) {
-            const float mh = __shfl_sync(0xffffffffu, m_l, h);
-            const float mref = (mh == -INFINITY) ? 0.f : mh;
-            const uint16_t pbits = f32_to_bf16_rn(exp2f(s[h] - mref));
-            s[h] = bf16_to_f32(pbits);
-            *reinterpret_cast<uint16_t*>(pcol + sw128_offset(HW * hh + h, kcol)) = pbits;
-          }
+          for (int h = 0; h < HW; ++h)
+            *reinterpret_cast<uint16_t*>(pcol + sw128_offset(HW * hh + h, kcol)) =
+                (uint16_t)((h & 1) ? (pk[h / 2] >> 16) : (pk[h / 2] & 0xffffu));
         }
-        l_l += warp_transpose_reduce32<false>(s);
         if (need && j > 0) {
           // O must hold the previous tile's P.V before it is rescaled
           const int pbp = C::NPB == 2 ? (int)((gt - 1) & 1) : 0;
