@@ -30,8 +30,8 @@
 // at REGS_OTHER), 8 and 11 QK issuers (alternate K chunks, two partial S^T
 // sums; warp 11 idle for 8-chunk rows), 9 and 10 PV issuers (units 0/2 and
 // 1/3), 12-17 K-ring producers (one per stage for 9-chunk rows, all six on
-// every stage for 8-chunk rows), 18-23 V-ring producers (three warps per V
-// slot).
+// every stage for 8-chunk rows), 18-23 V-ring producers (all six on every
+// V unit).
 #include "dsa_device.cuh"
 #include "dsa_kernels.h"
 
@@ -229,8 +229,10 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
       // costs several hundred cycles, so stages are filled side by side);
       // otherwise all six warps take part in every stage, lanes 0-2 of each.
       // V stream (warps 18-23): the
-      // three warps of group u fill V slot u with the 128-column units
-      // m = u, u+2 of every tile, sharing this CTA's 32 gathers of a unit.
+      // 128-column units m of every tile go to V slot m mod 2; all six
+      // warps take part in every unit, lanes 0-5 of each sharing this CTA's
+      // 32 gathers (a unit's refill sits on the P.V critical path twice per
+      // tile, so its issue time matters).
       // When this CTA's 64 slots of the tile are one contiguous run of rows,
       // each of its 64-row halves is one tiled load (box 64 columns x 64
       // rows) instead of 16 gathers.  The union lists distinct rows in
@@ -244,14 +246,13 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
       const int kw = warp - 12;                 // K stage owned (OWNED; none past the ring)
       // K request of this lane: 0-15 gathers, 16 the q chunk
       const int kreq = C::OWNED ? lane : kw * 3 + (lane < 3 ? lane : 32);
-      const int vg = (warp - 18) / 3;           // V slot owned
-      const int vsub = (warp - 18) % 3;
-      const int e = vsub * 11 + lane;           // V gather index 0..31 of this CTA
-      const bool issuer = kstream ? (kreq < 17) : (lane < 11 && e < 32);
+      // V: all six warps take part in every unit, lanes 0-5 of each
+      const int e = (warp - 18) * 6 + (lane < 6 ? lane : 32);   // V gather index 0..31 of this CTA
+      const bool issuer = kstream ? (kreq < 17) : (e < 32);
       const bool kgather = kstream && kreq < 16;
       const int rg = 16 * rank + (kstream ? (kreq & 15) : (e & 15));   // row group of the tile
       const int vcc = (e >> 4) & 1;             // V swizzle column
-      const bool leader = (lane == 0) && (kstream ? (C::OWNED || kw == 0) : vsub == 0);
+      const bool leader = (lane == 0) && (kstream ? (C::OWNED || kw == 0) : warp == 18);
       uint32_t gt = 0, pos = 0;
       int64_t last_armed = -1;
       bool ok = true;
@@ -298,7 +299,7 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
           } else {
             const int4 r = (issuer && !run) ? union_rows4(urow, U, a.N, j * BK + 4 * rg) : make_int4(-1, -1, -1, -1);
             for (int m = 0; m < 4; ++m, ++pos) {
-              if ((int)(pos % NVR) != vg) continue;
+              const int vg = (int)(pos % NVR);   // V slot of this unit
               if (!mbar_wait_warp(&bars[B_VR_EMPTY + vg], ((pos / NVR) & 1) ^ 1, abort_flag, err)) {
                 ok = false;
                 break;
@@ -328,7 +329,8 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
             if (!C::OWNED || (int)(p % C::NKR) == kw)
               mbar_wait_drain(&bars[B_KR_FULL + (int)(p % C::NKR)], (uint32_t)(p / C::NKR) & 1, err);
         } else {
-          mbar_wait_drain(&bars[B_VR_FULL + vg], (uint32_t)(last_armed / NVR) & 1, err);
+          for (int64_t p = last_armed; p >= 0 && p > last_armed - NVR; --p)
+            mbar_wait_drain(&bars[B_VR_FULL + (int)(p % NVR)], (uint32_t)(p / NVR) & 1, err);
         }
       }
       __syncwarp();
