@@ -18,7 +18,10 @@
 //               after its PV, so the next tiles' K loads are not held up by
 //               this tile's softmax.
 //   warp 8      one thread: S = Q K^T (M = 128 queries, N = 128 keys) into a
-//               double-buffered TMEM S, then O += P V with P read from TMEM.
+//               double-buffered TMEM S.
+//   warp 10     one thread: O += P V with P read from TMEM (two issuing
+//               threads: one thread's per-tile waits, fences and commits
+//               were the longer loop).
 //   warps 0-7   two threads per query row (TMEM lane): warp w holds row
 //               32(w%4) + lane and keys 64(w/4) .. +63 of each tile; mask,
 //               online softmax (base 2, lazy rescale) with the row max
@@ -33,7 +36,7 @@ namespace masked {
 constexpr int BQ = 128;
 constexpr int BKV = 128;
 constexpr int HK = BKV / 2;     // keys per softmax thread
-constexpr int NTHREADS = 320;   // 10 warps
+constexpr int NTHREADS = 352;   // 11 warps
 constexpr float kTau = 8.0f;
 
 template <int DQK, int DV>
@@ -50,7 +53,7 @@ struct Cfg {
   static constexpr uint32_t OFF_PAIR = OFF_MASK + 4 * BQ * 16u;  // [2][2][128] floats
   static constexpr uint32_t OFF_INFO = OFF_PAIR + 2 * 2 * BQ * 4u;  // key-tile index per info slot [4]
   static constexpr uint32_t OFF_BAR = OFF_INFO + 64u;
-  static constexpr int NBAR = 24;
+  static constexpr int NBAR = 26;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8u;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64u + 1024u;
   static_assert(SMEM_BYTES <= 227u * 1024u, "shared memory budget");
@@ -70,8 +73,8 @@ enum {
   B_S_EMPTY = 15,  // [2] P.V completed (P aliases S)
   B_P_FULL = 17,   // 256 arrivals
   B_PV_DONE = 18,
-  B_DRAIN = 19,
-  B_PAIR = 20,     // [4] the two softmax warps of a TMEM lane quarter (64 arrivals)
+  B_DRAIN = 19,     // [2] QK issuer, PV issuer
+  B_PAIR = 21,     // [4] the two softmax warps of a TMEM lane quarter (64 arrivals)
 };
 
 template <int DQK, int DV>
@@ -115,7 +118,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) masked_mha_kernel(const __grid_co
     for (int i = 0; i < 4; ++i) mbar_init(&bars[B_INFO + i], 1);
     mbar_init(&bars[B_P_FULL], 256);
     mbar_init(&bars[B_PV_DONE], 1);
-    mbar_init(&bars[B_DRAIN], 1);
+    mbar_init(&bars[B_DRAIN + 0], 1);
+    mbar_init(&bars[B_DRAIN + 1], 1);
     for (int i = 0; i < 4; ++i) mbar_init(&bars[B_PAIR + i], 64);
     *abort_flag = 0;
     fence_mbar_init();
@@ -206,18 +210,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) masked_mha_kernel(const __grid_co
     __syncwarp();
   } else if (warp == 8) {
     // ------------------------------------------------------------------
-    // tcgen05 issuer
+    // QK issuer: S = Q K^T for each key tile as soon as its K stage landed
+    // and its S buffer is free (the P.V of the tile two back completed)
     // ------------------------------------------------------------------
     if (lane == 0) {
       constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, BKV, false, false);
-      constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, DV, false, true);
       const uint32_t qs = sbase + C::OFF_Q;
       bool ok = mbar_wait(&bars[B_Q_FULL], 0, abort_flag, err);
       tc_fence_after();
-      uint32_t n = 0;  // tiles consumed (stage sequence)
-      auto issue_qk = [&](uint32_t i) -> bool {
-        const int s = i & 1;
-        if (!mbar_wait(&bars[B_S_EMPTY + s], ((i >> 1) & 1) ^ 1, abort_flag, err)) return false;
+      for (uint32_t n = 0; ok; ++n) {
+        const int s = n & 1;
+        if (!mbar_wait(&bars[B_K_FULL + s], (n >> 1) & 1, abort_flag, err)) break;
+        tc_fence_after();
+        if (stage_tile[n & 3] < 0) break;   // end marker
+        if (!mbar_wait(&bars[B_S_EMPTY + s], ((n >> 1) & 1) ^ 1, abort_flag, err)) break;
         tc_fence_after();
         const uint32_t ks = sbase + C::OFF_K + s * C::K_BYTES;
 #pragma unroll
@@ -226,28 +232,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) masked_mha_kernel(const __grid_co
                          sdesc_sw128(ks + c * (BKV * 128), 16, 1024), 2u, 2u, IDESC_QK, c > 0 ? 1u : 0u);
         mma_commit(&bars[B_S_FULL + s]);
         mma_commit(&bars[B_K_EMPTY + s]);
-        return true;
-      };
-      int cur_tile = -1;
-      if (ok) {
-        ok = mbar_wait(&bars[B_K_FULL + 0], 0, abort_flag, err);
-        if (ok) {
-          tc_fence_after();
-          cur_tile = stage_tile[0];
-          if (cur_tile >= 0) ok = issue_qk(0);
-        }
       }
-      while (ok && cur_tile >= 0) {
-        const uint32_t nx = n + 1;
-        // next stage: its QK overlaps this tile's softmax
-        if (!mbar_wait(&bars[B_K_FULL + (nx & 1)], (nx >> 1) & 1, abort_flag, err)) { ok = false; break; }
-        tc_fence_after();
-        const int nx_tile = stage_tile[nx & 3];
-        if (nx_tile >= 0 && !issue_qk(nx)) { ok = false; break; }
-        // O += P V for the current tile (P: 128 keys as 64 TMEM columns of bf16 pairs)
-        if (!mbar_wait(&bars[B_P_FULL], n & 1, abort_flag, err)) { ok = false; break; }
+      mma_commit(&bars[B_DRAIN + 0]);
+      mbar_wait(&bars[B_DRAIN + 0], 0, abort_flag, err);
+    }
+    __syncwarp();
+  } else if (warp == 10) {
+    // ------------------------------------------------------------------
+    // P.V issuer: O += P V once the softmax packed P (bf16, in the S
+    // columns) and the V stage landed; the tile sequence and its end come
+    // through the info ring.  A thread of its own, so that the next tiles'
+    // QK is never queued behind a wait for the softmax.
+    // ------------------------------------------------------------------
+    if (lane == 0) {
+      constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, DV, false, true);
+      for (uint32_t n = 0;; ++n) {
         const int s = n & 1;
-        if (!mbar_wait(&bars[B_V_FULL + s], (n >> 1) & 1, abort_flag, err)) { ok = false; break; }
+        const int is = n & 3;
+        if (!mbar_wait(&bars[B_INFO + is], (n >> 2) & 1, abort_flag, err)) break;
+        if (stage_tile[is] < 0) break;   // end marker
+        if (!mbar_wait(&bars[B_P_FULL], n & 1, abort_flag, err)) break;
+        if (!mbar_wait(&bars[B_V_FULL + s], (n >> 1) & 1, abort_flag, err)) break;
         tc_fence_after();
         const uint32_t vs = sbase + C::OFF_V + s * C::V_BYTES;
 #pragma unroll
@@ -258,11 +263,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) masked_mha_kernel(const __grid_co
         mma_commit(&bars[B_PV_DONE]);
         mma_commit(&bars[B_V_EMPTY + s]);
         mma_commit(&bars[B_S_EMPTY + s]);
-        n = nx;
-        cur_tile = nx_tile;
       }
-      mma_commit(&bars[B_DRAIN]);
-      mbar_wait(&bars[B_DRAIN], 0, abort_flag, err);
+      mma_commit(&bars[B_DRAIN + 1]);
+      mbar_wait(&bars[B_DRAIN + 1], 0, abort_flag, err);
     }
     __syncwarp();
   } else {
