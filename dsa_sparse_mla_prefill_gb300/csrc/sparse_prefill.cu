@@ -555,12 +555,12 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
           }
         }
         if (tid == 0) DSA_TRACE(a.tr, gt, 4);
-        // the previous PV must be done before P is overwritten or O rescaled
-        if (!mbar_wait_warp(&bars[B_P_EMPTY], (gt & 1) ^ 1, abort_flag, err)) { ok = false; break; }
-        if (tid == 0) DSA_TRACE(a.tr, gt, 5);
-        tc_fence_after();
+        // Everything that does not touch P^T or O first: the new running
+        // max, the rescale factors, P (bf16, packed in registers) and the
+        // row sums; only the O rescale and the P^T stores wait for the
+        // previous P.V, so the exponentials overlap it.
+        float alpha[H];
         if (need) {
-          float alpha[H];
 #pragma unroll
           for (int h = 0; h < H; ++h) {
             const float mn = fmaxf(m_run[h], tmax[h]);
@@ -568,32 +568,43 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
             m_run[h] = mn;
             l_part[h] *= alpha[h];
           }
-          if (j > 0) {
-#pragma unroll 1
-            for (int m = 0; m < 4; ++m) {
-              float o[H];
-              const uint32_t ta = tmem + lane_off + C::COL_O + ob * (4 * H) + m * H;
-              tmem_ld_cols<H>(ta, o);
-              tmem_ld_wait();
+        }
+        uint32_t pk[H / 2];
 #pragma unroll
-              for (int h = 0; h < H; ++h) o[h] *= alpha[h];
-              tmem_st_cols<H>(ta, o);
-            }
-            tmem_st_wait();
+        for (int h = 0; h < H; h += 2) {
+          const float mr0 = (m_run[h] == -INFINITY) ? 0.f : m_run[h];
+          const float mr1 = (m_run[h + 1] == -INFINITY) ? 0.f : m_run[h + 1];
+          const uint16_t b0 = f32_to_bf16_rn(exp2f(s[h] - mr0));
+          const uint16_t b1 = f32_to_bf16_rn(exp2f(s[h + 1] - mr1));
+          l_part[h] += bf16_to_f32(b0);
+          l_part[h + 1] += bf16_to_f32(b1);
+          pk[h / 2] = (uint32_t)b0 | ((uint32_t)b1 << 16);
+        }
+        // the previous PV must be done before P is overwritten or O rescaled
+        if (!mbar_wait_warp(&bars[B_P_EMPTY], (gt & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+        if (tid == 0) DSA_TRACE(a.tr, gt, 5);
+        tc_fence_after();
+        if (need && j > 0) {
+#pragma unroll 1
+          for (int m = 0; m < 4; ++m) {
+            float o[H];
+            const uint32_t ta = tmem + lane_off + C::COL_O + ob * (4 * H) + m * H;
+            tmem_ld_cols<H>(ta, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int h = 0; h < H; ++h) o[h] *= alpha[h];
+            tmem_st_cols<H>(ta, o);
           }
+          tmem_st_wait();
         }
         // P^T[h][key] (K-major swizzled, 2 columns of 64 keys)
         {
           const uint32_t kcol = tid & 63;
           uint8_t* pcol = p_tile + (tid >> 6) * (H * 128);
 #pragma unroll
-          for (int h = 0; h < H; ++h) {
-            const float mref = (m_run[h] == -INFINITY) ? 0.f : m_run[h];
-            const float p = exp2f(s[h] - mref);
-            const uint16_t pb = f32_to_bf16_rn(p);
-            l_part[h] += bf16_to_f32(pb);
-            *reinterpret_cast<uint16_t*>(pcol + sw128_offset(h, kcol)) = pb;
-          }
+          for (int h = 0; h < H; ++h)
+            *reinterpret_cast<uint16_t*>(pcol + sw128_offset(h, kcol)) =
+                (uint16_t)((h & 1) ? (pk[h / 2] >> 16) : (pk[h / 2] & 0xffffu));
         }
         fence_proxy_async_smem();
         tc_fence_before();
