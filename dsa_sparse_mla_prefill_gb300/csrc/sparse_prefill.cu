@@ -265,8 +265,10 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
       //                every tile into the K ring; warp 8+s owns K slot s
       //                and issues the whole chunk (lane l: rows 4l..4l+3).
       //   warps 14-19: the four 128-column V units of every tile into the
-      //                V ring; the three warps of group u own V slot u
-      //                (units m = u, u+2), 64 gather4 shared between them.
+      //                V ring (unit m in slot m mod 2); all six warps take
+      //                part in every unit, lanes 0-10 of each sharing its
+      //                64 gather4 (a unit's refill is on the P.V critical
+      //                path twice per tile, so its issue time matters).
       // Neither stream waits on the other, so QK of the next tile streams
       // while this tile's softmax runs and V lands ahead of PV.  TMA issue
       // cost is serial per warp, so many issuing warps keep many copies in
@@ -276,13 +278,11 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
       // ----------------------------------------------------------------
       const bool kstream = warp < 8 + C::NKR;
       const int kw = warp - 8;                      // K slot owned (K stream)
-      const int vgroup = (warp - 14) / 3;           // V slot owned (V stream)
-      const int vsub = (warp - 14) % 3;
-      const int e = vsub * 22 + lane;               // V gather index 0..63 (valid for e < 64, lane < 22)
-      const bool v_issuer = !kstream && lane < 22 && e < 64;
+      const int e = (warp - 14) * 11 + (lane < 11 ? lane : 64);   // V gather index 0..63 of a unit
+      const bool v_issuer = !kstream && e < 64;
       const int g = kstream ? lane : (e & 31);       // row group
       const int vcc = e >> 5;                       // V swizzle column
-      const bool leader = (lane == 0) && (kstream || vsub == 0);
+      const bool leader = (lane == 0) && (kstream || warp == 14);
       const uint32_t q_s = sbase + C::OFF_Q;
       int lt = 0, lt_nz = 0;
       uint32_t gt = 0, pos = 0;  // tiles and stages of this stream so far
@@ -327,7 +327,7 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
               }
             } else {
               for (int m = 0; m < 4; ++m, ++pos) {
-                if ((int)(pos % C::NVR) != vgroup) continue;
+                const int vgroup = (int)(pos % C::NVR);   // V slot of this unit
                 if (!mbar_wait_warp(&bars[B_VR_EMPTY + vgroup], ((pos / C::NVR) & 1) ^ 1, abort_flag, err)) {
                   ok = false;
                   break;
@@ -356,7 +356,8 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
           if (kstream)
             mbar_wait_drain(&bars[B_KR_FULL + kw], (uint32_t)(last_armed / C::NKR) & 1, err);
           else
-            mbar_wait_drain(&bars[B_VR_FULL + vgroup], (uint32_t)(last_armed / C::NVR) & 1, err);
+            for (int64_t p = last_armed; p >= 0 && p > last_armed - C::NVR; --p)
+              mbar_wait_drain(&bars[B_VR_FULL + (int)(p % C::NVR)], (uint32_t)(p / C::NVR) & 1, err);
         }
       }
       __syncwarp();
