@@ -114,3 +114,76 @@ def test_tma_gather4_multicast_cluster(selftest):
             for p in range(8):
                 want = bits[src, col + 8 * p: col + 8 * p + 8] if 0 <= src < N else np.zeros(8, np.uint16)
                 assert np.array_equal(imgs[rank, r, p ^ (r & 7)], want), (rank, r, p)
+
+
+# ---------------------------------------------------------------------------
+# Timing probes of the self-test library (the measurements behind the
+# kernels' issue structure).  Cycle counts depend on the GPU and on what else
+# runs, so these check only that every probe completes with no bounded wait
+# running out and reports positive, self-consistent counts.
+# ---------------------------------------------------------------------------
+def _lib():
+    import dsa_sparse_mla_prefill_gb300 as dsa
+    return ctypes.CDLL(os.path.join(os.path.dirname(dsa.__file__), "libdsa_selftest.so"))
+
+
+@pytest.mark.parametrize("mode", [3, 8, 9, 10, 11, 12, 13, 14, 15, 16, 17, 18, 19, 20, 21, 22, 23, 24, 25, 26, 27, 28])
+def test_mma_issue_timing_modes(selftest, mode):
+    fn = _lib().dsa_selftest_mma_timing
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_int] * 3 + [ctypes.c_void_p] * 3
+    out = torch.zeros(2, dtype=torch.int64, device="cuda")
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    rc = fn(64, 144, mode, out.data_ptr(), status.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert int(status[1]) == 0, "bounded wait ran out"
+    total = int(out[1])
+    # at least the 36 MMAs one issuing warp ends with, at ~20 cycles or more each
+    assert 36 * 20 < total < 10_000_000, total
+
+
+@pytest.mark.parametrize("mc", [0, 1])
+def test_gather4_rate_probe(selftest, mc):
+    fn = _lib().dsa_selftest_gather4_rate
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                   ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                   ctypes.c_void_p]
+    N, ld, grid, per = 4096, 576, 8, 256
+    g = torch.Generator().manual_seed(3)
+    kv = torch.randn(N, ld, generator=g).to(torch.bfloat16).cuda()
+    rows = torch.randint(0, N, (grid * per * 4,), generator=g, dtype=torch.int32).cuda()
+    out = torch.zeros(grid, dtype=torch.int64, device="cuda")
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    for flags in (0, 3, 4, 8):
+        rc = fn(kv.data_ptr(), N, ld, rows.data_ptr(), grid, per, 8, 4, mc, flags, out.data_ptr(), status.data_ptr(),
+                torch.cuda.current_stream().cuda_stream)
+        assert rc == 0
+        torch.cuda.synchronize()
+        assert int(status[1]) == 0
+        assert (out > 0).all()
+
+
+@pytest.mark.parametrize("mc,flags,warps,lanes", [(0, 0, 8, 4), (1, 0, 6, 3), (0, 32, 6, 32), (1, 32, 6, 16),
+                                                  (0, 16, 8, 4), (0, 64 | 128 | 4, 8, 4)])
+def test_ring_turnaround_probe(selftest, mc, flags, warps, lanes):
+    fn = _lib().dsa_selftest_ring_rate
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p] + [ctypes.c_int] * 9 + \
+        [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    N, ld, grid, ntiles = 4096, 576, 4, 4
+    stages = warps if flags & 32 else 6
+    g = torch.Generator().manual_seed(5)
+    kv = torch.randn(N, ld, generator=g).to(torch.bfloat16).cuda()
+    rows = torch.sort(torch.randint(0, N, (grid // 2 * ntiles, 128), generator=g, dtype=torch.int32), dim=1)
+    rows = rows.values.reshape(-1).cuda()
+    out = torch.zeros(grid, dtype=torch.int64, device="cuda")
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    rc = fn(kv.data_ptr(), N, ld, rows.data_ptr(), ntiles, grid, 9 * ntiles, stages, warps, lanes, mc, 100, flags,
+            out.data_ptr(), status.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert int(status[1]) == 0
+    # every stage is held 100 cycles by the consumer
+    assert (out >= 9 * ntiles * 100).all(), out
