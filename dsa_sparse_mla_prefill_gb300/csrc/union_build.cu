@@ -20,6 +20,7 @@ namespace dsa {
 namespace unionb {
 
 constexpr int NT = 512;
+constexpr int GMAX = 8;   // tokens per group (one mask bit each)
 
 __device__ __forceinline__ void group_of(const ReqTable& rq, int G, int g, int& t0, int& n) {
   int r = 0;
@@ -74,16 +75,44 @@ __global__ void __launch_bounds__(NT) union_build_kernel(UnionArgs a) {
   for (int i = threadIdx.x; i < a.union_pad / 4; i += NT) maskw[i] = 0u;
   __syncthreads();
 
-  // 1) bitmap of every valid row of the group's tokens
+  // 1) bitmap of every valid row of the group's tokens.  Register path: each
+  // thread loads entries 4t .. 4t+3 of all the group's token rows up front
+  // (independent 16-byte loads, one memory latency) and keeps them for step
+  // 4; otherwise a strided loop over each row.
+  const bool vec = a.k <= 4 * NT && (a.k & 3) == 0 && (a.ld & 3) == 0 &&
+                   (reinterpret_cast<uintptr_t>(a.idx) & 15u) == 0;
+  int4 xs[GMAX];
   int bad = 0;
-  for (int j = 0; j < n; ++j) {
-    const int32_t* row = a.idx + (size_t)(t0 + j) * a.ld;
-    for (int e = threadIdx.x; e < a.k; e += NT) {
-      const int x = __ldg(row + e);
-      if (x >= 0 && x < a.N) {
-        atomicOr(&bitmap[x >> 5], 1u << (x & 31));
-      } else if (x != -1) {
-        ++bad;
+  if (vec) {
+#pragma unroll
+    for (int j = 0; j < GMAX; ++j) {
+      xs[j] = make_int4(-1, -1, -1, -1);
+      if (j < n && 4 * (int)threadIdx.x < a.k)
+        xs[j] = __ldg(reinterpret_cast<const int4*>(a.idx + (size_t)(t0 + j) * a.ld) + threadIdx.x);
+    }
+#pragma unroll
+    for (int j = 0; j < GMAX; ++j) {
+      const int v[4] = {xs[j].x, xs[j].y, xs[j].z, xs[j].w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int x = v[c];
+        if (x >= 0 && x < a.N) {
+          atomicOr(&bitmap[x >> 5], 1u << (x & 31));
+        } else if (x != -1) {
+          ++bad;
+        }
+      }
+    }
+  } else {
+    for (int j = 0; j < n; ++j) {
+      const int32_t* row = a.idx + (size_t)(t0 + j) * a.ld;
+      for (int e = threadIdx.x; e < a.k; e += NT) {
+        const int x = __ldg(row + e);
+        if (x >= 0 && x < a.N) {
+          atomicOr(&bitmap[x >> 5], 1u << (x & 31));
+        } else if (x != -1) {
+          ++bad;
+        }
       }
     }
   }
@@ -123,15 +152,25 @@ __global__ void __launch_bounds__(NT) union_build_kernel(UnionArgs a) {
   for (uint32_t u = Ucap + threadIdx.x; u < (uint32_t)a.union_pad; u += NT) urow[u] = -1;
 
   // 4) membership bits: slot of row x = prefix[x>>5] + popc(bits below x)
-  for (int j = 0; j < n; ++j) {
-    const int32_t* row = a.idx + (size_t)(t0 + j) * a.ld;
-    for (int e = threadIdx.x; e < a.k; e += NT) {
-      const int x = __ldg(row + e);
-      if (x >= 0 && x < a.N) {
-        const uint32_t w = (uint32_t)x >> 5;
-        const uint32_t pos = prefix[w] + __popc(bitmap[w] & ((1u << (x & 31)) - 1u));
-        if (pos < Ucap) atomicOr(&maskw[pos >> 2], (1u << j) << ((pos & 3) * 8));
-      }
+  auto member = [&](int x, int j) {
+    if (x >= 0 && x < a.N) {
+      const uint32_t w = (uint32_t)x >> 5;
+      const uint32_t pos = prefix[w] + __popc(bitmap[w] & ((1u << (x & 31)) - 1u));
+      if (pos < Ucap) atomicOr(&maskw[pos >> 2], (1u << j) << ((pos & 3) * 8));
+    }
+  };
+  if (vec) {
+#pragma unroll
+    for (int j = 0; j < GMAX; ++j) {
+      member(xs[j].x, j);
+      member(xs[j].y, j);
+      member(xs[j].z, j);
+      member(xs[j].w, j);
+    }
+  } else {
+    for (int j = 0; j < n; ++j) {
+      const int32_t* row = a.idx + (size_t)(t0 + j) * a.ld;
+      for (int e = threadIdx.x; e < a.k; e += NT) member(__ldg(row + e), j);
     }
   }
   __syncthreads();
