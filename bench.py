@@ -20,6 +20,7 @@ the data path); time is the max over ranks.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -284,8 +285,8 @@ def run_modes(dev, stream, peaks, steps, warmup, flush):
     out = {}
     steps = max(3, min(steps, 10))
 
-    def sparse_block(name, grouped=True, per_token=True):
-        w = WORKLOADS[name]
+    def sparse_block(name, grouped=True, per_token=True, w=None):
+        w = WORKLOADS[name] if w is None else w
         log(f"mode {name}")
         x = make_sparse_inputs(w)
         q, kv = to_dev(x.q, dev), to_dev(x.kv, dev)
@@ -335,6 +336,15 @@ def run_modes(dev, stream, peaks, steps, warmup, flush):
     out["grouped_21k_of_32k"] = sparse_block("grouped_21k_of_32k")
     torch.cuda.empty_cache()
     out["nope_2x8192"] = sparse_block("nope_2x8192")
+    torch.cuda.empty_cache()
+    # the headline workload in grouped form (H = 32: G = 4 tokens per group)
+    out["v32_h32_16k_grouped"] = sparse_block("v32_h32_16k", per_token=False)
+    torch.cuda.empty_cache()
+    # wide-union stress variant of the grouped workload: every token draws its
+    # replacements independently, so the 8-token unions grow
+    wide = dataclasses.replace(WORKLOADS["grouped_21k_of_32k"], name="grouped_21k_of_32k_wide",
+                               index_gen="locality_wide")
+    out["grouped_21k_of_32k_wide"] = sparse_block("grouped_21k_of_32k_wide", w=wide)
     torch.cuda.empty_cache()
     # masked dense MHA
     w = WORKLOADS["masked_2x8192"]

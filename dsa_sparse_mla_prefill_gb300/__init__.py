@@ -51,6 +51,7 @@ _SIGNATURES = {
     "dsa_grouped_prefill": (_I, [_VP, _VP, _I, _I, _VP, _VP, _VP, _I, _I, _I32P, _I, _I, _I, _I, _I, _F, _VP,
                                  _VP, _VP]),
     "dsa_topk_to_key_mask": (_I, [_VP, _I, _I, _I, _I32P, _I32P, _I, _VP, _I, _VP]),
+    "dsa_local_to_global": (_I, [_VP, _I, _I, _I, _I32P, _I32P, _I, _VP, _I, _I, _I, _VP, _VP]),
     "dsa_masked_mha_prefill": (_I, [_VP, _VP, _VP, _VP, _I, _I32P, _I32P, _I, _I, _I, _I, _I, _F, _VP, _VP,
                                     _VP]),
     "dsa_last_device_error": (_I, [_VP, ctypes.POINTER(ctypes.c_uint32)]),
@@ -214,6 +215,27 @@ def dsa_topk_to_key_mask(idx, k: int, words: int, cu_seqlens_q=None, cu_seqlens_
     nreq = 0 if aq is None else len(aq) - 1
     _check(lib().dsa_topk_to_key_mask(idx.data_ptr(), T, k, ld, pq, pk, nreq, out.data_ptr(), words,
                                       _stream(stream, idx.device)), "dsa_topk_to_key_mask")
+    return out
+
+
+def dsa_local_to_global(idx_local, k: int, kv_lens, block_table, block_size: int, N: int, cu_seqlens_q=None,
+                        out=None, stream=None):
+    """Request-local KV positions [T, ld] -> physical rows of a paged KV cache
+    through block_table [num_req, max_blocks] (device int32).  kv_lens: host
+    KV length per request.  Returns idx_global [T, ld] (may be ``out`` =
+    ``idx_local`` for in place)."""
+    import torch
+    _need(idx_local, torch.int32, "idx_local", 2)
+    _need(block_table, torch.int32, "block_table", 2)
+    T, ld = idx_local.shape
+    if out is None:
+        out = torch.empty_like(idx_local)
+    aq, pq = _host_i32(cu_seqlens_q)
+    al, pl = _host_i32(kv_lens)
+    nreq = 0 if aq is None else len(aq) - 1
+    _check(lib().dsa_local_to_global(idx_local.data_ptr(), T, k, ld, pq, pl, nreq, block_table.data_ptr(),
+                                     block_table.shape[1], block_size, N, out.data_ptr(),
+                                     _stream(stream, idx_local.device)), "dsa_local_to_global")
     return out
 
 

@@ -2,6 +2,7 @@
 // launches for the entry points declared in include/dsa.h.
 #include <cstdint>
 #include <cstring>
+#include <vector>
 
 #include <cuda_runtime.h>
 
@@ -265,6 +266,46 @@ int dsa_topk_to_key_mask(const int32_t* idx, int T, int k, int ld, const int32_t
   a.ld = ld;
   a.words = words;
   return dsa::launch_topk_to_key_mask(a, (cudaStream_t)stream) == 0 ? DSA_OK : DSA_ERR_CUDA;
+}
+
+int dsa_local_to_global(const int32_t* idx_local, int T, int k, int ld, const int32_t* cu_seqlens_q_host,
+                        const int32_t* kv_lens_host, int num_req, const int32_t* block_table, int max_blocks,
+                        int block_size, int N, int32_t* idx_global, dsa_stream_t stream) {
+  if (T < 0 || k < 0 || ld < k || block_size < 1 || max_blocks < 1 || N < 0) return DSA_ERR_INVALID_ARG;
+  if (kv_lens_host == nullptr) return DSA_ERR_INVALID_ARG;
+  if (cu_seqlens_q_host == nullptr) num_req = 1;
+  if (num_req < 1) return DSA_ERR_INVALID_ARG;
+  if (num_req > dsa::kMaxReq) return DSA_ERR_UNSUPPORTED;
+  // cumulative KV lengths stand in for the KV offsets of the request table
+  std::vector<int32_t> cu_kv(num_req + 1, 0);
+  for (int r = 0; r < num_req; ++r) {
+    if (kv_lens_host[r] < 0 || (int64_t)kv_lens_host[r] > (int64_t)max_blocks * block_size)
+      return DSA_ERR_INVALID_ARG;
+    if ((int64_t)cu_kv[r] + kv_lens_host[r] > INT32_MAX) return DSA_ERR_UNSUPPORTED;
+    cu_kv[r + 1] = cu_kv[r] + kv_lens_host[r];
+  }
+  dsa::ConvertArgs a;
+  const int32_t one_req[2] = {0, T};   // NULL cu_seqlens_q: one request of T tokens
+  int st = fill_req(a.req, cu_seqlens_q_host ? cu_seqlens_q_host : one_req, cu_kv.data(), num_req, T, -1, 0);
+  if (st != DSA_OK) return st;
+  if (T == 0) return DSA_OK;
+  if (!idx_local || !idx_global || !block_table || !aligned4(idx_local) || !aligned4(idx_global) ||
+      !aligned4(block_table))
+    return DSA_ERR_INVALID_ARG;
+  DevInfo* d;
+  if (!dev_info(&d)) return DSA_ERR_CUDA;
+  a.idx_local = idx_local;
+  a.idx_global = idx_global;
+  a.block_table = block_table;
+  a.err = d->err;
+  a.T = T;
+  a.k = k;
+  a.ld = ld;
+  a.max_blocks = max_blocks;
+  a.block_size = block_size;
+  a.N = N;
+  a.vec = (ld % 4 == 0) && aligned16(idx_local) && aligned16(idx_global) ? 1 : 0;
+  return dsa::launch_local_to_global(a, (cudaStream_t)stream) == 0 ? DSA_OK : DSA_ERR_CUDA;
 }
 
 int dsa_masked_mha_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint32_t* key_mask,

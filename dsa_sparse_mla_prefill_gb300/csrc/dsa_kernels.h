@@ -59,6 +59,16 @@ struct KeyMaskArgs {
   ReqTable req;
 };
 
+struct ConvertArgs {
+  const int32_t* idx_local;    // [T, ld] request-local positions
+  int32_t* idx_global;         // [T, ld] physical rows (may alias idx_local)
+  const int32_t* block_table;  // [num_req, max_blocks] physical block ids
+  unsigned int* err;
+  int T, k, ld, max_blocks, block_size, N;
+  int vec;                     // 16-byte row accesses (ld % 4 == 0, aligned pointers)
+  ReqTable req;                // cu_q: token offsets; cu_kv: cumulative KV lengths
+};
+
 struct GroupedArgs {
   CUtensorMap tmap_kv;      // kv rows for tile::gather4 (box 64 columns x 1 row, 128B swizzle)
   CUtensorMap tmap_q;       // q viewed [T*H, d_qk], box 64 columns x 64 rows
@@ -108,6 +118,7 @@ inline int union_build_smem_bytes(int N, int union_pad) {
 int launch_sparse_prefill(const SparseArgs& a, int num_sms, cudaStream_t stream);
 int launch_union_build(const UnionArgs& a, cudaStream_t stream);
 int launch_topk_to_key_mask(const KeyMaskArgs& a, cudaStream_t stream);
+int launch_local_to_global(const ConvertArgs& a, cudaStream_t stream);
 int launch_grouped_prefill(const GroupedArgs& a, int num_sms, cudaStream_t stream);
 int launch_masked_mha(const MaskedArgs& a, int num_sms, cudaStream_t stream);
 

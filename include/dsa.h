@@ -163,6 +163,33 @@ int dsa_topk_to_key_mask(const int32_t* idx, int T, int k, int ld, const int32_t
                          dsa_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Request-local -> physical KV rows ("[Perf][DSA] Grouped sparse prefill
+ * ...", How: the selected positions are mapped to physical rows of the paged
+ * KV cache through the request -> global index conversion).  Run it on the
+ * per-token index rows before dsa_sparse_prefill / dsa_union_build, so that
+ * the union is sorted by physical row as dsa_grouped_prefill requires.
+ *
+ * idx_local    [T, ld] int32: position x in the KV sequence of the token's
+ *              request (0 <= x < kv_len), -1 = absent; first k columns used.
+ * cu_seqlens_q HOST int32 [num_req + 1] or NULL (one request of T tokens).
+ * kv_lens      HOST int32 [num_req]: KV length of each request.
+ * block_table  DEVICE int32 [num_req, max_blocks]: physical block of each
+ *              logical block of block_size positions; negative = unmapped.
+ * N            physical KV rows (rows outside [0, N) are not produced).
+ * idx_global   out [T, ld] int32: block_table[r][x / block_size] * block_size
+ *              + x % block_size for every valid x; -1 for -1 entries, for
+ *              columns >= k and for every other entry (positions outside
+ *              [0, kv_len), unmapped blocks, rows outside [0, N)), which are
+ *              also counted in counts[0] of dsa_last_device_error.
+ *              idx_global may equal idx_local (in place).
+ * Requires block_size >= 1, max_blocks >= 1, kv_len <= max_blocks *
+ * block_size for every request; idx pointers 4-byte aligned.
+ * ---------------------------------------------------------------------- */
+int dsa_local_to_global(const int32_t* idx_local, int T, int k, int ld, const int32_t* cu_seqlens_q_host,
+                        const int32_t* kv_lens_host, int num_req, const int32_t* block_table, int max_blocks,
+                        int block_size, int N, int32_t* idx_global, dsa_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Masked dense MHA simulating DSA ("[2/N][Attention] Enable masked MHA for
  * sparse MLA prefills", Purpose; "[Perf][GLM-5.3-Flash] ...", Purpose): per
  * head, token t of request r attends to the keys n of its request whose mask

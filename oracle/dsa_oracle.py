@@ -18,7 +18,8 @@ Sources (page title, section):
   // num_heads consecutive tokens of a request into 128 pseudo-heads over the
   union of their top-k rows, with a head-group mask restoring each token's own
   top-k, with an exact result); How (sorted union via bitmap -> prefix-sum compaction,
-  per-token membership bitmask, q gathered into [groups, 128, 576], padding
+  per-token membership bitmask, request-local positions mapped to physical
+  rows of the paged KV cache, q gathered into [groups, 128, 576], padding
   rows dropped); review snippet (union_pad / words sizing, the grouped gate).
 * [P2] "[Perf][GLM-5.3-Flash] Dense/masked-MHA sparse prefill for the NoPE
   (256, 0, 256) layout + skip the NoPE K concat": Purpose (masked MHA over
@@ -36,7 +37,12 @@ Readings where the pages are silent (each listed in the design notes):
 * causality is carried entirely by the indices (sparse) or the mask (masked);
 * pseudo-head p = j*H + h for token j of a group and head h;
 * the head-group mask is one uint8 per union slot, bit j = token j of the group;
-* the union list is strictly ascending, padded with -1 (mask 0) to union_pad.
+* the union list is strictly ascending, padded with -1 (mask 0) to union_pad;
+* a paged KV cache maps position x of request r to physical row
+  block_table[r][x // block_size] * block_size + x % block_size; positions
+  outside the request, unmapped blocks (negative ids) and rows outside the
+  table map to -1 and are counted (this reading of the conversion the pages
+  name without printing it).
 """
 from __future__ import annotations
 
@@ -245,6 +251,39 @@ def topk_to_key_mask(idx, k: int, cu_seqlens_q, cu_seqlens_kv, words: int):
             for x in n:
                 km[t, x >> 5] |= np.uint32(1 << (int(x) & 31))
     return km
+
+
+def local_to_global(idx_local, k: int, cu_seqlens_q, kv_lens, block_table, block_size: int, N: int):
+    """Request-local positions -> physical rows [P3 How: positions mapped to
+    physical rows of the paged KV cache].  Token t of request r, entry j < k
+    with position x: row = block_table[r][x // block_size] * block_size +
+    x % block_size when 0 <= x < kv_lens[r], the block id is >= 0 and the row
+    lies in [0, N); -1 stays -1; columns j >= k and every other entry give
+    -1.  Returns (int32 [T, ld], number of entries that were neither -1 nor
+    mapped among the first k columns)."""
+    idx_local = np.asarray(idx_local, dtype=np.int64)
+    bt = np.asarray(block_table, dtype=np.int64)
+    T, ld = idx_local.shape
+    cq = [0, T] if cu_seqlens_q is None else [int(x) for x in cu_seqlens_q]
+    out = np.full((T, ld), -1, dtype=np.int32)
+    bad = 0
+    for r in range(len(cq) - 1):
+        kv_len = int(kv_lens[r])
+        for t in range(cq[r], cq[r + 1]):
+            for j in range(min(k, ld)):
+                x = int(idx_local[t, j])
+                if x == -1:
+                    continue
+                if x < 0 or x >= kv_len:
+                    bad += 1
+                    continue
+                blk = int(bt[r, x // block_size])
+                row = blk * block_size + x % block_size
+                if blk < 0 or row >= N:
+                    bad += 1
+                    continue
+                out[t, j] = row
+    return out, bad
 
 
 def masked_mha_prefill(q_bits, k_bits, v_bits, key_mask, cu_seqlens_q, cu_seqlens_kv,

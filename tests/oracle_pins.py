@@ -393,10 +393,86 @@ def pin_masked_dense_causal_sdpa(seed=11) -> bool:
     return bool(np.max(np.abs(o - ref)) <= 1e-12)
 
 
+def pin_local_to_global_paged_round_trip(seed=12) -> bool:
+    """Paged storage round trip: each request's KV rows are copied block by
+    block into a shuffled physical table through its block table; the row the
+    oracle returns for position x must hold the request's row x.  Invalid
+    entries (past the request, unmapped block, below -1) come back -1 and are
+    counted; -1 and columns at or past k come back -1 uncounted."""
+    rng = np.random.default_rng(seed)
+    B = 4
+    kv_lens = [13, 7, 0, 21]
+    nb = [-(-n // B) for n in kv_lens]
+    max_blocks = max(nb) + 1
+    total_blocks = sum(nb) + 3
+    phys_ids = rng.permutation(total_blocks)
+    bt = np.full((len(kv_lens), max_blocks), -1, dtype=np.int32)
+    pos = 0
+    for r, n in enumerate(nb):
+        bt[r, :n] = phys_ids[pos:pos + n]
+        pos += n
+    N = total_blocks * B
+    local = [rng.integers(0, 1 << 30, size=n) for n in kv_lens]
+    phys = np.full(N, -7, dtype=np.int64)
+    for r in range(len(kv_lens)):
+        for b in range(nb[r]):
+            seg = local[r][b * B:(b + 1) * B]
+            phys[bt[r, b] * B: bt[r, b] * B + len(seg)] = seg
+    q_lens = [3, 2, 2, 4]
+    cq = np.concatenate([[0], np.cumsum(q_lens)])
+    k, ld = 6, 8
+    T = int(cq[-1])
+    idx = np.full((T, ld), -1, dtype=np.int32)
+    want_bad = 0
+    for r in range(len(kv_lens)):
+        for t in range(cq[r], cq[r + 1]):
+            n = min(kv_lens[r], 4)
+            idx[t, :n] = rng.choice(kv_lens[r], size=n, replace=False) if n else []
+            idx[t, 4] = kv_lens[r] + 2          # past the request
+            idx[t, 5] = -3                      # below -1
+            idx[t, 6] = 0 if kv_lens[r] else -1  # column >= k: ignored
+            want_bad += 2
+    out, bad = O.local_to_global(idx, k, cq, kv_lens, bt, B, N)
+    ok = bad == want_bad
+    for r in range(len(kv_lens)):
+        for t in range(cq[r], cq[r + 1]):
+            for j in range(ld):
+                x = int(idx[t, j])
+                if j < k and 0 <= x < kv_lens[r]:
+                    ok &= int(out[t, j]) >= 0 and phys[int(out[t, j])] == local[r][x]
+                else:
+                    ok &= int(out[t, j]) == -1
+    return bool(ok)
+
+
+def pin_local_to_global_contiguous(seed=13) -> bool:
+    """Closed form: requests laid out back to back in whole blocks (block ids
+    consecutive from the request's first block) map position x to
+    first_row + x."""
+    rng = np.random.default_rng(seed)
+    B, kv_lens = 8, [20, 5, 33]
+    nb = [-(-n // B) for n in kv_lens]
+    first = np.concatenate([[0], np.cumsum(nb)])[:-1]
+    bt = np.full((3, max(nb)), -1, dtype=np.int32)
+    for r in range(3):
+        bt[r, :nb[r]] = first[r] + np.arange(nb[r])
+    cq = [0, 2, 3, 6]
+    idx = np.full((6, 5), -1, dtype=np.int32)
+    for r in range(3):
+        for t in range(cq[r], cq[r + 1]):
+            idx[t] = rng.integers(0, kv_lens[r], size=5)
+    out, bad = O.local_to_global(idx, 5, cq, kv_lens, bt, B, int(sum(nb)) * B)
+    want = np.empty_like(idx)
+    for r in range(3):
+        want[cq[r]:cq[r + 1]] = idx[cq[r]:cq[r + 1]] + first[r] * B
+    return bad == 0 and bool(np.array_equal(out, want))
+
+
 ALL_PINS = [pin_bruteforce, pin_single_key, pin_zero_query, pin_equal_keys, pin_two_keys_closed_form,
             pin_order_and_padding_invariance, pin_dense_causal_sdpa, pin_union_worked_example,
             pin_union_bruteforce, pin_union_popcounts, pin_grouped_equals_per_token,
-            pin_key_mask_bruteforce, pin_masked_equals_sparse, pin_masked_dense_causal_sdpa]
+            pin_key_mask_bruteforce, pin_masked_equals_sparse, pin_masked_dense_causal_sdpa,
+            pin_local_to_global_paged_round_trip, pin_local_to_global_contiguous]
 
 
 def run_all_pins():

@@ -111,6 +111,25 @@ def test_argument_validation_without_gpu(lib):
                                           bad, _vp(16), _vp(16), None) == dsa.DSA_ERR_INVALID_ARG
     # key mask: one-sided offsets are rejected
     assert lib.dsa_topk_to_key_mask(_vp(16), 8, 4, 4, cu, None, 2, _vp(16), 4, None) == dsa.DSA_ERR_INVALID_ARG
+    # local -> physical rows: block size, table width, KV lengths, request offsets
+    kl = (ctypes.c_int32 * 2)(40, 8)
+    cu2 = (ctypes.c_int32 * 3)(0, 3, 8)
+    ok_args = dict(idx=_vp(16), T=8, k=4, ld=4, cq=cu2, kl=kl, nreq=2, bt=_vp(16), mb=3, B=16, N=100, out=_vp(16))
+
+    def l2g(**kw):
+        a = dict(ok_args, **kw)
+        return lib.dsa_local_to_global(a["idx"], a["T"], a["k"], a["ld"], a["cq"], a["kl"], a["nreq"], a["bt"],
+                                       a["mb"], a["B"], a["N"], a["out"], None)
+    assert l2g(B=0) == dsa.DSA_ERR_INVALID_ARG
+    assert l2g(mb=0) == dsa.DSA_ERR_INVALID_ARG
+    assert l2g(k=5) == dsa.DSA_ERR_INVALID_ARG                       # k > ld
+    assert l2g(kl=None) == dsa.DSA_ERR_INVALID_ARG
+    assert l2g(kl=(ctypes.c_int32 * 2)(49, 8)) == dsa.DSA_ERR_INVALID_ARG   # more positions than 3 blocks of 16
+    assert l2g(kl=(ctypes.c_int32 * 2)(-1, 8)) == dsa.DSA_ERR_INVALID_ARG
+    assert l2g(cq=(ctypes.c_int32 * 3)(0, 3, 7)) == dsa.DSA_ERR_INVALID_ARG  # offsets do not add up to T
+    assert l2g(bt=None) == dsa.DSA_ERR_INVALID_ARG
+    assert l2g(out=ctypes.c_void_p(18)) == dsa.DSA_ERR_INVALID_ARG           # misaligned output
+    assert l2g(T=0, cq=None, nreq=0) == dsa.DSA_OK
 
 
 def test_python_binding_refuses_cpu_tensors(lib):

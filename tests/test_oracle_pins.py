@@ -26,6 +26,7 @@ _orig_union = O.union_build
 _orig_grouped = O.grouped_prefill
 _orig_keymask = O.topk_to_key_mask
 _orig_masked = O.masked_mha_prefill
+_orig_l2g = O.local_to_global
 
 
 def _attend_lse_base2(qf, K, V, scale):
@@ -110,6 +111,27 @@ def _masked_shared_head(q, k, v, km, cq, ck, scale, tokens=None):
     return _orig_masked(q, np.repeat(k[:, :1], k.shape[1], axis=1), v, km, cq, ck, scale, tokens)
 
 
+def _l2g_div_mod_swapped(idx, k, cq, kv_lens, bt, B, N):
+    idx = np.asarray(idx)
+    out = np.full(idx.shape, -1, dtype=np.int32)
+    cqq = [0, idx.shape[0]] if cq is None else list(cq)
+    for r in range(len(cqq) - 1):
+        for t in range(cqq[r], cqq[r + 1]):
+            for j in range(min(k, idx.shape[1])):
+                x = int(idx[t, j])
+                if 0 <= x < kv_lens[r] and x % B < bt.shape[1] and bt[r, x % B] >= 0:
+                    out[t, j] = int(bt[r, x % B]) * B + x // B
+    return out, 0
+
+
+def _l2g_first_request_table(idx, k, cq, kv_lens, bt, B, N):
+    return _orig_l2g(idx, k, cq, kv_lens, np.repeat(np.asarray(bt)[:1], len(bt), axis=0), B, N)
+
+
+def _l2g_no_range_check(idx, k, cq, kv_lens, bt, B, N):
+    return _orig_l2g(idx, k, cq, [np.asarray(bt).shape[1] * B] * len(kv_lens), bt, B, N)
+
+
 MUTATIONS = [
     ("attend", _attend_lse_base2),
     ("attend", _attend_sign),
@@ -125,6 +147,9 @@ MUTATIONS = [
     ("grouped_prefill", _grouped_head_major),
     ("topk_to_key_mask", _keymask_no_offset),
     ("masked_mha_prefill", _masked_shared_head),
+    ("local_to_global", _l2g_div_mod_swapped),
+    ("local_to_global", _l2g_first_request_table),
+    ("local_to_global", _l2g_no_range_check),
 ]
 
 
