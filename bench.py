@@ -278,7 +278,8 @@ def oracle_pool(cores):
 # ----------------------------------------------------------------------------
 # modes: the other forms on their own workloads
 # ----------------------------------------------------------------------------
-def run_modes(dev, stream, peaks, steps, warmup, flush):
+def run_modes(dev, stream, peaks, steps, warmup, flush, only=None):
+    """Times the other forms on their own workloads (``only``: a subset of the names)."""
     import torch
     import dsa_sparse_mla_prefill_gb300 as dsa
     from synth import WORKLOADS, make_masked_inputs, make_sparse_inputs
@@ -333,48 +334,71 @@ def run_modes(dev, stream, peaks, steps, warmup, flush):
                 res["grouped"] = {"unavailable": str(e)}
         return res
 
-    out["grouped_21k_of_32k"] = sparse_block("grouped_21k_of_32k")
-    torch.cuda.empty_cache()
-    out["nope_2x8192"] = sparse_block("nope_2x8192")
-    torch.cuda.empty_cache()
+    def want(name):
+        return only is None or name in only
+
+    for name in ("grouped_21k_of_32k", "nope_2x8192"):
+        if want(name):
+            out[name] = sparse_block(name)
+            torch.cuda.empty_cache()
     # the headline workload in grouped form (H = 32: G = 4 tokens per group)
-    out["v32_h32_16k_grouped"] = sparse_block("v32_h32_16k", per_token=False)
-    torch.cuda.empty_cache()
+    if want("v32_h32_16k_grouped"):
+        out["v32_h32_16k_grouped"] = sparse_block("v32_h32_16k", per_token=False)
+        torch.cuda.empty_cache()
     # wide-union stress variant of the grouped workload: every token draws its
     # replacements independently, so the 8-token unions grow
-    wide = dataclasses.replace(WORKLOADS["grouped_21k_of_32k"], name="grouped_21k_of_32k_wide",
-                               index_gen="locality_wide")
-    out["grouped_21k_of_32k_wide"] = sparse_block("grouped_21k_of_32k_wide", w=wide)
-    torch.cuda.empty_cache()
-    # masked dense MHA
-    w = WORKLOADS["masked_2x8192"]
-    log("mode masked_2x8192")
-    x = make_masked_inputs(w)
-    words = (max(w.kv_lens) + 31) // 32
-    words = (words + 3) // 4 * 4
-    idx = torch.from_numpy(x.idx).to(dev)
-    km = torch.empty((w.T, words), dtype=torch.int32, device=dev)
-    kfn = lambda: dsa.dsa_topk_to_key_mask(idx, w.k, words, cu_seqlens_q=x.cu_seqlens_q,
-                                           cu_seqlens_kv=x.cu_seqlens_kv, out=km)
-    ms_k = statistics.median(timed_steps(kfn, steps, warmup, stream, flush))
-    res = {"T": w.T, "H": w.H, "d_qk": w.d_qk, "d_v": w.d_v, "key_mask": {"ms": ms_k}}
-    try:
-        q, k, v = to_dev(x.q, dev), to_dev(x.k, dev), to_dev(x.v, dev)
-        o = torch.empty((w.T, w.H, w.d_v), dtype=torch.bfloat16, device=dev)
-        l = torch.empty((w.T, w.H), dtype=torch.float32, device=dev)
-        mfn = lambda: dsa.dsa_masked_mha_prefill(q, k, v, km, w.scale, cu_seqlens_q=x.cu_seqlens_q,
-                                                 cu_seqlens_kv=x.cu_seqlens_kv, out=o, lse=l)
-        mfn()
-        ms_m = statistics.median(timed_steps(mfn, steps, warmup, stream, flush))
-        pairs = int((x.idx[:, :w.k] >= 0).sum())
-        useful = 2.0 * w.H * pairs * (w.d_qk + w.d_v)
-        causal = sum(2.0 * w.H * (n * (n + 1) / 2) * (w.d_qk + w.d_v) for n in w.q_lens)
-        res["masked"] = {"ms": ms_m, "query_tokens_per_s": w.T / ms_m * 1e3, "useful_tflops": useful / ms_m / 1e9,
-                         "dense_causal_tflops": causal / ms_m / 1e9,
-                         "tensor_frac_dense_causal": causal / ms_m / 1e9 / peaks["bf16_tflops"]}
-    except dsa.DSAError as e:
-        res["masked"] = {"unavailable": str(e)}
-    out["masked_2x8192"] = res
+    if want("grouped_21k_of_32k_wide"):
+        wide = dataclasses.replace(WORKLOADS["grouped_21k_of_32k"], name="grouped_21k_of_32k_wide",
+                                   index_gen="locality_wide")
+        out["grouped_21k_of_32k_wide"] = sparse_block("grouped_21k_of_32k_wide", w=wide)
+        torch.cuda.empty_cache()
+    # masked dense MHA: DeepSeek-V3.2 geometry (contiguous per-head q/k/v),
+    # then the GLM NoPE and GLM-5 geometries with k and v read as views of one
+    # per-head projection output and the RoPE key columns shared
+    def masked_block(name):
+        w = WORKLOADS[name]
+        log(f"mode {name}")
+        x = make_masked_inputs(w)
+        words = (max(w.kv_lens) + 31) // 32
+        words = (words + 3) // 4 * 4
+        idx = torch.from_numpy(x.idx).to(dev)
+        km = torch.empty((w.T, words), dtype=torch.int32, device=dev)
+        kfn = lambda: dsa.dsa_topk_to_key_mask(idx, w.k, words, cu_seqlens_q=x.cu_seqlens_q,
+                                               cu_seqlens_kv=x.cu_seqlens_kv, out=km)
+        ms_k = statistics.median(timed_steps(kfn, steps, warmup, stream, flush))
+        res = {"T": w.T, "H": w.H, "d_qk": w.d_qk, "d_rope": w.d_rope, "d_v": w.d_v, "key_mask": {"ms": ms_k}}
+        try:
+            q = to_dev(x.q, dev)
+            o = torch.empty((w.T, w.H, w.d_v), dtype=torch.bfloat16, device=dev)
+            l = torch.empty((w.T, w.H), dtype=torch.float32, device=dev)
+            if w.split_kv:
+                dn = w.d_qk - w.d_rope
+                kvp = to_dev(x.kvp, dev)
+                k_pe = to_dev(x.k_pe, dev) if x.k_pe is not None else None
+                k, v = kvp[..., :dn], kvp[..., dn:]
+                mfn = lambda: dsa.dsa_masked_mha_prefill_strided(q, k, v, km, w.scale, k_pe=k_pe,
+                                                                 cu_seqlens_q=x.cu_seqlens_q,
+                                                                 cu_seqlens_kv=x.cu_seqlens_kv, out=o, lse=l)
+            else:
+                k, v = to_dev(x.k, dev), to_dev(x.v, dev)
+                mfn = lambda: dsa.dsa_masked_mha_prefill(q, k, v, km, w.scale, cu_seqlens_q=x.cu_seqlens_q,
+                                                         cu_seqlens_kv=x.cu_seqlens_kv, out=o, lse=l)
+            mfn()
+            ms_m = statistics.median(timed_steps(mfn, steps, warmup, stream, flush))
+            pairs = int((x.idx[:, :w.k] >= 0).sum())
+            useful = 2.0 * w.H * pairs * (w.d_qk + w.d_v)
+            causal = sum(2.0 * w.H * (n * (n + 1) / 2) * (w.d_qk + w.d_v) for n in w.q_lens)
+            res["masked"] = {"ms": ms_m, "query_tokens_per_s": w.T / ms_m * 1e3,
+                             "useful_tflops": useful / ms_m / 1e9, "dense_causal_tflops": causal / ms_m / 1e9,
+                             "tensor_frac_dense_causal": causal / ms_m / 1e9 / peaks["bf16_tflops"]}
+        except dsa.DSAError as e:
+            res["masked"] = {"unavailable": str(e)}
+        return res
+
+    for name in ("masked_2x8192", "masked_nope_2x8192", "masked_glm5_2x8192"):
+        if want(name):
+            out[name] = masked_block(name)
+            torch.cuda.empty_cache()
     return out
 
 
@@ -600,15 +624,24 @@ def run_profile_case(args):
             else:
                 fn = lambda: dsa.dsa_grouped_prefill(q, kv, u, ul, m, w.G, w.scale, cu_seqlens_q=x.cu_seqlens_q)
     elif args.profile == "masked":
-        base = WORKLOADS["masked_2x8192"]
-        w = scaled_down(base, (n,), (base.kv_lens[0],), name=f"masked_last{n}")
+        base = WORKLOADS[args.profile_workload or "masked_2x8192"]
+        w = scaled_down(base, (n,), (base.kv_lens[0],), name=f"{base.name}_last{n}")
         x = make_masked_inputs(w)
         words = ((max(w.kv_lens) + 31) // 32 + 3) // 4 * 4
         idx = torch.from_numpy(x.idx).to(dev)
         km = dsa.dsa_topk_to_key_mask(idx, w.k, words, cu_seqlens_q=x.cu_seqlens_q, cu_seqlens_kv=x.cu_seqlens_kv)
-        q, k, v = to_dev(x.q, dev), to_dev(x.k, dev), to_dev(x.v, dev)
-        fn = lambda: dsa.dsa_masked_mha_prefill(q, k, v, km, w.scale, cu_seqlens_q=x.cu_seqlens_q,
-                                                cu_seqlens_kv=x.cu_seqlens_kv)
+        q = to_dev(x.q, dev)
+        if w.split_kv:
+            dn = w.d_qk - w.d_rope
+            kvp = to_dev(x.kvp, dev)
+            k_pe = to_dev(x.k_pe, dev) if x.k_pe is not None else None
+            fn = lambda: dsa.dsa_masked_mha_prefill_strided(q, kvp[..., :dn], kvp[..., dn:], km, w.scale, k_pe=k_pe,
+                                                            cu_seqlens_q=x.cu_seqlens_q,
+                                                            cu_seqlens_kv=x.cu_seqlens_kv)
+        else:
+            k, v = to_dev(x.k, dev), to_dev(x.v, dev)
+            fn = lambda: dsa.dsa_masked_mha_prefill(q, k, v, km, w.scale, cu_seqlens_q=x.cu_seqlens_q,
+                                                    cu_seqlens_kv=x.cu_seqlens_kv)
     else:
         raise ValueError(args.profile)
     ms = timed_steps(fn, args.steps, args.warmup, torch.cuda.current_stream(dev))
@@ -634,7 +667,7 @@ def main():
                     help="run a small case of one kernel (for ncu) instead of the benchmark")
     ap.add_argument("--profile-tokens", type=int, default=2048)
     ap.add_argument("--profile-workload", default=None,
-                    help="profile mode (sparse, union, grouped): base workload, e.g. nope_2x8192")
+                    help="profile mode: base workload, e.g. nope_2x8192 or masked_nope_2x8192")
     ap.add_argument("--trace", type=int, default=0, help="profile mode: record a per-tile timeline of N tiles")
     ap.add_argument("--trace-out", default=None, help="profile mode: save the raw timeline (.npy)")
     args = ap.parse_args()

@@ -13,6 +13,7 @@ Forms (see the header for the exact contracts):
   dsa_grouped_prefill     G = 128/H tokens as 128 pseudo-heads over the union
   dsa_topk_to_key_mask    packed per-token key mask from the top-k rows
   dsa_masked_mha_prefill  masked dense MHA with per-head q/k/v
+  dsa_masked_mha_prefill_strided  the same on strided views, RoPE key columns shared
 """
 from __future__ import annotations
 
@@ -40,6 +41,7 @@ _VP = ctypes.c_void_p
 _I = ctypes.c_int
 _F = ctypes.c_float
 _I32P = ctypes.POINTER(ctypes.c_int32)
+_L = ctypes.c_int64
 
 _SIGNATURES = {
     "dsa_status_string": (ctypes.c_char_p, [_I]),
@@ -54,6 +56,8 @@ _SIGNATURES = {
     "dsa_local_to_global": (_I, [_VP, _I, _I, _I, _I32P, _I32P, _I, _VP, _I, _I, _I, _VP, _VP]),
     "dsa_masked_mha_prefill": (_I, [_VP, _VP, _VP, _VP, _I, _I32P, _I32P, _I, _I, _I, _I, _I, _F, _VP, _VP,
                                     _VP]),
+    "dsa_masked_mha_prefill_strided": (_I, [_VP, _L, _L, _VP, _L, _L, _VP, _L, _VP, _L, _L, _VP, _I, _I32P, _I32P,
+                                            _I, _I, _I, _I, _I, _I, _F, _VP, _VP, _VP]),
     "dsa_last_device_error": (_I, [_VP, ctypes.POINTER(ctypes.c_uint32)]),
     "dsa_debug_trace": (_I, [_VP, _I]),
 }
@@ -263,6 +267,43 @@ def dsa_masked_mha_prefill(q, k, v, key_mask, scale: float, cu_seqlens_q=None, c
                                         key_mask.shape[1], pq, pk, nreq, T, H, d_qk, d_v, float(scale),
                                         out.data_ptr(), lse.data_ptr(), _stream(stream, q.device)),
            "dsa_masked_mha_prefill")
+    return out, lse
+
+
+def dsa_masked_mha_prefill_strided(q, k, v, key_mask, scale: float, k_pe=None, cu_seqlens_q=None,
+                                   cu_seqlens_kv=None, out=None, lse=None, stream=None):
+    """Masked dense MHA on strided views.  q [T, H, d_qk], k [Nk, H, d_qk - d_rope] and
+    v [Nk, H, d_v] bf16 with unit stride in the last dimension (e.g. k = kv[..., :256] and
+    v = kv[..., 256:] of one [Nk, H, 512] projection output, no copies); k_pe [Nk, d_rope]
+    (d_rope = 64) holds the RoPE key columns shared by all heads, or None (d_rope = 0).
+    Returns (out [T, H, d_v], lse [T, H])."""
+    import torch
+    for name, x in (("q", q), ("k", k), ("v", v)):
+        if x.dtype != torch.bfloat16 or x.dim() != 3 or x.stride(2) != 1:
+            raise TypeError(f"{name} must be a 3-D bf16 tensor with unit stride in its last dimension")
+    if key_mask.dtype != torch.int32 or key_mask.dim() != 2 or not key_mask.is_contiguous():
+        raise TypeError("key_mask must be a contiguous 2-D int32 tensor (bit pattern of uint32 words)")
+    d_rope, pe_ptr, pe_stride = 0, None, 0
+    if k_pe is not None:
+        if k_pe.dtype != torch.bfloat16 or k_pe.dim() != 2 or k_pe.stride(1) != 1:
+            raise TypeError("k_pe must be a 2-D bf16 tensor with unit stride in its last dimension")
+        d_rope, pe_ptr, pe_stride = k_pe.shape[1], k_pe.data_ptr(), k_pe.stride(0)
+    T, H, d_qk = q.shape
+    d_v = v.shape[2]
+    if k.shape[2] + d_rope != d_qk:
+        raise ValueError("k columns + k_pe columns must equal q's head dim")
+    if out is None:
+        out = torch.empty((T, H, d_v), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
+    aq, pq = _host_i32(cu_seqlens_q)
+    ak, pk = _host_i32(cu_seqlens_kv)
+    nreq = 0 if aq is None else len(aq) - 1
+    _check(lib().dsa_masked_mha_prefill_strided(
+        q.data_ptr(), q.stride(0), q.stride(1), k.data_ptr(), k.stride(0), k.stride(1), pe_ptr, pe_stride,
+        v.data_ptr(), v.stride(0), v.stride(1), key_mask.data_ptr(), key_mask.shape[1], pq, pk, nreq, T, H,
+        d_qk, d_rope, d_v, float(scale), out.data_ptr(), lse.data_ptr(), _stream(stream, q.device)),
+        "dsa_masked_mha_prefill_strided")
     return out, lse
 
 

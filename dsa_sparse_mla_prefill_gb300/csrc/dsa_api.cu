@@ -308,21 +308,35 @@ int dsa_local_to_global(const int32_t* idx_local, int T, int k, int ld, const in
   return dsa::launch_local_to_global(a, (cudaStream_t)stream) == 0 ? DSA_OK : DSA_ERR_CUDA;
 }
 
-int dsa_masked_mha_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint32_t* key_mask,
-                           int words, const int32_t* cu_seqlens_q_host, const int32_t* cu_seqlens_kv_host,
-                           int num_req, int T, int H, int d_qk, int d_v, float scale, uint16_t* out, float* lse,
-                           dsa_stream_t stream) {
+int dsa_masked_mha_prefill_strided(const uint16_t* q, int64_t q_stride_t, int64_t q_stride_h, const uint16_t* k,
+                                   int64_t k_stride_t, int64_t k_stride_h, const uint16_t* k_pe,
+                                   int64_t k_pe_stride_t, const uint16_t* v, int64_t v_stride_t, int64_t v_stride_h,
+                                   const uint32_t* key_mask, int words, const int32_t* cu_seqlens_q_host,
+                                   const int32_t* cu_seqlens_kv_host, int num_req, int T, int H, int d_qk,
+                                   int d_rope, int d_v, float scale, uint16_t* out, float* lse, dsa_stream_t stream) {
   if (T < 0 || H < 1 || words < 1) return DSA_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !(scale < INFINITY)) return DSA_ERR_INVALID_ARG;
   if ((cu_seqlens_q_host == nullptr) != (cu_seqlens_kv_host == nullptr)) return DSA_ERR_INVALID_ARG;
-  if (!(d_qk == 192 && d_v == 128)) return DSA_ERR_UNSUPPORTED;
+  if (!((d_qk == 192 && d_v == 128) || (d_qk == 256 && d_v == 256))) return DSA_ERR_UNSUPPORTED;
+  if (d_rope != 0 && d_rope != 64) return DSA_ERR_UNSUPPORTED;
   if (T == 0) return DSA_OK;
-  if (!q || !k || !v || !key_mask || !out || !lse) return DSA_ERR_INVALID_ARG;
+  const int d_k = d_qk - d_rope;   // columns of each key row read from k
+  if (!q || !k || !v || !key_mask || !out || !lse || (d_rope > 0 && !k_pe)) return DSA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(key_mask) || !aligned16(out) ||
-      !aligned4(lse))
+      !aligned4(lse) || (d_rope > 0 && !aligned16(k_pe)))
     return DSA_ERR_INVALID_ARG;
+  // strides in elements: multiples of 8 (16 bytes, the TMA rule), heads and
+  // rows not overlapping
+  auto strides_ok = [&](int64_t st, int64_t sh, int cols) {
+    return (st % 8) == 0 && (sh % 8) == 0 && sh >= cols && st >= (int64_t)H * sh;
+  };
+  if (!strides_ok(q_stride_t, q_stride_h, d_qk) || !strides_ok(k_stride_t, k_stride_h, d_k) ||
+      !strides_ok(v_stride_t, v_stride_h, d_v))
+    return DSA_ERR_INVALID_ARG;
+  if (d_rope > 0 && ((k_pe_stride_t % 8) != 0 || k_pe_stride_t < d_rope)) return DSA_ERR_INVALID_ARG;
   if ((words & 3) != 0) return DSA_ERR_INVALID_ARG;  // 128-key tiles read 4 words per row
   dsa::MaskedArgs a;
+  memset(&a, 0, sizeof(a));
   // query tiles of 128 per request
   int st = fill_req(a.req, cu_seqlens_q_host, cu_seqlens_kv_host, num_req, T, cu_seqlens_kv_host ? -1 : T, 128);
   if (st != DSA_OK) return st;
@@ -330,9 +344,7 @@ int dsa_masked_mha_prefill(const uint16_t* q, const uint16_t* k, const uint16_t*
     if (a.req.cu_kv[r + 1] - a.req.cu_kv[r] > 32 * words) return DSA_ERR_INVALID_ARG;
   DevInfo* d;
   if (!dev_info(&d)) return DSA_ERR_CUDA;
-  a.q = q;
-  a.k = k;
-  a.v = v;
+  a.k_chunks = d_k / 64;
   a.key_mask = key_mask;
   a.out = out;
   a.lse = lse;
@@ -347,11 +359,23 @@ int dsa_masked_mha_prefill(const uint16_t* q, const uint16_t* k, const uint16_t*
   a.tr = g_trace;
   // (with no keys no key tile is loaded; the maps still need one row)
   const int64_t nk = a.req.cu_kv[a.req.num_req] > 0 ? a.req.cu_kv[a.req.num_req] : 1;
-  if (!dsa::make_head_tile_map(&a.tmap_q, q, T, H, d_qk, 128) || !dsa::make_head_tile_map(&a.tmap_k, k, nk, H, d_qk, 128) ||
-      !dsa::make_head_tile_map(&a.tmap_v, v, nk, H, d_v, 128))
+  const int v_box = d_v > 128 ? 64 : 128;   // keys per V stage of the kernel
+  if (!dsa::make_head_tile_map_strided(&a.tmap_q, q, T, H, d_qk, q_stride_h, q_stride_t, 128) ||
+      !dsa::make_head_tile_map_strided(&a.tmap_k, k, nk, H, d_k, k_stride_h, k_stride_t, 128) ||
+      !dsa::make_head_tile_map_strided(&a.tmap_v, v, nk, H, d_v, v_stride_h, v_stride_t, v_box) ||
+      (d_rope > 0 && !dsa::make_tile_map(&a.tmap_kpe, k_pe, nk, d_rope, k_pe_stride_t, 128)))
     return DSA_ERR_CUDA;
   const int r = dsa::launch_masked_mha(a, d->num_sms, (cudaStream_t)stream);
   return r == 0 ? DSA_OK : (r == -2 ? DSA_ERR_UNSUPPORTED : DSA_ERR_CUDA);
+}
+
+int dsa_masked_mha_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint32_t* key_mask,
+                           int words, const int32_t* cu_seqlens_q_host, const int32_t* cu_seqlens_kv_host,
+                           int num_req, int T, int H, int d_qk, int d_v, float scale, uint16_t* out, float* lse,
+                           dsa_stream_t stream) {
+  return dsa_masked_mha_prefill_strided(q, (int64_t)H * d_qk, d_qk, k, (int64_t)H * d_qk, d_qk, nullptr, 0, v,
+                                        (int64_t)H * d_v, d_v, key_mask, words, cu_seqlens_q_host,
+                                        cu_seqlens_kv_host, num_req, T, H, d_qk, 0, d_v, scale, out, lse, stream);
 }
 
 int dsa_debug_trace(void* device_buffer, int capacity) {

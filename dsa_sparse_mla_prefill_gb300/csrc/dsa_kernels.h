@@ -88,12 +88,11 @@ struct GroupedArgs {
 };
 
 struct MaskedArgs {
-  CUtensorMap tmap_q;   // q [T, H, d_qk]: box 64 columns x 1 head x 128 rows
-  CUtensorMap tmap_k;   // k [Nk, H, d_qk]: same box
-  CUtensorMap tmap_v;   // v [Nk, H, d_v]: same box
-  const uint16_t* q;    // [T, H, d_qk]
-  const uint16_t* k;    // [Nk, H, d_qk]
-  const uint16_t* v;    // [Nk, H, d_v]
+  CUtensorMap tmap_q;   // q [T, H, d_qk] (strided): box 64 columns x 1 head x 128 rows
+  CUtensorMap tmap_k;   // k [Nk, H, 64 * k_chunks] (strided): same box
+  CUtensorMap tmap_v;   // v [Nk, H, d_v] (strided): box 64 columns x 1 head x (128 or 64) rows
+  CUtensorMap tmap_kpe; // shared RoPE columns [Nk, d_qk - 64 * k_chunks]: box 64 columns x 128 rows
+  int k_chunks;         // 64-column chunks of each key row read from tmap_k (the rest from tmap_kpe)
   const uint32_t* key_mask;  // [T, words]
   uint16_t* out;        // [T, H, d_v]
   float* lse;           // [T, H]

@@ -60,22 +60,28 @@ inline bool make_tile_map(CUtensorMap* m, const void* base, int64_t rows, int64_
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 3-D bf16 map over a [rows, heads, cols] tensor (row pitch heads*cols
-// elements): box = 64 columns x 1 head x box_rows rows, 128-byte swizzle, so
-// a box of one head lands as box_rows consecutive 128-byte rows, the K-major
-// layout of one swizzle column of an MMA operand.  Rows outside [0, rows)
-// read as zeros.
-inline bool make_head_tile_map(CUtensorMap* m, const void* base, int64_t rows, int64_t heads, int64_t cols,
-                               int box_rows) {
+// 3-D bf16 map over a strided [rows, heads, cols] view (element strides
+// stride_h between heads and stride_t between rows, both multiples of 8):
+// box = 64 columns x 1 head x box_rows rows, 128-byte swizzle, so a box of
+// one head lands as box_rows consecutive 128-byte rows, the K-major layout of
+// one swizzle column of an MMA operand.  Rows outside [0, rows) read as zeros.
+inline bool make_head_tile_map_strided(CUtensorMap* m, const void* base, int64_t rows, int64_t heads, int64_t cols,
+                                       int64_t stride_h, int64_t stride_t, int box_rows) {
   EncodeTiledFn fn = encode_tiled_fn();
   if (fn == nullptr || rows < 1 || heads < 1 || cols < 64 || box_rows < 1 || box_rows > 256) return false;
   cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)heads, (cuuint64_t)rows};
-  cuuint64_t strides[2] = {(cuuint64_t)cols * 2u, (cuuint64_t)heads * cols * 2u};
+  cuuint64_t strides[2] = {(cuuint64_t)stride_h * 2u, (cuuint64_t)stride_t * 2u};
   cuuint32_t box[3] = {64u, 1u, (cuuint32_t)box_rows};
   cuuint32_t es[3] = {1u, 1u, 1u};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The same over a contiguous [rows, heads, cols] tensor.
+inline bool make_head_tile_map(CUtensorMap* m, const void* base, int64_t rows, int64_t heads, int64_t cols,
+                               int box_rows) {
+  return make_head_tile_map_strided(m, base, rows, heads, cols, cols, heads * cols, box_rows);
 }
 
 }  // namespace dsa

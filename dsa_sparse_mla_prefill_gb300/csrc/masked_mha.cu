@@ -7,21 +7,35 @@
 // query t of request r:
 //     out[t,h,:] = softmax_{n : bit n of key_mask[t]}( scale * q[t,h,:] . k[c_r+n,h,:] ) . v[c_r+n,h,:]
 //
+// Geometries ("[Perf][GLM-5.3-Flash] ...", Purpose and review snippets: the
+// masked-MHA allow-list): (d_qk, d_v) = (192, 128) for DeepSeek-V3.2 and
+// (256, 256) for GLM-5 (192 + 64 RoPE columns) and GLM-5.3-Flash (NoPE, 256
+// + 0).  q, k and v are read through strided 3-D tensor maps, so k and v may
+// be views into the per-head kv projection (no copy); when the RoPE columns
+// are shared by all heads they come from their own [Nk, 64] buffer and the
+// concatenated K is never formed ("skip the NoPE K concat", and the same for
+// the RoPE part).
+//
 // One CTA per (128-query tile, head), FlashAttention-style over 128-key
 // tiles of the request:
-//   warp 9      TMA: the q tile and each k/v tile as 3-D boxes of one head
-//               (64 columns x 1 head x 128 rows, 128B-swizzled); before a
-//               key tile it reads the tile's 4 mask words of every query
-//               row and skips tiles where every bit is zero (the whole upper
-//               causal triangle, and any empty tile).  K and V have their
-//               own 2-stage rings: a K stage returns after its QK, a V stage
-//               after its PV, so the next tiles' K loads are not held up by
-//               this tile's softmax.
+//   warp 9      TMA: the q tile and each k tile as 3-D boxes of one head
+//               (64 columns x 1 head x rows, 128B-swizzled; the shared RoPE
+//               columns as 2-D boxes); before a key tile it reads the tile's
+//               4 mask words of every query row and skips tiles where every
+//               bit is zero (the whole upper causal triangle, and any empty
+//               tile).  K and V have their own 2-stage rings: a K stage
+//               returns after its QK, a V stage after its PV, so the next
+//               tiles' K loads are not held up by this tile's softmax.  At
+//               d_qk = 192 a K stage is the whole 128-key tile and a V stage
+//               too; at 256 (64 KB per tile) a K stage is half the columns
+//               and a V stage half the keys, so both rings fit next to q.
 //   warp 8      one thread: S = Q K^T (M = 128 queries, N = 128 keys) into a
 //               double-buffered TMEM S.
 //   warp 10     one thread: O += P V with P read from TMEM (two issuing
 //               threads: one thread's per-tile waits, fences and commits
 //               were the longer loop).
+//   warp 11     TMA: the v tiles, following the tile sequence that warp 9
+//               posts, so K loads never wait behind a V stage.
 //   warps 0-7   two threads per query row (TMEM lane): warp w holds row
 //               32(w%4) + lane and keys 64(w/4) .. +63 of each tile; mask,
 //               online softmax (base 2, lazy rescale) with the row max
@@ -36,16 +50,21 @@ namespace masked {
 constexpr int BQ = 128;
 constexpr int BKV = 128;
 constexpr int HK = BKV / 2;     // keys per softmax thread
-constexpr int NTHREADS = 352;   // 11 warps
+constexpr int NTHREADS = 384;   // 12 warps
 constexpr float kTau = 8.0f;
 
 template <int DQK, int DV>
 struct Cfg {
   static constexpr int QC = DQK / 64;   // swizzle columns of q / k
   static constexpr int VC = DV / 64;    // swizzle columns of v
+  static constexpr int KSC = DQK > 192 ? 2 : QC;   // swizzle columns per K stage (all 128 keys)
+  static constexpr int KPT = QC / KSC;             // K stages per key tile
+  static constexpr int VR = DV > 128 ? 64 : BKV;   // keys per V stage (all DV columns)
+  static constexpr int VPT = BKV / VR;             // V stages per key tile
+  static_assert(QC % KSC == 0 && BKV % VR == 0 && VR % 64 == 0, "stage split");
   static constexpr uint32_t Q_BYTES = QC * BQ * 128u;
-  static constexpr uint32_t K_BYTES = QC * BKV * 128u;
-  static constexpr uint32_t V_BYTES = VC * BKV * 128u;
+  static constexpr uint32_t K_BYTES = KSC * BKV * 128u;   // one K stage
+  static constexpr uint32_t V_BYTES = VC * VR * 128u;     // one V stage
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;             // [2]
   static constexpr uint32_t OFF_V = OFF_K + 2 * K_BYTES;         // [2]
@@ -143,7 +162,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) masked_mha_kernel(const __grid_co
         tma_load_3d(sbase + C::OFF_Q + c * (BQ * 128), &a.tmap_q, c * 64, h, q0, &bars[B_Q_FULL]);
     }
     const uint32_t* km = a.key_mask;
-    uint32_t st = 0;  // stages used
+    uint32_t st = 0;    // key tiles posted
+    uint32_t nku = 0;   // K stage uses issued
     bool ok = true;
     for (int j = 0; j < ntk && ok; ++j) {
       // the tile's 4 mask words of query rows lane, lane+32, lane+64, lane+96
@@ -157,39 +177,49 @@ __global__ void __launch_bounds__(NTHREADS, 1) masked_mha_kernel(const __grid_co
         any |= w[i].x | w[i].y | w[i].z | w[i].w;
       }
       if (!__any_sync(0xffffffffu, any != 0)) continue;
-      // Info slot st % 4 is rewritten only after QK(st-2) completed, which
-      // follows P.V(st-4) and hence the softmax of tile st-4 that read it.
-      const int s = st & 1;
+      // K stage use u = st * KPT + i goes to stage u % 2.  Info slot st % 4
+      // is rewritten only after the QK of the tile before completed its
+      // first K stage; that QK waited for the P.V of tile st-3, which
+      // followed the softmax and the P.V of tile st-4 that read the slot.
       const int is = st & 3;
-      if (!mbar_wait_warp(&bars[B_K_EMPTY + s], ((st >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+      const int kr = kv0 + j * BKV;   // first key row of the tile
+      // keys past the request read the next request's rows (their mask bits
+      // are zero) or, past the table, zeros
 #pragma unroll
-      for (int i = 0; i < 4; ++i) reinterpret_cast<uint4*>(smem + C::OFF_MASK + is * BQ * 16)[lane + 32 * i] = w[i];
-      if (lane == 0) stage_tile[is] = j;
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&bars[B_INFO + is]);
-        mbar_arrive_expect_tx(&bars[B_K_FULL + s], C::K_BYTES);
-        // keys past the request read the next request's rows (their mask
-        // bits are zero) or, past the table, zeros
-        for (int c = 0; c < C::QC; ++c)
-          tma_load_3d(sbase + C::OFF_K + s * C::K_BYTES + c * (BKV * 128), &a.tmap_k, c * 64, h, kv0 + j * BKV,
-                      &bars[B_K_FULL + s]);
+      for (int i = 0; i < C::KPT && ok; ++i) {
+        const uint32_t u = nku;   // == st * KPT + i
+        const int s = u & 1;
+        if (!mbar_wait_warp(&bars[B_K_EMPTY + s], ((u >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+        if (i == 0) {
+#pragma unroll
+          for (int m = 0; m < 4; ++m)
+            reinterpret_cast<uint4*>(smem + C::OFF_MASK + is * BQ * 16)[lane + 32 * m] = w[m];
+          if (lane == 0) stage_tile[is] = j;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[B_INFO + is]);
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars[B_K_FULL + s], C::K_BYTES);
+          for (int c = 0; c < C::KSC; ++c) {
+            const int cg = i * C::KSC + c;   // swizzle column of the head's key row
+            const uint32_t dst = sbase + C::OFF_K + s * C::K_BYTES + c * (BKV * 128);
+            if (cg < a.k_chunks)
+              tma_load_3d(dst, &a.tmap_k, cg * 64, h, kr, &bars[B_K_FULL + s]);
+            else   // shared RoPE columns
+              tma_load_2d(dst, &a.tmap_kpe, (cg - a.k_chunks) * 64, kr, &bars[B_K_FULL + s]);
+          }
+        }
+        ++nku;
       }
-      if (!mbar_wait_warp(&bars[B_V_EMPTY + s], ((st >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&bars[B_V_FULL + s], C::V_BYTES);
-        for (int c = 0; c < C::VC; ++c)
-          tma_load_3d(sbase + C::OFF_V + s * C::V_BYTES + c * (BKV * 128), &a.tmap_v, c * 64, h, kv0 + j * BKV,
-                      &bars[B_V_FULL + s]);
-      }
+      if (!ok) break;
       ++st;
     }
     bool marked = false;
     if (ok) {
       // end marker (to the softmax through the info ring, to the MMA issuer
       // through a K stage without bytes)
-      const int s = st & 1;
-      marked = mbar_wait_warp(&bars[B_K_EMPTY + s], ((st >> 1) & 1) ^ 1, abort_flag, err);
+      const int s = nku & 1;
+      marked = mbar_wait_warp(&bars[B_K_EMPTY + s], ((nku >> 1) & 1) ^ 1, abort_flag, err);
       if (marked && lane == 0) {
         stage_tile[st & 3] = -1;
         mbar_arrive(&bars[B_INFO + (st & 3)]);
@@ -197,16 +227,49 @@ __global__ void __launch_bounds__(NTHREADS, 1) masked_mha_kernel(const __grid_co
       }
     }
     // Let copies still in flight land before the CTA can exit: q, and the
-    // last data phase of each K and V stage barrier.  Once the end marker is
-    // posted on K stage st, that barrier's data phase st-2 was consumed
-    // already (and its parity now names the marker's successor phase).
+    // last data phase of each K stage barrier (counted by the uses issued,
+    // so a tile whose loads stopped half way is covered too).  Once the end
+    // marker is posted on K stage use nku, that barrier's data phase nku-2
+    // was consumed already (and its parity now names the marker's successor
+    // phase).
     if (lane == 0) {
       mbar_wait_drain(&bars[B_Q_FULL], 0, err);
-      for (uint32_t i = (st > 2 ? st - 2 : 0); i < st; ++i) {
-        if (!(marked && i + 2 == st)) mbar_wait_drain(&bars[B_K_FULL + (i & 1)], (i >> 1) & 1, err);
-        mbar_wait_drain(&bars[B_V_FULL + (i & 1)], (i >> 1) & 1, err);
+      for (uint32_t i = (nku > 2 ? nku - 2 : 0); i < nku; ++i)
+        if (!(marked && i + 2 == nku)) mbar_wait_drain(&bars[B_K_FULL + (i & 1)], (i >> 1) & 1, err);
+    }
+    __syncwarp();
+  } else if (warp == 11) {
+    // ------------------------------------------------------------------
+    // V producer: the tile sequence comes through the info ring, so the K
+    // stream (warp 9) runs ahead of the V stream.  It reads info slot n
+    // before it can load V of tile n+1, which the P.V of tile n+1 needs
+    // before slot n is rewritten for tile n+4.
+    // ------------------------------------------------------------------
+    uint32_t nvu = 0;   // V stage uses issued
+    bool ok = true;
+    for (uint32_t n = 0; ok; ++n) {
+      const int is = n & 3;
+      if (!mbar_wait_warp(&bars[B_INFO + is], (n >> 2) & 1, abort_flag, err)) break;
+      const int tile = stage_tile[is];
+      if (tile < 0) break;
+      const int kr = kv0 + tile * BKV;
+#pragma unroll
+      for (int i = 0; i < C::VPT; ++i) {
+        const uint32_t u = nvu;   // == n * VPT + i: keys i*VR .. of the tile
+        const int s = u & 1;
+        if (!mbar_wait_warp(&bars[B_V_EMPTY + s], ((u >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars[B_V_FULL + s], C::V_BYTES);
+          for (int c = 0; c < C::VC; ++c)
+            tma_load_3d(sbase + C::OFF_V + s * C::V_BYTES + c * (C::VR * 128), &a.tmap_v, c * 64, h, kr + i * C::VR,
+                        &bars[B_V_FULL + s]);
+        }
+        ++nvu;
       }
     }
+    if (lane == 0)
+      for (uint32_t i = (nvu > 2 ? nvu - 2 : 0); i < nvu; ++i)
+        mbar_wait_drain(&bars[B_V_FULL + (i & 1)], (i >> 1) & 1, err);
     __syncwarp();
   } else if (warp == 8) {
     // ------------------------------------------------------------------
@@ -219,19 +282,30 @@ __global__ void __launch_bounds__(NTHREADS, 1) masked_mha_kernel(const __grid_co
       bool ok = mbar_wait(&bars[B_Q_FULL], 0, abort_flag, err);
       tc_fence_after();
       for (uint32_t n = 0; ok; ++n) {
-        const int s = n & 1;
-        if (!mbar_wait(&bars[B_K_FULL + s], (n >> 1) & 1, abort_flag, err)) break;
-        tc_fence_after();
-        if (stage_tile[n & 3] < 0) break;   // end marker
-        if (!mbar_wait(&bars[B_S_EMPTY + s], ((n >> 1) & 1) ^ 1, abort_flag, err)) break;
-        tc_fence_after();
-        const uint32_t ks = sbase + C::OFF_K + s * C::K_BYTES;
+        const int sb = n & 1;   // S buffer
+        bool end = false;
 #pragma unroll
-        for (int c = 0; c < C::QC; ++c)
-          mma_bf16_ss_x4(tmem + C::COL_S + s * 128, sdesc_sw128(qs + c * (BQ * 128), 16, 1024),
-                         sdesc_sw128(ks + c * (BKV * 128), 16, 1024), 2u, 2u, IDESC_QK, c > 0 ? 1u : 0u);
-        mma_commit(&bars[B_S_FULL + s]);
-        mma_commit(&bars[B_K_EMPTY + s]);
+        for (int i = 0; i < C::KPT; ++i) {
+          const uint32_t u = n * C::KPT + i;   // K stage use
+          const int s = u & 1;
+          if (!mbar_wait(&bars[B_K_FULL + s], (u >> 1) & 1, abort_flag, err)) { ok = false; break; }
+          tc_fence_after();
+          if (i == 0) {
+            if (stage_tile[n & 3] < 0) { end = true; break; }   // end marker
+            if (!mbar_wait(&bars[B_S_EMPTY + sb], ((n >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+            tc_fence_after();
+          }
+          const uint32_t ks = sbase + C::OFF_K + s * C::K_BYTES;
+#pragma unroll
+          for (int c = 0; c < C::KSC; ++c) {
+            const int cq = i * C::KSC + c;
+            mma_bf16_ss_x4(tmem + C::COL_S + sb * 128, sdesc_sw128(qs + cq * (BQ * 128), 16, 1024),
+                           sdesc_sw128(ks + c * (BKV * 128), 16, 1024), 2u, 2u, IDESC_QK, cq > 0 ? 1u : 0u);
+          }
+          mma_commit(&bars[B_K_EMPTY + s]);
+        }
+        if (!ok || end) break;
+        mma_commit(&bars[B_S_FULL + sb]);
       }
       mma_commit(&bars[B_DRAIN + 0]);
       mbar_wait(&bars[B_DRAIN + 0], 0, abort_flag, err);
@@ -246,23 +320,31 @@ __global__ void __launch_bounds__(NTHREADS, 1) masked_mha_kernel(const __grid_co
     // ------------------------------------------------------------------
     if (lane == 0) {
       constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, DV, false, true);
-      for (uint32_t n = 0;; ++n) {
-        const int s = n & 1;
+      bool ok = true;
+      for (uint32_t n = 0; ok; ++n) {
+        const int sb = n & 1;   // S buffer holding P
         const int is = n & 3;
         if (!mbar_wait(&bars[B_INFO + is], (n >> 2) & 1, abort_flag, err)) break;
         if (stage_tile[is] < 0) break;   // end marker
         if (!mbar_wait(&bars[B_P_FULL], n & 1, abort_flag, err)) break;
-        if (!mbar_wait(&bars[B_V_FULL + s], (n >> 1) & 1, abort_flag, err)) break;
-        tc_fence_after();
-        const uint32_t vs = sbase + C::OFF_V + s * C::V_BYTES;
 #pragma unroll
-        for (int half = 0; half < 2; ++half)
-          mma_bf16_ts_x4(tmem + C::COL_O, tmem + C::COL_S + s * 128 + half * 32,
-                         sdesc_sw128(vs + half * 4 * 2048, BKV * 128, 1024), 8u, 128u, IDESC_PV,
-                         (n > 0 || half > 0) ? 1u : 0u);
+        for (int i = 0; i < C::VPT; ++i) {
+          const uint32_t u = n * C::VPT + i;   // V stage use: keys i*VR .. of the tile
+          const int s = u & 1;
+          if (!mbar_wait(&bars[B_V_FULL + s], (u >> 1) & 1, abort_flag, err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t vs = sbase + C::OFF_V + s * C::V_BYTES;
+          // 64 keys per x4 batch: P columns (bf16 pairs) of those keys, V rows of those keys
+#pragma unroll
+          for (int g = 0; g < C::VR / 64; ++g)
+            mma_bf16_ts_x4(tmem + C::COL_O, tmem + C::COL_S + sb * 128 + (i * C::VR + g * 64) / 2,
+                           sdesc_sw128(vs + g * 64 * 128, C::VR * 128, 1024), 8u, 128u, IDESC_PV,
+                           (n > 0 || i > 0 || g > 0) ? 1u : 0u);
+          mma_commit(&bars[B_V_EMPTY + s]);
+        }
+        if (!ok) break;
         mma_commit(&bars[B_PV_DONE]);
-        mma_commit(&bars[B_V_EMPTY + s]);
-        mma_commit(&bars[B_S_EMPTY + s]);
+        mma_commit(&bars[B_S_EMPTY + sb]);
       }
       mma_commit(&bars[B_DRAIN + 1]);
       mbar_wait(&bars[B_DRAIN + 1], 0, abort_flag, err);
@@ -392,6 +474,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) masked_mha_kernel(const __grid_co
 
 template <int DQK, int DV>
 static int launch_t(const MaskedArgs& a, cudaStream_t stream) {
+  static_assert(Cfg<DQK, DV>::SMEM_BYTES <= 227u * 1024u, "shared memory budget");
   using C = Cfg<DQK, DV>;
   static int attr_set[64] = {0};
   int dev = 0;
@@ -412,6 +495,7 @@ static int launch_t(const MaskedArgs& a, cudaStream_t stream) {
 
 int launch_masked_mha(const MaskedArgs& a, int /*num_sms*/, cudaStream_t stream) {
   if (a.d_qk == 192 && a.d_v == 128) return masked::launch_t<192, 128>(a, stream);
+  if (a.d_qk == 256 && a.d_v == 256) return masked::launch_t<256, 256>(a, stream);
   return -2;
 }
 

@@ -199,14 +199,44 @@ int dsa_local_to_global(const int32_t* idx_local, int T, int k, int ld, const in
  *     Nk = cu_seqlens_kv[num_req].
  * key_mask [T, words] uint32 as written by dsa_topk_to_key_mask.
  * out [T, H, d_v] bf16 (out); lse [T, H] fp32 (out, natural log).
- * (d_qk, d_v) = (192, 128) (the DeepSeek-V3.2 geometry on the allow-list).
+ * (d_qk, d_v) = (192, 128) (DeepSeek-V3.2) or (256, 256) (GLM-5 and the
+ * GLM-5.3-Flash NoPE layout), the geometries of the masked-MHA allow-list
+ * ("[Perf][GLM-5.3-Flash] ...", review snippets); others return
+ * DSA_ERR_UNSUPPORTED.  Any H >= 1.
  * scale must be positive and finite (the kernel takes the row max on
  * unscaled scores); otherwise DSA_ERR_INVALID_ARG.
+ * Chunked context: a request's queries may be the last q_len of its kv_len
+ * keys (cu_seqlens_q and cu_seqlens_kv differ); the mask rows of the chunk's
+ * tokens are rows of the whole prompt's mask.
  * ---------------------------------------------------------------------- */
 int dsa_masked_mha_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint32_t* key_mask,
                            int words, const int32_t* cu_seqlens_q_host, const int32_t* cu_seqlens_kv_host,
                            int num_req, int T, int H, int d_qk, int d_v, float scale, uint16_t* out, float* lse,
                            dsa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * The same with strided per-head operands and the key's RoPE columns in a
+ * buffer of their own ("[Perf][GLM-5.3-Flash] ...", commit messages: with no
+ * RoPE part the concatenated K is k_nope itself, so no copy; here neither
+ * layout forms the concatenated K).  Key row n of head h is
+ *     [ k[n * k_stride_t + h * k_stride_h + 0 .. d_qk - d_rope - 1],
+ *       k_pe[n * k_pe_stride_t + 0 .. d_rope - 1] ]
+ * and q[t, h, :] = q[t * q_stride_t + h * q_stride_h + ...], v likewise, so
+ * k and v may be views into the per-head kv projection output (e.g. k =
+ * kv[..., :256], v = kv[..., 256:] of a [Nk, H, 512] tensor).
+ *
+ * Strides are in elements, multiples of 8 (16 bytes), with stride_h >= the
+ * columns read and stride_t >= H * stride_h; k_pe_stride_t >= d_rope and a
+ * multiple of 8.  d_rope = 0 (k_pe unused, may be NULL) or 64 (k_pe [Nk, 64]
+ * shared by all heads, required).  d_qk - d_rope must be a multiple of 64.
+ * out is contiguous [T, H, d_v].  Everything else as dsa_masked_mha_prefill.
+ * ---------------------------------------------------------------------- */
+int dsa_masked_mha_prefill_strided(const uint16_t* q, int64_t q_stride_t, int64_t q_stride_h, const uint16_t* k,
+                                   int64_t k_stride_t, int64_t k_stride_h, const uint16_t* k_pe,
+                                   int64_t k_pe_stride_t, const uint16_t* v, int64_t v_stride_t, int64_t v_stride_h,
+                                   const uint32_t* key_mask, int words, const int32_t* cu_seqlens_q_host,
+                                   const int32_t* cu_seqlens_kv_host, int num_req, int T, int H, int d_qk,
+                                   int d_rope, int d_v, float scale, uint16_t* out, float* lse, dsa_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Device error counters of the current device.  Synchronizes `stream`, then

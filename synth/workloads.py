@@ -16,7 +16,10 @@ Shapes and structure follow the workloads the pages measure:
 * the NoPE layout (512 + 0) with a 2176-column index buffer padded with -1
   (same page, GLM comment);
 * masked dense MHA with per-head q/k/v of 192/128 dims and 128 heads
-  ("[2/N][Attention] Enable masked MHA for sparse MLA prefills", Purpose).
+  ("[2/N][Attention] Enable masked MHA for sparse MLA prefills", Purpose),
+  and of 256/256 dims with 64 heads, with or without 64 shared RoPE key
+  columns ("[Perf][GLM-5.3-Flash] ...", commit messages: the GLM-5 and
+  GLM-5.3-Flash NoPE layouts).
 
 Values are N(0, 1) rounded to bfloat16 (round-to-nearest-even), returned as
 raw uint16 bit patterns.
@@ -158,6 +161,8 @@ class Workload:
     G: int = 0                     # grouped-mode tokens per group (0 = per-token only)
     seed: int = 0
     notes: str = ""
+    d_rope: int = 0                # masked: key columns shared by all heads (the RoPE part)
+    split_kv: bool = False         # masked: k and v drawn as one [N, H, d_qk - d_rope + d_v] projection
 
     @property
     def T(self) -> int:
@@ -209,6 +214,20 @@ WORKLOADS = {
         d_qk=192, d_v=128, k=2048, ld=2048, scale=1.0 / math.sqrt(192.0),
         index_gen="locality", G=0, seed=4,
         notes="per-token key mask = locality top-2048 (dense when t < 2048)"),
+    # GLM-5.3-Flash NoPE layout (64 heads, qk 256 + rope 0, v 256): k and v
+    # are the two halves of one per-head projection output.
+    "masked_nope_2x8192": Workload(
+        name="masked_nope_2x8192", mode="masked", q_lens=(8192, 8192), kv_lens=(8192, 8192), H=64,
+        d_qk=256, d_v=256, k=2048, ld=2048, scale=1.0 / 16.0,
+        index_gen="locality", G=0, seed=5, d_rope=0, split_kv=True,
+        notes="per-token key mask = locality top-2048; k = kv[..., :256], v = kv[..., 256:]"),
+    # GLM-5 layout (64 heads, qk 192 + rope 64, v 256): the RoPE key columns
+    # are one [N, 64] block shared by all heads.
+    "masked_glm5_2x8192": Workload(
+        name="masked_glm5_2x8192", mode="masked", q_lens=(8192, 8192), kv_lens=(8192, 8192), H=64,
+        d_qk=256, d_v=256, k=2048, ld=2048, scale=1.0 / 16.0,
+        index_gen="locality", G=0, seed=6, d_rope=64, split_kv=True,
+        notes="per-token key mask = locality top-2048; k = [kv[..., :192], k_pe], v = kv[..., 192:]"),
 }
 
 
@@ -221,7 +240,8 @@ def scaled_down(w: Workload, q_lens, kv_lens, k=None, ld=None, H=None, name=None
         H=w.H if H is None else H, d_qk=w.d_qk, d_v=w.d_v, k=k,
         ld=(k if ld is None else ld), scale=w.scale,
         index_gen=w.index_gen if index_gen is None else index_gen,
-        G=w.G if G is None else G, seed=w.seed if seed is None else seed, notes="scaled")
+        G=w.G if G is None else G, seed=w.seed if seed is None else seed, notes="scaled",
+        d_rope=w.d_rope, split_kv=w.split_kv)
 
 
 def make_indices(w: Workload, rng: np.random.Generator, locality_block: int = 8) -> np.ndarray:
@@ -253,11 +273,13 @@ class SparseInputs:
 class MaskedInputs:
     w: Workload
     q: np.ndarray          # [T, H, d_qk] bf16 bits
-    k: np.ndarray          # [N, H, d_qk] bf16 bits
+    k: np.ndarray          # [N, H, d_qk] bf16 bits (every head's whole key row)
     v: np.ndarray          # [N, H, d_v] bf16 bits
     idx: np.ndarray        # [T, ld] int32 global rows (source of the key mask)
     cu_seqlens_q: np.ndarray
     cu_seqlens_kv: np.ndarray
+    kvp: np.ndarray = None   # split_kv: [N, H, d_qk - d_rope + d_v], k = kvp[..., :d_qk - d_rope], v = the rest
+    k_pe: np.ndarray = None  # d_rope > 0: [N, d_rope], the last d_rope columns of every head's key row
 
 
 def make_sparse_inputs(w: Workload, with_values: bool = True) -> SparseInputs:
@@ -278,10 +300,21 @@ def make_masked_inputs(w: Workload, with_values: bool = True) -> MaskedInputs:
     rng = np.random.default_rng(w.seed)
     idx = make_indices(w, rng)
     vrng = np.random.default_rng([w.seed, 1])
-    if with_values:
+    kvp = k_pe = None
+    if with_values and w.split_kv:
+        dn = w.d_qk - w.d_rope
+        q = normal_bf16(vrng, (w.T, w.H, w.d_qk))
+        kvp = normal_bf16(vrng, (w.N, w.H, dn + w.d_v))
+        k = np.empty((w.N, w.H, w.d_qk), dtype=np.uint16)
+        k[..., :dn] = kvp[..., :dn]
+        if w.d_rope:
+            k_pe = normal_bf16(vrng, (w.N, w.d_rope))
+            k[..., dn:] = k_pe[:, None, :]
+        v = np.ascontiguousarray(kvp[..., dn:])
+    elif with_values:
         q = normal_bf16(vrng, (w.T, w.H, w.d_qk))
         k = normal_bf16(vrng, (w.N, w.H, w.d_qk))
         v = normal_bf16(vrng, (w.N, w.H, w.d_v))
     else:
         q = k = v = None
-    return MaskedInputs(w, q, k, v, idx, w.cu_seqlens_q(), w.cu_seqlens_kv())
+    return MaskedInputs(w, q, k, v, idx, w.cu_seqlens_q(), w.cu_seqlens_kv(), kvp, k_pe)

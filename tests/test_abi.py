@@ -109,6 +109,29 @@ def test_argument_validation_without_gpu(lib):
     for bad in (0.0, -1.0, float("inf"), float("nan")):
         assert lib.dsa_masked_mha_prefill(_vp(16), _vp(16), _vp(16), _vp(16), 4, None, None, 0, 8, 4, 192, 128,
                                           bad, _vp(16), _vp(16), None) == dsa.DSA_ERR_INVALID_ARG
+    # strided masked MHA: geometry, RoPE width, the shared RoPE buffer, strides
+    H = 4
+    sok = dict(q=_vp(16), qt=H * 256, qh=256, k=_vp(16), kt=H * 512, kh=512, pe=None, pet=0, v=_vp(16),
+               vt=H * 512, vh=512, T=8, dqk=256, dr=0, dv=256)
+
+    def mstr(**kw):
+        a = dict(sok, **kw)
+        return lib.dsa_masked_mha_prefill_strided(a["q"], a["qt"], a["qh"], a["k"], a["kt"], a["kh"], a["pe"],
+                                                  a["pet"], a["v"], a["vt"], a["vh"], _vp(16), 4, None, None, 0,
+                                                  a["T"], H, a["dqk"], a["dr"], a["dv"], 0.0625, _vp(16), _vp(16),
+                                                  None)
+    assert mstr(dqk=576, dv=512) == dsa.DSA_ERR_UNSUPPORTED
+    assert mstr(dqk=256, dv=128) == dsa.DSA_ERR_UNSUPPORTED
+    assert mstr(dr=32) == dsa.DSA_ERR_UNSUPPORTED
+    assert mstr(dr=64) == dsa.DSA_ERR_INVALID_ARG                      # RoPE columns without their buffer
+    assert mstr(dr=64, pe=_vp(16), pet=32) == dsa.DSA_ERR_INVALID_ARG   # RoPE row stride below 64
+    assert mstr(dr=64, pe=ctypes.c_void_p(24), pet=64) == dsa.DSA_ERR_INVALID_ARG  # misaligned RoPE buffer
+    assert mstr(kh=516, kt=H * 516) == dsa.DSA_ERR_INVALID_ARG          # head stride not a multiple of 8
+    assert mstr(kh=128, kt=H * 128) == dsa.DSA_ERR_INVALID_ARG          # heads overlap (256 columns read)
+    assert mstr(vt=H * 512 - 8) == dsa.DSA_ERR_INVALID_ARG              # rows overlap
+    assert mstr(qh=248, qt=H * 248) == dsa.DSA_ERR_INVALID_ARG          # q heads overlap
+    assert mstr(q=ctypes.c_void_p(40)) == dsa.DSA_ERR_INVALID_ARG       # misaligned q
+    assert mstr(T=0) == dsa.DSA_OK
     # key mask: one-sided offsets are rejected
     assert lib.dsa_topk_to_key_mask(_vp(16), 8, 4, 4, cu, None, 2, _vp(16), 4, None) == dsa.DSA_ERR_INVALID_ARG
     # local -> physical rows: block size, table width, KV lengths, request offsets

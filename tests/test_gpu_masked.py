@@ -103,3 +103,111 @@ def test_masked_full_size_sampled():
     ro, rl = O.masked_mha_prefill(x.q, x.k, x.v, km, x.cu_seqlens_q, x.cu_seqlens_kv, w.scale, tokens=toks)
     res = O.compare(o[toks], l[toks], ro, rl)
     assert res["ok"], res
+
+
+# ----------------------------------------------------------------------------
+# strided operands and the shared RoPE key columns (the GLM-5 and GLM-5.3-Flash
+# NoPE geometries, d_qk = d_v = 256, and DeepSeek-V3.2's 192/128)
+# ----------------------------------------------------------------------------
+def split_inputs(seed, q_lens, kv_lens, H, k, d_qk, d_rope, d_v, q_pad=0):
+    """idx, q, one per-head projection kvp [Nk, H, d_qk - d_rope + d_v] (k = its first
+    columns, v the rest), the shared RoPE block k_pe [Nk, d_rope], and the whole key rows
+    k [Nk, H, d_qk] and v for the oracle.  q is returned inside a wider [T, H, d_qk + q_pad]
+    buffer when q_pad > 0, so the kernel reads it through a head stride."""
+    rng = np.random.default_rng(seed)
+    cq = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    ck = np.concatenate([[0], np.cumsum(kv_lens)]).astype(np.int32)
+    rows = []
+    for r, (nq, nk) in enumerate(zip(q_lens, kv_lens)):
+        rows.append(locality_topk(rng, np.arange(nk - nq, nk), k, k, kv_offset=int(ck[r])))
+    idx = np.concatenate(rows)
+    T, N, dn = int(cq[-1]), int(ck[-1]), d_qk - d_rope
+    qbuf = normal_bf16(rng, (T, H, d_qk + q_pad))
+    kvp = normal_bf16(rng, (N, H, dn + d_v))
+    k_pe = normal_bf16(rng, (N, d_rope)) if d_rope else None
+    kfull = np.empty((N, H, d_qk), dtype=np.uint16)
+    kfull[..., :dn] = kvp[..., :dn]
+    if d_rope:
+        kfull[..., dn:] = k_pe[:, None, :]
+    return dict(idx=idx, cq=cq, ck=ck, qbuf=qbuf, q=np.ascontiguousarray(qbuf[..., :d_qk]), kvp=kvp, k_pe=k_pe,
+                k=kfull, v=np.ascontiguousarray(kvp[..., dn:]), dn=dn)
+
+
+def run_strided(x, kk, scale, words):
+    """The strided call on device views: k = kvp[..., :dn], v = kvp[..., dn:], q a view of
+    its (possibly wider) buffer, k_pe shared.  Returns key mask bits, out, lse."""
+    import dsa_sparse_mla_prefill_gb300 as dsa
+    d_qk = x["q"].shape[2]
+    km = dsa.dsa_topk_to_key_mask(i32(x["idx"]), kk, words, cu_seqlens_q=x["cq"], cu_seqlens_kv=x["ck"])
+    kvp = bf(x["kvp"])
+    k, v = kvp[..., :x["dn"]], kvp[..., x["dn"]:]
+    assert not k.is_contiguous() and not v.is_contiguous()
+    q = bf(x["qbuf"])[..., :d_qk]
+    k_pe = bf(x["k_pe"]) if x["k_pe"] is not None else None
+    T, H = q.shape[:2]
+    out = torch.full((T, H, v.shape[2]), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((T, H), float("nan"), dtype=torch.float32, device="cuda")
+    dsa.dsa_masked_mha_prefill_strided(q, k, v, km, scale, k_pe=k_pe, cu_seqlens_q=x["cq"],
+                                       cu_seqlens_kv=x["ck"], out=out, lse=lse)
+    torch.cuda.synchronize()
+    st, counts = dsa.dsa_last_device_error()
+    assert st == 0, counts
+    return km, out, lse
+
+
+@pytest.mark.parametrize("d_qk,d_rope,d_v", [(256, 0, 256), (256, 64, 256), (192, 64, 128)])
+@pytest.mark.parametrize("q_lens,kv_lens,H,k,q_pad", [
+    ([150, 200], [150, 200], 3, 64, 0),        # two causal requests, partial query tiles
+    ([97, 130], [400, 130], 2, 96, 8),         # chunked context, q read through a head stride
+    ([300], [300], 2, 300, 0),                 # dense causal
+])
+def test_masked_strided_geometries(d_qk, d_rope, d_v, q_lens, kv_lens, H, k, q_pad):
+    x = split_inputs(d_qk + d_rope + len(q_lens), q_lens, kv_lens, H, k, d_qk, d_rope, d_v, q_pad)
+    words = words_for(kv_lens)
+    scale = 1.0 / np.sqrt(d_qk)
+    km, o, l = run_strided(x, k, scale, words)
+    ref_km = O.topk_to_key_mask(x["idx"], k, x["cq"], x["ck"], words)
+    assert np.array_equal(km.cpu().numpy().view(np.uint32), ref_km)
+    ro, rl = O.masked_mha_prefill(x["q"], x["k"], x["v"], ref_km, x["cq"], x["ck"], scale)
+    res = O.compare(f32(o), l.cpu().numpy().astype(np.float64), ro, rl)
+    assert res["ok"], res
+
+
+@pytest.mark.parametrize("d_qk,d_rope,d_v", [(256, 0, 256), (256, 64, 256), (192, 64, 128)])
+def test_masked_strided_equals_contiguous(d_qk, d_rope, d_v):
+    """Reading k and v through strides (and the RoPE columns from their own block) gives
+    bit for bit what the contiguous call gives on the concatenated copies."""
+    import dsa_sparse_mla_prefill_gb300 as dsa
+    x = split_inputs(11, [260, 140], [300, 140], 3, 80, d_qk, d_rope, d_v)
+    words = words_for([300, 140])
+    km, o1, l1 = run_strided(x, 80, 0.07, words)
+    o2, l2 = dsa.dsa_masked_mha_prefill(bf(x["q"]), bf(x["k"]), bf(x["v"]), km, 0.07, cu_seqlens_q=x["cq"],
+                                        cu_seqlens_kv=x["ck"])
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("name", ["masked_nope_2x8192", "masked_glm5_2x8192"])
+def test_masked_256_full_size_sampled(name):
+    import dsa_sparse_mla_prefill_gb300 as dsa
+    w = WORKLOADS[name]
+    x = make_masked_inputs(w)
+    words = words_for(w.kv_lens)
+    km = dsa.dsa_topk_to_key_mask(i32(x.idx), w.k, words, cu_seqlens_q=x.cu_seqlens_q,
+                                  cu_seqlens_kv=x.cu_seqlens_kv)
+    dn = w.d_qk - w.d_rope
+    kvp = bf(x.kvp)
+    k_pe = bf(x.k_pe) if x.k_pe is not None else None
+    o, l = dsa.dsa_masked_mha_prefill_strided(bf(x.q), kvp[..., :dn], kvp[..., dn:], km, w.scale, k_pe=k_pe,
+                                              cu_seqlens_q=x.cu_seqlens_q, cu_seqlens_kv=x.cu_seqlens_kv)
+    torch.cuda.synchronize()
+    st, counts = dsa.dsa_last_device_error()
+    assert st == 0, counts
+    of, lf = f32(o), l.cpu().numpy().astype(np.float64)
+    assert np.isfinite(of).all() and np.isfinite(lf).all()
+    rng = np.random.default_rng(6)
+    toks = stratified_tokens(w.T, 16, rng, must=[0, 127, 128, 2047, 2048, 8191, 8192, 8193, 16383])
+    kmh = km.cpu().numpy().view(np.uint32)
+    ro, rl = O.masked_mha_prefill(x.q, x.k, x.v, kmh, x.cu_seqlens_q, x.cu_seqlens_kv, w.scale, tokens=toks)
+    res = O.compare(of[toks], lf[toks], ro, rl)
+    assert res["ok"], res
