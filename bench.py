@@ -599,6 +599,80 @@ def traced_launch(fn, cap, out_path=None):
     return out
 
 
+def measure_forms(L, dev, stream, flush, steps, warmup):
+    """The three forms on one causal request of L tokens, DeepSeek-V3.2 at TP4
+    (H = 32, top-2048; latent 576/512 for per-token and grouped with G = 4,
+    per-head 192/128 for masked, the same indices): median ms of each kernel,
+    the union rows and the device error counts."""
+    import torch
+    import dsa_sparse_mla_prefill_gb300 as dsa
+    from synth import Workload, make_masked_inputs, make_sparse_inputs
+    common = dict(q_lens=(L,), kv_lens=(L,), H=32, k=2048, ld=2048, scale=1.0 / math.sqrt(192.0),
+                  index_gen="locality", seed=7)
+    ws = Workload(name=f"causal_{L}", mode="sparse", d_qk=576, d_v=512, G=4, **common)
+    wm = Workload(name=f"causal_{L}", mode="masked", d_qk=192, d_v=128, **common)
+    x = make_sparse_inputs(ws)
+    q, kv = to_dev(x.q, dev), to_dev(x.kv, dev)
+    idx = torch.from_numpy(x.idx).to(dev)
+    med = lambda fn: statistics.median(timed_steps(fn, steps, warmup, stream, flush))
+    res = {"L": L, "H": 32, "k": 2048}
+    o = torch.empty((L, 32, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((L, 32), dtype=torch.float32, device=dev)
+    res["per_token_ms"] = med(lambda: dsa.dsa_sparse_prefill(q, kv, idx, ws.k, ws.scale, out=o, lse=lse))
+    upad = dsa.dsa_union_pad(4, ws.k, 128)
+    ng = dsa.dsa_num_groups(x.cu_seqlens_q, L, 4)
+    u = torch.empty((ng, upad), dtype=torch.int32, device=dev)
+    ul = torch.empty((ng,), dtype=torch.int32, device=dev)
+    m = torch.empty((ng, upad), dtype=torch.uint8, device=dev)
+    res["union_ms"] = med(lambda: dsa.dsa_union_build(idx, ws.k, 4, L, cu_seqlens_q=x.cu_seqlens_q,
+                                                      union_pad=upad, out=(u, ul, m)))
+    res["union_rows"] = int(ul.sum().item())
+    res["grouped_ms"] = med(lambda: dsa.dsa_grouped_prefill(q, kv, u, ul, m, 4, ws.scale,
+                                                            cu_seqlens_q=x.cu_seqlens_q, out=o, lse=lse))
+    del q, kv, o, u, ul, m
+    torch.cuda.empty_cache()
+    xm = make_masked_inputs(wm)
+    assert np.array_equal(xm.idx, x.idx)
+    words = ((L + 31) // 32 + 3) // 4 * 4
+    km = torch.empty((L, words), dtype=torch.int32, device=dev)
+    res["key_mask_ms"] = med(lambda: dsa.dsa_topk_to_key_mask(idx, wm.k, words, cu_seqlens_q=xm.cu_seqlens_q,
+                                                              cu_seqlens_kv=xm.cu_seqlens_kv, out=km))
+    qm, mk, mv = to_dev(xm.q, dev), to_dev(xm.k, dev), to_dev(xm.v, dev)
+    om = torch.empty((L, 32, 128), dtype=torch.bfloat16, device=dev)
+    res["masked_ms"] = med(lambda: dsa.dsa_masked_mha_prefill(qm, mk, mv, km, wm.scale, cu_seqlens_q=xm.cu_seqlens_q,
+                                                              cu_seqlens_kv=xm.cu_seqlens_kv, out=om, lse=lse))
+    st, counts = dsa.dsa_last_device_error()
+    res["device_errors"] = counts
+    del qm, mk, mv, om, km, idx
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_form_sweep(args):
+    """measure_forms at each prompt length of --sweep-forms, one JSON line
+    each, with the form model's prediction beside the measurement: the
+    crossovers the form dispatcher is calibrated on."""
+    import torch
+    import dsa_sparse_mla_prefill_gb300 as dsa
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    flush_buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = lambda: flush_buf.zero_()
+    steps = max(3, min(args.steps, 10))
+    for L in [int(v) for v in args.sweep_forms.split(",")]:
+        res = measure_forms(L, dev, stream, flush, steps, args.warmup)
+        measured = {"per_token": res["per_token_ms"], "grouped": res["union_ms"] + res["grouped_ms"],
+                    "masked": res["key_mask_ms"] + res["masked_ms"]}
+        form, pred, _ = dsa.dsa_choose_form([L], [L], 32, 2048, 576, (192, 128), union_rows=res["union_rows"])
+        res["measured_best"] = min(measured, key=measured.get)
+        res["model_choice"] = form
+        res["model_ms"] = pred
+        print(json.dumps(res), flush=True)
+        if any(res["device_errors"][1:3]):
+            raise SystemExit(1)
+
+
 def run_profile_case(args):
     """A small, bounded case of one kernel for ncu captures: inputs larger than
     the L2 but a few hundred MB at most; runs warmup + steps launches."""
@@ -668,6 +742,8 @@ def main():
     ap.add_argument("--profile-tokens", type=int, default=2048)
     ap.add_argument("--profile-workload", default=None,
                     help="profile mode: base workload, e.g. nope_2x8192 or masked_nope_2x8192")
+    ap.add_argument("--sweep-forms", default=None,
+                    help="comma list of prompt lengths: time per-token, grouped and masked on one causal request each")
     ap.add_argument("--trace", type=int, default=0, help="profile mode: record a per-tile timeline of N tiles")
     ap.add_argument("--trace-out", default=None, help="profile mode: save the raw timeline (.npy)")
     args = ap.parse_args()
@@ -675,6 +751,8 @@ def main():
         args.warmup = 3
     if args.profile:
         run_profile_case(args)
+    elif args.sweep_forms:
+        run_form_sweep(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

@@ -14,6 +14,7 @@ Forms (see the header for the exact contracts):
   dsa_topk_to_key_mask    packed per-token key mask from the top-k rows
   dsa_masked_mha_prefill  masked dense MHA with per-head q/k/v
   dsa_masked_mha_prefill_strided  the same on strided views, RoPE key columns shared
+  dsa_choose_form         predicted time of each form and the fastest (host only)
 """
 from __future__ import annotations
 
@@ -43,6 +44,27 @@ _F = ctypes.c_float
 _I32P = ctypes.POINTER(ctypes.c_int32)
 _L = ctypes.c_int64
 
+FORMS = ("per_token", "grouped", "masked")
+
+
+class FormCalibration(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_double) for n in (
+        "hbm_gbs", "bf16_tflops", "per_token_frac", "per_token_ms0", "union_frac", "union_ms0",
+        "grouped_frac_576", "grouped_frac_512", "grouped_ms0", "masked_frac_192", "masked_frac_256", "masked_ms0",
+        "key_mask_frac", "key_mask_ms0", "union_growth")]
+
+
+class FormQuery(ctypes.Structure):
+    _fields_ = [("num_req", ctypes.c_int), ("q_lens", ctypes.POINTER(ctypes.c_int32)),
+                ("kv_lens", ctypes.POINTER(ctypes.c_int32)), ("H", ctypes.c_int), ("k", ctypes.c_int),
+                ("d_qk", ctypes.c_int), ("masked_d_qk", ctypes.c_int), ("masked_d_v", ctypes.c_int),
+                ("union_rows", ctypes.c_double)]
+
+
+class FormEstimate(ctypes.Structure):
+    _fields_ = [("ms", ctypes.c_double * 3), ("form", ctypes.c_int), ("union_rows", ctypes.c_double)]
+
+
 _SIGNATURES = {
     "dsa_status_string": (ctypes.c_char_p, [_I]),
     "dsa_version": (_I, []),
@@ -58,6 +80,9 @@ _SIGNATURES = {
                                     _VP]),
     "dsa_masked_mha_prefill_strided": (_I, [_VP, _L, _L, _VP, _L, _L, _VP, _L, _VP, _L, _L, _VP, _I, _I32P, _I32P,
                                             _I, _I, _I, _I, _I, _I, _F, _VP, _VP, _VP]),
+    "dsa_form_calibration_default": (_I, [ctypes.POINTER(FormCalibration)]),
+    "dsa_choose_form": (_I, [ctypes.POINTER(FormQuery), ctypes.POINTER(FormCalibration),
+                             ctypes.POINTER(FormEstimate)]),
     "dsa_last_device_error": (_I, [_VP, ctypes.POINTER(ctypes.c_uint32)]),
     "dsa_debug_trace": (_I, [_VP, _I]),
 }
@@ -305,6 +330,33 @@ def dsa_masked_mha_prefill_strided(q, k, v, key_mask, scale: float, k_pe=None, c
         d_qk, d_rope, d_v, float(scale), out.data_ptr(), lse.data_ptr(), _stream(stream, q.device)),
         "dsa_masked_mha_prefill_strided")
     return out, lse
+
+
+def dsa_form_calibration_default() -> FormCalibration:
+    """The GB300 calibration of the form model (fields as in include/dsa.h)."""
+    c = FormCalibration()
+    _check(lib().dsa_form_calibration_default(ctypes.byref(c)), "dsa_form_calibration_default")
+    return c
+
+
+def dsa_choose_form(q_lens, kv_lens, H: int, k: int, d_qk: int = 576, masked_dims=None, union_rows=None,
+                    calibration: FormCalibration = None):
+    """Predicted ms of each form and the fastest applicable one (host only).  q_lens / kv_lens
+    per request (queries are the last q_len positions); masked_dims = (d_qk, d_v) of the per-head
+    tensors when the masked form can run; union_rows = sum of union_len after dsa_union_build
+    (else estimated).  Returns (form name, {form name: ms or None}, union rows used)."""
+    ql = np.ascontiguousarray(q_lens, dtype=np.int32)
+    kl = np.ascontiguousarray(kv_lens, dtype=np.int32)
+    if ql.shape != kl.shape or ql.ndim != 1:
+        raise ValueError("q_lens and kv_lens must be 1-D of the same length")
+    md = (0, 0) if masked_dims is None else tuple(int(x) for x in masked_dims)
+    q = FormQuery(len(ql), ql.ctypes.data_as(_I32P), kl.ctypes.data_as(_I32P), int(H), int(k), int(d_qk), md[0],
+                  md[1], -1.0 if union_rows is None else float(union_rows))
+    e = FormEstimate()
+    _check(lib().dsa_choose_form(ctypes.byref(q), None if calibration is None else ctypes.byref(calibration),
+                                 ctypes.byref(e)), "dsa_choose_form")
+    ms = {name: (e.ms[i] if e.ms[i] >= 0 else None) for i, name in enumerate(FORMS)}
+    return FORMS[e.form], ms, e.union_rows
 
 
 def dsa_last_device_error(stream=None, device=None):

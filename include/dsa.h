@@ -250,6 +250,67 @@ int dsa_masked_mha_prefill_strided(const uint16_t* q, int64_t q_stride_t, int64_
 int dsa_last_device_error(dsa_stream_t stream, uint32_t* counts);
 
 /* ------------------------------------------------------------------------
+ * Form choice (host only, no GPU call).  "[Perf][GLM-5.3-Flash] ...", commit
+ * messages: prompts within the top-k budget run dense MHA, longer ones masked
+ * MHA up to a length threshold (36k tokens at TP4, 64k at TP8) and the
+ * per-token kernel beyond; "[Perf][DSA] Grouped sparse prefill ...", How:
+ * the grouped form may take everything longer than the top-k budget.  Here
+ * the three exact forms are compared by predicted time, each form's work (its
+ * dominant kernel's roofline quantity) over the fraction of the measured peak
+ * that form reaches, plus fixed costs:
+ *   per-token  sum_t n_t * 2 d_qk bytes gathered (n_t = min(k, position + 1))
+ *              + q, out, indices, lse bytes, at per_token_frac of HBM;
+ *   grouped    2 * 128 * U * (d_qk + 512) FLOPs (U = sum of union rows) at
+ *              grouped_frac of bf16, + the union build (T * k * 4 bytes at
+ *              union_frac of HBM); only where 128 % H == 0 and 128 / H <= 8;
+ *   masked     2 * H * sum_r (q_r (q_r + 1) / 2 + q_r * ctx_r) * (d_qk + d_v)
+ *              FLOPs at masked_frac of bf16, + the key mask; only for the
+ *              masked geometries (192, 128) and (256, 256), i.e. where the
+ *              caller has per-head k and v.
+ * U comes from the caller (sum of union_len after dsa_union_build) or is
+ * estimated per group as min(last position + 1, n_last (1 + union_growth)).
+ * ---------------------------------------------------------------------- */
+enum dsa_form { DSA_FORM_PER_TOKEN = 0, DSA_FORM_GROUPED = 1, DSA_FORM_MASKED = 2 };
+
+typedef struct dsa_form_calibration {
+  double hbm_gbs, bf16_tflops;               /* measured peaks */
+  double per_token_frac, per_token_ms0;      /* of HBM; fixed ms */
+  double union_frac, union_ms0;              /* union build: of HBM on index bytes; fixed ms */
+  double grouped_frac_576, grouped_frac_512; /* of bf16, by latent key width */
+  double grouped_ms0;
+  double masked_frac_192, masked_frac_256;   /* of bf16, by per-head d_qk */
+  double masked_ms0;
+  double key_mask_frac, key_mask_ms0;        /* key mask: of HBM on index + mask bytes */
+  double union_growth;                       /* union of a group / one token's rows - 1 */
+} dsa_form_calibration;
+
+typedef struct dsa_form_query {
+  int num_req;
+  const int32_t* q_lens;     /* HOST [num_req] query tokens (the last q_len positions) */
+  const int32_t* kv_lens;    /* HOST [num_req] KV positions, >= q_len */
+  int H;                     /* query heads on this GPU */
+  int k;                     /* top-k per token */
+  int d_qk;                  /* latent key width of the sparse forms: 576 or 512 */
+  int masked_d_qk;           /* per-head geometry when the masked form can run, else 0 */
+  int masked_d_v;
+  double union_rows;         /* sum of union rows if known, else < 0 (estimated) */
+} dsa_form_query;
+
+typedef struct dsa_form_estimate {
+  double ms[3];              /* predicted ms by dsa_form; < 0 = not applicable */
+  int form;                  /* the fastest applicable form */
+  double union_rows;         /* union rows used for the grouped estimate */
+} dsa_form_estimate;
+
+/* The calibration measured on GB300 (defaults of dsa_choose_form). */
+int dsa_form_calibration_default(dsa_form_calibration* calib);
+
+/* Fills *out; calib NULL = the GB300 default.  DSA_ERR_INVALID_ARG on null
+ * pointers, num_req < 1, H < 1, k < 1, kv_len < q_len or a non-positive
+ * fraction; DSA_ERR_UNSUPPORTED for d_qk other than 512 / 576. */
+int dsa_choose_form(const dsa_form_query* query, const dsa_form_calibration* calib, dsa_form_estimate* out);
+
+/* ------------------------------------------------------------------------
  * Diagnostic timeline (no counterpart on the pages; a profiling aid).  While
  * a buffer is set, the first two CTAs of every per-token, grouped and masked
  * launch write clock64() stamps of up to 8 pipeline events for each of their
