@@ -9,6 +9,7 @@ there is no CPU fallback: without the built library every call raises.
 
 Forms (see the header for the exact contracts):
   dsa_sparse_prefill      per-token sparse attention over each token's top-k rows
+  dsa_sparse_prefill_host the same from and to host memory, copies overlapped with the kernel
   dsa_union_build         sorted union per group + head-group membership mask
   dsa_grouped_prefill     G = 128/H tokens as 128 pseudo-heads over the union
   dsa_topk_to_key_mask    packed per-token key mask from the top-k rows
@@ -80,6 +81,9 @@ _SIGNATURES = {
                                     _VP]),
     "dsa_masked_mha_prefill_strided": (_I, [_VP, _L, _L, _VP, _L, _L, _VP, _L, _VP, _L, _L, _VP, _I, _I32P, _I32P,
                                             _I, _I, _I, _I, _I, _I, _F, _VP, _VP, _VP]),
+    "dsa_sparse_prefill_host_workspace": (_L, [_I, _I, _I, _I, _I, _I, _I, _I, _I]),
+    "dsa_sparse_prefill_host": (_I, [_VP, _VP, _I, _I, _I, _VP, _I, _I, _I, _I, _I, _I, _F, _VP, _VP, _VP, _L, _I,
+                                     _VP]),
     "dsa_form_calibration_default": (_I, [ctypes.POINTER(FormCalibration)]),
     "dsa_choose_form": (_I, [ctypes.POINTER(FormQuery), ctypes.POINTER(FormCalibration),
                              ctypes.POINTER(FormEstimate)]),
@@ -205,6 +209,51 @@ def dsa_sparse_prefill(q, kv, idx, k: int, scale: float, d_v: int = 512, out=Non
     _check(lib().dsa_sparse_prefill(q.data_ptr(), kv.data_ptr(), N, ld_kv, idx.data_ptr(), T, H, d_qk, d_v, k,
                                     idx.shape[1], float(scale), out.data_ptr(), lse.data_ptr(),
                                     _stream(stream, q.device)), "dsa_sparse_prefill")
+    return out, lse
+
+
+def _host_tensor(t, dtype, name, ndim):
+    import torch
+    if not isinstance(t, torch.Tensor) or t.dtype != dtype or t.dim() != ndim:
+        raise TypeError(f"{name} must be a {ndim}-D {dtype} tensor")
+    if t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous host tensor (pinned for overlapped copies)")
+    return t
+
+
+def dsa_sparse_prefill_host_workspace(T: int, N: int, ld_kv: int, H: int, d_qk: int, ld: int, chunk_tokens: int,
+                                      kv_on_host: bool = True, d_v: int = 512) -> int:
+    """Device workspace bytes dsa_sparse_prefill_host needs for these shapes."""
+    n = lib().dsa_sparse_prefill_host_workspace(T, N, ld_kv, H, d_qk, d_v, ld, chunk_tokens, int(bool(kv_on_host)))
+    if n < 0:
+        raise DSAError(DSA_ERR_INVALID_ARG, "dsa_sparse_prefill_host_workspace")
+    return int(n)
+
+
+def dsa_sparse_prefill_host(q, kv, idx, k: int, scale: float, out, lse, workspace, chunk_tokens: int = 2048,
+                            stream=None):
+    """Per-token sparse prefill from and to host memory: q [T, H, d_qk] bf16, idx [T, ld] int32,
+    out [T, H, 512] bf16 and lse [T, H] fp32 are host tensors (pinned, for the copies to overlap
+    the kernel), kv [N, ld_kv] bf16 a host or CUDA tensor, workspace a CUDA uint8 tensor of
+    dsa_sparse_prefill_host_workspace bytes.  Asynchronous on `stream` (synchronize before
+    reading out and lse)."""
+    import torch
+    _host_tensor(q, torch.bfloat16, "q", 3)
+    _host_tensor(idx, torch.int32, "idx", 2)
+    _host_tensor(out, torch.bfloat16, "out", 3)
+    _host_tensor(lse, torch.float32, "lse", 2)
+    if kv.dtype != torch.bfloat16 or kv.dim() != 2 or not kv.is_contiguous():
+        raise TypeError("kv must be a contiguous 2-D bf16 tensor")
+    _need(workspace, torch.uint8, "workspace", 1)
+    T, H, d_qk = q.shape
+    N, ld_kv = kv.shape
+    if idx.shape[0] != T or out.shape[0] != T or lse.shape != (T, H):
+        raise ValueError("q, idx, out and lse must cover the same tokens")
+    _check(lib().dsa_sparse_prefill_host(q.data_ptr(), kv.data_ptr(), 0 if kv.is_cuda else 1, N, ld_kv,
+                                         idx.data_ptr(), T, H, d_qk, out.shape[2], k, idx.shape[1], float(scale),
+                                         out.data_ptr(), lse.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                                         int(chunk_tokens), _stream(stream, workspace.device)),
+           "dsa_sparse_prefill_host")
     return out, lse
 
 

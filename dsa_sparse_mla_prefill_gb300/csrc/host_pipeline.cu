@@ -1,0 +1,153 @@
+// Per-token sparse prefill from and to host memory, with the copies
+// overlapped with the attention (host code only).
+//
+// The tokens go through in chunks; three internal streams per device carry
+// the host -> device copies of a chunk's q and indices, the per-token kernel
+// of the chunk, and the device -> host copies of its out and lse, so that
+// chunk i+1 arrives and chunk i-1 leaves while chunk i is computed.  A ring
+// of NB device buffer sets in the caller's workspace holds the chunks in
+// flight; events order each buffer's reuse (the copy into set b waits for the
+// kernel that last read it, the kernel for the copy that last drained it).
+// The caller's stream is joined at both ends: the copies start after the work
+// queued on it so far, and work queued on it after the call starts once the
+// last chunk is back in host memory.
+#include <cstdint>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "../../include/dsa.h"
+
+namespace {
+
+constexpr int NB = 3;          // buffer sets in flight
+constexpr int kMaxDev = 64;
+constexpr int64_t kAlign = 256;
+
+struct Pipe {
+  bool init = false;
+  cudaStream_t h2d = nullptr, cmp = nullptr, d2h = nullptr;
+  cudaEvent_t entry = nullptr, kv_in = nullptr, exit = nullptr;
+  cudaEvent_t in[NB] = {}, done[NB] = {}, out[NB] = {};
+};
+Pipe g_pipe[kMaxDev];
+
+bool pipe_of(Pipe** p) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return false;
+  Pipe& s = g_pipe[dev];
+  if (!s.init) {
+    const unsigned ef = cudaEventDisableTiming;
+    if (cudaStreamCreateWithFlags(&s.h2d, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&s.cmp, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&s.d2h, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&s.entry, ef) != cudaSuccess || cudaEventCreateWithFlags(&s.kv_in, ef) != cudaSuccess ||
+        cudaEventCreateWithFlags(&s.exit, ef) != cudaSuccess)
+      return false;
+    for (int b = 0; b < NB; ++b)
+      if (cudaEventCreateWithFlags(&s.in[b], ef) != cudaSuccess ||
+          cudaEventCreateWithFlags(&s.done[b], ef) != cudaSuccess ||
+          cudaEventCreateWithFlags(&s.out[b], ef) != cudaSuccess)
+        return false;
+    s.init = true;
+  }
+  *p = &s;
+  return true;
+}
+
+int64_t up(int64_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+// Byte sizes of one buffer set and of the whole workspace.
+struct Layout {
+  int64_t q, idx, out, lse, set, kv, total;
+};
+
+Layout layout(int chunk, int N, int ld_kv, int H, int d_qk, int d_v, int ld, bool kv_host) {
+  Layout l;
+  l.q = up((int64_t)chunk * H * d_qk * 2);
+  l.idx = up((int64_t)chunk * ld * 4);
+  l.out = up((int64_t)chunk * H * d_v * 2);
+  l.lse = up((int64_t)chunk * H * 4);
+  l.set = l.q + l.idx + l.out + l.lse;
+  l.kv = kv_host ? up((int64_t)N * ld_kv * 2) : 0;
+  l.total = l.kv + NB * l.set;
+  return l;
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t dsa_sparse_prefill_host_workspace(int T, int N, int ld_kv, int H, int d_qk, int d_v, int ld,
+                                          int chunk_tokens, int kv_on_host) {
+  if (T < 0 || N < 0 || ld_kv < 1 || H < 1 || d_qk < 1 || d_v < 1 || ld < 1 || chunk_tokens < 1) return -1;
+  const int chunk = chunk_tokens < T ? chunk_tokens : (T > 0 ? T : 1);
+  return layout(chunk, N, ld_kv, H, d_qk, d_v, ld, kv_on_host != 0).total;
+}
+
+int dsa_sparse_prefill_host(const uint16_t* q, const uint16_t* kv, int kv_on_host, int N, int ld_kv,
+                            const int32_t* idx, int T, int H, int d_qk, int d_v, int k, int ld, float scale,
+                            uint16_t* out, float* lse, void* workspace, int64_t workspace_bytes, int chunk_tokens,
+                            dsa_stream_t stream) {
+  if (T < 0 || N < 0 || k < 0 || ld < k || ld_kv < d_qk || chunk_tokens < 1) return DSA_ERR_INVALID_ARG;
+  if (!(H == 16 || H == 32) || !(d_qk == 576 || d_qk == 512) || d_v != 512 || k > 2048) return DSA_ERR_UNSUPPORTED;
+  if ((ld_kv & 7) != 0) return DSA_ERR_INVALID_ARG;
+  if (T == 0) return DSA_OK;
+  if (!q || (!kv && N > 0) || !idx || !out || !lse || !workspace) return DSA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return DSA_ERR_INVALID_ARG;
+  const int chunk = chunk_tokens < T ? chunk_tokens : T;
+  const bool kv_host = kv_on_host != 0 && N > 0;
+  const Layout L = layout(chunk, N, ld_kv, H, d_qk, d_v, ld, kv_host);
+  if (workspace_bytes < L.total) return DSA_ERR_INVALID_ARG;
+  Pipe* p;
+  if (!pipe_of(&p)) return DSA_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  // start after the work already queued on the caller's stream
+  if (!ok(cudaEventRecord(p->entry, (cudaStream_t)stream)) || !ok(cudaStreamWaitEvent(p->h2d, p->entry, 0)) ||
+      !ok(cudaStreamWaitEvent(p->cmp, p->entry, 0)) || !ok(cudaStreamWaitEvent(p->d2h, p->entry, 0)))
+    return DSA_ERR_CUDA;
+  const uint16_t* kv_dev = kv;
+  if (kv_host) {
+    if (!ok(cudaMemcpyAsync(ws, kv, (size_t)N * ld_kv * 2, cudaMemcpyHostToDevice, p->h2d)) ||
+        !ok(cudaEventRecord(p->kv_in, p->h2d)) || !ok(cudaStreamWaitEvent(p->cmp, p->kv_in, 0)))
+      return DSA_ERR_CUDA;
+    kv_dev = reinterpret_cast<const uint16_t*>(ws);
+  }
+  const int nchunks = (T + chunk - 1) / chunk;
+  for (int i = 0; i < nchunks; ++i) {
+    const int b = i % NB;
+    const int64_t t0 = (int64_t)i * chunk;
+    const int n = (int)((T - t0) < chunk ? (T - t0) : chunk);
+    uint8_t* set = ws + L.kv + b * L.set;
+    uint16_t* dq = reinterpret_cast<uint16_t*>(set);
+    int32_t* didx = reinterpret_cast<int32_t*>(set + L.q);
+    uint16_t* dout = reinterpret_cast<uint16_t*>(set + L.q + L.idx);
+    float* dlse = reinterpret_cast<float*>(set + L.q + L.idx + L.out);
+    // inputs of chunk i, once the kernel of chunk i - NB has read set b
+    if (i >= NB && !ok(cudaStreamWaitEvent(p->h2d, p->done[b], 0))) return DSA_ERR_CUDA;
+    if (!ok(cudaMemcpyAsync(dq, q + t0 * H * d_qk, (size_t)n * H * d_qk * 2, cudaMemcpyHostToDevice, p->h2d)) ||
+        !ok(cudaMemcpyAsync(didx, idx + t0 * ld, (size_t)n * ld * 4, cudaMemcpyHostToDevice, p->h2d)) ||
+        !ok(cudaEventRecord(p->in[b], p->h2d)))
+      return DSA_ERR_CUDA;
+    // the kernel, once its inputs are in and set b's previous outputs left
+    if (!ok(cudaStreamWaitEvent(p->cmp, p->in[b], 0)) || (i >= NB && !ok(cudaStreamWaitEvent(p->cmp, p->out[b], 0))))
+      return DSA_ERR_CUDA;
+    const int st = dsa_sparse_prefill(dq, kv_dev, N, ld_kv, didx, n, H, d_qk, d_v, k, ld, scale, dout, dlse,
+                                      (dsa_stream_t)p->cmp);
+    if (st != DSA_OK) return st;
+    if (!ok(cudaEventRecord(p->done[b], p->cmp))) return DSA_ERR_CUDA;
+    // outputs of chunk i back to the host
+    if (!ok(cudaStreamWaitEvent(p->d2h, p->done[b], 0)) ||
+        !ok(cudaMemcpyAsync(out + t0 * H * d_v, dout, (size_t)n * H * d_v * 2, cudaMemcpyDeviceToHost, p->d2h)) ||
+        !ok(cudaMemcpyAsync(lse + t0 * H, dlse, (size_t)n * H * 4, cudaMemcpyDeviceToHost, p->d2h)) ||
+        !ok(cudaEventRecord(p->out[b], p->d2h)))
+      return DSA_ERR_CUDA;
+  }
+  // the caller's stream continues once the last outputs are in host memory
+  if (!ok(cudaEventRecord(p->exit, p->d2h)) || !ok(cudaStreamWaitEvent((cudaStream_t)stream, p->exit, 0)))
+    return DSA_ERR_CUDA;
+  return DSA_OK;
+}
+
+}  // extern "C"

@@ -250,6 +250,37 @@ int dsa_masked_mha_prefill_strided(const uint16_t* q, int64_t q_stride_t, int64_
 int dsa_last_device_error(dsa_stream_t stream, uint32_t* counts);
 
 /* ------------------------------------------------------------------------
+ * dsa_sparse_prefill from and to HOST memory, with the copies overlapped
+ * with the attention (the end-to-end call: inputs that live on the host,
+ * results wanted there).  The tokens go through in chunks of chunk_tokens;
+ * three internal streams of the library carry the host -> device copies of
+ * a chunk's q and indices, the per-token kernel of the chunk, and the device
+ * -> host copies of its out and lse, so chunk i+1 arrives and chunk i-1
+ * leaves while chunk i is computed (3 chunks in flight).
+ *
+ * q, idx, out, lse: HOST pointers, laid out as for dsa_sparse_prefill;
+ *   page-locked (pinned) memory is needed for the copies to overlap.
+ * kv: HOST (kv_on_host = 1, copied once per call) or DEVICE (0) [N, ld_kv].
+ * workspace: DEVICE scratch, 256-byte aligned, of at least
+ *   dsa_sparse_prefill_host_workspace(...) bytes (same arguments); the
+ *   library allocates nothing.  Calls that share a workspace must be
+ *   ordered on one stream.
+ * stream: the copies start after the work queued on it before the call, and
+ *   work queued on it after the call waits for the last outputs to be back
+ *   in host memory (synchronize the stream before reading out and lse).
+ * Shapes and errors as dsa_sparse_prefill; DSA_ERR_INVALID_ARG also for
+ * chunk_tokens < 1 or a workspace that is too small or misaligned.  A CUDA
+ * error part way returns DSA_ERR_CUDA with earlier chunks already queued.
+ * ---------------------------------------------------------------------- */
+int64_t dsa_sparse_prefill_host_workspace(int T, int N, int ld_kv, int H, int d_qk, int d_v, int ld,
+                                          int chunk_tokens, int kv_on_host);
+
+int dsa_sparse_prefill_host(const uint16_t* q, const uint16_t* kv, int kv_on_host, int N, int ld_kv,
+                            const int32_t* idx, int T, int H, int d_qk, int d_v, int k, int ld, float scale,
+                            uint16_t* out, float* lse, void* workspace, int64_t workspace_bytes, int chunk_tokens,
+                            dsa_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Form choice (host only, no GPU call).  "[Perf][GLM-5.3-Flash] ...", commit
  * messages: prompts within the top-k budget run dense MHA, longer ones masked
  * MHA up to a length threshold (36k tokens at TP4, 64k at TP8) and the

@@ -132,6 +132,21 @@ def test_argument_validation_without_gpu(lib):
     assert mstr(qh=248, qt=H * 248) == dsa.DSA_ERR_INVALID_ARG          # q heads overlap
     assert mstr(q=ctypes.c_void_p(40)) == dsa.DSA_ERR_INVALID_ARG       # misaligned q
     assert mstr(T=0) == dsa.DSA_OK
+    # host-memory per-token call: workspace size, chunking, alignment, shapes
+    ws = lib.dsa_sparse_prefill_host_workspace(1000, 1200, 576, 16, 576, 512, 64, 300, 1)
+    assert ws >= 1200 * 576 * 2 + 3 * 300 * (16 * 576 * 2 + 64 * 4 + 16 * 512 * 2 + 16 * 4)
+    assert lib.dsa_sparse_prefill_host_workspace(1000, 1200, 576, 16, 576, 512, 64, 0, 1) == -1
+
+    def hostcall(T=1000, H=16, ws_ptr=256, ws_bytes=ws, chunk=300, kv=_vp(16)):
+        return lib.dsa_sparse_prefill_host(_vp(16), kv, 1, 1200, 576, _vp(16), T, H, 576, 512, 64, 64, 0.1,
+                                           _vp(16), _vp(16), ctypes.c_void_p(ws_ptr), ws_bytes, chunk, None)
+    assert hostcall(ws_bytes=ws - 1) == dsa.DSA_ERR_INVALID_ARG
+    assert hostcall(chunk=0) == dsa.DSA_ERR_INVALID_ARG
+    assert hostcall(ws_ptr=128) == dsa.DSA_ERR_INVALID_ARG
+    assert hostcall(ws_ptr=0) == dsa.DSA_ERR_INVALID_ARG
+    assert hostcall(kv=None) == dsa.DSA_ERR_INVALID_ARG
+    assert hostcall(H=24) == dsa.DSA_ERR_UNSUPPORTED
+    assert hostcall(T=0) == dsa.DSA_OK
     # key mask: one-sided offsets are rejected
     assert lib.dsa_topk_to_key_mask(_vp(16), 8, 4, 4, cu, None, 2, _vp(16), 4, None) == dsa.DSA_ERR_INVALID_ARG
     # local -> physical rows: block size, table width, KV lengths, request offsets

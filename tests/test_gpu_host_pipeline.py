@@ -1,0 +1,75 @@
+"""dsa_sparse_prefill_host (host buffers, copies overlapped with the kernel in
+chunks) against the device call on the same inputs: the same kernel runs on
+every token, so out and lse must be bit for bit equal, for ragged chunks, more
+chunks than buffer sets, kv on the host or on the device, and two calls in a
+row through one workspace.  The device call itself is checked against the
+oracle in test_gpu_sparse.py."""
+import numpy as np
+import pytest
+
+from gpu_util import bf, i32, need_gpu, torch
+from synth import WORKLOADS, make_sparse_inputs, scaled_down
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    need_gpu()
+
+
+def pinned(a, dtype=None):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.view(dtype)
+    return t.pin_memory()
+
+
+@pytest.mark.parametrize("chunk,kv_on_host", [(300, True), (300, False), (97, True), (5000, True)])
+def test_host_call_equals_device_call(chunk, kv_on_host):
+    import dsa_sparse_mla_prefill_gb300 as dsa
+    w = scaled_down(WORKLOADS["v32_h32_16k"], (1000,), (1200,), k=256, ld=264, seed=17)
+    x = make_sparse_inputs(w)
+    q, kv, idx = bf(x.q), bf(x.kv), i32(x.idx)
+    ref_o, ref_l = dsa.dsa_sparse_prefill(q, kv, idx, w.k, w.scale)
+    hq = pinned(x.q.view(np.int16), torch.bfloat16)
+    hkv = pinned(x.kv.view(np.int16), torch.bfloat16) if kv_on_host else kv
+    hidx = pinned(x.idx)
+    ws = torch.empty(dsa.dsa_sparse_prefill_host_workspace(w.T, w.N, w.d_qk, w.H, w.d_qk, w.ld, chunk, kv_on_host),
+                     dtype=torch.uint8, device="cuda")
+    for rep in range(2):   # the second call reuses the workspace and the library's streams
+        ho = torch.full((w.T, w.H, 512), float("nan"), dtype=torch.bfloat16).pin_memory()
+        hl = torch.full((w.T, w.H), float("nan"), dtype=torch.float32).pin_memory()
+        dsa.dsa_sparse_prefill_host(hq, hkv, hidx, w.k, w.scale, ho, hl, ws, chunk_tokens=chunk)
+        torch.cuda.current_stream().synchronize()
+        st, counts = dsa.dsa_last_device_error()
+        assert st == 0, counts
+        assert torch.equal(ho, ref_o.cpu()), rep
+        assert torch.equal(hl, ref_l.cpu()), rep
+
+
+def test_host_call_orders_with_the_callers_stream():
+    """Work queued on the caller's stream before the call (here: writing the kv the call
+    reads, on the device) is seen by it, and work queued after it sees its outputs."""
+    import dsa_sparse_mla_prefill_gb300 as dsa
+    w = scaled_down(WORKLOADS["v32_h32_16k"], (600,), (700,), k=128, ld=128, seed=18)
+    x = make_sparse_inputs(w)
+    s = torch.cuda.Stream()
+    kv_src = bf(x.kv)
+    kv = torch.zeros_like(kv_src)
+    hq = pinned(x.q.view(np.int16), torch.bfloat16)
+    hidx = pinned(x.idx)
+    ho = torch.empty((w.T, w.H, 512), dtype=torch.bfloat16).pin_memory()
+    hl = torch.empty((w.T, w.H), dtype=torch.float32).pin_memory()
+    ws = torch.empty(dsa.dsa_sparse_prefill_host_workspace(w.T, w.N, w.d_qk, w.H, w.d_qk, w.ld, 128, False),
+                     dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        torch.cuda._sleep(20_000_000)   # keep the stream busy so the copy below lands late
+        kv.copy_(kv_src)
+        dsa.dsa_sparse_prefill_host(hq, kv, hidx, w.k, w.scale, ho, hl, ws, chunk_tokens=128, stream=s)
+        done = torch.cuda.Event()
+        done.record(s)
+    done.synchronize()
+    ref_o, ref_l = dsa.dsa_sparse_prefill(bf(x.q), kv_src, i32(x.idx), w.k, w.scale)
+    assert torch.equal(ho, ref_o.cpu()) and torch.equal(hl, ref_l.cpu())
