@@ -89,6 +89,7 @@ _SIGNATURES = {
                              ctypes.POINTER(FormEstimate)]),
     "dsa_last_device_error": (_I, [_VP, ctypes.POINTER(ctypes.c_uint32)]),
     "dsa_debug_trace": (_I, [_VP, _I]),
+    "dsa_debug_wait_timeout": (_I, [_VP]),
 }
 
 EXPORTED = tuple(_SIGNATURES)
@@ -406,6 +407,13 @@ def dsa_choose_form(q_lens, kv_lens, H: int, k: int, d_qk: int = 576, masked_dim
                                  ctypes.byref(e)), "dsa_choose_form")
     ms = {name: (e.ms[i] if e.ms[i] >= 0 else None) for i, name in enumerate(FORMS)}
     return FORMS[e.form], ms, e.union_rows
+
+
+def dsa_debug_wait_timeout(stream=None, device=None):
+    """Queues the failure-path check: one CTA whose bounded wait runs out (about 2 s)."""
+    import torch
+    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    _check(lib().dsa_debug_wait_timeout(_stream(stream, dev)), "dsa_debug_wait_timeout")
 
 
 def dsa_last_device_error(stream=None, device=None):

@@ -391,6 +391,12 @@ int dsa_debug_trace(void* device_buffer, int capacity) {
   return DSA_OK;
 }
 
+int dsa_debug_wait_timeout(dsa_stream_t stream) {
+  DevInfo* d;
+  if (!dev_info(&d)) return DSA_ERR_CUDA;
+  return dsa::launch_wait_timeout(d->err, (cudaStream_t)stream) == 0 ? DSA_OK : DSA_ERR_CUDA;
+}
+
 int dsa_last_device_error(dsa_stream_t stream, uint32_t* counts) {
   if (!counts) return DSA_ERR_INVALID_ARG;
   DevInfo* d;

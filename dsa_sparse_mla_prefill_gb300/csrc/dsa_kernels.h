@@ -120,5 +120,6 @@ int launch_topk_to_key_mask(const KeyMaskArgs& a, cudaStream_t stream);
 int launch_local_to_global(const ConvertArgs& a, cudaStream_t stream);
 int launch_grouped_prefill(const GroupedArgs& a, int num_sms, cudaStream_t stream);
 int launch_masked_mha(const MaskedArgs& a, int num_sms, cudaStream_t stream);
+int launch_wait_timeout(unsigned int* err, cudaStream_t stream);
 
 }  // namespace dsa

@@ -342,6 +342,16 @@ int dsa_form_calibration_default(dsa_form_calibration* calib);
 int dsa_choose_form(const dsa_form_query* query, const dsa_form_calibration* calib, dsa_form_estimate* out);
 
 /* ------------------------------------------------------------------------
+ * Failure-path check (no counterpart on the pages).  Launches one CTA whose
+ * bounded wait on an mbarrier that nothing completes runs out after the
+ * library's wait limit (2 s): the kernel records the timeout, releases the
+ * tensor memory it holds and returns, as every pipeline kernel does when a
+ * wait runs out.  Afterwards dsa_last_device_error reports counts[1] >= 1
+ * and DSA_ERR_DEVICE, and the context stays usable.  Asynchronous on stream.
+ * ---------------------------------------------------------------------- */
+int dsa_debug_wait_timeout(dsa_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Diagnostic timeline (no counterpart on the pages; a profiling aid).  While
  * a buffer is set, the first two CTAs of every per-token, grouped and masked
  * launch write clock64() stamps of up to 8 pipeline events for each of their
