@@ -11,8 +11,16 @@
 // The caller's stream is joined at both ends: the copies start after the work
 // queued on it so far, and work queued on it after the call starts once the
 // last chunk is back in host memory.
+//
+// Chunk sizes: the per-token kernel runs one persistent CTA per SM with the
+// tokens dealt round-robin, so a chunk that is a multiple of the SM count
+// leaves no CTA a token behind the others; the middle chunks are the largest
+// such multiple the workspace allows, and the first and last chunks ramp
+// (one, two, four ... tokens per SM) so that the copy before the first
+// kernel and the copy after the last are short.
 #include <cstdint>
 #include <cstring>
+#include <vector>
 
 #include <cuda_runtime.h>
 
@@ -26,6 +34,7 @@ constexpr int64_t kAlign = 256;
 
 struct Pipe {
   bool init = false;
+  int num_sms = 0;
   cudaStream_t h2d = nullptr, cmp = nullptr, d2h = nullptr;
   cudaEvent_t entry = nullptr, kv_in = nullptr, exit = nullptr;
   cudaEvent_t in[NB] = {}, done[NB] = {}, out[NB] = {};
@@ -44,6 +53,8 @@ bool pipe_of(Pipe** p) {
         cudaEventCreateWithFlags(&s.entry, ef) != cudaSuccess || cudaEventCreateWithFlags(&s.kv_in, ef) != cudaSuccess ||
         cudaEventCreateWithFlags(&s.exit, ef) != cudaSuccess)
       return false;
+    if (cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || s.num_sms < 1)
+      return false;
     for (int b = 0; b < NB; ++b)
       if (cudaEventCreateWithFlags(&s.in[b], ef) != cudaSuccess ||
           cudaEventCreateWithFlags(&s.done[b], ef) != cudaSuccess ||
@@ -56,6 +67,27 @@ bool pipe_of(Pipe** p) {
 }
 
 int64_t up(int64_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+// Chunk sizes for T tokens, none above `cap`, as described at the top.
+std::vector<int> plan_chunks(int T, int cap, int unit) {
+  std::vector<int> out;
+  const int full = cap >= unit ? cap / unit * unit : cap;
+  std::vector<int> ramp;   // unit, 2 unit, 4 unit, ... below the full size
+  int64_t ramp_sum = 0;
+  for (int64_t r = unit; r < full && 2 * (ramp_sum + r) + full <= T; r *= 2) {
+    ramp.push_back((int)r);
+    ramp_sum += r;
+  }
+  for (int r : ramp) out.push_back(r);
+  int64_t mid = T - 2 * ramp_sum;
+  while (mid > 0) {
+    const int n = (int)(mid < full ? mid : full);
+    out.push_back(n);
+    mid -= n;
+  }
+  for (int i = (int)ramp.size() - 1; i >= 0; --i) out.push_back(ramp[i]);
+  return out;
+}
 
 // Byte sizes of one buffer set and of the whole workspace.
 struct Layout {
@@ -114,11 +146,12 @@ int dsa_sparse_prefill_host(const uint16_t* q, const uint16_t* kv, int kv_on_hos
       return DSA_ERR_CUDA;
     kv_dev = reinterpret_cast<const uint16_t*>(ws);
   }
-  const int nchunks = (T + chunk - 1) / chunk;
-  for (int i = 0; i < nchunks; ++i) {
+  const std::vector<int> plan = plan_chunks(T, chunk, p->num_sms);
+  const int nchunks = (int)plan.size();
+  int64_t t0 = 0;
+  for (int i = 0; i < nchunks; t0 += plan[i], ++i) {
     const int b = i % NB;
-    const int64_t t0 = (int64_t)i * chunk;
-    const int n = (int)((T - t0) < chunk ? (T - t0) : chunk);
+    const int n = plan[i];
     uint8_t* set = ws + L.kv + b * L.set;
     uint16_t* dq = reinterpret_cast<uint16_t*>(set);
     int32_t* didx = reinterpret_cast<int32_t*>(set + L.q);

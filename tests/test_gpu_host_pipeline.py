@@ -25,10 +25,13 @@ def pinned(a, dtype=None):
     return t.pin_memory()
 
 
-@pytest.mark.parametrize("chunk,kv_on_host", [(300, True), (300, False), (97, True), (5000, True)])
-def test_host_call_equals_device_call(chunk, kv_on_host):
+@pytest.mark.parametrize("T,chunk,kv_on_host", [
+    (1000, 300, True), (1000, 300, False), (1000, 97, True), (1000, 5000, True),
+    (3000, 1216, True),     # ramped first and last chunks (one and two tokens per SM), then full ones
+])
+def test_host_call_equals_device_call(T, chunk, kv_on_host):
     import dsa_sparse_mla_prefill_gb300 as dsa
-    w = scaled_down(WORKLOADS["v32_h32_16k"], (1000,), (1200,), k=256, ld=264, seed=17)
+    w = scaled_down(WORKLOADS["v32_h32_16k"], (T,), (T + 200,), k=256, ld=264, seed=17)
     x = make_sparse_inputs(w)
     q, kv, idx = bf(x.q), bf(x.kv), i32(x.idx)
     ref_o, ref_l = dsa.dsa_sparse_prefill(q, kv, idx, w.k, w.scale)
