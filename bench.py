@@ -739,7 +739,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-modes", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-chunk", type=int, default=1024, help="tokens per chunk of the host-buffer call")
+    ap.add_argument("--e2e-chunk", type=int, default=1216, help="tokens per chunk of the host-buffer call (8 per SM)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work per core")
     ap.add_argument("--profile", choices=["sparse", "union", "grouped", "masked"], default=None,
                     help="run a small case of one kernel (for ncu) instead of the benchmark")
