@@ -109,6 +109,54 @@ def test_per_token_prefill_over_paged_kv():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+def test_grouped_prefill_over_paged_kv():
+    """Converted indices feed the union build (sorted by physical row) and the grouped
+    form over the paged table: union and mask bit-exact against the oracle on the same
+    converted rows, and the output equal to the per-token oracle on the contiguous table."""
+    import dsa_sparse_mla_prefill_gb300 as dsa
+    rng = np.random.default_rng(22)
+    H, d_qk, B, k, G = 16, 576, 16, 96, 8
+    kv_lens, q_lens = [260, 190], [45, 30]
+    cq = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    ck = np.concatenate([[0], np.cumsum(kv_lens)])
+    T, Ncont = int(cq[-1]), int(ck[-1])
+    kv_cont = normal_bf16(rng, (Ncont, d_qk))
+    q = normal_bf16(rng, (T, H, d_qk))
+    nb = [-(-n // B) for n in kv_lens]
+    total = sum(nb) + 4
+    ids = rng.permutation(total)
+    bt = np.full((2, max(nb)), -1, dtype=np.int32)
+    bt[0, :nb[0]] = ids[:nb[0]]
+    bt[1, :nb[1]] = ids[nb[0]:nb[0] + nb[1]]
+    kv_phys = normal_bf16(rng, (total * B, d_qk))
+    for r in range(2):
+        for x in range(kv_lens[r]):
+            kv_phys[bt[r, x // B] * B + x % B] = kv_cont[ck[r] + x]
+    local = np.full((T, k), -1, dtype=np.int32)
+    for r in range(2):
+        for t in range(cq[r], cq[r + 1]):
+            # causal, with the neighbouring tokens sharing most of their rows
+            pos = kv_lens[r] - q_lens[r] + (t - cq[r])
+            n = min(k, pos + 1)
+            local[t, :n] = rng.choice(pos + 1, size=n, replace=False)
+    glob_cont = np.where(local >= 0, local + np.repeat(ck[:-1], q_lens)[:, None], -1).astype(np.int32)
+    N = total * B
+    rows = dsa.dsa_local_to_global(i32(local), k, np.asarray(kv_lens, np.int32), i32(bt), B, N, cu_seqlens_q=cq)
+    upad = dsa.dsa_union_pad(G, k, 128)
+    u, ul, m = dsa.dsa_union_build(rows, k, G, N, cu_seqlens_q=cq, union_pad=upad)
+    o, l = dsa.dsa_grouped_prefill(bf(q), bf(kv_phys), u, ul, m, G, 0.07, cu_seqlens_q=cq)
+    torch.cuda.synchronize()
+    st, counts = dsa.dsa_last_device_error()
+    assert st == 0, counts
+    rows_h = rows.cpu().numpy()
+    ru, rl, rm = O.union_build(rows_h, k, G, N, cq, upad)
+    assert np.array_equal(u.cpu().numpy(), ru) and np.array_equal(ul.cpu().numpy(), rl)
+    assert np.array_equal(m.cpu().numpy(), rm)
+    ro, rlse = O.sparse_prefill(q, kv_cont, glob_cont, k, 0.07, d_qk, 512)
+    res = O.compare(f32(o), l.cpu().numpy().astype(np.float64), ro, rlse)
+    assert res["ok"], res
+
+
 def test_convert_full_size_sampled():
     """The headline index shape (16384 x 2048) through a shuffled 64-row block
     table; sampled tokens against the oracle, and every valid entry mapped."""
