@@ -21,9 +21,10 @@
  *    laid out as stated; bf16 tensors are passed as uint16_t bit patterns.
  *    Arrays documented as HOST are read during the call (their values are
  *    copied into the launch) and may be freed when it returns.
- *  - Nothing is allocated on any call.  Every compute call is asynchronous
- *    on `stream` (NULL = the legacy default stream) and returns once the
- *    kernel is queued.
+ *  - No memory is allocated on any call (dsa_sparse_prefill_host creates
+ *    three streams and a few events per device on its first use).  Every
+ *    compute call is asynchronous on `stream` (NULL = the legacy default
+ *    stream) and returns once the work is queued.
  *  - Return value: DSA_OK, or an error code; on an error nothing was
  *    launched.  DSA_ERR_INVALID_ARG: a null pointer, a negative or
  *    inconsistent size, a misaligned pointer or stride.  DSA_ERR_UNSUPPORTED:
