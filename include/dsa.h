@@ -272,6 +272,8 @@ int dsa_last_device_error(dsa_stream_t stream, uint32_t* counts);
  * Shapes and errors as dsa_sparse_prefill; DSA_ERR_INVALID_ARG also for
  * chunk_tokens < 1 or a workspace that is too small or misaligned.  A CUDA
  * error part way returns DSA_ERR_CUDA with earlier chunks already queued.
+ * The library's streams and events are per device and shared by all calls:
+ * calls on one device must not run from several host threads at once.
  * ---------------------------------------------------------------------- */
 int64_t dsa_sparse_prefill_host_workspace(int T, int N, int ld_kv, int H, int d_qk, int d_v, int ld,
                                           int chunk_tokens, int kv_on_host);
