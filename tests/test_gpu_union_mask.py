@@ -45,6 +45,17 @@ def test_union_random_ragged(G):
     _check_union(idx, 200, G, 3000, cu, union_block=16)
 
 
+@pytest.mark.parametrize("G,N", [(8, 200_000), (2, 200_000), (8, 60_000)])
+def test_union_large_tables(G, N):
+    """Tables large enough that G per-token bitmaps no longer fit the builder's shared-memory
+    budget (G = 8, N = 200k: the single-bitmap variant), and ones where they still do."""
+    rng = np.random.default_rng(N + G)
+    q_lens = [37, 27]
+    cu = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    idx = _rows(rng, int(cu[-1]), N, 384, 392)
+    _check_union(idx, 384, G, N, cu)
+
+
 def test_union_tiny_uniform_config():
     w = WORKLOADS["tiny_uniform_512"]
     idx = make_indices(w, np.random.default_rng(w.seed))
