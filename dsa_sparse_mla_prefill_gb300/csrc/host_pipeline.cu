@@ -20,6 +20,7 @@
 // kernel and the copy after the last are short.
 #include <cstdint>
 #include <cstring>
+#include <initializer_list>
 #include <vector>
 
 #include <cuda_runtime.h>
@@ -41,25 +42,49 @@ struct Pipe {
 };
 Pipe g_pipe[kMaxDev];
 
+// Releases whatever a failed set-up created, so that a later call starts clean.
+void pipe_release(Pipe& s) {
+  for (cudaStream_t* st : {&s.h2d, &s.cmp, &s.d2h})
+    if (*st) {
+      cudaStreamDestroy(*st);
+      *st = nullptr;
+    }
+  for (cudaEvent_t* ev : {&s.entry, &s.kv_in, &s.exit})
+    if (*ev) {
+      cudaEventDestroy(*ev);
+      *ev = nullptr;
+    }
+  for (int b = 0; b < NB; ++b)
+    for (cudaEvent_t* ev : {&s.in[b], &s.done[b], &s.out[b]})
+      if (*ev) {
+        cudaEventDestroy(*ev);
+        *ev = nullptr;
+      }
+}
+
 bool pipe_of(Pipe** p) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return false;
   Pipe& s = g_pipe[dev];
   if (!s.init) {
     const unsigned ef = cudaEventDisableTiming;
-    if (cudaStreamCreateWithFlags(&s.h2d, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaStreamCreateWithFlags(&s.cmp, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaStreamCreateWithFlags(&s.d2h, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaEventCreateWithFlags(&s.entry, ef) != cudaSuccess || cudaEventCreateWithFlags(&s.kv_in, ef) != cudaSuccess ||
-        cudaEventCreateWithFlags(&s.exit, ef) != cudaSuccess)
+    bool ok = cudaStreamCreateWithFlags(&s.h2d, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&s.cmp, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&s.d2h, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&s.entry, ef) == cudaSuccess &&
+              cudaEventCreateWithFlags(&s.kv_in, ef) == cudaSuccess &&
+              cudaEventCreateWithFlags(&s.exit, ef) == cudaSuccess &&
+              cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+              s.num_sms >= 1;
+    for (int b = 0; b < NB && ok; ++b)
+      ok = cudaEventCreateWithFlags(&s.in[b], ef) == cudaSuccess &&
+           cudaEventCreateWithFlags(&s.done[b], ef) == cudaSuccess &&
+           cudaEventCreateWithFlags(&s.out[b], ef) == cudaSuccess;
+    if (!ok) {
+      pipe_release(s);
+      cudaGetLastError();
       return false;
-    if (cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || s.num_sms < 1)
-      return false;
-    for (int b = 0; b < NB; ++b)
-      if (cudaEventCreateWithFlags(&s.in[b], ef) != cudaSuccess ||
-          cudaEventCreateWithFlags(&s.done[b], ef) != cudaSuccess ||
-          cudaEventCreateWithFlags(&s.out[b], ef) != cudaSuccess)
-        return false;
+    }
     s.init = true;
   }
   *p = &s;
