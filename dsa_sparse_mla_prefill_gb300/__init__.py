@@ -82,6 +82,7 @@ _SIGNATURES = {
     "dsa_masked_mha_prefill_strided": (_I, [_VP, _L, _L, _VP, _L, _L, _VP, _L, _VP, _L, _L, _VP, _I, _I32P, _I32P,
                                             _I, _I, _I, _I, _I, _I, _F, _VP, _VP, _VP]),
     "dsa_sparse_prefill_host_workspace": (_L, [_I, _I, _I, _I, _I, _I, _I, _I, _I]),
+    "dsa_sparse_prefill_host_plan": (_I, [_I, _I, _I, _I32P, _I, ctypes.POINTER(ctypes.c_int)]),
     "dsa_sparse_prefill_host": (_I, [_VP, _VP, _I, _I, _I, _VP, _I, _I, _I, _I, _I, _I, _F, _VP, _VP, _VP, _L, _I,
                                      _VP]),
     "dsa_form_calibration_default": (_I, [ctypes.POINTER(FormCalibration)]),
@@ -229,6 +230,18 @@ def dsa_sparse_prefill_host_workspace(T: int, N: int, ld_kv: int, H: int, d_qk: 
     if n < 0:
         raise DSAError(DSA_ERR_INVALID_ARG, "dsa_sparse_prefill_host_workspace")
     return int(n)
+
+
+def dsa_sparse_prefill_host_plan(T: int, chunk_tokens: int, num_sms: int) -> list:
+    """Chunk sizes the host-buffer call uses for T tokens on num_sms SMs (host only)."""
+    n = ctypes.c_int(0)
+    st = lib().dsa_sparse_prefill_host_plan(T, chunk_tokens, num_sms, None, 0, ctypes.byref(n))
+    if st != DSA_OK and n.value == 0:
+        _check(st, "dsa_sparse_prefill_host_plan")   # bad sizes
+    buf = (ctypes.c_int32 * max(1, n.value))()
+    _check(lib().dsa_sparse_prefill_host_plan(T, chunk_tokens, num_sms, buf, n.value, ctypes.byref(n)),
+           "dsa_sparse_prefill_host_plan")
+    return [int(buf[i]) for i in range(n.value)]
 
 
 def dsa_sparse_prefill_host(q, kv, idx, k: int, scale: float, out, lse, workspace, chunk_tokens: int = 2048,

@@ -135,6 +135,20 @@ Layout layout(int chunk, int N, int ld_kv, int H, int d_qk, int d_v, int ld, boo
 
 extern "C" {
 
+int dsa_sparse_prefill_host_plan(int T, int chunk_tokens, int num_sms, int32_t* sizes, int max_chunks,
+                                 int* num_chunks) {
+  if (T < 0 || chunk_tokens < 1 || num_sms < 1 || max_chunks < 0 || !num_chunks || (max_chunks > 0 && !sizes))
+    return DSA_ERR_INVALID_ARG;
+  if (T == 0) {
+    *num_chunks = 0;
+    return DSA_OK;
+  }
+  const std::vector<int> plan = plan_chunks(T, chunk_tokens < T ? chunk_tokens : T, num_sms);
+  *num_chunks = (int)plan.size();
+  for (int i = 0; i < (int)plan.size() && i < max_chunks; ++i) sizes[i] = plan[i];
+  return (int)plan.size() <= max_chunks ? DSA_OK : DSA_ERR_INVALID_ARG;
+}
+
 int64_t dsa_sparse_prefill_host_workspace(int T, int N, int ld_kv, int H, int d_qk, int d_v, int ld,
                                           int chunk_tokens, int kv_on_host) {
   if (T < 0 || N < 0 || ld_kv < 1 || H < 1 || d_qk < 1 || d_v < 1 || ld < 1 || chunk_tokens < 1) return -1;

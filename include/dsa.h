@@ -278,6 +278,16 @@ int dsa_last_device_error(dsa_stream_t stream, uint32_t* counts);
 int64_t dsa_sparse_prefill_host_workspace(int T, int N, int ld_kv, int H, int d_qk, int d_v, int ld,
                                           int chunk_tokens, int kv_on_host);
 
+/* The chunk sizes dsa_sparse_prefill_host uses for T tokens on a GPU with
+ * num_sms SMs (host only): middle chunks of the largest multiple of num_sms
+ * not above min(chunk_tokens, T) (the persistent kernel deals tokens to one
+ * CTA per SM, so no CTA is left a token behind), and first and last chunks
+ * that ramp num_sms, 2 num_sms, 4 num_sms ... while the ramps still leave
+ * room for a full chunk.  Writes up to max_chunks sizes (HOST int32) and
+ * *num_chunks; DSA_ERR_INVALID_ARG if they do not fit or for bad sizes. */
+int dsa_sparse_prefill_host_plan(int T, int chunk_tokens, int num_sms, int32_t* sizes, int max_chunks,
+                                 int* num_chunks);
+
 int dsa_sparse_prefill_host(const uint16_t* q, const uint16_t* kv, int kv_on_host, int N, int ld_kv,
                             const int32_t* idx, int T, int H, int d_qk, int d_v, int k, int ld, float scale,
                             uint16_t* out, float* lse, void* workspace, int64_t workspace_bytes, int chunk_tokens,
