@@ -42,7 +42,10 @@ Readings where the pages are silent (each listed in the design notes):
   block_table[r][x // block_size] * block_size + x % block_size; positions
   outside the request, unmapped blocks (negative ids) and rows outside the
   table map to -1 and are counted (this reading of the conversion the pages
-  name without printing it).
+  name without printing it);
+* an FP8 KV row (the pages keep bf16 KV and refuse quantized caches; this is
+  the plainest layout for the latent row): 512 float8 e4m3 NoPE values with
+  one fp32 scale (block amax / 448) per 128 of them, the RoPE columns bf16.
 """
 from __future__ import annotations
 
@@ -316,6 +319,89 @@ def masked_mha_prefill(q_bits, k_bits, v_bits, key_mask, cu_seqlens_q, cu_seqlen
             out[i, h] = o[0]
             lse[i, h] = l[0]
     return out, lse
+
+
+# ----------------------------------------------------------------------------
+# FP8 latent rows (a storage format for the KV cache; the pages keep bf16 KV,
+# so this is the plainest reading of the "FP8 KV cache" step: the 512 NoPE
+# columns as float8 e4m3 with one fp32 scale per 128 of them, the RoPE
+# columns kept bf16; row = 512 codes | 4 scales | 2 * d_rope bytes)
+# ----------------------------------------------------------------------------
+E4M3_MAX = 448.0
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """float8 e4m3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no
+    infinities, S.1111.111 = NaN) to float64, from its definition."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    val = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    val = sign * val
+    return np.where((e == 15) & (m == 7), np.nan, val)
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """float32 values to e4m3 codes: the nearest finite e4m3 value, ties to the
+    even code, magnitudes beyond 448 saturated to 448; the sign is kept (also
+    for values that round to zero).  Written as a search over the 127
+    non-negative finite codes."""
+    x = np.asarray(x, dtype=np.float32).astype(np.float64)
+    grid = e4m3_decode(np.arange(0x7F, dtype=np.uint8))       # codes 0x00..0x7E, ascending
+    a = np.minimum(np.abs(x), E4M3_MAX)
+    hi = np.clip(np.searchsorted(grid, a, side="left"), 0, 0x7E)
+    lo = np.maximum(hi - 1, 0)
+    dlo = a - grid[lo]
+    dhi = grid[hi] - a
+    pick = np.where(dlo < dhi, lo, np.where(dhi < dlo, hi, np.where(lo % 2 == 0, lo, hi)))
+    pick = np.where(grid[hi] == a, hi, pick)
+    return (pick | np.where(np.signbit(x), 0x80, 0)).astype(np.uint8)
+
+
+def _f32_to_bf16_bits(x) -> np.ndarray:
+    """float32 to bf16 bits, round to nearest even (finite inputs)."""
+    u = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return r.astype(np.uint16)
+
+
+def kv_fp8_row_bytes(d_rope: int) -> int:
+    return 512 + 16 + 2 * d_rope
+
+
+def kv_fp8_quantize(kv_bits, d_rope: int) -> np.ndarray:
+    """bf16 latent rows [N, >= 512 + d_rope] to FP8 rows [N, row_bytes] uint8.
+    Block b (columns 128b .. 128b+127): scale = amax / 448 in float32 (1 when
+    the block is all zero), codes = e4m3(x / scale) with the division in
+    float32; the RoPE columns are copied."""
+    kv_bits = np.asarray(kv_bits, dtype=np.uint16)
+    N = kv_bits.shape[0]
+    x = (kv_bits[:, :512].astype(np.uint32) << 16).view(np.float32).reshape(N, 4, 128)
+    amax = np.abs(x).max(axis=2)
+    scale = np.where(amax > 0, (amax / np.float32(E4M3_MAX)).astype(np.float32), np.float32(1.0))
+    codes = e4m3_encode((x / scale[:, :, None]).astype(np.float32)).reshape(N, 512)
+    out = np.zeros((N, kv_fp8_row_bytes(d_rope)), dtype=np.uint8)
+    out[:, :512] = codes
+    out[:, 512:528] = scale.astype("<f4").view(np.uint8).reshape(N, 16)
+    if d_rope:
+        out[:, 528:] = np.ascontiguousarray(kv_bits[:, 512:512 + d_rope]).astype("<u2").view(np.uint8)
+    return out
+
+
+def kv_fp8_dequantize(rows, d_rope: int) -> np.ndarray:
+    """FP8 rows to bf16 latent rows [N, 512 + d_rope]: e4m3 value times its
+    block's scale in float32, rounded to bf16; RoPE columns copied."""
+    rows = np.asarray(rows, dtype=np.uint8)
+    N = rows.shape[0]
+    vals = e4m3_decode(rows[:, :512]).astype(np.float32).reshape(N, 4, 128)
+    scale = np.ascontiguousarray(rows[:, 512:528]).view("<f4").reshape(N, 4)
+    prod = (vals * scale[:, :, None]).astype(np.float32).reshape(N, 512)
+    out = np.zeros((N, 512 + d_rope), dtype=np.uint16)
+    out[:, :512] = _f32_to_bf16_bits(prod)
+    if d_rope:
+        out[:, 512:] = np.ascontiguousarray(rows[:, 528:528 + 2 * d_rope]).view("<u2")
+    return out
 
 
 # ----------------------------------------------------------------------------

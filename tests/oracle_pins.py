@@ -468,11 +468,75 @@ def pin_local_to_global_contiguous(seed=13) -> bool:
     return bad == 0 and bool(np.array_equal(out, want))
 
 
+def pin_e4m3_decode_closed_forms() -> bool:
+    """float8 e4m3 codes whose values follow from the format by hand: 1 =
+    0.0111.000, the largest finite 448 = 0.1111.110 (2^8 x 1.75), the smallest
+    normal 2^-6 = 0.0001.000, the smallest subnormal 2^-9 = 0.0000.001,
+    7 x 2^-9 = 0.0000.111, -1, NaN = 0.1111.111, +0 and -0."""
+    codes = [0x38, 0x7E, 0x08, 0x01, 0x07, 0xB8, 0x00, 0x80]
+    want = [1.0, 448.0, 2.0 ** -6, 2.0 ** -9, 7 * 2.0 ** -9, -1.0, 0.0, -0.0]
+    got = O.e4m3_decode(codes)
+    return bool(np.array_equal(got, want) and np.isnan(O.e4m3_decode([0x7F, 0xFF])).all()
+                and np.signbit(got[-1]))
+
+
+def pin_e4m3_encode_library() -> bool:
+    """Rounding to e4m3 equals torch's float8_e4m3fn conversion (a library
+    routine) on random magnitudes over the whole range and on every midpoint
+    between neighbouring values (ties to even), both signs."""
+    import torch
+    rng = np.random.default_rng(13)
+    x = (rng.standard_normal(50000) * np.exp2(rng.integers(-12, 9, 50000))).astype(np.float32)
+    x = x[np.abs(x) <= 448.0]
+    grid = O.e4m3_decode(np.arange(0x7F, dtype=np.uint8))
+    mid = ((grid[:-1] + grid[1:]) / 2).astype(np.float32)
+    x = np.concatenate([x, mid, -mid])
+    lib = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    return bool(np.array_equal(O.e4m3_encode(x), lib))
+
+
+def pin_kv_fp8_round_trip(seed=14) -> bool:
+    """FP8 rows: a block whose values are e4m3 values times a power of two
+    (its amax 448 times that power) comes back exactly; random blocks come
+    back within half an e4m3 step (2^-4 relative, 2^-10 of the scale for
+    subnormal codes) plus bf16 rounding; the scale is amax / 448; an all-zero
+    block has scale 1 and codes 0; the RoPE columns pass through."""
+    rng = np.random.default_rng(seed)
+    N, d_rope = 6, 64
+    grid = O.e4m3_decode(rng.integers(0, 0x7F, size=(N, 512)).astype(np.uint8))
+    grid[:, ::128] = 448.0
+    sgn = np.where(rng.random((N, 512)) < 0.5, -1.0, 1.0)
+    exact = (sgn * grid * np.exp2(rng.integers(-20, 10, size=(N, 1)))).astype(np.float32)
+    def bits(f):
+        return (np.asarray(f, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    rope = rng.integers(0, 1 << 16, size=(N, d_rope)).astype(np.uint16)
+    rope = np.where(((rope >> 7) & 0xFF) == 0xFF, rope & 0x807F, rope)   # finite bf16 patterns
+    kv = np.concatenate([bits(exact), rope], axis=1)
+    rows = O.kv_fp8_quantize(kv, d_rope)
+    ok = np.array_equal(O.kv_fp8_dequantize(rows, d_rope), kv)
+    r = (rng.standard_normal((N, 512)) * np.exp2(rng.integers(-8, 8, size=(N, 1)))).astype(np.float32)
+    r[2, 128:256] = 0.0
+    kv2 = np.concatenate([bits(r), rope], axis=1)
+    x = (kv2[:, :512].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    rows2 = O.kv_fp8_quantize(kv2, d_rope)
+    back = (O.kv_fp8_dequantize(rows2, d_rope)[:, :512].astype(np.uint32) << 16).view(np.float32)
+    scale = np.ascontiguousarray(rows2[:, 512:528]).view("<f4").reshape(N, 4).astype(np.float64)
+    amax = np.abs(x.reshape(N, 4, 128)).max(axis=2)
+    ok &= bool(np.allclose(scale, np.where(amax > 0, amax / 448.0, 1.0), rtol=2 ** -23, atol=0))
+    s = np.repeat(scale, 128, axis=1)
+    tol = np.maximum(np.abs(x) * 2.0 ** -4, s * 2.0 ** -10) * (1 + 2.0 ** -7) + np.abs(x) * 2.0 ** -8
+    ok &= bool(np.all(np.abs(back - x) <= tol))
+    ok &= bool(np.all(rows2[2, 128:256] == 0) and scale[2, 1] == 1.0)
+    ok &= bool(np.array_equal(O.kv_fp8_dequantize(rows2, d_rope)[:, 512:], rope))
+    return ok
+
+
 ALL_PINS = [pin_bruteforce, pin_single_key, pin_zero_query, pin_equal_keys, pin_two_keys_closed_form,
             pin_order_and_padding_invariance, pin_dense_causal_sdpa, pin_union_worked_example,
             pin_union_bruteforce, pin_union_popcounts, pin_grouped_equals_per_token,
             pin_key_mask_bruteforce, pin_masked_equals_sparse, pin_masked_dense_causal_sdpa,
-            pin_local_to_global_paged_round_trip, pin_local_to_global_contiguous]
+            pin_local_to_global_paged_round_trip, pin_local_to_global_contiguous,
+            pin_e4m3_decode_closed_forms, pin_e4m3_encode_library, pin_kv_fp8_round_trip]
 
 
 def run_all_pins():

@@ -132,6 +132,40 @@ def _l2g_no_range_check(idx, k, cq, kv_lens, bt, B, N):
     return _orig_l2g(idx, k, cq, [np.asarray(bt).shape[1] * B] * len(kv_lens), bt, B, N)
 
 
+_orig_e4m3_decode = O.e4m3_decode
+_orig_e4m3_encode = O.e4m3_encode
+
+
+def _e4m3_bias8(codes):
+    return _orig_e4m3_decode(codes) / 2.0
+
+
+def _e4m3_ties_away(x):
+    x32 = np.asarray(x, dtype=np.float32)
+    c = _orig_e4m3_encode(x32)
+    grid = _orig_e4m3_decode(np.arange(0x7F, dtype=np.uint8))
+    a = np.abs(x32.astype(np.float64))
+    lo = c & 0x7F
+    up = np.minimum(lo + 1, 0x7E)
+    tie = (lo < 0x7E) & (a == (grid[lo] + grid[up]) / 2)
+    return np.where(tie, up | (c & 0x80), c).astype(np.uint8)
+
+
+def _fp8_scale_per_64(kv_bits, d_rope):
+    kv_bits = np.asarray(kv_bits, dtype=np.uint16)
+    N = kv_bits.shape[0]
+    x = (kv_bits[:, :512].astype(np.uint32) << 16).view(np.float32).reshape(N, 8, 64)
+    amax = np.abs(x).max(axis=2)
+    scale = np.where(amax > 0, (amax / np.float32(448.0)).astype(np.float32), np.float32(1.0))
+    codes = O.e4m3_encode((x / scale[:, :, None]).astype(np.float32)).reshape(N, 512)
+    out = np.zeros((N, O.kv_fp8_row_bytes(d_rope)), dtype=np.uint8)
+    out[:, :512] = codes
+    out[:, 512:528] = scale[:, ::2].astype("<f4").view(np.uint8).reshape(N, 16)
+    if d_rope:
+        out[:, 528:] = np.ascontiguousarray(kv_bits[:, 512:512 + d_rope]).astype("<u2").view(np.uint8)
+    return out
+
+
 MUTATIONS = [
     ("attend", _attend_lse_base2),
     ("attend", _attend_sign),
@@ -150,6 +184,9 @@ MUTATIONS = [
     ("local_to_global", _l2g_div_mod_swapped),
     ("local_to_global", _l2g_first_request_table),
     ("local_to_global", _l2g_no_range_check),
+    ("e4m3_decode", _e4m3_bias8),
+    ("e4m3_encode", _e4m3_ties_away),
+    ("kv_fp8_quantize", _fp8_scale_per_64),
 ]
 
 
