@@ -353,6 +353,37 @@ def run_modes(dev, stream, peaks, steps, warmup, flush, only=None):
                                    index_gen="locality_wide")
         out["grouped_21k_of_32k_wide"] = sparse_block("grouped_21k_of_32k_wide", w=wide)
         torch.cuda.empty_cache()
+    # the headline workload over an FP8 KV cache: the cache is written once
+    # (quantize), each step dequantizes it and runs the per-token kernel
+    if want("v32_h32_16k_fp8kv"):
+        w = WORKLOADS["v32_h32_16k"]
+        log("mode v32_h32_16k_fp8kv")
+        x = make_sparse_inputs(w)
+        q, kv = to_dev(x.q, dev), to_dev(x.kv, dev)
+        idx = torch.from_numpy(x.idx).to(dev)
+        fp8 = torch.empty((w.N, dsa.dsa_kv_fp8_row_bytes(64)), dtype=torch.uint8, device=dev)
+        deq = torch.empty((w.N, w.d_qk), dtype=torch.bfloat16, device=dev)
+        o = torch.empty((w.T, w.H, 512), dtype=torch.bfloat16, device=dev)
+        l = torch.empty((w.T, w.H), dtype=torch.float32, device=dev)
+        ms_q = statistics.median(timed_steps(lambda: dsa.dsa_kv_fp8_quantize(kv, 64, out=fp8), steps, warmup,
+                                             stream, flush))
+        ms_d = statistics.median(timed_steps(lambda: dsa.dsa_kv_fp8_dequantize(fp8, 64, out=deq), steps, warmup,
+                                             stream, flush))
+        def fp8_step():
+            dsa.dsa_kv_fp8_dequantize(fp8, 64, out=deq)
+            dsa.dsa_sparse_prefill(q, deq, idx, w.k, w.scale, out=o, lse=l)
+        ms_s = statistics.median(timed_steps(fp8_step, steps, warmup, stream, flush))
+        rb = dsa.dsa_kv_fp8_row_bytes(64)
+        qbytes = w.N * (w.d_qk * 2 + rb)
+        dbytes = w.N * (rb + w.d_qk * 2)
+        out["v32_h32_16k_fp8kv"] = {
+            "cache_bytes": w.N * rb, "cache_bytes_bf16": w.N * w.d_qk * 2,
+            "quantize": {"ms": ms_q, "gbs": qbytes / ms_q / 1e6, "hbm_frac": qbytes / ms_q / 1e6 / peaks["hbm_gbs"]},
+            "dequantize": {"ms": ms_d, "gbs": dbytes / ms_d / 1e6, "hbm_frac": dbytes / ms_d / 1e6 / peaks["hbm_gbs"]},
+            "dequantize_plus_per_token": {"ms": ms_s, "query_tokens_per_s": w.T / ms_s * 1e3}}
+        del q, kv, idx, fp8, deq, o, l
+        torch.cuda.empty_cache()
+
     # masked dense MHA: DeepSeek-V3.2 geometry (contiguous per-head q/k/v),
     # then the GLM NoPE and GLM-5 geometries with k and v read as views of one
     # per-head projection output and the RoPE key columns shared

@@ -16,6 +16,7 @@ Forms (see the header for the exact contracts):
   dsa_masked_mha_prefill  masked dense MHA with per-head q/k/v
   dsa_masked_mha_prefill_strided  the same on strided views, RoPE key columns shared
   dsa_choose_form         predicted time of each form and the fastest (host only)
+  dsa_kv_fp8_quantize / dsa_kv_fp8_dequantize  FP8 latent rows of the KV cache
 """
 from __future__ import annotations
 
@@ -85,6 +86,9 @@ _SIGNATURES = {
     "dsa_sparse_prefill_host_plan": (_I, [_I, _I, _I, _I32P, _I, ctypes.POINTER(ctypes.c_int)]),
     "dsa_sparse_prefill_host": (_I, [_VP, _VP, _I, _I, _I, _VP, _I, _I, _I, _I, _I, _I, _F, _VP, _VP, _VP, _L, _I,
                                      _VP]),
+    "dsa_kv_fp8_row_bytes": (_L, [_I]),
+    "dsa_kv_fp8_quantize": (_I, [_VP, _I, _I, _I, _VP, _VP]),
+    "dsa_kv_fp8_dequantize": (_I, [_VP, _I, _I, _VP, _I, _VP]),
     "dsa_form_calibration_default": (_I, [ctypes.POINTER(FormCalibration)]),
     "dsa_choose_form": (_I, [ctypes.POINTER(FormQuery), ctypes.POINTER(FormCalibration),
                              ctypes.POINTER(FormEstimate)]),
@@ -393,6 +397,41 @@ def dsa_masked_mha_prefill_strided(q, k, v, key_mask, scale: float, k_pe=None, c
         d_qk, d_rope, d_v, float(scale), out.data_ptr(), lse.data_ptr(), _stream(stream, q.device)),
         "dsa_masked_mha_prefill_strided")
     return out, lse
+
+
+def dsa_kv_fp8_row_bytes(d_rope: int) -> int:
+    n = int(lib().dsa_kv_fp8_row_bytes(int(d_rope)))
+    if n < 0:
+        raise DSAError(DSA_ERR_UNSUPPORTED, "dsa_kv_fp8_row_bytes")
+    return n
+
+
+def dsa_kv_fp8_quantize(kv, d_rope: int = 64, out=None, stream=None):
+    """bf16 latent rows kv [N, ld_kv] (CUDA) to FP8 rows [N, dsa_kv_fp8_row_bytes(d_rope)] uint8."""
+    import torch
+    _need(kv, torch.bfloat16, "kv", 2)
+    N, ld = kv.shape
+    if out is None:
+        out = torch.empty((N, dsa_kv_fp8_row_bytes(d_rope)), dtype=torch.uint8, device=kv.device)
+    _need(out, torch.uint8, "out", 2)
+    _check(lib().dsa_kv_fp8_quantize(kv.data_ptr(), N, ld, int(d_rope), out.data_ptr(), _stream(stream, kv.device)),
+           "dsa_kv_fp8_quantize")
+    return out
+
+
+def dsa_kv_fp8_dequantize(fp8, d_rope: int = 64, out=None, stream=None):
+    """FP8 rows [N, row_bytes] uint8 (CUDA) to bf16 latent rows [N, 512 + d_rope] (or into out [N, ld_kv])."""
+    import torch
+    _need(fp8, torch.uint8, "fp8", 2)
+    N = fp8.shape[0]
+    if fp8.shape[1] != dsa_kv_fp8_row_bytes(d_rope):
+        raise ValueError("fp8 rows must be dsa_kv_fp8_row_bytes(d_rope) bytes wide")
+    if out is None:
+        out = torch.empty((N, 512 + d_rope), dtype=torch.bfloat16, device=fp8.device)
+    _need(out, torch.bfloat16, "out", 2)
+    _check(lib().dsa_kv_fp8_dequantize(fp8.data_ptr(), N, int(d_rope), out.data_ptr(), out.shape[1],
+                                       _stream(stream, fp8.device)), "dsa_kv_fp8_dequantize")
+    return out
 
 
 def dsa_form_calibration_default() -> FormCalibration:

@@ -22,7 +22,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB_SOURCES = ["dsa_api.cu", "sparse_prefill.cu", "union_build.cu", "key_mask.cu", "grouped_prefill.cu",
                "masked_mha.cu", "index_convert.cu", "dispatch.cu", "host_pipeline.cu",
-               "wait_probe.cu"]
+               "wait_probe.cu", "kv_fp8.cu"]
 SELFTEST_SOURCES = ["selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-use_fast_math", "-Xcompiler", "-fPIC", "-Xptxas", "-v",

@@ -391,6 +391,36 @@ int dsa_debug_trace(void* device_buffer, int capacity) {
   return DSA_OK;
 }
 
+int64_t dsa_kv_fp8_row_bytes(int d_rope) { return (d_rope == 0 || d_rope == 64) ? 528 + 2 * d_rope : -1; }
+
+static int kv_fp8_call(const uint16_t* kv, uint16_t* kv_out, uint8_t* fp8, const void* fp8_in, int N, int ld_kv,
+                       int d_rope, bool quantize, dsa_stream_t stream) {
+  if (N < 0 || ld_kv < 512 + d_rope || (ld_kv & 7) != 0) return DSA_ERR_INVALID_ARG;
+  if (d_rope != 0 && d_rope != 64) return DSA_ERR_UNSUPPORTED;
+  if (N == 0) return DSA_OK;
+  const void* bf = quantize ? (const void*)kv : (const void*)kv_out;
+  const void* f8 = quantize ? (const void*)fp8 : fp8_in;
+  if (!bf || !f8 || !aligned16(bf) || !aligned16(f8)) return DSA_ERR_INVALID_ARG;
+  DevInfo* d;
+  if (!dev_info(&d)) return DSA_ERR_CUDA;
+  dsa::Fp8KvArgs a;
+  a.kv = kv;
+  a.kv_out = kv_out;
+  a.fp8 = quantize ? fp8 : const_cast<uint8_t*>(static_cast<const uint8_t*>(fp8_in));
+  a.N = N;
+  a.ld_kv = ld_kv;
+  a.d_rope = d_rope;
+  return dsa::launch_kv_fp8(a, quantize, d->num_sms, (cudaStream_t)stream) == 0 ? DSA_OK : DSA_ERR_CUDA;
+}
+
+int dsa_kv_fp8_quantize(const uint16_t* kv, int N, int ld_kv, int d_rope, uint8_t* kv_fp8, dsa_stream_t stream) {
+  return kv_fp8_call(kv, nullptr, kv_fp8, nullptr, N, ld_kv, d_rope, true, stream);
+}
+
+int dsa_kv_fp8_dequantize(const uint8_t* kv_fp8, int N, int d_rope, uint16_t* kv, int ld_kv, dsa_stream_t stream) {
+  return kv_fp8_call(nullptr, kv, nullptr, kv_fp8, N, ld_kv, d_rope, false, stream);
+}
+
 int dsa_debug_wait_timeout(dsa_stream_t stream) {
   DevInfo* d;
   if (!dev_info(&d)) return DSA_ERR_CUDA;

@@ -51,6 +51,13 @@ struct UnionArgs {
   ReqTable req;
 };
 
+struct Fp8KvArgs {
+  const uint16_t* kv;   // quantize: bf16 rows [N, ld_kv]
+  uint16_t* kv_out;     // dequantize: bf16 rows [N, ld_kv]
+  uint8_t* fp8;         // FP8 rows [N, 528 + 2 d_rope] (quantize writes, dequantize reads)
+  int N, ld_kv, d_rope;
+};
+
 struct KeyMaskArgs {
   const int32_t* idx;   // [T, ld] global rows
   uint32_t* key_mask;   // [T, words]
@@ -130,5 +137,6 @@ int launch_local_to_global(const ConvertArgs& a, cudaStream_t stream);
 int launch_grouped_prefill(const GroupedArgs& a, int num_sms, cudaStream_t stream);
 int launch_masked_mha(const MaskedArgs& a, int num_sms, cudaStream_t stream);
 int launch_wait_timeout(unsigned int* err, cudaStream_t stream);
+int launch_kv_fp8(const Fp8KvArgs& a, bool quantize, int num_sms, cudaStream_t stream);
 
 }  // namespace dsa

@@ -294,6 +294,27 @@ int dsa_sparse_prefill_host(const uint16_t* q, const uint16_t* kv, int kv_on_hos
                             dsa_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * FP8 latent rows for the KV cache.  The pages keep the cache in bf16 (the
+ * grouped gate in "[Perf][DSA] Grouped sparse prefill ...", review
+ * snippets, refuses a quantized cache); an FP8 row here holds the 512 NoPE
+ * columns as float8 e4m3 with one fp32 scale per 128 of them, then the RoPE
+ * columns in bf16:
+ *     bytes [0, 512) codes | [512, 528) 4 scales | [528, 528 + 2 d_rope) RoPE
+ * (656 bytes per row at d_rope = 64, 528 for the NoPE layout; rows packed).
+ * Quantize: scale = block amax / 448 (1 for an all-zero block), code =
+ * e4m3(x / scale) with the division in IEEE float32 and round-to-nearest-even
+ * conversion saturating at 448.  Dequantize: e4m3 value times the block's
+ * scale in float32, rounded to bf16; the attention forms then run on the
+ * bf16 rows.
+ * kv: DEVICE bf16 [N, ld_kv], ld_kv >= 512 + d_rope and a multiple of 8;
+ * kv_fp8: DEVICE [N, dsa_kv_fp8_row_bytes(d_rope)]; both 16-byte aligned.
+ * d_rope in {0, 64}, else DSA_ERR_UNSUPPORTED.
+ * ---------------------------------------------------------------------- */
+int64_t dsa_kv_fp8_row_bytes(int d_rope);
+int dsa_kv_fp8_quantize(const uint16_t* kv, int N, int ld_kv, int d_rope, uint8_t* kv_fp8, dsa_stream_t stream);
+int dsa_kv_fp8_dequantize(const uint8_t* kv_fp8, int N, int d_rope, uint16_t* kv, int ld_kv, dsa_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Form choice (host only, no GPU call).  "[Perf][GLM-5.3-Flash] ...", commit
  * messages: prompts within the top-k budget run dense MHA, longer ones masked
  * MHA up to a length threshold (36k tokens at TP4, 64k at TP8) and the

@@ -147,6 +147,15 @@ def test_argument_validation_without_gpu(lib):
     assert hostcall(kv=None) == dsa.DSA_ERR_INVALID_ARG
     assert hostcall(H=24) == dsa.DSA_ERR_UNSUPPORTED
     assert hostcall(T=0) == dsa.DSA_OK
+    # FP8 rows: row width, RoPE width, row stride, alignment
+    assert lib.dsa_kv_fp8_row_bytes(64) == 656 and lib.dsa_kv_fp8_row_bytes(0) == 528
+    assert lib.dsa_kv_fp8_row_bytes(32) == -1
+    assert lib.dsa_kv_fp8_quantize(_vp(16), 10, 576, 32, _vp(16), None) == dsa.DSA_ERR_UNSUPPORTED
+    assert lib.dsa_kv_fp8_quantize(_vp(16), 10, 570, 64, _vp(16), None) == dsa.DSA_ERR_INVALID_ARG   # ld < 576
+    assert lib.dsa_kv_fp8_quantize(_vp(16), 10, 580, 64, _vp(16), None) == dsa.DSA_ERR_INVALID_ARG   # ld % 8
+    assert lib.dsa_kv_fp8_quantize(ctypes.c_void_p(8), 10, 576, 64, _vp(16), None) == dsa.DSA_ERR_INVALID_ARG
+    assert lib.dsa_kv_fp8_dequantize(None, 10, 64, _vp(16), 576, None) == dsa.DSA_ERR_INVALID_ARG
+    assert lib.dsa_kv_fp8_dequantize(_vp(16), 0, 64, _vp(16), 576, None) == dsa.DSA_OK
     # key mask: one-sided offsets are rejected
     assert lib.dsa_topk_to_key_mask(_vp(16), 8, 4, 4, cu, None, 2, _vp(16), 4, None) == dsa.DSA_ERR_INVALID_ARG
     # local -> physical rows: block size, table width, KV lengths, request offsets
