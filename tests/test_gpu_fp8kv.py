@@ -17,6 +17,11 @@ def _gpu():
     need_gpu()
 
 
+def bits(t):
+    """bf16 tensor -> its uint16 bit patterns (host numpy)."""
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
 def awkward_rows(rng, N, width):
     """bf16 rows with mixed magnitudes, an all-zero block, negative zeros and values far
     below their block's maximum (they round to zero or to subnormal codes)."""
@@ -43,7 +48,7 @@ def test_quantize_dequantize_bit_exact(d_rope, ld):
     # dequantize the oracle's rows (independent of the GPU quantizer)
     back = dsa.dsa_kv_fp8_dequantize(torch.from_numpy(want).cuda(), d_rope)
     torch.cuda.synchronize()
-    assert np.array_equal(back.cpu().numpy().view(np.uint16), O.kv_fp8_dequantize(want, d_rope))
+    assert np.array_equal(bits(back), O.kv_fp8_dequantize(want, d_rope))
 
 
 def test_dequantize_every_code():
@@ -60,7 +65,7 @@ def test_dequantize_every_code():
     rows[:, 528:] = (normal_bf16(rng, (N, 64)).astype("<u2")).view(np.uint8).reshape(N, 128)
     back = dsa.dsa_kv_fp8_dequantize(torch.from_numpy(rows).cuda(), 64)
     torch.cuda.synchronize()
-    assert np.array_equal(back.cpu().numpy().view(np.uint16), O.kv_fp8_dequantize(rows, 64))
+    assert np.array_equal(bits(back), O.kv_fp8_dequantize(rows, 64))
 
 
 def test_attention_over_fp8_cache():
@@ -80,7 +85,7 @@ def test_attention_over_fp8_cache():
     torch.cuda.synchronize()
     st, counts = dsa.dsa_last_device_error()
     assert st == 0, counts
-    assert np.array_equal(kv_deq.cpu().numpy().view(np.uint16), kv_deq_ref)
+    assert np.array_equal(bits(kv_deq), kv_deq_ref)
     ro, rl = O.sparse_prefill(x.q, kv_deq_ref, x.idx, w.k, w.scale, w.d_qk, w.d_v)
     for o, l in ((o1, l1), (o2, l2)):
         res = O.compare(f32(o), l.cpu().numpy().astype(np.float64), ro, rl)
@@ -96,4 +101,4 @@ def test_full_headline_table_bit_exact():
     back = dsa.dsa_kv_fp8_dequantize(got, 64)
     torch.cuda.synchronize()
     assert np.array_equal(got.cpu().numpy(), want)
-    assert np.array_equal(back.cpu().numpy().view(np.uint16), O.kv_fp8_dequantize(want, 64))
+    assert np.array_equal(bits(back), O.kv_fp8_dequantize(want, 64))
