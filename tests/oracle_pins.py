@@ -531,12 +531,110 @@ def pin_kv_fp8_round_trip(seed=14) -> bool:
     return ok
 
 
+# ----------------------------------------------------------------------------
+# the tolerance checker every parity test relies on
+# ----------------------------------------------------------------------------
+def _verdict(got_out, got_lse, ref_out, ref_lse):
+    return bool(O.compare(got_out, got_lse, ref_out, ref_lse)["ok"])
+
+
+def pin_compare_statistics() -> bool:
+    """Hand-worked statistics: out ref = (3, 4) (norm 5) against (3, 4.01):
+    max-abs 0.01, relative L2 0.01 / 5 = 0.002; lse ref (2, -inf, +inf) with
+    got (2.004, -inf, +inf): max-abs 0.004, relative L2 0.004 / 2 = 0.002."""
+    r = O.compare(np.array([3.0, 4.01]), np.array([2.004, -np.inf, np.inf]),
+                  np.array([3.0, 4.0]), np.array([2.0, -np.inf, np.inf]))
+    ok = bool(r["ok"]) and abs(r["out_max_abs"] - 0.01) < 1e-12 and abs(r["out_rel_l2"] - 0.002) < 1e-12
+    ok &= abs(r["lse_max_abs"] - 0.004) < 1e-12 and abs(r["lse_rel_l2"] - 0.002) < 1e-12
+    ok &= bool(r["lse_inf_match"]) and not r["nan"]
+    # identical inputs: every statistic zero
+    z = O.compare(np.ones((2, 3)), np.zeros(2), np.ones((2, 3)), np.zeros(2))
+    ok &= bool(z["ok"]) and z["out_max_abs"] == 0 and z["out_rel_l2"] == 0 and z["lse_max_abs"] == 0
+    # empty tensors pass
+    ok &= _verdict(np.zeros((0, 4, 8)), np.zeros((0, 4)), np.zeros((0, 4, 8)), np.zeros((0, 4)))
+    return ok
+
+
+def pin_compare_out_bounds() -> bool:
+    """Each out bound on its own, just inside and just outside.
+    rel-L2: ref = ones(10000) and got = ref (1 + e) give exactly e (the
+    difference over the norm of ref, not of got: at e = 0.00502 the ratio to
+    the norm of got would be 0.004995 and pass).  max-abs: one entry off by
+    0.019 / 0.021 in a 10^4-vector of ones (relative L2 0.0002)."""
+    n = 10000
+    ref = np.ones(n)
+    lse = np.zeros(4)
+    ok = _verdict(ref * (1 + 0.0049), lse, ref, lse)
+    ok &= not _verdict(ref * (1 + 0.00502), lse, ref, lse)
+    one = ref.copy()
+    one[123] += 0.019
+    ok &= _verdict(one, lse, ref, lse)
+    one[123] += 0.002
+    ok &= not _verdict(one, lse, ref, lse)
+    # all-zero reference: the plain norm of the difference is the measure
+    ok &= _verdict(np.full(4, 1e-3), lse, np.zeros(4), lse)
+    ok &= not _verdict(np.full(4, 3e-3), lse, np.zeros(4), lse)
+    return ok
+
+
+def pin_compare_lse_bounds() -> bool:
+    """The two lse bounds on their own, on the finite entries: ref 0.1 with
+    got 0.11 everywhere is within max-abs (0.01) but 10 % off in relative L2;
+    ref 100 with one of 1000 entries off by 0.03 is far within relative L2
+    (1e-5) but beyond max-abs.  A finite mismatch of 5 beside agreeing
+    infinities must fail."""
+    out = np.ones(8)
+    n = 1000
+    ok = not _verdict(out, np.full(n, 0.11), out, np.full(n, 0.1))
+    ok &= _verdict(out, np.full(n, 0.1 + 1e-4), out, np.full(n, 0.1))
+    big = np.full(n, 100.0)
+    g = big.copy()
+    g[7] += 0.03
+    ok &= not _verdict(out, g, out, big)
+    g[7] = 100.0 + 0.015
+    ok &= _verdict(out, g, out, big)
+    ref = np.array([-np.inf, 1.0, 2.0])
+    ok &= not _verdict(out, np.array([-np.inf, 6.0, 2.0]), out, ref)
+    return ok
+
+
+def pin_compare_infinities_and_nan() -> bool:
+    """lse infinities must coincide with their signs; a NaN anywhere, on
+    either side, fails; tensors of different shapes are an error, not a
+    broadcast."""
+    out = np.ones(4)
+    ref = np.array([-np.inf, 1.0])
+    ok = _verdict(out, np.array([-np.inf, 1.0]), out, ref)
+    ok &= not _verdict(out, np.array([0.0, 1.0]), out, ref)            # finite where ref is -inf
+    ok &= not _verdict(out, np.array([np.inf, 1.0]), out, ref)         # wrong sign
+    ok &= not _verdict(out, np.array([-np.inf, -np.inf]), out, ref)    # -inf where ref is finite
+    # NaN beside zeros: read as zero it would pass, so only NaN detection fails it
+    zo = np.zeros(4)
+    bad = zo.copy()
+    bad[2] = np.nan
+    zl = np.array([-np.inf, 0.0])
+    nl = np.array([-np.inf, np.nan])
+    ok &= _verdict(zo, zl, zo, zl)
+    ok &= not _verdict(bad, zl, zo, zl)
+    ok &= not _verdict(zo, nl, zo, zl)
+    ok &= not _verdict(zo, zl, bad, zl)
+    ok &= not _verdict(zo, zl, zo, nl)
+    try:
+        O.compare(np.ones((5, 1, 8)), np.zeros((5, 1)), np.ones((5, 3, 8)), np.zeros((5, 3)))
+        ok = False
+    except ValueError:
+        pass
+    return ok
+
+
 ALL_PINS = [pin_bruteforce, pin_single_key, pin_zero_query, pin_equal_keys, pin_two_keys_closed_form,
             pin_order_and_padding_invariance, pin_dense_causal_sdpa, pin_union_worked_example,
             pin_union_bruteforce, pin_union_popcounts, pin_grouped_equals_per_token,
             pin_key_mask_bruteforce, pin_masked_equals_sparse, pin_masked_dense_causal_sdpa,
             pin_local_to_global_paged_round_trip, pin_local_to_global_contiguous,
-            pin_e4m3_decode_closed_forms, pin_e4m3_encode_library, pin_kv_fp8_round_trip]
+            pin_e4m3_decode_closed_forms, pin_e4m3_encode_library, pin_kv_fp8_round_trip,
+            pin_compare_statistics, pin_compare_out_bounds, pin_compare_lse_bounds,
+            pin_compare_infinities_and_nan]
 
 
 def run_all_pins():

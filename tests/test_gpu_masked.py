@@ -69,7 +69,7 @@ def test_masked_all_tokens(q_lens, kv_lens, H, k):
 def test_masked_empty_rows_and_sparse_equivalence():
     """Tokens with an empty mask get out = 0, lse = -inf.  With every head's
     k/v equal to one shared latent row the masked form equals the per-token
-    sparse form of the same indices (spec invariant)."""
+    sparse form of the same indices (the masked form must reproduce the sparse gather semantics)."""
     rng = np.random.default_rng(3)
     T, N, H, k = 140, 260, 4, 40
     kv = normal_bf16(rng, (N, 192))

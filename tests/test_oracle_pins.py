@@ -166,6 +166,62 @@ def _fp8_scale_per_64(kv_bits, d_rope):
     return out
 
 
+_orig_compare = O.compare
+
+
+def _compare_rel_over_got(got_out, got_lse, ref_out, ref_lse, max_abs=2e-2, rel_l2=5e-3):
+    # relative L2 against the norm of the result instead of the reference
+    r = _orig_compare(got_out, got_lse, ref_out, ref_lse, max_abs, rel_l2)
+    go = np.asarray(got_out, dtype=np.float64)
+    d = np.abs(go - np.asarray(ref_out, dtype=np.float64))
+    den = float(np.sqrt((go ** 2).sum()))
+    r["out_rel_l2"] = float(np.sqrt((d ** 2).sum()) / den) if den > 0 else 0.0
+    r["ok"] = (not r["nan"]) and r["lse_inf_match"] and r["out_max_abs"] <= max_abs and \
+        r["out_rel_l2"] <= rel_l2 and r["lse_max_abs"] <= max_abs and r["lse_rel_l2"] <= rel_l2
+    return r
+
+
+def _compare_inf_always_same(got_out, got_lse, ref_out, ref_lse, max_abs=2e-2, rel_l2=5e-3):
+    gl = np.nan_to_num(np.asarray(got_lse, dtype=np.float64), posinf=0.0, neginf=0.0)
+    rl = np.nan_to_num(np.asarray(ref_lse, dtype=np.float64), posinf=0.0, neginf=0.0)
+    r = _orig_compare(got_out, np.where(np.isinf(got_lse), rl, gl), ref_out, rl, max_abs, rel_l2)
+    return r
+
+
+def _compare_ignores_lse_rel(got_out, got_lse, ref_out, ref_lse, max_abs=2e-2, rel_l2=5e-3):
+    r = _orig_compare(got_out, got_lse, ref_out, ref_lse, max_abs, rel_l2)
+    r["ok"] = (not r["nan"]) and r["lse_inf_match"] and r["out_max_abs"] <= max_abs and \
+        r["out_rel_l2"] <= rel_l2 and r["lse_max_abs"] <= max_abs
+    return r
+
+
+def _compare_ignores_out_max(got_out, got_lse, ref_out, ref_lse, max_abs=2e-2, rel_l2=5e-3):
+    r = _orig_compare(got_out, got_lse, ref_out, ref_lse, max_abs, rel_l2)
+    r["ok"] = (not r["nan"]) and r["lse_inf_match"] and r["out_rel_l2"] <= rel_l2 and \
+        r["lse_max_abs"] <= max_abs and r["lse_rel_l2"] <= rel_l2
+    return r
+
+
+def _compare_nan_blind(got_out, got_lse, ref_out, ref_lse, max_abs=2e-2, rel_l2=5e-3):
+    f = lambda a: np.nan_to_num(np.asarray(a, dtype=np.float64), nan=0.0, posinf=np.inf, neginf=-np.inf)
+    return _orig_compare(f(got_out), f(got_lse), f(ref_out), f(ref_lse), max_abs, rel_l2)
+
+
+def _compare_fin_masks_large(got_out, got_lse, ref_out, ref_lse, max_abs=2e-2, rel_l2=5e-3):
+    # finite lse entries that differ by more than 1 are dropped from the check
+    gl = np.asarray(got_lse, dtype=np.float64).copy()
+    rl = np.asarray(ref_lse, dtype=np.float64)
+    far = np.isfinite(gl) & np.isfinite(rl) & (np.abs(gl - rl) > 1.0)
+    gl[far] = rl[far]
+    return _orig_compare(got_out, gl, ref_out, rl, max_abs, rel_l2)
+
+
+def _compare_broadcasts(got_out, got_lse, ref_out, ref_lse, max_abs=2e-2, rel_l2=5e-3):
+    go, ro = np.broadcast_arrays(np.asarray(got_out, dtype=np.float64), np.asarray(ref_out, dtype=np.float64))
+    gl, rl = np.broadcast_arrays(np.asarray(got_lse, dtype=np.float64), np.asarray(ref_lse, dtype=np.float64))
+    return _orig_compare(go, gl, ro, rl, max_abs, rel_l2)
+
+
 MUTATIONS = [
     ("attend", _attend_lse_base2),
     ("attend", _attend_sign),
@@ -187,6 +243,13 @@ MUTATIONS = [
     ("e4m3_decode", _e4m3_bias8),
     ("e4m3_encode", _e4m3_ties_away),
     ("kv_fp8_quantize", _fp8_scale_per_64),
+    ("compare", _compare_rel_over_got),
+    ("compare", _compare_inf_always_same),
+    ("compare", _compare_ignores_lse_rel),
+    ("compare", _compare_ignores_out_max),
+    ("compare", _compare_nan_blind),
+    ("compare", _compare_fin_masks_large),
+    ("compare", _compare_broadcasts),
 ]
 
 
