@@ -10,6 +10,7 @@ there is no CPU fallback: without the built library every call raises.
 Forms (see the header for the exact contracts):
   dsa_sparse_prefill      per-token sparse attention over each token's top-k rows
   dsa_sparse_prefill_host the same from and to host memory, copies overlapped with the kernel
+  dsa_sparse_prefill_host_noalloc  the same without a workspace (fixed library scratch)
   dsa_union_build         sorted union per group + head-group membership mask
   dsa_grouped_prefill     G = 128/H tokens as 128 pseudo-heads over the union
   dsa_topk_to_key_mask    packed per-token key mask from the top-k rows
@@ -86,6 +87,8 @@ _SIGNATURES = {
     "dsa_sparse_prefill_host_plan": (_I, [_I, _I, _I, _I32P, _I, ctypes.POINTER(ctypes.c_int)]),
     "dsa_sparse_prefill_host": (_I, [_VP, _VP, _I, _I, _I, _VP, _I, _I, _I, _I, _I, _I, _F, _VP, _VP, _VP, _L, _I,
                                      _VP]),
+    "dsa_sparse_prefill_host_noalloc": (_I, [_VP, _VP, _I, _I, _I, _VP, _I, _I, _I, _I, _I, _I, _F, _VP, _VP, _I,
+                                             _VP]),
     "dsa_kv_fp8_row_bytes": (_L, [_I]),
     "dsa_kv_fp8_quantize": (_I, [_VP, _I, _I, _I, _VP, _VP]),
     "dsa_kv_fp8_dequantize": (_I, [_VP, _I, _I, _VP, _I, _VP]),
@@ -272,6 +275,36 @@ def dsa_sparse_prefill_host(q, kv, idx, k: int, scale: float, out, lse, workspac
                                          out.data_ptr(), lse.data_ptr(), workspace.data_ptr(), workspace.numel(),
                                          int(chunk_tokens), _stream(stream, workspace.device)),
            "dsa_sparse_prefill_host")
+    return out, lse
+
+
+HOST_NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def dsa_sparse_prefill_host_noalloc(q, kv, idx, k: int, scale: float, out, lse, chunk_tokens: int = 152,
+                                    stream=None):
+    """dsa_sparse_prefill_host for callers that cannot allocate device memory: the same
+    arguments without a workspace; the library's fixed 64 MiB device scratch holds the
+    chunks in flight.  Shapes whose buffers need more (dsa_sparse_prefill_host_workspace)
+    raise DSAError(DSA_ERR_UNSUPPORTED); lower chunk_tokens then.  Calls that overlap on
+    the GPU share the scratch and race: keep them on one stream."""
+    import torch
+    _host_tensor(q, torch.bfloat16, "q", 3)
+    _host_tensor(idx, torch.int32, "idx", 2)
+    _host_tensor(out, torch.bfloat16, "out", 3)
+    _host_tensor(lse, torch.float32, "lse", 2)
+    if kv.dtype != torch.bfloat16 or kv.dim() != 2 or not kv.is_contiguous():
+        raise TypeError("kv must be a contiguous 2-D bf16 tensor")
+    T, H, d_qk = q.shape
+    N, ld_kv = kv.shape
+    if idx.shape[0] != T or out.shape[0] != T or lse.shape != (T, H):
+        raise ValueError("q, idx, out and lse must cover the same tokens")
+    dev = kv.device if kv.is_cuda else torch.device("cuda", torch.cuda.current_device())
+    _check(lib().dsa_sparse_prefill_host_noalloc(q.data_ptr(), kv.data_ptr(), 0 if kv.is_cuda else 1, N, ld_kv,
+                                                 idx.data_ptr(), T, H, d_qk, out.shape[2], k, idx.shape[1],
+                                                 float(scale), out.data_ptr(), lse.data_ptr(), int(chunk_tokens),
+                                                 _stream(stream, dev)),
+           "dsa_sparse_prefill_host_noalloc")
     return out, lse
 
 

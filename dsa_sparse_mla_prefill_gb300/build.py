@@ -21,7 +21,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB_SOURCES = ["dsa_api.cu", "sparse_prefill.cu", "union_build.cu", "key_mask.cu", "grouped_prefill.cu",
-               "masked_mha.cu", "index_convert.cu", "dispatch.cu", "host_pipeline.cu",
+               "masked_mha.cu", "index_convert.cu", "dispatch.cu", "host_pipeline.cu", "host_noalloc.cu",
                "wait_probe.cu", "kv_fp8.cu"]
 SELFTEST_SOURCES = ["selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

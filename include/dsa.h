@@ -294,6 +294,41 @@ int dsa_sparse_prefill_host(const uint16_t* q, const uint16_t* kv, int kv_on_hos
                             dsa_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * dsa_sparse_prefill_host for callers that cannot give the library device
+ * memory (no counterpart on the pages; it exists for the deployment, not
+ * for the method).  Some host programs cannot call cudaMalloc for a
+ * workspace: their allocator has reserved the whole GPU up front, so a
+ * private allocation would fail, or their runtime forbids device
+ * allocation once it is serving.  This call takes no workspace: its buffer
+ * sets live in a fixed scratch array of DSA_HOST_NOALLOC_SCRATCH_BYTES
+ * (64 MiB) that belongs to the library's device image, held on every GPU
+ * where the library's device code is loaded until the process exits.  The
+ * call allocates and frees nothing.
+ *
+ * Arguments, results and errors as dsa_sparse_prefill_host (out and lse are
+ * bit for bit the same), with one more error: DSA_ERR_UNSUPPORTED when
+ * dsa_sparse_prefill_host_workspace(...) for these arguments exceeds
+ * DSA_HOST_NOALLOC_SCRATCH_BYTES; a smaller chunk_tokens, or kv already in
+ * device memory, needs less (the 16384-token, H = 32, top-2048 chunk fits
+ * with chunk_tokens = 152 and kv on the host).
+ *
+ * - Set-up: the first call on a device looks up the scratch array's device
+ *   address with that device current (and creates the library's copy
+ *   streams, as dsa_sparse_prefill_host does); make that first call before
+ *   any stream capture.
+ * - Every call on a device shares the one array, which keeps whatever the
+ *   last call left there; nothing in it needs to start at zero, since each
+ *   call writes every byte it reads.  Calls whose work overlaps on the GPU
+ *   (different streams, or several host threads) race on the array: order
+ *   them on one stream.
+ * ---------------------------------------------------------------------- */
+#define DSA_HOST_NOALLOC_SCRATCH_BYTES (64ull << 20)
+
+int dsa_sparse_prefill_host_noalloc(const uint16_t* q, const uint16_t* kv, int kv_on_host, int N, int ld_kv,
+                                    const int32_t* idx, int T, int H, int d_qk, int d_v, int k, int ld, float scale,
+                                    uint16_t* out, float* lse, int chunk_tokens, dsa_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * FP8 latent rows for the KV cache.  The pages keep the cache in bf16 (the
  * grouped gate in "[Perf][DSA] Grouped sparse prefill ...", review
  * snippets, refuses a quantized cache); an FP8 row here holds the 512 NoPE
