@@ -437,6 +437,15 @@ def run_modes(dev, stream, peaks, steps, warmup, flush, only=None):
 # ----------------------------------------------------------------------------
 # arms
 # ----------------------------------------------------------------------------
+def headline_config(w, x, world):
+    """The workload description both arms print (same keys, same values)."""
+    return {"workload": w.name, "T": w.T, "N": w.N, "H": w.H, "d_qk": w.d_qk, "d_v": w.d_v, "k": w.k,
+            "ld": w.ld, "index_gen": "locality (8-token blocks, 2048 base + 352-position shared pool)",
+            "valid_pairs": int((x.idx[:, :w.k] >= 0).sum()),
+            "l2": "flushed before every timed step (256 MiB write, outside the events)",
+            "parallelism": f"replica per GPU x{world}"}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -472,7 +481,8 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     step = lambda: dsa.dsa_sparse_prefill(q, kv, idx, w.k, w.scale, out=out, lse=lse)
 
-    # correctness guard on a few tokens (oracle, rank 0) before timing
+    # one untimed step first: the device error counters must be clean (no
+    # out-of-range index, no bounded wait that ran out) before anything is timed
     step()
     torch.cuda.synchronize()
     st, counts = dsa.dsa_last_device_error()
@@ -530,6 +540,16 @@ def run_ours(args):
     h2d = hq.numel() * 2 + hkv.numel() * 2 + hidx.numel() * 4
     d2h = hout.numel() * 2 + hlse.numel() * 4
     e2e_ms = max_over_ranks(e2e_ms, dist, dev)
+    # the copy engines alone on the same pinned buffers: one host -> device copy
+    # of q and one device -> host copy of out per step (what bounds the e2e step
+    # when the kernel is shorter than its copies)
+    dq = torch.empty(hq.shape, dtype=hq.dtype, device=dev)
+    dout = torch.empty(hout.shape, dtype=hout.dtype, device=dev)
+    h2d_ms = statistics.median(timed_steps(lambda: dq.copy_(hq, non_blocking=True), 5, 2, stream))
+    d2h_ms = statistics.median(timed_steps(lambda: hout.copy_(dout, non_blocking=True), 5, 2, stream))
+    h2d_gbs = hq.numel() * 2 / h2d_ms / 1e6
+    d2h_gbs = hout.numel() * 2 / d2h_ms / 1e6
+    del dq, dout
 
     log(f"e2e: {e2e_ms:.3f} ms/step")
     src_hash = kernel_source_hash(["sparse_prefill.cu", "dsa_device.cuh"])
@@ -539,29 +559,49 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "query-tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "T": w.T, "N": w.N, "H": w.H, "d_qk": w.d_qk, "d_v": w.d_v, "k": w.k,
-                   "ld": w.ld, "index_gen": "locality (8-token blocks, 2048 base + 352-position shared pool)",
-                   "valid_pairs": pairs, "l2": "flushed before every timed step (256 MiB write, outside the events)",
-                   "parallelism": f"replica per GPU x{world}"},
+        "config": headline_config(w, x, world),
         "useful_tflops": world * flops / (ms_step / 1e3) / 1e12,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "basis": "logical bytes: every selected row once per token (the form's defining re-gather) "
+                              "+ q, out, indices, lse, over the kernel time; the 18.9 MB KV table stays in the "
+                              "L2, so DRAM carries only `traffic` of it and the kernel is bound by its gather "
+                              "issue rate, not by DRAM",
+                     "dram_gbs": (traffic / (ms_step / 1e3) / 1e9) if traffic else None,
                      "kernel": "dsa::sparse::sparse_prefill_kernel<32,9>",
                      "algorithmic_bytes": abytes, "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)"},
         "hot_l2": {"ms_per_step": hot_ms, "value": job_throughput(w.T, world, hot_ms), "unit": "query-tokens/s",
                    "l2": "not flushed between steps"},
         "e2e": {"value": job_throughput(w.T, world, e2e_ms), "unit": "query-tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "call": "dsa_sparse_prefill_host",
-                "chunk_tokens": chunk},
+                "chunk_tokens": chunk, "kernel_ms": ms_step,
+                "h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs,
+                "copy_floor_ms": max(h2d / h2d_gbs, d2h / d2h_gbs) / 1e6,
+                "note": "copy floor = the larger direction's bytes at the rate measured for one plain copy of "
+                        "the same pinned buffers; the step cannot be shorter than it or than the kernel"},
         "gpu_launches": args.steps,
         "clocks": clocks.summary(),
     }
     if rank == 0 and not args.no_modes:
         del hq, hkv, hidx, hout, hlse, ws
         try:
-            line["modes"] = run_modes(dev, stream, peaks, args.steps, args.warmup, flush)
+            modes = run_modes(dev, stream, peaks, args.steps, args.warmup, flush)
         except Exception as e:  # report, never hide the headline
-            line["modes"] = {"error": repr(e)}
+            modes = {"error": repr(e)}
+        # the grouped form on its own workload (21504 queries after 11264
+        # cached rows, H = 16, G = 8) as a top-level key, ahead of `modes`
+        g = modes.get("grouped_21k_of_32k", {})
+        if "grouped" in g and "union_build" in g:
+            grouped = {"workload": "grouped_21k_of_32k", "ms": g["grouped"].get("ms"),
+                       "union_build_ms": g["union_build"]["ms"],
+                       "with_union_build_ms": g["grouped"].get("with_union_build_ms"),
+                       "union_plus_useful_tflops": g["grouped"].get("union_plus_useful_tflops"),
+                       "tensor_frac": g["grouped"].get("tensor_frac"),
+                       "peak_tflops": peaks["bf16_tflops"], "union_mean": g.get("union_mean")}
+            keys = list(line)
+            at = keys.index("roofline") + 1
+            line = {k: line[k] for k in keys[:at]} | {"grouped": grouped} | {k: line[k] for k in keys[at:]}
+        line["modes"] = modes
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         log("cpu baseline")
         line["cpu_baseline"] = cpu_baseline(w, x, budget_s=args.cpu_budget, pool=pool, cores=cores)
@@ -574,8 +614,41 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def _attach_shared(spec):
+    """Views of the arrays the parent placed in shared memory (name, shape, dtype)."""
+    from multiprocessing import shared_memory
+    global _SHM
+    _SHM = []
+    out = []
+    for name, shape, dtype in spec:
+        shm = shared_memory.SharedMemory(name=name)
+        _SHM.append(shm)
+        out.append(np.ndarray(shape, dtype=dtype, buffer=shm.buf))
+    return out
+
+
+def _oracle_pass_worker(args):
+    """The oracle over the tokens [lo, hi) of the shared workload, 16 per call.
+    Returns the seconds it took."""
+    spec, lo, hi, k, scale, d_qk, d_v = args
+    q, kv, idx = _attach_shared(spec)
+    from oracle.dsa_oracle import sparse_prefill
+    t0 = time.perf_counter()
+    for s in range(lo, hi, 16):
+        e = min(hi, s + 16)
+        sparse_prefill(q[s:e], kv, idx[s:e], k, scale, d_qk, d_v)
+    return time.perf_counter() - t0
+
+
 def run_reference(args):
-    """The oracle timed on the host cores on the headline workload; rank 0 only."""
+    """The oracle, as it stands, timed on the host cores on the headline
+    workload (rank 0 only; the other ranks exit).  The inputs sit in shared
+    memory; each timed step is one pass of all cores over the same tokens: the
+    whole 16384-token chunk when K such passes (and W warm-up passes over a
+    quarter of it) fit in about five minutes, else a fixed share of it spread
+    over the chunk (stated in the line).  ms_per_step is
+    the measured wall time of a step; value = tokens per step / that time."""
+    from multiprocessing import shared_memory
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -584,25 +657,62 @@ def run_reference(args):
     w = WORKLOADS[HEADLINE]
     x = make_sparse_inputs(w)
     cores = os.cpu_count() or 1
+    shms, spec = [], []
+    for a in (x.q, x.kv, x.idx):
+        a = np.ascontiguousarray(a)
+        shm = shared_memory.SharedMemory(create=True, size=max(1, a.nbytes))
+        np.ndarray(a.shape, dtype=a.dtype, buffer=shm.buf)[...] = a
+        shms.append(shm)
+        spec.append((shm.name, a.shape, a.dtype.str))
     pool = oracle_pool(cores)
-    budget = max(2.0, min(args.cpu_budget, 150.0 / max(1, args.steps + args.warmup)))
-    for _ in range(args.warmup):
-        cpu_baseline(w, x, budget_s=budget / 4, pool=pool, cores=cores)
-    vals, secs, samples = [], [], []
-    for _ in range(args.steps):
-        r = cpu_baseline(w, x, budget_s=budget, pool=pool, cores=cores)
-        vals.append(r["value"])
-        secs.append(r["seconds"])
-        samples.append(r["sample"])
-    pool.close()
-    pool.join()
-    value = statistics.mean(vals)
+    try:
+        def one_pass(n):
+            # core c takes n / cores consecutive tokens starting at its
+            # c / cores point of the chunk: the whole chunk when n = T, else
+            # equal ranges spread over the chunk (early and late positions)
+            width = -(-n // cores)
+            tasks = []
+            for c in range(cores):
+                lo = w.T * c // cores
+                hi = min(lo + width, w.T * (c + 1) // cores)
+                if hi > lo:
+                    tasks.append((spec, lo, hi, w.k, w.scale, w.d_qk, w.d_v))
+            t0 = time.perf_counter()
+            pool.map(_oracle_pass_worker, tasks)
+            return time.perf_counter() - t0, sum(t[2] - t[1] for t in tasks)
+
+        # rate estimate from a small pass, then the largest share that fits
+        est_s, est_n = one_pass(min(w.T, 32 * cores))
+        per_token = est_s / est_n
+        # warm-up passes take a quarter of the step's tokens; the K timed
+        # passes and the warm-up together stay within about five minutes
+        budget = 300.0 / max(1, args.steps + args.warmup / 4)
+        n = w.T if per_token * w.T <= budget else max(16 * cores, int(budget / per_token) // (16 * cores) * 16 * cores)
+        for _ in range(args.warmup):
+            one_pass(max(cores, n // 4))
+        secs = []
+        for _ in range(args.steps):
+            sec, done = one_pass(n)
+            secs.append(sec)
+    finally:
+        pool.close()
+        pool.join()
+        for shm in shms:
+            shm.close()
+            shm.unlink()
+    step_s = statistics.mean(secs)
+    value = done / step_s
+    full = done == w.T
+    sample = (f"{'all' if full else 'a share of'} {done} of {w.T} tokens of {w.name} per step "
+              f"({'one whole pass' if full else 'contiguous ranges spread over the chunk'}), fp64 numpy oracle in "
+              f"batches of 16, {cores} spawn workers x 1 BLAS thread, inputs in shared memory; "
+              f"{args.steps} timed passes of {step_s:.2f} s")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "query-tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": w.T / value * 1e3,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "T": w.T, "N": w.N, "H": w.H, "d_qk": w.d_qk, "d_v": w.d_v, "k": w.k},
+            "config": headline_config(w, x, world),
             "cpu_baseline": {"value": value, "unit": "query-tokens/s", "cores": cores, "kind": "oracle",
-                             "sample": samples[-1]},
+                             "sample": sample},
             "e2e": {"value": value, "unit": "query-tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
     print(json.dumps(line), flush=True)

@@ -251,19 +251,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// The same gather delivered to every CTA of the cluster named in cta_mask,
-// at the same shared-memory offset, each completing on its own barrier at
-// the offset of `bar`.
-__device__ __forceinline__ void tma_gather4_mc(uint32_t dst, const CUtensorMap* map, int x, int r0, int r1, int r2,
-                                               int r3, uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.multicast::cluster "
-      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar)),
-      "h"(cta_mask)
-      : "memory");
-}
-
 // TMA tiled 2-D load of one box (columns x .. x+63, rows y .. y+box-1).
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
   asm volatile(
@@ -273,16 +260,82 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// The same tiled load delivered to every CTA of the cluster named in
-// cta_mask, at the same shared-memory offset, each completing on its own
-// barrier at the offset of `bar`.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
-                                               uint16_t cta_mask) {
+// ---------------------------------------------------------------------------
+// CTA pairs (cta_group::2).  Two CTAs of a cluster (ranks 2i, 2i+1) act as
+// one: a pair MMA issued by one thread of the even CTA computes an M = 256
+// tile whose A rows 0-127 and B columns 0..N/2-1 come from the even CTA's
+// shared memory and A rows 128-255 and B columns N/2..N-1 from the odd
+// CTA's (same offsets), and writes D rows 0-127 to the even CTA's tensor
+// memory and rows 128-255 to the odd CTA's (same address).  Every tcgen05
+// instruction of such a kernel uses cta_group::2; allocation, relinquish and
+// deallocation are executed by one warp of each CTA of the pair.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Four accumulating pair MMAs (see mma_bf16_ss_x4): A and B descriptors
+// address the same offsets in both CTAs' shared memory.
+__device__ __forceinline__ void mma_pair_bf16_ss_x4(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t da,
+                                                    uint32_t db, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
-      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(cta_mask)
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %5, %6, %3, 1;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %7, %8, %3, 1;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %9, %10, %3, 1;\n\t}"
+      ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "l"(a + da), "l"(b + db), "l"(a + 2ull * da),
+      "l"(b + 2ull * db), "l"(a + 3ull * da), "l"(b + 3ull * db)
       : "memory");
+}
+
+// One arrival on the barrier at the offset of `bar` in every CTA of
+// cta_mask once every pair tcgen05 op issued so far by this thread has
+// completed (the completion signal; no data moves).
+__device__ __forceinline__ void mma_pair_commit(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+
+// TMA loads into this CTA's own shared memory whose bytes complete on a
+// barrier of either CTA of the pair (`bar_cluster`: a shared::cluster
+// address, e.g. map_peer(smem_u32(bar), 0) for the even CTA's barrier), so
+// that the pair's MMA issuer learns of both CTAs' operands on one barrier.
+__device__ __forceinline__ void tma_gather4_pair(uint32_t dst, const CUtensorMap* map, int x, int r0, int r1, int r2,
+                                                 int r3, uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.cta_group::2 "
+      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar_cluster)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                                 uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
+      : "memory");
+}
+
+// Arrive-and-expect on a barrier given by its shared::cluster address (a
+// barrier of this CTA or of the peer).
+__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t bar_cluster, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(bar_cluster),
+               "r"(bytes)
+               : "memory");
 }
 
 // Bounded wait that ignores the CTA abort flag: used on the way out to let

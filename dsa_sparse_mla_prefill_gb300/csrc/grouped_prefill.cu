@@ -10,12 +10,12 @@
 //
 // A group is processed by a cluster of two CTAs that split the pseudo-heads:
 // CTA r owns pseudo-heads 64r .. 64r+63 (its q rows: 64 x D_QK) and the
-// matching 64 columns of the output.  Every union row is
-// fetched once per cluster: each CTA issues the tile::gather4 loads for half
-// of a tile's rows with cluster multicast, so both CTAs receive the whole
-// tile, and a stage is refilled only after both CTAs' MMAs released it
-// (tcgen05.commit multicast to both CTAs' barriers).  No scores cross the
-// cluster.  Within a CTA the data path is the per-token one with 64 heads:
+// matching 64 columns of the output.  Each CTA gathers every union row of
+// the group into its own shared memory (plain tile::gather4 loads, no
+// multicast) and releases each stage with its own MMA commit; the pair shares
+// nothing but the group, whose rows the two CTAs read from L2 at the same
+// time.  No scores cross the cluster.  Within a CTA the data path is the
+// per-token one with 64 heads:
 //   S^T = K q^T with the union slots on the M side (M = 128 slots, N = 64),
 //   streamed chunk by chunk through a K ring whose stages hold a K chunk
 //   (128 slots x 64 columns) and the matching q chunk (64 rows x 64
@@ -46,7 +46,6 @@ constexpr int REGS_SOFTMAX = 144;
 constexpr int REGS_OTHER = 48;   // 8*32*144 + 16*32*48 <= 768*80
 constexpr int NKW = 6;           // K producer warps (one per K stage)
 constexpr int NVR = 2;           // V ring slots: unit m in slot m mod 2, PV issuer m mod 2
-constexpr uint16_t kPair = 3;    // multicast mask: both CTAs of the cluster
 constexpr float kTau = 8.0f;     // lazy-rescale threshold (log2 units)
 
 template <int NC>
@@ -99,9 +98,9 @@ enum {
   B_DRAIN = 10,      // [4] one per MMA issuer
   B_SMX_SYNC = 14,   // [2] one per head half (4 warps)
   B_KR_FULL = 16,    // [NKR <= 6]
-  B_KR_EMPTY = 22,   // [NKR <= 6] one QK commit from each CTA
+  B_KR_EMPTY = 22,   // [NKR <= 6] one QK commit
   B_VR_FULL = 28,    // [NVR]
-  B_VR_EMPTY = 30,   // [NVR] one PV commit from each CTA
+  B_VR_EMPTY = 30,   // [NVR] one PV commit
 };
 static_assert(NVR <= 2, "barrier layout");
 
@@ -197,11 +196,11 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
     for (int i = 0; i < 4; ++i) mbar_init(&bars[B_DRAIN + i], 1);
     for (int i = 0; i < C::NKR; ++i) {
       mbar_init(&bars[B_KR_FULL + i], 1);
-      mbar_init(&bars[B_KR_EMPTY + i], 2);
+      mbar_init(&bars[B_KR_EMPTY + i], 1);
     }
     for (int i = 0; i < NVR; ++i) {
       mbar_init(&bars[B_VR_FULL + i], 1);
-      mbar_init(&bars[B_VR_EMPTY + i], 2);
+      mbar_init(&bars[B_VR_EMPTY + i], 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -212,7 +211,7 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // the peer's barriers exist before any copy or commit reaches them
+  cluster_sync();  // both CTAs of the pair start together
   tc_fence_after();
   const uint32_t tmem = *tmem_base_ptr;
 
@@ -221,37 +220,39 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
     if (warp >= 12) {
       // ----------------------------------------------------------------
       // TMA producers.  K stream (warps 12-17): a stage holds K chunk c of a
-      // tile (slots x columns 64c .. 64c+63) plus q chunk c of this CTA's 64
-      // pseudo-heads; requests 0-15 gather this CTA's 16 row groups (slots
-      // 64 rank .. +63) for both CTAs, request 16 loads the local q chunk.
-      // OWNED: warp 12+s fills stage s with every chunk that maps there,
-      // lanes 0-16 issuing (a warp's per-stage loop of wait, arm and issue
-      // costs several hundred cycles, so stages are filled side by side);
-      // otherwise all six warps take part in every stage, lanes 0-2 of each.
-      // V stream (warps 18-23): the
-      // 128-column units m of every tile go to V slot m mod 2; all six
-      // warps take part in every unit, lanes 0-5 of each sharing this CTA's
-      // 32 gathers (a unit's refill sits on the P.V critical path twice per
+      // tile (128 slots x columns 64c .. 64c+63) plus q chunk c of this CTA's
+      // 64 pseudo-heads; requests 0-31 gather the tile's 32 row groups of 4
+      // slots, request 32 loads the q chunk.  OWNED: warp 12+s fills stage s
+      // with every chunk that maps there, lane l gathering row group l and
+      // lane 0 also loading q (a warp's per-stage loop of wait, arm and
+      // issue costs several hundred cycles, so stages are filled side by
+      // side); otherwise all six warps take part in every stage, lanes 0-5
+      // of each.  V stream (warps 18-23): the 128-column units m of every
+      // tile go to V slot m mod 2; all six warps take part in every unit,
+      // lanes 0-10 of each sharing its 64 gathers (32 row groups x 2 swizzle
+      // columns; a unit's refill sits on the P.V critical path twice per
       // tile, so its issue time matters).
-      // When this CTA's 64 slots of the tile are one contiguous run of rows,
-      // each of its 64-row halves is one tiled load (box 64 columns x 64
-      // rows) instead of 16 gathers.  The union lists distinct rows in
-      // ascending order, so the run test needs only the two end slots.
-      // A stage's leader (lane 0 of its K warp, or of warp 12, and of the
-      // group's first warp for V) arms the full byte count of the stage: both CTAs' halves land in
-      // both.  Every warp of a slot passes through each of its phases in
-      // order.
+      // When a 64-slot half of the tile is one contiguous run of rows, the
+      // half is one tiled load (box 64 columns x 64 rows) instead of 16
+      // gathers.  The union lists distinct rows in ascending order, so the
+      // run test needs only the half's two end slots.
+      // A stage's leader (lane 0 of its K warp, or of warp 12, and of warp
+      // 18 for V) arms the full byte count of the stage.  Every warp of a
+      // slot passes through each of its phases in order.
       // ----------------------------------------------------------------
       const bool kstream = warp < 18;
       const int kw = warp - 12;                 // K stage owned (OWNED; none past the ring)
-      // K request of this lane: 0-15 gathers, 16 the q chunk
-      const int kreq = C::OWNED ? lane : kw * 3 + (lane < 3 ? lane : 32);
-      // V: all six warps take part in every unit, lanes 0-5 of each
-      const int e = (warp - 18) * 6 + (lane < 6 ? lane : 32);   // V gather index 0..31 of this CTA
-      const bool issuer = kstream ? (kreq < 17) : (e < 32);
-      const bool kgather = kstream && kreq < 16;
-      const int rg = 16 * rank + (kstream ? (kreq & 15) : (e & 15));   // row group of the tile
-      const int vcc = (e >> 4) & 1;             // V swizzle column
+      // K request of this lane: 0-31 gathers, 32 the q chunk (OWNED: lane 0
+      // issues its gather and the q chunk)
+      const int kreq = C::OWNED ? lane : kw * 6 + (lane < 6 ? lane : 64);
+      const bool kq = kstream && (C::OWNED ? lane == 0 : kreq == 32);
+      // V: all six warps take part in every unit, lanes 0-10 of each
+      const int e = (warp - 18) * 11 + (lane < 11 ? lane : 64);   // V gather index 0..63
+      const bool issuer = kstream ? (kreq < 33) : (e < 64);
+      const bool kgather = kstream && kreq < 32;
+      const int rg = kstream ? (kreq & 31) : (e & 31);   // row group of the tile
+      const int hf = rg >> 4;                            // its 64-slot half
+      const int vcc = (e >> 5) & 1;             // V swizzle column
       const bool leader = (lane == 0) && (kstream ? (C::OWNED || kw == 0) : warp == 18);
       uint32_t gt = 0, pos = 0;
       int64_t last_armed = -1;
@@ -265,15 +266,16 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
         const int32_t* urow = a.union_idx + (size_t)g * a.union_pad;
         for (int j = 0; j < ntiles && ok; ++j, ++gt) {
           if (warp == 12 && lane == 0) DSA_TRACE(a.tr, gt, 0);
-          const int u0 = j * BK + HC * rank;   // this CTA's 64 slots of the tile
+          const int u0 = j * BK + 64 * hf;     // this lane's 64-slot half of the tile
           int first = -1;
           bool run = false;
-          if (u0 + HC - 1 < U) {
+          if (u0 + 63 < U) {
             first = __ldg(urow + u0);
-            const int last = __ldg(urow + u0 + HC - 1);
-            run = first >= 0 && last < a.N && last - first == HC - 1;
+            const int last = __ldg(urow + u0 + 63);
+            run = first >= 0 && last < a.N && last - first == 63;
           }
-          const uint32_t half_off = (uint32_t)rank * (C::CHUNK_BYTES / 2);
+          const uint32_t half_off = (uint32_t)hf * (C::CHUNK_BYTES / 2);
+          const bool run_lead = (rg & 15) == 0;   // issues the half's tiled load
           if (kstream) {
             const int4 r = (kgather && !run) ? union_rows4(urow, U, a.N, j * BK + 4 * rg) : make_int4(-1, -1, -1, -1);
             for (int c = 0; c < NC; ++c, ++pos) {
@@ -285,13 +287,14 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
               }
               const uint32_t stage = sbase + C::OFF_KR + ks * C::KSTAGE_BYTES;
               if (leader) mbar_arrive_expect_tx(&bars[B_KR_FULL + ks], C::KSTAGE_BYTES);
-              if (run) {
-                if (kreq == 0)
-                  tma_load_2d_mc(stage + half_off, &a.tmap_kv_blk, c * 64, first, &bars[B_KR_FULL + ks], kPair);
-              } else if (kgather) {
-                tma_gather4_mc(stage + rg * 512, &a.tmap_kv, c * 64, r.x, r.y, r.z, r.w, &bars[B_KR_FULL + ks], kPair);
+              if (kgather) {
+                if (run) {
+                  if (run_lead) tma_load_2d(stage + half_off, &a.tmap_kv_blk, c * 64, first, &bars[B_KR_FULL + ks]);
+                } else {
+                  tma_gather4(stage + rg * 512, &a.tmap_kv, c * 64, r.x, r.y, r.z, r.w, &bars[B_KR_FULL + ks]);
+                }
               }
-              if (issuer && !kgather)
+              if (kq)
                 // q rows t0*H + 64 rank .. +63 of q viewed [T*H, D_QK], columns 64c ..
                 tma_load_2d(stage + C::CHUNK_BYTES, &a.tmap_q, c * 64, t0 * H + HC * rank, &bars[B_KR_FULL + ks]);
               last_armed = pos;
@@ -307,12 +310,11 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
               if (leader) mbar_arrive_expect_tx(&bars[B_VR_FULL + vg], C::UNIT_BYTES);
               const uint32_t vdst = sbase + C::OFF_VR + vg * C::UNIT_BYTES + vcc * C::CHUNK_BYTES;
               if (run) {
-                if (issuer && (e & 15) == 0)
-                  tma_load_2d_mc(vdst + half_off, &a.tmap_kv_blk, (2 * m + vcc) * 64, first, &bars[B_VR_FULL + vg],
-                                 kPair);
+                if (issuer && run_lead)
+                  tma_load_2d(vdst + half_off, &a.tmap_kv_blk, (2 * m + vcc) * 64, first, &bars[B_VR_FULL + vg]);
               } else if (issuer) {
-                tma_gather4_mc(vdst + rg * 512, &a.tmap_kv, (2 * m + vcc) * 64, r.x, r.y, r.z, r.w,
-                               &bars[B_VR_FULL + vg], kPair);
+                tma_gather4(vdst + rg * 512, &a.tmap_kv, (2 * m + vcc) * 64, r.x, r.y, r.z, r.w,
+                            &bars[B_VR_FULL + vg]);
               }
               last_armed = pos;
             }
@@ -321,7 +323,7 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
       }
       // Let copies still in flight land before the CTA can exit: the last
       // phase of every stage this warp's leader armed completes only once
-      // both CTAs' bytes have landed here.
+      // all of its bytes have landed.
       if (leader && last_armed >= 0) {
         if (kstream) {
           // the last phase of every stage this leader armed
@@ -342,8 +344,8 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
       // belongs to one of them), each summing into its own partial S^T; the
       // softmax adds the two.  One thread issuing every chunk spends most of
       // its time in the per-chunk wait, fence and commit, not in MMAs.
-      // Each K chunk is released to both CTAs' producers once its MMAs
-      // complete; S_FULL takes one commit from each issuer.
+      // Each K chunk is released to the producers once its MMAs complete;
+      // S_FULL takes one commit from each issuer.
       // ----------------------------------------------------------------
       const uint32_t qa = warp == 8 ? 0u : 1u;
       if (lane == 0) {
@@ -369,7 +371,7 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
               const uint32_t stage = sbase + C::OFF_KR + slot * C::KSTAGE_BYTES;
               mma_bf16_ss_x4(d_s, sdesc_sw128(stage, 16, 1024), sdesc_sw128(stage + C::CHUNK_BYTES, 16, 1024), 2u, 2u,
                              IDESC_QK, first ? 0u : 1u);
-              mma_commit_mc(&bars[B_KR_EMPTY + slot], kPair);
+              mma_commit(&bars[B_KR_EMPTY + slot]);
               first = false;
             }
             if (!ok) break;
@@ -384,8 +386,8 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
     } else if (warp == 9 || warp == 10) {
       // ----------------------------------------------------------------
       // PV issuers: O^T += V^T P^T, warp 9 for units 0 and 2, warp 10 for
-      // units 1 and 3 (V slot = unit mod 2); each unit released to both
-      // CTAs' producers once its MMAs complete
+      // units 1 and 3 (V slot = unit mod 2); each unit released to the
+      // producers once its MMAs complete
       // ----------------------------------------------------------------
       const int pvi = warp - 9;
       if (lane == 0) {
@@ -422,7 +424,7 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
                 const uint64_t bdesc = sdesc_sw128(p_base + pb * C::P_BYTES + hf * (HC * 128), 16, 1024);
                 mma_bf16_ss_x4(d_o, adesc, bdesc, 128u, 2u, IDESC_PV, (j > 0 || hf > 0) ? 1u : 0u);
               }
-              mma_commit_mc(&bars[B_VR_EMPTY + pvi], kPair);
+              mma_commit(&bars[B_VR_EMPTY + pvi]);
             }
             if (!ok) break;
             mma_commit(&bars[B_P_EMPTY + pb]);

@@ -94,6 +94,31 @@ def test_grouped_full_size_sampled(name):
     assert res["ok"], res
 
 
+@pytest.mark.parametrize("name,index_gen", [("v32_h32_16k", None), ("grouped_21k_of_32k", "locality_wide")])
+def test_grouped_full_size_bench_launches(name, index_gen):
+    """The grouped launches the bench times beyond the two above: the 16384-token
+    H = 32 chunk as groups of G = 4 (union ~2.2k per group), and the wide-union
+    stress variant of the 21504-token workload (every token draws its own
+    replacements, union ~4.3k per group).  Union list, lengths and mask bit-exact
+    over the whole buffers; sampled tokens against the per-token oracle."""
+    w = WORKLOADS[name]
+    if index_gen is not None:
+        w = dataclasses.replace(w, name=name + "_wide", index_gen=index_gen)
+    x = make_sparse_inputs(w)
+    (u, ul, m), o, l = run_grouped(x.q, x.kv, x.idx, w.k, w.G, w.N, x.cu_seqlens_q, w.scale)
+    upad = O.union_pad(w.G, w.k, 128)
+    ru, rl, rm = O.union_build(x.idx, w.k, w.G, w.N, x.cu_seqlens_q, upad)
+    assert np.array_equal(ul, rl) and np.array_equal(u, ru) and np.array_equal(m, rm)
+    if index_gen is not None:
+        assert float(rl.mean()) > 3000   # the wide variant really widens the union
+    assert np.isfinite(o).all() and np.isfinite(l).all()
+    rng = np.random.default_rng(78)
+    toks = stratified_tokens(w.T, 40, rng, must=[1, 3, 4, 7, 8, 2047, 2048, 8191, 8192, w.T - 4, w.T - 8])
+    ro, rl2 = O.sparse_prefill(x.q, x.kv, x.idx, w.k, w.scale, w.d_qk, w.d_v, tokens=toks)
+    res = O.compare(o[toks], l[toks], ro, rl2)
+    assert res["ok"], res
+
+
 @pytest.mark.parametrize("H,G", [(16, 8), (32, 4)])
 def test_grouped_contiguous_runs(H, G):
     """Unions made of long runs of consecutive rows: dense sliding windows in
