@@ -190,6 +190,13 @@ __device__ __forceinline__ void st_async_v4(uint32_t remote_addr, uint32_t a, ui
                : "memory");
 }
 
+// The same for one 32-bit value.
+__device__ __forceinline__ void st_async_f32(uint32_t remote_addr, float v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(remote_addr),
+               "r"(__float_as_uint(v)), "r"(remote_bar)
+               : "memory");
+}
+
 // Arrival on a peer CTA's barrier without release semantics: for signalling
 // that values loaded earlier are no longer needed, when every one of those
 // loads has already been consumed by an instruction before the arrival (so
@@ -328,6 +335,19 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
       : "memory");
+}
+
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from this CTA's shared memory into a peer CTA's, by the copy engine (the
+// async proxy); the bytes complete on `bar_cluster`, a barrier of the
+// destination CTA.  The source may be rewritten once the destination has
+// observed the barrier phase (every byte was read by then).
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
+                                                  uint32_t bar_cluster) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst_cluster),
+               "r"(src), "r"(bytes), "r"(bar_cluster)
+               : "memory");
 }
 
 // Arrive-and-expect on a barrier given by its shared::cluster address (a

@@ -8,102 +8,109 @@
 // exactly its own top-k and the result equals the per-token form while each
 // union row is gathered once per group instead of once per token.
 //
-// A group is processed by a cluster of two CTAs that split the pseudo-heads:
-// CTA r owns pseudo-heads 64r .. 64r+63 (its q rows: 64 x D_QK) and the
-// matching 64 columns of the output.  Each CTA gathers every union row of
-// the group into its own shared memory (plain tile::gather4 loads, no
-// multicast) and releases each stage with its own MMA commit; the pair shares
-// nothing but the group, whose rows the two CTAs read from L2 at the same
-// time.  No scores cross the cluster.  Within a CTA the data path is the
-// per-token one with 64 heads:
-//   S^T = K q^T with the union slots on the M side (M = 128 slots, N = 64),
-//   streamed chunk by chunk through a K ring whose stages hold a K chunk
-//   (128 slots x 64 columns) and the matching q chunk (64 rows x 64
-//   columns, re-read from L2 every tile: q is not kept resident, which
-//   leaves room for five stages);
-//   O^T += V^T P^T per 128-column V unit (V re-gathered into a V ring, an L2
-//   hit), O^T = 4 x 64 TMEM columns, P^T in shared memory (one or two buffers);
-//   the online softmax (base 2, lazy rescale) runs with thread i <-> slot i
-//   (TMEM lane i) in eight warps, two per lane quarter, each holding 32 of
-//   the 64 pseudo-heads.
-// Warp roles (24 warps): 0-7 softmax (at REGS_SOFTMAX registers, the others
-// at REGS_OTHER), 8 and 11 QK issuers (alternate K chunks, two partial S^T
-// sums; warp 11 idle for 8-chunk rows), 9 and 10 PV issuers (units 0/2 and
-// 1/3), 12-17 K-ring producers (one per stage for 9-chunk rows, all six on
-// every stage for 8-chunk rows), 18-23 V-ring producers (all six on every
-// V unit).
+// A group is processed by a pair of CTAs (a 2-CTA cluster) acting as one
+// through cta_group::2 tensor-core instructions.  The union is walked in
+// pair tiles of 256 slots; CTA r owns slots 128r .. 128r+127 of each.
+//   S^T = K q^T      M = 256 pair MMAs, 16 columns each: A = the 256 slots'
+//                    key rows (CTA r supplies its own 128, gathered into its
+//                    own shared memory), B = q of the 128 pseudo-heads (CTA r
+//                    supplies pseudo-heads 64r .. 64r+63); CTA r's tensor
+//                    memory receives S^T for its 128 slots x all 128 heads.
+//   softmax          in each CTA, thread i <-> slot i (TMEM lane i); the
+//                    running max of every pseudo-head is agreed between the
+//                    two CTAs once per tile (an 8-warp barrier across the
+//                    pair), so P of both halves shares one reference.
+//   O^T += V^T P^T   M = 256 pair MMAs over the tile's 256 slots: A = V^T,
+//                    CTA r supplying output columns 256b + 128r .. +127 of
+//                    M-block b (it gathers those columns of all 256 slots),
+//                    B = P^T, CTA r supplying pseudo-heads 64r .. 64r+63 for
+//                    all 256 slots (the softmax of each CTA stages its slots'
+//                    P of the peer's heads and the copy engine moves it into
+//                    the peer's shared memory); O^T of CTA r = its 256 output columns x 128
+//                    heads, the whole 512 x 128 output between the pair.
+// Each CTA thus gathers per 256 slots its 128 key rows (all D_QK columns)
+// and 256 rows x 256 value columns: half the gather of one CTA doing the
+// whole group, with no data loaded for the other CTA (no TMA multicast).
+// TMA loads of both CTAs complete on the even CTA's barriers
+// (cp.async.bulk.tensor .cta_group::2), where the single MMA-issuing thread
+// of each stream waits; every MMA completion is committed to both CTAs'
+// barriers.
+//
+// Warp roles (24 warps): 0-7 softmax (two per TMEM lane quarter: warp w
+// holds slots 32(w%4) .. +31 and pseudo-heads 64(w/4) .. +63, as two blocks
+// of 32), 8 QK issuer (and tensor-memory allocation), 9 PV issuer (issuers
+// run in the even CTA only), 10-15 K-ring producers, 16-23 V-ring producers
+// (the warps of a stream share every stage).
 #include "dsa_device.cuh"
 #include "dsa_kernels.h"
 
 namespace dsa {
 namespace grouped {
 
-constexpr int BK = 128;          // union slots per tile (the MMA's M)
-constexpr int HC = 64;           // pseudo-heads per CTA (the MMA's N)
-constexpr int HW = 32;           // pseudo-heads per softmax warp
+constexpr int BK = 128;          // slots per CTA per pair tile (the pair MMA's M / 2)
+constexpr int PT = 2 * BK;       // slots per pair tile
+constexpr int HP = 128;          // pseudo-heads (the pair MMA's N)
+constexpr int HC = 64;           // pseudo-heads whose q / P this CTA supplies
 constexpr int NTHREADS = 768;    // 24 warps, launched at 80 registers each
-constexpr int REGS_SOFTMAX = 144;
-constexpr int REGS_OTHER = 48;   // 8*32*144 + 16*32*48 <= 768*80
-constexpr int NKW = 6;           // K producer warps (one per K stage)
-constexpr int NVR = 2;           // V ring slots: unit m in slot m mod 2, PV issuer m mod 2
+constexpr int REGS_SOFTMAX = 160;
+constexpr int REGS_OTHER = 40;   // 8*32*160 + 16*32*40 = 768*80
+constexpr int KW0 = 10, NKWARP = 6, KLANES = 6;    // K producers: warps 10-15, lanes 0-5 (33 requests)
+constexpr int VW0 = 16, NVWARP = 8, VLANES = 8;    // V producers: warps 16-23, lanes 0-7 (64 requests)
 constexpr float kTau = 8.0f;     // lazy-rescale threshold (log2 units)
+constexpr uint16_t kBoth = 3;    // commit to both CTAs' barriers
 
-template <int NC>
 struct Cfg {
-  // QK issuing threads: two for the 9-chunk (NoPE + RoPE) rows, where one
-  // thread's per-chunk wait, fence and commit set the tile period; one for
-  // 8-chunk rows, where two made the softmax the slower stage (measured)
-  static constexpr int NQ = (NC % 2) ? 2 : 1;
-  // K ring stages (K chunk + q chunk each); even with two issuers, so that
-  // stage s is issuer s & 1's.  With two issuers the softmax keeps ahead of
-  // P.V, so one P^T buffer serves and its 16 KB go to the K ring.
-  static constexpr int NKR = NQ == 2 ? 6 : 5;
-  static constexpr int NPB = NQ == 2 ? 1 : 2;   // P^T buffers
-  // slack for aligning the dynamic shared memory to 1024 bytes; the 6-stage
-  // layout has no room for it and requires an aligned base (checked at
-  // entry: the launch stops and counts an early stop otherwise)
-  static constexpr uint32_t ALIGN_SLACK = NQ == 2 ? 0u : 1024u;
-  // K producers: with two issuers warp 12+s owns stage s (17 lanes issue a
-  // stage); with one, all six warps take part in every stage (3 lanes each).
-  // Both measured per layout: each is the faster one where it is used.
-  static constexpr bool OWNED = NQ == 2;
   static constexpr uint32_t CHUNK_BYTES = BK * 128u;          // 128 slots x 64 columns
   static constexpr uint32_t UNIT_BYTES = 2u * CHUNK_BYTES;    // 128 slots x 128 columns
-  static constexpr uint32_t Q_CHUNK = HC * 128u;              // 64 rows x 64 columns
+  static constexpr uint32_t Q_CHUNK = HC * 128u;              // 64 pseudo-heads x 64 columns
   static constexpr uint32_t KSTAGE_BYTES = CHUNK_BYTES + Q_CHUNK;
-  static constexpr uint32_t P_BYTES = 2u * HC * 128u;         // one buffer: 128 slots = 2 swizzle columns
-  static constexpr uint32_t RED_BYTES = 2u * 2u * 4u * HW * 4u;  // [parity][half][warp][head]
+  static constexpr uint32_t P_BYTES = PT * 128u;              // 256 slots x 64 heads, MN-major
+  static constexpr int NKR = 3;    // K stages
+  static constexpr int NPB = 2;    // P buffers
+  static constexpr int NVR = 2;    // V slots
+  // softmax exchange: [parity][head block][block of 32 heads][8 warps of the pair][32]
+  static constexpr uint32_t RED_BYTES = 2u * 2u * 2u * 8u * 32u * 4u;
+  // each softmax warp's copy of -(running max) of its 64 heads, read back by
+  // every lane as broadcast loads
+  static constexpr uint32_t NEGM_BYTES = 8u * 64u * 4u;
   static constexpr uint32_t OFF_KR = 0;
   static constexpr uint32_t OFF_VR = OFF_KR + NKR * KSTAGE_BYTES;
-  static_assert(NKR <= NKW && (NQ == 1 || NKR % 2 == 0), "K ring layout: one producer warp per stage");
   static constexpr uint32_t OFF_P = OFF_VR + NVR * UNIT_BYTES;
-  static constexpr uint32_t OFF_RED = OFF_P + NPB * P_BYTES;
-  static constexpr uint32_t OFF_BAR = OFF_RED + RED_BYTES;
-  static constexpr int NBAR = 32;
+  // P of this CTA's slots for the peer's heads, staged for one bulk copy
+  // per warp into the peer's P buffer
+  static constexpr uint32_t STG_BYTES = BK * 128u;
+  static constexpr uint32_t OFF_STG = OFF_P + NPB * P_BYTES;
+  static constexpr uint32_t OFF_RED = OFF_STG + STG_BYTES;
+  static constexpr uint32_t OFF_NEGM = OFF_RED + RED_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_NEGM + NEGM_BYTES;
+  static constexpr int NBAR = 40;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8u;
-  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 128u + ALIGN_SLACK;
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64u;
+  // no alignment slack: the dynamic shared memory must start 1024-aligned
+  // (checked at entry)
   static_assert(SMEM_BYTES <= 227u * 1024u, "shared memory budget");
-  static constexpr uint32_t COL_O = 0;       // O^T: 4 units x 64 columns
-  static constexpr uint32_t COL_S = 256;     // S^T: 2 buffers x 2 partial sums x 64 columns
+  static_assert(NKWARP * KLANES >= 33 && NVWARP * VLANES >= 64 && VW0 + NVWARP == NTHREADS / 32, "producers");
+  static constexpr uint32_t COL_O = 0;     // O^T: 2 M-blocks x 128 heads
+  static constexpr uint32_t COL_S = 256;   // S^T: 2 buffers x 128 heads
   static constexpr uint32_t TMEM_COLS = 512;
 };
 
 enum {
-  B_S_FULL = 0,      // [2] one commit per QK issuer
-  B_S_EMPTY = 2,     // [2]
-  B_P_FULL = 4,      // [NPB] 256 arrivals (softmax threads)
-  B_P_EMPTY = 6,     // [NPB] one commit per PV issuer
-  B_O_FULL = 8,      // one commit per PV issuer
-  B_O_EMPTY = 9,     // 256 arrivals
-  B_DRAIN = 10,      // [4] one per MMA issuer
-  B_SMX_SYNC = 14,   // [2] one per head half (4 warps)
-  B_KR_FULL = 16,    // [NKR <= 6]
-  B_KR_EMPTY = 22,   // [NKR <= 6] one QK commit
-  B_VR_FULL = 28,    // [NVR]
-  B_VR_EMPTY = 30,   // [NVR] one PV commit
+  B_KF = 0,      // [NKR <= 4] even CTA: one arrive.expect_tx (both CTAs' bytes)
+  B_KE = 4,      // [NKR] one commit
+  B_VF = 8,      // [NVR <= 4] even CTA: one arrive.expect_tx
+  B_VE = 12,     // [NVR] one commit
+  B_SF = 16,     // [2] one commit
+  B_SE = 18,     // [2] even CTA: the 16 softmax warps of the pair
+  B_PF = 20,     // [NPB] even CTA: one relay arrival from the odd CTA (its P_RX completed)
+  B_PE = 22,     // [NPB] one commit (the P.V that read P buffer b is done)
+  B_OF = 24,     // one commit
+  B_OE = 25,     // even CTA: the 16 softmax warps of the pair
+  B_XB = 26,     // [parity][head block][block of 32]: 4 local warps + the peer's 4 x 128 bytes
+  B_DRAIN = 34,  // [2] one per MMA issuer
+  B_PRX = 36,    // [NPB] P buffer b complete: this CTA's 8 softmax warps + 16 KB copied in by the peer
+  B_STG = 38,    // the staging rows were copied out: the peer's acknowledgement of the last copy
 };
-static_assert(NVR <= 2, "barrier layout");
-
 
 __device__ __forceinline__ void group_of(const ReqTable& rq, int G, int g, int& t0, int& n) {
   int r = 0;
@@ -112,9 +119,8 @@ __device__ __forceinline__ void group_of(const ReqTable& rq, int G, int g, int& 
   n = min(G, rq.cu_q[r + 1] - t0);
 }
 
-// The four union slots 4rg .. 4rg+3 of tile j (row indices; -1 past the
-// union or out of range, which TMA reads as zeros).  Nothing at or past U is
-// read: a tile may run past the padded row.
+// The four union slots u .. u+3 (row indices; -1 past the union or out of
+// range, which TMA reads as zeros).  Nothing at or past U is read.
 __device__ __forceinline__ int4 union_rows4(const int32_t* urow, int U, int N, int u) {
   int4 r = make_int4(-1, -1, -1, -1);
   if (u + 3 < U) {
@@ -129,6 +135,16 @@ __device__ __forceinline__ int4 union_rows4(const int32_t* urow, int U, int N, i
   if (r.z < 0 || r.z >= N) r.z = -1;
   if (r.w < 0 || r.w >= N) r.w = -1;
   return r;
+}
+
+// The first row of the 64 union slots u0 .. u0+63 when they are one run of
+// consecutive rows inside the table (the union is sorted and distinct, so the
+// two end slots decide), else -1.
+__device__ __forceinline__ int run_start(const int32_t* urow, int U, int N, int u0) {
+  if (u0 + 63 >= U) return -1;
+  const int first = __ldg(urow + u0);
+  const int last = __ldg(urow + u0 + 63);
+  return (first >= 0 && last < N && last - first == 63) ? first : -1;
 }
 
 // Warp-level transposed max/sum reduction over 32 lanes for 32 values per
@@ -154,499 +170,577 @@ __device__ __forceinline__ float warp_transpose_reduce32(float* v) {
   return v[0];
 }
 
+// One arrival of the calling warp (lane 0, once every lane of the warp is
+// done) on a barrier of the even CTA, given by its offset in this CTA.
+__device__ __forceinline__ void warp_arrive_leader(uint64_t* bar) {
+  __syncwarp();
+  if (lane_id() == 0) mbar_arrive_remote(map_peer(smem_u32(bar), 0));
+}
+
 template <int NC>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
-  using C = Cfg<NC>;
+  using C = Cfg;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
-  if (C::ALIGN_SLACK == 0 && (raw_u32 & 1023u) != 0) {
+  if ((raw_u32 & 1023u) != 0) {
     // same base in every CTA of the launch: the whole grid stops here
     if (threadIdx.x == 0) atomicAdd(a.err + ERR_TIMEOUT, 1u);
     return;
   }
-  uint8_t* smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
-  const uint32_t sbase = smem_u32(smem);
+  uint8_t* smem = smem_raw;
+  const uint32_t sbase = raw_u32;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile uint32_t* tmem_base_ptr = misc;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
-  float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
   unsigned int* err = a.err;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int rank = (int)cluster_ctarank();
+  const bool leader = rank == 0;
   const int H = a.H;
   const int G = a.G;
   const int cid = (int)cluster_id_x();
   const int ncl = (int)nclusters_x();
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars[B_S_FULL + i], C::NQ);
-      mbar_init(&bars[B_S_EMPTY + i], 256);
-      mbar_init(&bars[B_SMX_SYNC + i], 128);
-    }
-    for (int i = 0; i < C::NPB; ++i) {
-      mbar_init(&bars[B_P_FULL + i], 256);
-      mbar_init(&bars[B_P_EMPTY + i], 2);
-    }
-    mbar_init(&bars[B_O_FULL], 2);
-    mbar_init(&bars[B_O_EMPTY], 256);
-    for (int i = 0; i < 4; ++i) mbar_init(&bars[B_DRAIN + i], 1);
     for (int i = 0; i < C::NKR; ++i) {
-      mbar_init(&bars[B_KR_FULL + i], 1);
-      mbar_init(&bars[B_KR_EMPTY + i], 1);
+      mbar_init(&bars[B_KF + i], 1);
+      mbar_init(&bars[B_KE + i], 1);
     }
-    for (int i = 0; i < NVR; ++i) {
-      mbar_init(&bars[B_VR_FULL + i], 1);
-      mbar_init(&bars[B_VR_EMPTY + i], 1);
+    for (int i = 0; i < C::NVR; ++i) {
+      mbar_init(&bars[B_VF + i], 1);
+      mbar_init(&bars[B_VE + i], 1);
     }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars[B_SF + i], 1);
+      mbar_init(&bars[B_SE + i], 16);
+      mbar_init(&bars[B_DRAIN + i], 1);
+    }
+    for (int i = 0; i < 8; ++i) mbar_init(&bars[B_XB + i], 4);
+    for (int i = 0; i < C::NPB; ++i) {
+      mbar_init(&bars[B_PF + i], 1);
+      mbar_init(&bars[B_PRX + i], 8);
+      mbar_init(&bars[B_PE + i], 1);
+    }
+    mbar_init(&bars[B_STG], 1);
+    mbar_init(&bars[B_OF], 1);
+    mbar_init(&bars[B_OE], 16);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 8) {
-    tmem_alloc(const_cast<uint32_t*>(tmem_base_ptr), C::TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_pair(const_cast<uint32_t*>(tmem_base_ptr), C::TMEM_COLS);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // both CTAs of the pair start together
+  cluster_sync();  // both CTAs' barriers exist before any copy, commit or arrival reaches them
   tc_fence_after();
   const uint32_t tmem = *tmem_base_ptr;
 
   if (warp >= 8) {
     regs_dec<REGS_OTHER>();
-    if (warp >= 12) {
+    if (warp >= 10) {
       // ----------------------------------------------------------------
-      // TMA producers.  K stream (warps 12-17): a stage holds K chunk c of a
-      // tile (128 slots x columns 64c .. 64c+63) plus q chunk c of this CTA's
-      // 64 pseudo-heads; requests 0-31 gather the tile's 32 row groups of 4
-      // slots, request 32 loads the q chunk.  OWNED: warp 12+s fills stage s
-      // with every chunk that maps there, lane l gathering row group l and
-      // lane 0 also loading q (a warp's per-stage loop of wait, arm and
-      // issue costs several hundred cycles, so stages are filled side by
-      // side); otherwise all six warps take part in every stage, lanes 0-5
-      // of each.  V stream (warps 18-23): the 128-column units m of every
-      // tile go to V slot m mod 2; all six warps take part in every unit,
-      // lanes 0-10 of each sharing its 64 gathers (32 row groups x 2 swizzle
-      // columns; a unit's refill sits on the P.V critical path twice per
-      // tile, so its issue time matters).
-      // When a 64-slot half of the tile is one contiguous run of rows, the
-      // half is one tiled load (box 64 columns x 64 rows) instead of 16
-      // gathers.  The union lists distinct rows in ascending order, so the
-      // run test needs only the half's two end slots.
-      // A stage's leader (lane 0 of its K warp, or of warp 12, and of warp
-      // 18 for V) arms the full byte count of the stage.  Every warp of a
-      // slot passes through each of its phases in order.
+      // TMA producers (both CTAs).  Every load lands in this CTA's own
+      // shared memory and completes on the even CTA's barrier, where the
+      // issuer of the MMAs that read it waits; the even CTA's producer arms
+      // the bytes of both CTAs.  A stage is refilled once the MMAs that read
+      // it have completed in the pair (commit to both CTAs' EMPTY barriers).
+      // A warp issues its TMA requests one after another (the SM's request
+      // rate grows with the number of warps issuing), so every stage and
+      // unit is shared by the warps of its stream:
+      //   K (warps 10-15): chunk c of a pair tile = this CTA's 128 slots x
+      //     columns 64c .. 64c+63 (requests 0-31: slots 4e .. 4e+3) + q chunk
+      //     c of its 64 pseudo-heads (request 32); lanes 0-5 of each warp.
+      //   V (warps 16-23): unit u = 2b + h of a pair tile = the tile's slots
+      //     128h .. 128h+127 x this CTA's columns 256b + 128r .. +127, as two
+      //     64-column swizzle columns (requests 0-63: slots 4(e % 32) .. +3,
+      //     swizzle column e / 32); lanes 0-7 of each warp.
+      // A 64-slot half that is one run of consecutive rows is one tiled load
+      // (box 64 columns x 64 rows) instead of 16 gathers.
       // ----------------------------------------------------------------
-      const bool kstream = warp < 18;
-      const int kw = warp - 12;                 // K stage owned (OWNED; none past the ring)
-      // K request of this lane: 0-31 gathers, 32 the q chunk (OWNED: lane 0
-      // issues its gather and the q chunk)
-      const int kreq = C::OWNED ? lane : kw * 6 + (lane < 6 ? lane : 64);
-      const bool kq = kstream && (C::OWNED ? lane == 0 : kreq == 32);
-      // V: all six warps take part in every unit, lanes 0-10 of each
-      const int e = (warp - 18) * 11 + (lane < 11 ? lane : 64);   // V gather index 0..63
-      const bool issuer = kstream ? (kreq < 33) : (e < 64);
-      const bool kgather = kstream && kreq < 32;
-      const int rg = kstream ? (kreq & 31) : (e & 31);   // row group of the tile
-      const int hf = rg >> 4;                            // its 64-slot half
-      const int vcc = (e >> 5) & 1;             // V swizzle column
-      const bool leader = (lane == 0) && (kstream ? (C::OWNED || kw == 0) : warp == 18);
+      const bool kstream = warp < VW0;
+      const int e = kstream ? (warp - KW0) * KLANES + (lane < KLANES ? lane : 64)   // K request 0..32
+                            : (warp - VW0) * VLANES + (lane < VLANES ? lane : 64);  // V request 0..63
+      const bool kgather = kstream && e < 32;
+      const bool kq = kstream && e == 32;
+      const bool vgather = !kstream && e < 64;
+      const int rg = e & 31;                                    // row group (4 slots) of 128
+      const int vcc = (e >> 5) & 1;                             // V swizzle column
+      const bool arm = leader && lane == 0 && (warp == KW0 || warp == VW0);
       uint32_t gt = 0, pos = 0;
-      int64_t last_armed = -1;
       bool ok = true;
       for (int g = cid; g < a.num_groups && ok; g += ncl) {
         int t0, n;
         group_of(a.req, G, g, t0, n);
         const int U = min(__ldg(a.union_len + g), a.union_pad);
-        const int ntiles = (U + BK - 1) / BK;
+        const int ntiles = (U + PT - 1) / PT;
         if (ntiles == 0) continue;
         const int32_t* urow = a.union_idx + (size_t)g * a.union_pad;
         for (int j = 0; j < ntiles && ok; ++j, ++gt) {
-          if (warp == 12 && lane == 0) DSA_TRACE(a.tr, gt, 0);
-          const int u0 = j * BK + 64 * hf;     // this lane's 64-slot half of the tile
-          int first = -1;
-          bool run = false;
-          if (u0 + 63 < U) {
-            first = __ldg(urow + u0);
-            const int last = __ldg(urow + u0 + 63);
-            run = first >= 0 && last < a.N && last - first == 63;
-          }
-          const uint32_t half_off = (uint32_t)hf * (C::CHUNK_BYTES / 2);
-          const bool run_lead = (rg & 15) == 0;   // issues the half's tiled load
           if (kstream) {
-            const int4 r = (kgather && !run) ? union_rows4(urow, U, a.N, j * BK + 4 * rg) : make_int4(-1, -1, -1, -1);
+            const int u0 = j * PT + BK * rank;             // this CTA's 128 slots
+            const int first = kgather ? run_start(urow, U, a.N, u0 + 64 * (rg >> 4)) : -1;
+            const int4 r = (kgather && first < 0) ? union_rows4(urow, U, a.N, u0 + 4 * rg)
+                                                   : make_int4(-1, -1, -1, -1);
+#pragma unroll 1
             for (int c = 0; c < NC; ++c, ++pos) {
               const int ks = (int)(pos % C::NKR);
-              if (C::OWNED && ks != kw) continue;
-              if (!mbar_wait_warp(&bars[B_KR_EMPTY + ks], ((pos / C::NKR) & 1) ^ 1, abort_flag, err)) {
+              if (!mbar_wait_cluster_warp(&bars[B_KE + ks], ((pos / C::NKR) & 1) ^ 1, abort_flag, err)) {
                 ok = false;
                 break;
               }
+              const uint32_t full0 = map_peer(smem_u32(&bars[B_KF + ks]), 0);
+              if (arm) mbar_arrive_expect_tx(&bars[B_KF + ks], 2u * C::KSTAGE_BYTES);
               const uint32_t stage = sbase + C::OFF_KR + ks * C::KSTAGE_BYTES;
-              if (leader) mbar_arrive_expect_tx(&bars[B_KR_FULL + ks], C::KSTAGE_BYTES);
               if (kgather) {
-                if (run) {
-                  if (run_lead) tma_load_2d(stage + half_off, &a.tmap_kv_blk, c * 64, first, &bars[B_KR_FULL + ks]);
+                if (first >= 0) {
+                  if ((rg & 15) == 0)
+                    tma_load_2d_pair(stage + (rg >> 4) * (C::CHUNK_BYTES / 2), &a.tmap_kv_blk, c * 64, first, full0);
                 } else {
-                  tma_gather4(stage + rg * 512, &a.tmap_kv, c * 64, r.x, r.y, r.z, r.w, &bars[B_KR_FULL + ks]);
+                  tma_gather4_pair(stage + rg * 512, &a.tmap_kv, c * 64, r.x, r.y, r.z, r.w, full0);
                 }
               }
-              if (kq)
-                // q rows t0*H + 64 rank .. +63 of q viewed [T*H, D_QK], columns 64c ..
-                tma_load_2d(stage + C::CHUNK_BYTES, &a.tmap_q, c * 64, t0 * H + HC * rank, &bars[B_KR_FULL + ks]);
-              last_armed = pos;
+              // q rows t0*H + 64 rank .. +63 of q viewed [T*H, D_QK], columns 64c ..
+              if (kq) tma_load_2d_pair(stage + C::CHUNK_BYTES, &a.tmap_q, c * 64, t0 * H + HC * rank, full0);
             }
           } else {
-            const int4 r = (issuer && !run) ? union_rows4(urow, U, a.N, j * BK + 4 * rg) : make_int4(-1, -1, -1, -1);
-            for (int m = 0; m < 4; ++m, ++pos) {
-              const int vg = (int)(pos % NVR);   // V slot of this unit
-              if (!mbar_wait_warp(&bars[B_VR_EMPTY + vg], ((pos / NVR) & 1) ^ 1, abort_flag, err)) {
+            for (int u = 0; u < 4 && ok; ++u, ++pos) {
+              const int b = u >> 1, hh = u & 1;
+              const int vg = (int)(pos % C::NVR);
+              if (!mbar_wait_cluster_warp(&bars[B_VE + vg], ((pos / C::NVR) & 1) ^ 1, abort_flag, err)) {
                 ok = false;
                 break;
               }
-              if (leader) mbar_arrive_expect_tx(&bars[B_VR_FULL + vg], C::UNIT_BYTES);
-              const uint32_t vdst = sbase + C::OFF_VR + vg * C::UNIT_BYTES + vcc * C::CHUNK_BYTES;
-              if (run) {
-                if (issuer && run_lead)
-                  tma_load_2d(vdst + half_off, &a.tmap_kv_blk, (2 * m + vcc) * 64, first, &bars[B_VR_FULL + vg]);
-              } else if (issuer) {
-                tma_gather4(vdst + rg * 512, &a.tmap_kv, (2 * m + vcc) * 64, r.x, r.y, r.z, r.w,
-                            &bars[B_VR_FULL + vg]);
+              const uint32_t full0 = map_peer(smem_u32(&bars[B_VF + vg]), 0);
+              if (arm) mbar_arrive_expect_tx(&bars[B_VF + vg], 2u * C::UNIT_BYTES);
+              if (vgather) {
+                const int u0 = j * PT + BK * hh;
+                const int first = run_start(urow, U, a.N, u0 + 64 * (rg >> 4));
+                const int col = 256 * b + 128 * rank + 64 * vcc;
+                const uint32_t vdst = sbase + C::OFF_VR + vg * C::UNIT_BYTES + vcc * C::CHUNK_BYTES;
+                if (first >= 0) {
+                  if ((rg & 15) == 0)
+                    tma_load_2d_pair(vdst + (rg >> 4) * (C::CHUNK_BYTES / 2), &a.tmap_kv_blk, col, first, full0);
+                } else {
+                  const int4 r = union_rows4(urow, U, a.N, u0 + 4 * rg);
+                  tma_gather4_pair(vdst + rg * 512, &a.tmap_kv, col, r.x, r.y, r.z, r.w, full0);
+                }
               }
-              last_armed = pos;
             }
           }
         }
       }
-      // Let copies still in flight land before the CTA can exit: the last
-      // phase of every stage this warp's leader armed completes only once
-      // all of its bytes have landed.
-      if (leader && last_armed >= 0) {
-        if (kstream) {
-          // the last phase of every stage this leader armed
-          for (int64_t p = last_armed; p >= 0 && p > last_armed - C::NKR; --p)
-            if (!C::OWNED || (int)(p % C::NKR) == kw)
-              mbar_wait_drain(&bars[B_KR_FULL + (int)(p % C::NKR)], (uint32_t)(p / C::NKR) & 1, err);
-        } else {
-          for (int64_t p = last_armed; p >= 0 && p > last_armed - NVR; --p)
-            mbar_wait_drain(&bars[B_VR_FULL + (int)(p % NVR)], (uint32_t)(p / NVR) & 1, err);
+      if (!ok) {
+        // a wait ran out: loads already issued land within microseconds;
+        // give them that long before this CTA (their target) can leave
+        const uint64_t t0 = globaltimer();
+        while (globaltimer() - t0 < 20000ull) {
         }
       }
       __syncwarp();
-    } else if (warp == 8 || (warp == 11 && C::NQ == 2)) {
+    } else if (warp == 8) {
       // ----------------------------------------------------------------
-      // QK issuers: S^T = K q^T chunk by chunk.  With two issuing threads
-      // the chunks alternate between them (warp 8 takes ring positions of
-      // even parity, warp 11 odd ones; with an even ring size each stage
-      // belongs to one of them), each summing into its own partial S^T; the
-      // softmax adds the two.  One thread issuing every chunk spends most of
-      // its time in the per-chunk wait, fence and commit, not in MMAs.
-      // Each K chunk is released to the producers once its MMAs complete;
-      // S_FULL takes one commit from each issuer.
+      // QK issuer (even CTA): S^T = K q^T, chunk by chunk, into the S double
+      // buffer; each K stage goes back to both CTAs' producers once its MMAs
+      // complete, and S_FULL is committed to both CTAs' softmax.
       // ----------------------------------------------------------------
-      const uint32_t qa = warp == 8 ? 0u : 1u;
-      if (lane == 0) {
-        constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, HC, false, false);
+      if (leader && lane == 0) {
+        constexpr uint32_t IDESC_QK = idesc_bf16_f32(256, HP, false, false);
         uint32_t gt = 0, kpos = 0;
         bool ok = true;
         for (int g = cid; g < a.num_groups && ok; g += ncl) {
           const int U = min(__ldg(a.union_len + g), a.union_pad);
-          const int ntiles = (U + BK - 1) / BK;
-          if (ntiles == 0) continue;
+          const int ntiles = (U + PT - 1) / PT;
           for (int j = 0; j < ntiles && ok; ++j, ++gt) {
             const int sb = gt & 1;
-            const uint32_t d_s = tmem + C::COL_S + (2 * sb + qa) * HC;
-            if (!mbar_wait(&bars[B_S_EMPTY + sb], ((gt >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
-            if (qa == 0) DSA_TRACE(a.tr, gt, 2);
+            const uint32_t d_s = tmem + C::COL_S + sb * HP;
+            if (!mbar_wait_cluster(&bars[B_SE + sb], ((gt >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+            DSA_TRACE(a.tr, gt, 2);
             tc_fence_after();
-            bool first = true;
+#pragma unroll 1
             for (int c = 0; c < NC; ++c, ++kpos) {
-              if (C::NQ == 2 && (kpos & 1u) != qa) continue;
               const uint32_t slot = kpos % C::NKR;
-              if (!mbar_wait(&bars[B_KR_FULL + slot], (kpos / C::NKR) & 1, abort_flag, err)) { ok = false; break; }
+              if (!mbar_wait_cluster(&bars[B_KF + slot], (kpos / C::NKR) & 1, abort_flag, err)) {
+                ok = false;
+                break;
+              }
               tc_fence_after();
               const uint32_t stage = sbase + C::OFF_KR + slot * C::KSTAGE_BYTES;
-              mma_bf16_ss_x4(d_s, sdesc_sw128(stage, 16, 1024), sdesc_sw128(stage + C::CHUNK_BYTES, 16, 1024), 2u, 2u,
-                             IDESC_QK, first ? 0u : 1u);
-              mma_commit(&bars[B_KR_EMPTY + slot]);
-              first = false;
+              mma_pair_bf16_ss_x4(d_s, sdesc_sw128(stage, 16, 1024), sdesc_sw128(stage + C::CHUNK_BYTES, 16, 1024),
+                                  2u, 2u, IDESC_QK, c > 0 ? 1u : 0u);
+              mma_pair_commit(&bars[B_KE + slot], kBoth);
             }
             if (!ok) break;
-            if (qa == 0) DSA_TRACE(a.tr, gt, 1);
-            mma_commit(&bars[B_S_FULL + sb]);
+            mma_pair_commit(&bars[B_SF + sb], kBoth);
           }
         }
-        mma_commit(&bars[B_DRAIN + 2 + qa]);
-        mbar_wait(&bars[B_DRAIN + 2 + qa], 0, abort_flag, err);
-      }
-      __syncwarp();
-    } else if (warp == 9 || warp == 10) {
-      // ----------------------------------------------------------------
-      // PV issuers: O^T += V^T P^T, warp 9 for units 0 and 2, warp 10 for
-      // units 1 and 3 (V slot = unit mod 2); each unit released to the
-      // producers once its MMAs complete
-      // ----------------------------------------------------------------
-      const int pvi = warp - 9;
-      if (lane == 0) {
-        constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, HC, true, false);
-        const uint32_t p_base = sbase + C::OFF_P;
-        uint32_t gt = 0, lgq = 0;
+        mma_pair_commit(&bars[B_DRAIN + 0], 1);
+        mbar_wait(&bars[B_DRAIN + 0], 0, abort_flag, err);
+      } else if (!leader && lane == 0) {
+        // relay (odd CTA): once this CTA's P buffer is complete (its softmax
+        // done, the peer's copy landed), tell the even CTA's P.V issuer, and
+        // tell the even CTA that its staging rows may be rewritten
+        const uint32_t stg0 = map_peer(smem_u32(&bars[B_STG]), 0);
+        uint32_t gt = 0;
         bool ok = true;
         for (int g = cid; g < a.num_groups && ok; g += ncl) {
           const int U = min(__ldg(a.union_len + g), a.union_pad);
-          const int ntiles = (U + BK - 1) / BK;
+          const int ntiles = (U + PT - 1) / PT;
+          for (int j = 0; j < ntiles; ++j, ++gt) {
+            const int pb = gt & 1;
+            if (!mbar_wait_cluster(&bars[B_PRX + pb], (gt >> 1) & 1, abort_flag, err)) { ok = false; break; }
+            mbar_arrive_remote(map_peer(smem_u32(&bars[B_PF + pb]), 0));
+            mbar_arrive_remote(stg0);
+          }
+        }
+      }
+      __syncwarp();
+    } else if (warp == 9) {
+      // ----------------------------------------------------------------
+      // PV issuer (even CTA): O^T += V^T P^T for the tile's four V units
+      // (M-block b, slot half h); each unit goes back to both CTAs'
+      // producers once its MMAs complete; P_EMPTY and (last tile of a
+      // group) O_FULL are committed to both CTAs.
+      // ----------------------------------------------------------------
+      if (leader && lane == 0) {
+        constexpr uint32_t IDESC_PV = idesc_bf16_f32(256, HP, true, true);
+        const uint32_t stg1 = map_peer(smem_u32(&bars[B_STG]), 1);
+        uint32_t gt = 0, vpos = 0, lgq = 0;
+        bool ok = true;
+        for (int g = cid; g < a.num_groups && ok; g += ncl) {
+          const int U = min(__ldg(a.union_len + g), a.union_pad);
+          const int ntiles = (U + PT - 1) / PT;
           if (ntiles == 0) continue;
           for (int j = 0; j < ntiles && ok; ++j, ++gt) {
-            const int pb = C::NPB == 2 ? (int)(gt & 1) : 0;
-            const uint32_t pph = C::NPB == 2 ? (gt >> 1) : gt;   // phase of P buffer pb
-            if (!mbar_wait(&bars[B_P_FULL + pb], pph & 1, abort_flag, err)) { ok = false; break; }
-            if (pvi == 0) DSA_TRACE(a.tr, gt, 7);
+            // this CTA's P buffer and rescale (then the odd CTA may reuse its
+            // staging rows, whose copy has landed here), then the peer's
+            // (relayed)
+            const int pb = gt & 1;
+            const uint32_t pph = (gt >> 1) & 1;
+            if (!mbar_wait_cluster(&bars[B_PRX + pb], pph, abort_flag, err)) { ok = false; break; }
+            mbar_arrive_remote(stg1);
+            if (!mbar_wait_cluster(&bars[B_PF + pb], pph, abort_flag, err)) { ok = false; break; }
+            DSA_TRACE(a.tr, gt, 7);
+            if (j == 0 && !mbar_wait_cluster(&bars[B_OE], (lgq & 1) ^ 1, abort_flag, err)) { ok = false; break; }
             tc_fence_after();
-            if (j == 0) {
-              if (!mbar_wait(&bars[B_O_EMPTY], (lgq & 1) ^ 1, abort_flag, err)) { ok = false; break; }
-              tc_fence_after();
-            }
-            for (int m = pvi; m < 4 && ok; m += 2) {
-              const uint32_t vp = gt * 4 + m;
-              if (!mbar_wait(&bars[B_VR_FULL + pvi], (vp / NVR) & 1, abort_flag, err)) { ok = false; break; }
-              tc_fence_after();
-              const uint32_t ubase = sbase + C::OFF_VR + pvi * C::UNIT_BYTES;
-              const uint32_t d_o = tmem + C::COL_O + m * HC;
-#pragma unroll
-              for (int hf = 0; hf < 2; ++hf) {
-                // 16 slots (2048 B of V^T, MN-major; the unit's two swizzle
-                // columns CHUNK_BYTES apart) per MMA; P^T one 64-slot
-                // swizzle column per half
-                const uint64_t adesc = sdesc_sw128(ubase + hf * 4 * 2048, C::CHUNK_BYTES, 1024);
-                const uint64_t bdesc = sdesc_sw128(p_base + pb * C::P_BYTES + hf * (HC * 128), 16, 1024);
-                mma_bf16_ss_x4(d_o, adesc, bdesc, 128u, 2u, IDESC_PV, (j > 0 || hf > 0) ? 1u : 0u);
+            for (int u = 0; u < 4 && ok; ++u, ++vpos) {
+              const int b = u >> 1, hh = u & 1;
+              const uint32_t slot = vpos % C::NVR;
+              if (!mbar_wait_cluster(&bars[B_VF + slot], (vpos / C::NVR) & 1, abort_flag, err)) {
+                ok = false;
+                break;
               }
-              mma_commit(&bars[B_VR_EMPTY + pvi]);
+              tc_fence_after();
+              const uint32_t ubase = sbase + C::OFF_VR + slot * C::UNIT_BYTES;
+              const uint32_t d_o = tmem + C::COL_O + b * HP;
+              // 16 slots per MMA: V^T MN-major (the unit's two swizzle columns
+              // CHUNK_BYTES apart), P^T MN-major rows 128h + 64hf ..
+              uint64_t adesc = sdesc_sw128(ubase, C::CHUNK_BYTES, 1024);
+              uint64_t bdesc = sdesc_sw128(sbase + C::OFF_P + pb * C::P_BYTES + BK * hh * 128, C::P_BYTES, 1024);
+#pragma unroll 1
+              for (int hf = 0; hf < 2; ++hf) {
+                mma_pair_bf16_ss_x4(d_o, adesc, bdesc, 128u, 128u, IDESC_PV, (j > 0 || hh > 0 || hf > 0) ? 1u : 0u);
+                adesc += 4u * 128u;   // 64 slots = 8 KB, in 16-byte units of the start field
+                bdesc += 4u * 128u;
+              }
+              mma_pair_commit(&bars[B_VE + slot], kBoth);
             }
             if (!ok) break;
-            mma_commit(&bars[B_P_EMPTY + pb]);
-            if (j == ntiles - 1) mma_commit(&bars[B_O_FULL]);
+            mma_pair_commit(&bars[B_PE + pb], kBoth);
+            DSA_TRACE(a.tr, gt, 0);
+            if (j == ntiles - 1) mma_pair_commit(&bars[B_OF], kBoth);
           }
           ++lgq;
         }
-        mma_commit(&bars[B_DRAIN + pvi]);
-        mbar_wait(&bars[B_DRAIN + pvi], 0, abort_flag, err);
+        mma_pair_commit(&bars[B_DRAIN + 1], 1);
+        mbar_wait(&bars[B_DRAIN + 1], 0, abort_flag, err);
       }
       __syncwarp();
     }
   } else {
     regs_inc<REGS_SOFTMAX>();
     // ------------------------------------------------------------------
-    // softmax + epilogue: thread (key i = TMEM lane i, head half hh) holds
-    // the 32 local pseudo-heads 32hh .. 32hh+31 of union slot i of the tile.
-    // The running max and sum are per head and the same for every thread,
-    // so lane L keeps them for head L only and shuffles them out.
+    // softmax + epilogue: thread (slot i = TMEM lane i, head block hb) holds
+    // pseudo-heads 64hb .. 64hb+63 of slot i as two blocks of 32 (sub = 0,
+    // 1); lane L keeps the reference (running max) and this warp's running
+    // sum of heads 64hb + 32sub + L (scaled scores, base 2).  Every tile, the
+    // 8 warps of the pair that hold head block hb exchange their per-head
+    // tile maxima, block by block: each posts its 32 values into its own
+    // CTA's buffer (and arrives, arming the peer's 128 bytes) and into the
+    // peer's with st.async, which completes on the peer's barrier; block 0's
+    // exchange is in flight while block 1's maxima are taken, block 1's
+    // while block 0's P is made.  All 8 warps compute the same reference.
+    // It moves only when the tile max of a head exceeds it by more than
+    // kTau (lazy rescale), so O is rarely rescaled and P stays below 2^kTau.
     // ------------------------------------------------------------------
-    const int hh = warp >> 2;
-    const int key = (warp & 3) * 32 + lane;  // 0..127
-    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const float scale_log2 = a.scale * 1.4426950408889634f;
-    uint64_t* smx = &bars[B_SMX_SYNC + hh];
-    // token of local pseudo-head h: t_lo for h < split, t_lo + 1 after
-    const int base = HC * rank + HW * hh;
-    const int t_lo = base / H;
-    const int split = (t_lo + 1) * H - base;
-    uint32_t gt = 0, lgq = 0, sync_phase = 0;
+    const int hb = warp >> 2;
+    const int qw = warp & 3;
+    const int key = qw * 32 + lane;  // 0..127: this CTA's slot of the tile
+    const int slot8 = 4 * rank + qw; // this warp among the 8 of head block hb
+    const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
+    const float c_log2 = a.scale * 1.4426950408889634f;   // scale / ln 2 > 0
+    float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
+    const uint32_t red_peer = map_peer(smem_u32(red), rank ^ 1);
+    float* negm = reinterpret_cast<float*>(smem + C::OFF_NEGM) + warp * 64;
+    // this slot's P row: in this CTA's P buffer when it supplies heads of
+    // block hb (hb == rank), else in the staging buffer, whose rows of this
+    // warp are copied as one block into the peer's P buffer (rows 128 rank
+    // + 32 qw ..)
+    const bool p_local = hb == rank;
+    const uint32_t p_row = p_local ? smem_u32(smem + C::OFF_P) + (uint32_t)(BK * rank + key) * 128u
+                                   : smem_u32(smem + C::OFF_STG) + (uint32_t)key * 128u;
+    const uint32_t stg_warp = smem_u32(smem + C::OFF_STG) + (uint32_t)(32 * qw) * 128u;
+    const uint32_t peer_rows = map_peer(smem_u32(smem + C::OFF_P) + (uint32_t)(BK * rank + 32 * qw) * 128u, rank ^ 1);
+    uint32_t gt = 0, lgq = 0;
+    uint32_t xph[2] = {0, 0};   // exchanges of block 0 / 1 so far
     bool ok = true;
+
+    // Post this warp's 32 values (lane L: head 64hb + 32sub + L) of an
+    // exchange of block `sub`; returns the buffer parity it used.
+    auto post = [&](int sub, float v) -> uint32_t {
+      const uint32_t par = xph[sub] & 1;
+      const uint32_t bidx = (par * 2 + hb) * 2 + sub;
+      const uint32_t idx = (bidx * 8 + slot8) * 32 + lane;
+      red[idx] = v;
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(&bars[B_XB + bidx], 128u);
+      st_async_f32(red_peer + idx * 4u, v, map_peer(smem_u32(&bars[B_XB + bidx]), rank ^ 1));
+      return par;
+    };
+    // Wait for the exchange of block `sub` posted with parity `par`: all 8
+    // warps' values are then in red[.. bidx * 256 ..].
+    auto wait_x = [&](int sub, uint32_t par) -> bool {
+      const uint32_t bidx = (par * 2 + hb) * 2 + sub;
+      const bool w_ok = mbar_wait_cluster_warp(&bars[B_XB + bidx], (xph[sub] >> 1) & 1, abort_flag, err);
+      ++xph[sub];
+      return w_ok;
+    };
+    auto gathered = [&](int sub, uint32_t par, bool is_max) -> float {
+      const uint32_t base = (((par * 2 + hb) * 2 + sub) * 8) * 32 + lane;
+      float r = is_max ? -INFINITY : 0.f;
+#pragma unroll
+      for (int w8 = 0; w8 < 8; ++w8) r = is_max ? fmaxf(r, red[base + 32 * w8]) : r + red[base + 32 * w8];
+      return r;
+    };
+
     for (int g = cid; g < a.num_groups && ok; g += ncl) {
       int t0, n;
       group_of(a.req, G, g, t0, n);
       const int U = min(__ldg(a.union_len + g), a.union_pad);
-      const int ntiles = (U + BK - 1) / BK;
+      const int ntiles = (U + PT - 1) / PT;
       const int nrows = n * H;
       const uint8_t* mrow = a.mask + (size_t)g * a.union_pad;
       if (ntiles == 0) {
-        // no union rows: zero output, lse = -inf for this CTA's pseudo-heads
-        for (int h = 0; h < HW; ++h) {
-          const int p = base + h;
+        // no union rows: zero output and lse = -inf; CTA r writes columns
+        // 256b + 128r + key of the heads of block hb
+        for (int h = 0; h < 64; ++h) {
+          const int p = 64 * hb + h;
           if (p < nrows) {
-            for (int c = key; c < 512; c += 128) a.out[(size_t)(t0 * H + p) * 512 + c] = 0;
-            if (key == 0) a.lse[(size_t)t0 * H + p] = -INFINITY;
+            for (int b = 0; b < 2; ++b) a.out[(size_t)(t0 * H + p) * 512 + 256 * b + 128 * rank + key] = 0;
+            if (leader && key == 0) a.lse[(size_t)t0 * H + p] = -INFINITY;
           }
         }
         continue;
       }
-      float m_l = -INFINITY;  // running max of head `lane` (base 2, scaled)
-      float l_l = 0.f;        // this warp's running sum of head `lane`
+      // the token (bit of the mask byte) of each head of the two blocks
+      int t_lo[2], split[2];
+#pragma unroll
+      for (int sub = 0; sub < 2; ++sub) {
+        const int base = 64 * hb + 32 * sub;
+        t_lo[sub] = base / H;
+        split[sub] = (t_lo[sub] + 1) * H - base;
+      }
+      float m_l[2] = {-INFINITY, -INFINITY};   // reference of heads 64hb + 32sub + lane (scaled, base 2)
+      float l_l[2] = {0.f, 0.f};               // this warp's running sums of the same heads
       for (int j = 0; j < ntiles; ++j, ++gt) {
         const int sb = gt & 1;
-        const int pb = C::NPB == 2 ? (int)(gt & 1) : 0;
-        const uint32_t pph = C::NPB == 2 ? (gt >> 1) : gt;   // phase of P buffer pb
-        // this slot's membership byte (zero past the union)
-        const int u = j * BK + key;
+        const int u = j * PT + BK * rank + key;
         const uint32_t mbyte = (u < U) ? (uint32_t)__ldg(mrow + u) : 0u;
-        const bool on_lo = (mbyte >> t_lo) & 1u;
-        const bool on_hi = (mbyte >> (t_lo + 1)) & 1u;
-        if (!mbar_wait_warp(&bars[B_S_FULL + sb], (gt >> 1) & 1, abort_flag, err)) { ok = false; break; }
-        if (key == 0 && hh == 0) DSA_TRACE(a.tr, gt, 3);
+        if (!mbar_wait_cluster_warp(&bars[B_SF + sb], (gt >> 1) & 1, abort_flag, err)) { ok = false; break; }
+        if (key == 0 && hb == 0) DSA_TRACE(a.tr, gt, 3);
         tc_fence_after();
-        // S^T = the QK issuers' partial sums
-        float s[HW];
-        const uint32_t s_addr = tmem + lane_off + C::COL_S + 2 * sb * HC + HW * hh;
-        if constexpr (C::NQ == 2) {
+        float s[2][32];
+        const uint32_t s_addr = tmem + lane_off + C::COL_S + sb * HP + 64 * hb;
 #pragma unroll
-          for (int q16 = 0; q16 < HW / 16; ++q16) {
-            float t[16];
-            tmem_ld16(s_addr + 16 * q16, s + 16 * q16);
-            tmem_ld16(s_addr + HC + 16 * q16, t);
-            tmem_ld_wait();
-#pragma unroll
-            for (int h = 0; h < 16; ++h) s[16 * q16 + h] += t[h];
-          }
-        } else {
-#pragma unroll
-          for (int q16 = 0; q16 < HW / 16; ++q16) tmem_ld16(s_addr + 16 * q16, s + 16 * q16);
-          tmem_ld_wait();
-        }
+        for (int q16 = 0; q16 < 4; ++q16) tmem_ld16(s_addr + 16 * q16, &s[q16 >> 1][16 * (q16 & 1)]);
+        tmem_ld_wait();
         tc_fence_before();
-        mbar_arrive(&bars[B_S_EMPTY + sb]);
-        if (key == 0 && hh == 0) DSA_TRACE(a.tr, gt, 5);
-        bool mine = false;
+        warp_arrive_leader(&bars[B_SE + sb]);
+        // mask (raw scores; the scale is positive, so maxima commute with
+        // it) and each block's per-head maxima over this warp's 32 slots,
+        // lane h keeping head h's, posted as soon as they are taken
+        uint32_t par[2];
 #pragma unroll
-        for (int h = 0; h < HW; ++h) {
-          const bool on = (h < split) ? on_lo : on_hi;
-          s[h] = on ? s[h] * scale_log2 : -INFINITY;
-          mine |= (s[h] > __shfl_sync(0xffffffffu, m_l, h) + kTau);
+        for (int sub = 0; sub < 2; ++sub) {
+          const bool on_lo = (mbyte >> t_lo[sub]) & 1u;
+          const bool on_hi = (mbyte >> (t_lo[sub] + 1)) & 1u;
+          float tmx = -INFINITY;
+#pragma unroll
+          for (int h = 0; h < 32; ++h) {
+            const bool on = (h < split[sub]) ? on_lo : on_hi;
+            s[sub][h] = on ? s[sub][h] : -INFINITY;
+            float r;
+            asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(s[sub][h]));
+            if (lane == h) tmx = r;
+          }
+          par[sub] = post(sub, tmx);
         }
-        // Lazy rescale: the tile max matters only when some score exceeds
-        // the running max by more than kTau.  Each warp of the head half
-        // votes; a warp that votes yes publishes its per-head max.  The new
-        // reference is the max over those warps, which bounds every score of
-        // the tile (the others lie within kTau of the old reference).
-        const bool wneed = __any_sync(0xffffffffu, mine);
-        float* redb = red + ((gt & 1) * 2 + hh) * (4 * HW);
-        volatile uint32_t* vote = misc + 4 + ((gt & 1) * 2 + hh) * 4;
-        if (wneed) {
-          float r[HW];
+        // P buffer pb (in both CTAs) is free once the P.V two tiles back is
+        // done; the staging rows once the peer acknowledged the last copy
+        const int pb = gt & 1;
+        if (!mbar_wait_cluster_warp(&bars[B_PE + pb], ((gt >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+        if (!p_local && !mbar_wait_cluster_warp(&bars[B_STG], (gt & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+        if (key == 0 && hb == 0) DSA_TRACE(a.tr, gt, 5);
+        const uint32_t p_dst = p_row + (p_local ? (uint32_t)pb * C::P_BYTES : 0u);
+        // block by block: the pair's tile max, the reference (the same in
+        // both CTAs: the same inputs in the same order), then P = 2^(c s - m)
+        // rounded to bf16 (0 for masked slots), stored as it is made: P^T of
+        // this slot, heads 64hb .. 64hb+63, row 128 rank + key of CTA hb's
+        // P buffer (or of the staging rows), 128 bytes = 8 chunks of 8
+        // heads, chunk c at (c ^ (row & 7)) * 16 (128-byte swizzle,
+        // MN-major); and the row sums of the rounded values
+        float alpha[2] = {1.f, 1.f};
+        const uint32_t sw = (uint32_t)(key & 7);
 #pragma unroll
-          for (int h = 0; h < HW; ++h) r[h] = s[h];
-          redb[(warp & 3) * HW + lane] = warp_transpose_reduce32<true>(r);
+        for (int sub = 0; sub < 2; ++sub) {
+          if (!wait_x(sub, par[sub])) { ok = false; break; }
+          const float tm = gathered(sub, par[sub], true) * c_log2;
+          if (tm > m_l[sub] + kTau) {
+            alpha[sub] = (m_l[sub] == -INFINITY) ? 0.f : exp2f(m_l[sub] - tm);
+            m_l[sub] = tm;
+            l_l[sub] *= alpha[sub];
+          }
+          negm[32 * sub + lane] = (m_l[sub] == -INFINITY) ? 0.f : -m_l[sub];
+          __syncwarp();
+          if (sub == 0 && key == 0 && hb == 0) DSA_TRACE(a.tr, gt, 4);
+#pragma unroll
+          for (int h = 0; h < 32; h += 8) {
+            const float4 n0 = *reinterpret_cast<const float4*>(negm + 32 * sub + h);
+            const float4 n1 = *reinterpret_cast<const float4*>(negm + 32 * sub + h + 4);
+            const uint32_t w0 = pack_bf16x2(exp2f(fmaf(s[sub][h + 0], c_log2, n0.x)),
+                                            exp2f(fmaf(s[sub][h + 1], c_log2, n0.y)));
+            const uint32_t w1 = pack_bf16x2(exp2f(fmaf(s[sub][h + 2], c_log2, n0.z)),
+                                            exp2f(fmaf(s[sub][h + 3], c_log2, n0.w)));
+            const uint32_t w2 = pack_bf16x2(exp2f(fmaf(s[sub][h + 4], c_log2, n1.x)),
+                                            exp2f(fmaf(s[sub][h + 5], c_log2, n1.y)));
+            const uint32_t w3 = pack_bf16x2(exp2f(fmaf(s[sub][h + 6], c_log2, n1.z)),
+                                            exp2f(fmaf(s[sub][h + 7], c_log2, n1.w)));
+            const uint32_t c = (uint32_t)(4 * sub + h / 8);
+            const uint32_t addr = p_dst + ((c ^ sw) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w0), "r"(w1), "r"(w2), "r"(w3)
+                         : "memory");
+            s[sub][h + 0] = __uint_as_float(w0 << 16);
+            s[sub][h + 1] = __uint_as_float(w0 & 0xffff0000u);
+            s[sub][h + 2] = __uint_as_float(w1 << 16);
+            s[sub][h + 3] = __uint_as_float(w1 & 0xffff0000u);
+            s[sub][h + 4] = __uint_as_float(w2 << 16);
+            s[sub][h + 5] = __uint_as_float(w2 & 0xffff0000u);
+            s[sub][h + 6] = __uint_as_float(w3 << 16);
+            s[sub][h + 7] = __uint_as_float(w3 & 0xffff0000u);
+          }
+          l_l[sub] += warp_transpose_reduce32<false>(s[sub]);
         }
-        if (lane == 0) vote[warp & 3] = wneed ? 1u : 0u;
-        if (!group_sync(smx, sync_phase, abort_flag, err)) { ok = false; break; }
-        uint32_t vw[4];
-#pragma unroll
-        for (int w = 0; w < 4; ++w) vw[w] = vote[w];
-        const bool need = (vw[0] | vw[1] | vw[2] | vw[3]) != 0;
-        if (key == 0 && hh == 0) DSA_TRACE(a.tr, gt, 4);
-        float alpha_l = 1.f;
-        if (need) {
-          float tm = -INFINITY;
-#pragma unroll
-          for (int w = 0; w < 4; ++w)
-            if (vw[w]) tm = fmaxf(tm, redb[w * HW + lane]);
-          const float mn = fmaxf(m_l, tm);
-          alpha_l = (m_l == -INFINITY) ? 0.f : exp2f(m_l - mn);
-          m_l = mn;
-          l_l *= alpha_l;
-        }
-        // P (bf16) and its row sums first, in registers: only the stores
-        // into the P^T buffer wait for the P.V that last read it (NPB tiles
-        // ago); s[] becomes the bf16-rounded P for the row sums
-        uint32_t pk[HW / 2];
-#pragma unroll
-        for (int h = 0; h < HW; h += 2) {
-          const float m0 = __shfl_sync(0xffffffffu, m_l, h);
-          const float m1 = __shfl_sync(0xffffffffu, m_l, h + 1);
-          const uint16_t b0 = f32_to_bf16_rn(exp2f(s[h] - ((m0 == -INFINITY) ? 0.f : m0)));
-          const uint16_t b1 = f32_to_bf16_rn(exp2f(s[h + 1] - ((m1 == -INFINITY) ? 0.f : m1)));
-          s[h] = bf16_to_f32(b0);
-          s[h + 1] = bf16_to_f32(b1);
-          pk[h / 2] = (uint32_t)b0 | ((uint32_t)b1 << 16);
-        }
-        l_l += warp_transpose_reduce32<false>(s);
-        if (!mbar_wait_warp(&bars[B_P_EMPTY + pb], (pph & 1) ^ 1, abort_flag, err)) { ok = false; break; }
-        // P^T[head][slot] (K-major swizzled, 2 columns of 64 slots)
-        {
-          const uint32_t kcol = key & 63;
-          uint8_t* pcol = smem + C::OFF_P + pb * C::P_BYTES + (key >> 6) * (HC * 128);
-#pragma unroll
-          for (int h = 0; h < HW; ++h)
-            *reinterpret_cast<uint16_t*>(pcol + sw128_offset(HW * hh + h, kcol)) =
-                (uint16_t)((h & 1) ? (pk[h / 2] >> 16) : (pk[h / 2] & 0xffffu));
-        }
-        if (need && j > 0) {
+        if (!ok) break;
+        if (key == 0 && hb == 0) DSA_TRACE(a.tr, gt, 1);
+        if (j > 0 && __any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
           // O must hold the previous tile's P.V before it is rescaled
-          const int pbp = C::NPB == 2 ? (int)((gt - 1) & 1) : 0;
-          const uint32_t pphp = C::NPB == 2 ? ((gt - 1) >> 1) : (gt - 1);
-          if (!mbar_wait_warp(&bars[B_P_EMPTY + pbp], pphp & 1, abort_flag, err)) {
+          if (!mbar_wait_cluster_warp(&bars[B_PE + (pb ^ 1)], ((gt - 1) >> 1) & 1, abort_flag, err)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          // O^T lane = output column 128m + key, TMEM columns = heads
+          // O^T lane = this CTA's output column of M-block b, TMEM columns = heads
 #pragma unroll 1
-          for (int m = 0; m < 4; ++m) {
-#pragma unroll
-            for (int q16 = 0; q16 < 2; ++q16) {
+          for (int b = 0; b < 2; ++b) {
+#pragma unroll 1
+            for (int q16 = 0; q16 < 4; ++q16) {
               float o[16];
-              const uint32_t ta = tmem + lane_off + C::COL_O + m * HC + HW * hh + 16 * q16;
+              const uint32_t ta = tmem + lane_off + C::COL_O + b * HP + 64 * hb + 16 * q16;
               tmem_ld16(ta, o);
               tmem_ld_wait();
+              const float av = (q16 >> 1) ? alpha[1] : alpha[0];
 #pragma unroll
-              for (int h = 0; h < 16; ++h) o[h] *= __shfl_sync(0xffffffffu, alpha_l, 16 * q16 + h);
+              for (int h = 0; h < 16; ++h) o[h] *= __shfl_sync(0xffffffffu, av, 16 * (q16 & 1) + h);
               tmem_st16(ta, o);
             }
           }
           tmem_st_wait();
         }
+        // P (and the rescale) visible to the tensor core; the peer-bound
+        // rows go out as one 4 KB copy; then this warp's arrival on P_RX
+        // (the warps holding this CTA's own heads also arm the 16 KB the
+        // peer copies in)
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(&bars[B_P_FULL + pb]);
-        if (key == 0 && hh == 0) DSA_TRACE(a.tr, gt, 6);
+        __syncwarp();
+        if (lane == 0) {
+          if (!p_local)
+            bulk_copy_to_peer(peer_rows + (uint32_t)pb * C::P_BYTES, stg_warp, 32u * 128u,
+                              map_peer(smem_u32(&bars[B_PRX + pb]), rank ^ 1));
+          if (p_local)
+            mbar_arrive_expect_tx(&bars[B_PRX + pb], 32u * 128u);
+          else
+            mbar_arrive(&bars[B_PRX + pb]);
+        }
+        if (key == 0 && hb == 0) DSA_TRACE(a.tr, gt, 6);
       }
       if (!ok) break;
-      // -------- epilogue --------
-      float* redb = red + ((gt & 1) * 2 + hh) * (4 * HW);  // not in use by the tile path now
-      if (!group_sync(smx, sync_phase, abort_flag, err)) { ok = false; break; }
-      redb[(warp & 3) * HW + lane] = l_l;
-      if (!group_sync(smx, sync_phase, abort_flag, err)) { ok = false; break; }
-      const float l = redb[0 * HW + lane] + redb[1 * HW + lane] + redb[2 * HW + lane] + redb[3 * HW + lane];
-      const float inv_l_l = (l > 0.f) ? 1.0f / l : 0.f;
-      if (warp == 4 * hh && base + lane < nrows)
-        a.lse[(size_t)t0 * H + base + lane] = (l > 0.f) ? (m_l + log2f(l)) * 0.6931471805599453f : -INFINITY;
-      if (!group_sync(smx, sync_phase, abort_flag, err)) { ok = false; break; }
-      if (!mbar_wait_warp(&bars[B_O_FULL], lgq & 1, abort_flag, err)) { ok = false; break; }
-      tc_fence_after();
-      uint16_t* out_g = a.out + (size_t)(t0 * H + base) * 512;
-#pragma unroll 1
-      for (int m = 0; m < 4; ++m) {
+      // -------- epilogue: the pair's sums, lse, O / l --------
+      float l[2];
 #pragma unroll
-        for (int q16 = 0; q16 < 2; ++q16) {
+      for (int sub = 0; sub < 2; ++sub) {
+        const uint32_t pp = post(sub, l_l[sub]);
+        if (!wait_x(sub, pp)) { ok = false; break; }
+        l[sub] = gathered(sub, pp, false);
+      }
+      if (!ok) break;
+      float inv_l[2];
+#pragma unroll
+      for (int sub = 0; sub < 2; ++sub) {
+        inv_l[sub] = (l[sub] > 0.f) ? 1.0f / l[sub] : 0.f;
+        const int p = 64 * hb + 32 * sub + lane;
+        if (leader && qw == 0 && p < nrows)
+          a.lse[(size_t)t0 * H + p] = (l[sub] > 0.f) ? (m_l[sub] + log2f(l[sub])) * 0.6931471805599453f : -INFINITY;
+      }
+      if (!mbar_wait_cluster_warp(&bars[B_OF], lgq & 1, abort_flag, err)) { ok = false; break; }
+      tc_fence_after();
+      uint16_t* out_g = a.out + (size_t)(t0 * H + 64 * hb) * 512 + 128 * rank + key;
+#pragma unroll 1
+      for (int b = 0; b < 2; ++b) {
+#pragma unroll 1
+        for (int q16 = 0; q16 < 4; ++q16) {
           float o[16];
-          tmem_ld16(tmem + lane_off + C::COL_O + m * HC + HW * hh + 16 * q16, o);
+          tmem_ld16(tmem + lane_off + C::COL_O + b * HP + 64 * hb + 16 * q16, o);
           tmem_ld_wait();
+          const float ilv = (q16 >> 1) ? inv_l[1] : inv_l[0];
 #pragma unroll
           for (int h = 0; h < 16; ++h) {
-            const float il = __shfl_sync(0xffffffffu, inv_l_l, 16 * q16 + h);
-            if (base + 16 * q16 + h < nrows) out_g[(16 * q16 + h) * 512 + m * 128 + key] = f32_to_bf16_rn(o[h] * il);
+            const int hl = 16 * q16 + h;   // head 64hb + hl
+            const float il = __shfl_sync(0xffffffffu, ilv, hl & 31);
+            if (64 * hb + hl < nrows) out_g[(size_t)hl * 512 + 256 * b] = f32_to_bf16_rn(o[h] * il);
           }
         }
       }
       tc_fence_before();
-      mbar_arrive(&bars[B_O_EMPTY]);
+      warp_arrive_leader(&bars[B_OE]);
       ++lgq;
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // no CTA leaves while its peer may still write into it
+  cluster_sync();  // neither CTA leaves or frees tensor memory while the pair may still use it
   tc_fence_after();
-  if (warp == 8) tmem_dealloc(tmem, C::TMEM_COLS);
+  if (warp == 8) tmem_dealloc_pair(tmem, C::TMEM_COLS);
 }
 
 template <int NC>
 static int launch_t(const GroupedArgs& a, int num_sms, cudaStream_t stream) {
-  using C = Cfg<NC>;
+  using C = Cfg;
   static int attr_set[64] = {0};
   static int max_clusters[64] = {0};
   int dev = 0;
