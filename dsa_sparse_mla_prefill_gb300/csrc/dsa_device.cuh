@@ -65,6 +65,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same with a suspend-time hint: a thread whose phase is not complete
+// sleeps until it completes (or the hint, in ns, runs out) instead of
+// returning at once, so waiting warps do not take issue slots from the warps
+// doing the work.
+constexpr uint32_t kSuspendHintNs = 50000;
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "n"(kSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits until the phase with the given parity has completed.  Returns false
 // (and raises the CTA's abort flag and the timeout counter) when the wait ran
 // out or another thread of the CTA already gave up.
@@ -74,7 +91,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
-    if (mbar_try_wait(a, parity)) return true;
+    if (mbar_try_wait_sleep(a, parity)) return true;
     if (*abort_flag) return false;
     if (globaltimer() - t0 > kWaitTimeoutNs) {
       *abort_flag = 1;
@@ -117,13 +134,24 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
       : "memory");
   return ok != 0;
 }
+__device__ __forceinline__ bool mbar_try_wait_cluster_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "n"(kSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                                   unsigned int* err) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait_cluster(a, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
-    if (mbar_try_wait_cluster(a, parity)) return true;
+    if (mbar_try_wait_cluster_sleep(a, parity)) return true;
     if (*abort_flag) return false;
     if (globaltimer() - t0 > kWaitTimeoutNs) {
       *abort_flag = 1;

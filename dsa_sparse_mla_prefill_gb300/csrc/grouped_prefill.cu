@@ -375,6 +375,7 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
               mma_pair_commit(&bars[B_KE + slot], kBoth);
             }
             if (!ok) break;
+            DSA_TRACE(a.tr, gt, 4);
             mma_pair_commit(&bars[B_SF + sb], kBoth);
           }
         }
@@ -393,8 +394,9 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
           for (int j = 0; j < ntiles; ++j, ++gt) {
             const int pb = gt & 1;
             if (!mbar_wait_cluster(&bars[B_PRX + pb], (gt >> 1) & 1, abort_flag, err)) { ok = false; break; }
+            DSA_TRACE(a.tr, gt, 2);
             mbar_arrive_remote(map_peer(smem_u32(&bars[B_PF + pb]), 0));
-            mbar_arrive_remote(stg0);
+            mbar_arrive_remote_relaxed(stg0);
           }
         }
       }
@@ -422,7 +424,8 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
             const int pb = gt & 1;
             const uint32_t pph = (gt >> 1) & 1;
             if (!mbar_wait_cluster(&bars[B_PRX + pb], pph, abort_flag, err)) { ok = false; break; }
-            mbar_arrive_remote(stg1);
+            // (a bare "read done" signal: no data of this thread to publish)
+            mbar_arrive_remote_relaxed(stg1);
             if (!mbar_wait_cluster(&bars[B_PF + pb], pph, abort_flag, err)) { ok = false; break; }
             DSA_TRACE(a.tr, gt, 7);
             if (j == 0 && !mbar_wait_cluster(&bars[B_OE], (lgq & 1) ^ 1, abort_flag, err)) { ok = false; break; }
@@ -576,12 +579,14 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
         uint32_t par[2];
 #pragma unroll
         for (int sub = 0; sub < 2; ++sub) {
+          // the block's 32 heads belong to one token, or (H = 16) to two
+          // split at head 16: split is 16 or at least 32 (H = 128 / G)
           const bool on_lo = (mbyte >> t_lo[sub]) & 1u;
-          const bool on_hi = (mbyte >> (t_lo[sub] + 1)) & 1u;
+          const bool on_hi = split[sub] < 32 ? ((mbyte >> (t_lo[sub] + 1)) & 1u) != 0 : on_lo;
           float tmx = -INFINITY;
 #pragma unroll
           for (int h = 0; h < 32; ++h) {
-            const bool on = (h < split[sub]) ? on_lo : on_hi;
+            const bool on = (h < 16) ? on_lo : on_hi;
             s[sub][h] = on ? s[sub][h] : -INFINITY;
             float r;
             asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(s[sub][h]));
@@ -616,7 +621,6 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
           }
           negm[32 * sub + lane] = (m_l[sub] == -INFINITY) ? 0.f : -m_l[sub];
           __syncwarp();
-          if (sub == 0 && key == 0 && hb == 0) DSA_TRACE(a.tr, gt, 4);
 #pragma unroll
           for (int h = 0; h < 32; h += 8) {
             const float4 n0 = *reinterpret_cast<const float4*>(negm + 32 * sub + h);
