@@ -39,7 +39,7 @@
 // Warp roles (24 warps): 0-7 softmax (two per TMEM lane quarter: warp w
 // holds slots 32(w%4) .. +31 and pseudo-heads 64(w/4) .. +63, as two blocks
 // of 32), 8 QK issuer (and tensor-memory allocation), 9 PV issuer (issuers
-// run in the even CTA only), 10-15 K-ring producers, 16-23 V-ring producers
+// run in the even CTA only), 10-16 K-ring producers, 17-23 V-ring producers
 // (the warps of a stream share every stage).
 #include "dsa_device.cuh"
 #include "dsa_kernels.h"
@@ -54,8 +54,8 @@ constexpr int HC = 64;           // pseudo-heads whose q / P this CTA supplies
 constexpr int NTHREADS = 768;    // 24 warps, launched at 80 registers each
 constexpr int REGS_SOFTMAX = 160;
 constexpr int REGS_OTHER = 40;   // 8*32*160 + 16*32*40 = 768*80
-constexpr int KW0 = 10, NKWARP = 6, KLANES = 6;    // K producers: warps 10-15, lanes 0-5 (33 requests)
-constexpr int VW0 = 16, NVWARP = 8, VLANES = 8;    // V producers: warps 16-23, lanes 0-7 (64 requests)
+constexpr int KW0 = 10, NKWARP = 7, KLANES = 5;    // K producers: warps 10-16, lanes 0-4 (33 requests)
+constexpr int VW0 = 17, NVWARP = 7, VLANES = 10;   // V producers: warps 17-23, lanes 0-9 (64 requests)
 constexpr float kTau = 8.0f;     // lazy-rescale threshold (log2 units)
 constexpr uint16_t kBoth = 3;    // commit to both CTAs' barriers
 
@@ -252,13 +252,13 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
       // A warp issues its TMA requests one after another (the SM's request
       // rate grows with the number of warps issuing), so every stage and
       // unit is shared by the warps of its stream:
-      //   K (warps 10-15): chunk c of a pair tile = this CTA's 128 slots x
+      //   K (warps 10-16): chunk c of a pair tile = this CTA's 128 slots x
       //     columns 64c .. 64c+63 (requests 0-31: slots 4e .. 4e+3) + q chunk
-      //     c of its 64 pseudo-heads (request 32); lanes 0-5 of each warp.
-      //   V (warps 16-23): unit u = 2b + h of a pair tile = the tile's slots
+      //     c of its 64 pseudo-heads (request 32); lanes 0-4 of each warp.
+      //   V (warps 17-23): unit u = 2b + h of a pair tile = the tile's slots
       //     128h .. 128h+127 x this CTA's columns 256b + 128r .. +127, as two
       //     64-column swizzle columns (requests 0-63: slots 4(e % 32) .. +3,
-      //     swizzle column e / 32); lanes 0-7 of each warp.
+      //     swizzle column e / 32); lanes 0-9 of each warp.
       // A 64-slot half that is one run of consecutive rows is one tiled load
       // (box 64 columns x 64 rows) instead of 16 gathers.
       // ----------------------------------------------------------------
@@ -583,16 +583,20 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
           // split at head 16: split is 16 or at least 32 (H = 128 / G)
           const bool on_lo = (mbyte >> t_lo[sub]) & 1u;
           const bool on_hi = split[sub] < 32 ? ((mbyte >> (t_lo[sub] + 1)) & 1u) != 0 : on_lo;
-          float tmx = -INFINITY;
+          // (each warp-wide max goes to this warp's negm area, every lane
+          // storing the same value to the same word; lane L reads head L's
+          // back: cheaper than selecting it lane by lane.  negm is rewritten
+          // with the reference only after these are read.)
 #pragma unroll
           for (int h = 0; h < 32; ++h) {
             const bool on = (h < 16) ? on_lo : on_hi;
             s[sub][h] = on ? s[sub][h] : -INFINITY;
             float r;
             asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(s[sub][h]));
-            if (lane == h) tmx = r;
+            negm[32 * sub + h] = r;
           }
-          par[sub] = post(sub, tmx);
+          __syncwarp();
+          par[sub] = post(sub, negm[32 * sub + lane]);
         }
         // P buffer pb (in both CTAs) is free once the P.V two tiles back is
         // done; the staging rows once the peer acknowledged the last copy
@@ -607,7 +611,7 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
         // this slot, heads 64hb .. 64hb+63, row 128 rank + key of CTA hb's
         // P buffer (or of the staging rows), 128 bytes = 8 chunks of 8
         // heads, chunk c at (c ^ (row & 7)) * 16 (128-byte swizzle,
-        // MN-major); and the row sums of the rounded values
+        // MN-major); and the row sums (of P before its rounding to bf16)
         float alpha[2] = {1.f, 1.f};
         const uint32_t sw = (uint32_t)(key & 7);
 #pragma unroll
@@ -625,26 +629,22 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
           for (int h = 0; h < 32; h += 8) {
             const float4 n0 = *reinterpret_cast<const float4*>(negm + 32 * sub + h);
             const float4 n1 = *reinterpret_cast<const float4*>(negm + 32 * sub + h + 4);
-            const uint32_t w0 = pack_bf16x2(exp2f(fmaf(s[sub][h + 0], c_log2, n0.x)),
-                                            exp2f(fmaf(s[sub][h + 1], c_log2, n0.y)));
-            const uint32_t w1 = pack_bf16x2(exp2f(fmaf(s[sub][h + 2], c_log2, n0.z)),
-                                            exp2f(fmaf(s[sub][h + 3], c_log2, n0.w)));
-            const uint32_t w2 = pack_bf16x2(exp2f(fmaf(s[sub][h + 4], c_log2, n1.x)),
-                                            exp2f(fmaf(s[sub][h + 5], c_log2, n1.y)));
-            const uint32_t w3 = pack_bf16x2(exp2f(fmaf(s[sub][h + 6], c_log2, n1.z)),
-                                            exp2f(fmaf(s[sub][h + 7], c_log2, n1.w)));
+            float p[8];
+            p[0] = exp2f(fmaf(s[sub][h + 0], c_log2, n0.x));
+            p[1] = exp2f(fmaf(s[sub][h + 1], c_log2, n0.y));
+            p[2] = exp2f(fmaf(s[sub][h + 2], c_log2, n0.z));
+            p[3] = exp2f(fmaf(s[sub][h + 3], c_log2, n0.w));
+            p[4] = exp2f(fmaf(s[sub][h + 4], c_log2, n1.x));
+            p[5] = exp2f(fmaf(s[sub][h + 5], c_log2, n1.y));
+            p[6] = exp2f(fmaf(s[sub][h + 6], c_log2, n1.z));
+            p[7] = exp2f(fmaf(s[sub][h + 7], c_log2, n1.w));
             const uint32_t c = (uint32_t)(4 * sub + h / 8);
             const uint32_t addr = p_dst + ((c ^ sw) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w0), "r"(w1), "r"(w2), "r"(w3)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pack_bf16x2(p[0], p[1])),
+                         "r"(pack_bf16x2(p[2], p[3])), "r"(pack_bf16x2(p[4], p[5])), "r"(pack_bf16x2(p[6], p[7]))
                          : "memory");
-            s[sub][h + 0] = __uint_as_float(w0 << 16);
-            s[sub][h + 1] = __uint_as_float(w0 & 0xffff0000u);
-            s[sub][h + 2] = __uint_as_float(w1 << 16);
-            s[sub][h + 3] = __uint_as_float(w1 & 0xffff0000u);
-            s[sub][h + 4] = __uint_as_float(w2 << 16);
-            s[sub][h + 5] = __uint_as_float(w2 & 0xffff0000u);
-            s[sub][h + 6] = __uint_as_float(w3 << 16);
-            s[sub][h + 7] = __uint_as_float(w3 & 0xffff0000u);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) s[sub][h + i] = p[i];
           }
           l_l[sub] += warp_transpose_reduce32<false>(s[sub]);
         }
