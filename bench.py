@@ -302,6 +302,14 @@ def run_modes(dev, stream, peaks, steps, warmup, flush, only=None):
             res["per_token"] = {"ms": ms, "query_tokens_per_s": w.T / ms * 1e3,
                                 "useful_tflops": flops / ms / 1e9, "logical_gbs": abytes / ms / 1e6,
                                 "hbm_frac_logical": abytes / ms / 1e6 / peaks["hbm_gbs"]}
+            # DRAM bytes from a committed ncu capture of this workload (scaled
+            # by tokens; none if the kernel changed since)
+            if w.H == 32 and w.d_qk == 576:
+                traffic = profiled_traffic("sparse_prefill_" + w.name, kernel_source_hash(
+                    ["sparse_prefill.cu", "dsa_device.cuh"]), w.T)
+                if traffic:
+                    res["per_token"].update(dram_bytes=traffic, dram_gbs=traffic / ms / 1e6,
+                                            dram_frac=traffic / ms / 1e6 / peaks["hbm_gbs"])
         if grouped:
             G = w.G
             upad = dsa.dsa_union_pad(G, w.k, 128)
@@ -342,6 +350,11 @@ def run_modes(dev, stream, peaks, steps, warmup, flush, only=None):
         if want(name):
             out[name] = sparse_block(name)
             torch.cuda.empty_cache()
+    # the headline shard at the tail of a 131072-row context: the 151 MB
+    # latent table does not fit in the L2 (per-token form only)
+    if want("v32_h32_16k_of_128k"):
+        out["v32_h32_16k_of_128k"] = sparse_block("v32_h32_16k_of_128k", grouped=False)
+        torch.cuda.empty_cache()
     # the headline workload in grouped form (H = 32: G = 4 tokens per group)
     if want("v32_h32_16k_grouped"):
         out["v32_h32_16k_grouped"] = sparse_block("v32_h32_16k", per_token=False)

@@ -196,6 +196,13 @@ WORKLOADS = {
         d_qk=576, d_v=512, k=2048, ld=2048, scale=1.0 / math.sqrt(192.0),
         index_gen="locality", G=4, seed=1,
         notes="1 request, 16384 causal tokens, locality top-2048"),
+    # The same shard at the tail of a 131072-row context: 16384 queries at
+    # positions 114688..131071, so the latent table (151 MB) exceeds the L2.
+    "v32_h32_16k_of_128k": Workload(
+        name="v32_h32_16k_of_128k", mode="sparse", q_lens=(16384,), kv_lens=(131072,), H=32,
+        d_qk=576, d_v=512, k=2048, ld=2048, scale=1.0 / math.sqrt(192.0),
+        index_gen="locality", G=4, seed=7,
+        notes="16384 queries after 114688 cached rows, locality top-2048; table larger than the L2"),
     # 21504 queries appended after 11264 cached rows (32768-row prompt), H=16, G=8.
     "grouped_21k_of_32k": Workload(
         name="grouped_21k_of_32k", mode="sparse", q_lens=(21504,), kv_lens=(32768,), H=16,

@@ -123,7 +123,7 @@ def test_many_tokens_per_cta_small_k():
     check(q, kv, idx, k, 1.0 / 16.0, 512)
 
 
-@pytest.mark.parametrize("name", ["v32_h32_16k", "nope_2x8192", "grouped_21k_of_32k"])
+@pytest.mark.parametrize("name", ["v32_h32_16k", "nope_2x8192", "grouped_21k_of_32k", "v32_h32_16k_of_128k"])
 def test_full_size_sampled(name):
     """Full-size workload, launched exactly as the bench does; the oracle
     checks a stratified sample of tokens (both ends, dense early tokens,
@@ -133,7 +133,7 @@ def test_full_size_sampled(name):
     o, l = run_gpu(x.q, x.kv, x.idx, w.k, w.scale)
     assert np.isfinite(o).all() and np.isfinite(l).all()
     rng = np.random.default_rng(123)
-    toks = stratified_tokens(w.T, 40, rng, must=[1, 2047, 2048, 8191, 8192, w.T // 2])
+    toks = stratified_tokens(w.T, 40, rng, must=[1, 2047, 2048, 8191, 8192, w.T // 2, w.T - 1])
     ro, rl = O.sparse_prefill(x.q, x.kv, x.idx, w.k, w.scale, w.d_qk, w.d_v, tokens=toks)
     res = O.compare(o[toks], l[toks], ro, rl)
     assert res["ok"], res
