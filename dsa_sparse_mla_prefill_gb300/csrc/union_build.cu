@@ -65,6 +65,24 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* w
   return before + x - v;
 }
 
+// Fills row[lo, hi) with v: single stores up to a 16-byte boundary, then
+// 16-byte stores (row is 16-byte aligned and hi a multiple of 4).
+__device__ __forceinline__ void fill_i32(int32_t* row, uint32_t lo, uint32_t hi, int32_t v) {
+  const uint32_t a4 = min((lo + 3u) & ~3u, hi);
+  for (uint32_t u = lo + threadIdx.x; u < a4; u += NT) row[u] = v;
+  int4* r4 = reinterpret_cast<int4*>(row);
+  const int4 v4 = make_int4(v, v, v, v);
+  for (uint32_t u = a4 / 4 + threadIdx.x; u < hi / 4; u += NT) r4[u] = v4;
+}
+
+// Zeroes n 32-bit words of shared memory at p (16-byte aligned): 16-byte
+// stores, then the tail.
+__device__ __forceinline__ void zero_smem(uint32_t* p, int n) {
+  uint4* p4 = reinterpret_cast<uint4*>(p);
+  for (int i = threadIdx.x; i < n / 4; i += NT) p4[i] = make_uint4(0u, 0u, 0u, 0u);
+  for (int i = (n & ~3) + threadIdx.x; i < n; i += NT) p[i] = 0u;
+}
+
 __global__ void __launch_bounds__(NT) union_build_kernel(UnionArgs a) {
   extern __shared__ __align__(16) uint32_t sm[];
   const int W = (a.N + 31) >> 5;
@@ -79,8 +97,8 @@ __global__ void __launch_bounds__(NT) union_build_kernel(UnionArgs a) {
   int t0, n;
   group_of(a.req, a.G, g, t0, n);
 
-  for (int i = threadIdx.x; i < W; i += NT) bitmap[i] = 0u;
-  for (int i = threadIdx.x; i < a.union_pad / 4; i += NT) maskw[i] = 0u;
+  zero_smem(bitmap, W);
+  zero_smem(maskw, a.union_pad / 4);
   __syncthreads();
 
   // 1) bitmap of every valid row of the group's tokens.  Register path: each
@@ -157,7 +175,7 @@ __global__ void __launch_bounds__(NT) union_build_kernel(UnionArgs a) {
       ++pos;
     }
   }
-  for (uint32_t u = Ucap + threadIdx.x; u < (uint32_t)a.union_pad; u += NT) urow[u] = -1;
+  fill_i32(urow, Ucap, (uint32_t)a.union_pad, -1);
 
   // 4) membership bits: slot of row x = prefix[x>>5] + popc(bits below x)
   auto member = [&](int x, int j) {
@@ -193,7 +211,7 @@ __global__ void __launch_bounds__(NT) union_build_kernel(UnionArgs a) {
 // Token-bitmap variant (see the top of the file).  Shared memory: G token
 // bitmaps of WS = Wp | 1 words each (an odd stride puts the G words of one
 // position in different banks), prefix[Wp], and the mask bytes of the row.
-__global__ void __launch_bounds__(NT) union_build_tokbits_kernel(UnionArgs a) {
+__global__ void __launch_bounds__(NT, 4) union_build_tokbits_kernel(UnionArgs a) {
   extern __shared__ __align__(16) uint32_t sm[];
   const int W = (a.N + 31) >> 5;
   const int Wp = (W + 3) & ~3;
@@ -209,8 +227,8 @@ __global__ void __launch_bounds__(NT) union_build_tokbits_kernel(UnionArgs a) {
   int t0, n;
   group_of(a.req, a.G, g, t0, n);
 
-  for (int i = threadIdx.x; i < a.G * WS; i += NT) tb[i] = 0u;
-  for (int i = threadIdx.x; i < a.union_pad / 4; i += NT) maskw[i] = 0u;
+  zero_smem(tb, a.G * WS);
+  zero_smem(maskw, a.union_pad / 4);
   __syncthreads();
 
   // 1) token j's bitmap from its valid rows (16-byte loads of entries 4t..4t+3
@@ -293,7 +311,7 @@ __global__ void __launch_bounds__(NT) union_build_tokbits_kernel(UnionArgs a) {
       ++pos;
     }
   }
-  for (uint32_t u = Ucap + threadIdx.x; u < (uint32_t)a.union_pad; u += NT) urow[u] = -1;
+  fill_i32(urow, Ucap, (uint32_t)a.union_pad, -1);
   __syncthreads();
 
   // 4) mask row out (16-byte stores; union_pad is a multiple of 16)
