@@ -172,10 +172,11 @@ def job_throughput(units_per_rank, world, ms_max):
 # ----------------------------------------------------------------------------
 # workloads and algorithmic work
 # ----------------------------------------------------------------------------
-def sparse_work(w, idx):
-    """Valid (token, key) pairs and algorithmic bytes / useful FLOPs of the per-token form."""
+def sparse_work(w, idx, row_bytes=None):
+    """Valid (token, key) pairs and algorithmic bytes / useful FLOPs of the per-token form
+    (row_bytes: bytes gathered per selected row, the bf16 row unless given)."""
     pairs = int((idx[:, :w.k] >= 0).sum())
-    row = w.d_qk * 2
+    row = w.d_qk * 2 if row_bytes is None else row_bytes
     bytes_ = pairs * row + w.T * w.H * w.d_qk * 2 + w.T * w.H * w.d_v * 2 + w.T * w.ld * 4 + w.T * w.H * 4
     flops = 2.0 * w.H * pairs * (w.d_qk + w.d_v)
     return pairs, bytes_, flops
@@ -367,7 +368,8 @@ def run_modes(dev, stream, peaks, steps, warmup, flush, only=None):
         out["grouped_21k_of_32k_wide"] = sparse_block("grouped_21k_of_32k_wide", w=wide)
         torch.cuda.empty_cache()
     # the headline workload over an FP8 KV cache: the cache is written once
-    # (quantize), each step dequantizes it and runs the per-token kernel
+    # (quantize); a step is either the per-token kernel reading the FP8 rows
+    # directly, or a dequantize to bf16 followed by the bf16 per-token kernel
     if want("v32_h32_16k_fp8kv"):
         w = WORKLOADS["v32_h32_16k"]
         log("mode v32_h32_16k_fp8kv")
@@ -386,14 +388,21 @@ def run_modes(dev, stream, peaks, steps, warmup, flush, only=None):
             dsa.dsa_kv_fp8_dequantize(fp8, 64, out=deq)
             dsa.dsa_sparse_prefill(q, deq, idx, w.k, w.scale, out=o, lse=l)
         ms_s = statistics.median(timed_steps(fp8_step, steps, warmup, stream, flush))
+        ms_f = statistics.median(timed_steps(lambda: dsa.dsa_sparse_prefill_fp8(q, fp8, idx, w.k, w.scale, out=o,
+                                                                                 lse=l), steps, warmup, stream, flush))
         rb = dsa.dsa_kv_fp8_row_bytes(64)
         qbytes = w.N * (w.d_qk * 2 + rb)
         dbytes = w.N * (rb + w.d_qk * 2)
+        _, fbytes, fflops = sparse_work(w, x.idx, row_bytes=rb)
         out["v32_h32_16k_fp8kv"] = {
             "cache_bytes": w.N * rb, "cache_bytes_bf16": w.N * w.d_qk * 2,
             "quantize": {"ms": ms_q, "gbs": qbytes / ms_q / 1e6, "hbm_frac": qbytes / ms_q / 1e6 / peaks["hbm_gbs"]},
             "dequantize": {"ms": ms_d, "gbs": dbytes / ms_d / 1e6, "hbm_frac": dbytes / ms_d / 1e6 / peaks["hbm_gbs"]},
-            "dequantize_plus_per_token": {"ms": ms_s, "query_tokens_per_s": w.T / ms_s * 1e3}}
+            "dequantize_plus_per_token": {"ms": ms_s, "query_tokens_per_s": w.T / ms_s * 1e3},
+            "per_token_fp8": {"ms": ms_f, "query_tokens_per_s": w.T / ms_f * 1e3,
+                              "algorithmic_bytes": fbytes, "row_bytes": rb, "logical_gbs": fbytes / ms_f / 1e6,
+                              "hbm_frac_logical": fbytes / ms_f / 1e6 / peaks["hbm_gbs"],
+                              "useful_tflops": fflops / ms_f / 1e9}}
         del q, kv, idx, fp8, deq, o, l
         torch.cuda.empty_cache()
 

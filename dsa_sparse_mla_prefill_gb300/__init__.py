@@ -92,6 +92,7 @@ _SIGNATURES = {
     "dsa_kv_fp8_row_bytes": (_L, [_I]),
     "dsa_kv_fp8_quantize": (_I, [_VP, _I, _I, _I, _VP, _VP]),
     "dsa_kv_fp8_dequantize": (_I, [_VP, _I, _I, _VP, _I, _VP]),
+    "dsa_sparse_prefill_fp8": (_I, [_VP, _VP, _I, _I, _VP, _I, _I, _I, _I, _I, _I, _F, _VP, _VP, _VP]),
     "dsa_form_calibration_default": (_I, [ctypes.POINTER(FormCalibration)]),
     "dsa_choose_form": (_I, [ctypes.POINTER(FormQuery), ctypes.POINTER(FormCalibration),
                              ctypes.POINTER(FormEstimate)]),
@@ -521,3 +522,29 @@ def dsa_debug_trace(buffer=None, capacity: int = 0):
     if buffer.numel() < 2 * capacity * 8 or not buffer.is_cuda:
         raise ValueError("trace buffer too small or not on the GPU")
     _check(lib().dsa_debug_trace(buffer.data_ptr(), capacity), "dsa_debug_trace")
+
+
+def dsa_sparse_prefill_fp8(q, kv_fp8, idx, k: int, scale: float, d_rope: int = 64, d_v: int = 512, out=None,
+                           lse=None, stream=None):
+    """Per-token sparse prefill over FP8 latent rows kv_fp8 [N, dsa_kv_fp8_row_bytes(d_rope)] uint8, read
+    and dequantized inside the kernel.  q [T, H, 512 + d_rope] bf16, idx [T, ld] int32 global rows.
+    Returns (out [T, H, d_v] bf16, lse [T, H] fp32), bit-equal to dsa_kv_fp8_dequantize followed by
+    dsa_sparse_prefill."""
+    import torch
+    _need(q, torch.bfloat16, "q", 3)
+    _need(kv_fp8, torch.uint8, "kv_fp8", 2)
+    _need(idx, torch.int32, "idx", 2)
+    T, H, d_qk = q.shape
+    N, rb = kv_fp8.shape
+    if rb != dsa_kv_fp8_row_bytes(d_rope):
+        raise ValueError("kv_fp8 rows must be dsa_kv_fp8_row_bytes(d_rope) bytes")
+    if idx.shape[0] != T:
+        raise ValueError("idx rows must match q tokens")
+    if out is None:
+        out = torch.empty((T, H, d_v), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
+    _check(lib().dsa_sparse_prefill_fp8(q.data_ptr(), kv_fp8.data_ptr(), N, int(d_rope), idx.data_ptr(), T, H, d_qk,
+                                        d_v, k, idx.shape[1], float(scale), out.data_ptr(), lse.data_ptr(),
+                                        _stream(stream, q.device)), "dsa_sparse_prefill_fp8")
+    return out, lse

@@ -169,6 +169,8 @@ int dsa_sparse_prefill(const uint16_t* q, const uint16_t* kv, int N, int ld_kv, 
   dsa::SparseArgs a;
   a.q = q;
   a.kv = kv;
+  a.kv8 = nullptr;
+  a.row_bytes = 0;
   a.idx = idx;
   a.out = out;
   a.lse = lse;
@@ -419,6 +421,47 @@ int dsa_kv_fp8_quantize(const uint16_t* kv, int N, int ld_kv, int d_rope, uint8_
 
 int dsa_kv_fp8_dequantize(const uint8_t* kv_fp8, int N, int d_rope, uint16_t* kv, int ld_kv, dsa_stream_t stream) {
   return kv_fp8_call(nullptr, kv, nullptr, kv_fp8, N, ld_kv, d_rope, false, stream);
+}
+
+int dsa_sparse_prefill_fp8(const uint16_t* q, const uint8_t* kv_fp8, int N, int d_rope, const int32_t* idx, int T,
+                           int H, int d_qk, int d_v, int k, int ld, float scale, uint16_t* out, float* lse,
+                           dsa_stream_t stream) {
+  if (T < 0 || N < 0 || k < 0 || ld < k) return DSA_ERR_INVALID_ARG;
+  if (!(H == 16 || H == 32) || !(d_rope == 0 || d_rope == 64) || d_qk != 512 + d_rope || d_v != 512 || k > 2048)
+    return DSA_ERR_UNSUPPORTED;
+  if (T == 0) return DSA_OK;
+  if (!q || (!kv_fp8 && N > 0) || !idx || !out || !lse) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv_fp8) || !aligned4(idx) || !aligned4(out) || !aligned4(lse))
+    return DSA_ERR_INVALID_ARG;
+  DevInfo* d;
+  if (!dev_info(&d)) return DSA_ERR_CUDA;
+  const int rb = (int)dsa_kv_fp8_row_bytes(d_rope);
+  dsa::SparseArgs a;
+  a.q = q;
+  a.kv = nullptr;
+  a.kv8 = kv_fp8;
+  a.row_bytes = rb;
+  a.idx = idx;
+  a.out = out;
+  a.lse = lse;
+  a.err = d->err;
+  a.T = T;
+  a.H = H;
+  a.d_qk = d_qk;
+  a.N = N;
+  a.ld_kv = 0;
+  a.k = k;
+  a.ld = ld;
+  a.scale = scale;
+  a.tr = g_trace;
+  // With N = 0 no tile is formed and the map is never used: it is encoded
+  // over q (T*H rows of 2*d_qk >= rb bytes) so that it is well formed.
+  if (!dsa::make_row_gather_map_u8(&a.tmap_kv, N > 0 ? (const void*)kv_fp8 : (const void*)q,
+                                   N > 0 ? N : (int64_t)T * H, N > 0 ? rb : 2 * d_qk))
+    return DSA_ERR_CUDA;
+  if (!dsa::make_tile_map(&a.tmap_q, q, (int64_t)T * H, d_qk, d_qk, H)) return DSA_ERR_CUDA;
+  const int r = dsa::launch_sparse_prefill_fp8(a, d->num_sms, (cudaStream_t)stream);
+  return r == 0 ? DSA_OK : (r == -2 ? DSA_ERR_UNSUPPORTED : DSA_ERR_CUDA);
 }
 
 int dsa_debug_wait_timeout(dsa_stream_t stream) {

@@ -6,6 +6,7 @@
 
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace dsa {
@@ -238,6 +239,62 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// ---------------------------------------------------------------------------
+// FP8 latent rows: float8 e4m3 codes times a per-block fp32 scale, rounded to
+// bf16.  Every e4m3 value is exact in f16 and f32; the product is one IEEE
+// float32 multiply that keeps subnormals (no .ftz, while the library is
+// otherwise built to flush them), then round-to-nearest-even to bf16.  The
+// dequantize kernel and the attention kernels that read FP8 rows share this
+// one routine, so the two paths give the same bits.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t f16x2_scaled_bf16x2(uint32_t h, float s) {
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));   // .x: the low half
+  float lo, hi;
+  asm("{.reg .b64 x, y, d;\n\t"
+      "mov.b64 x, {%2, %3};\n\t"
+      "mov.b64 y, {%4, %4};\n\t"
+      "mul.rn.f32x2 d, x, y;\n\t"
+      "mov.b64 {%0, %1}, d;}"
+      : "=f"(lo), "=f"(hi) : "f"(f.x), "f"(f.y), "f"(s));
+  return pack_bf16x2(lo, hi);
+}
+// four codes (byte i of w = code i) -> bf16 pairs: lo = codes 0, 1; hi = codes 2, 3
+__device__ __forceinline__ void e4m3x4_dequant_bf16x4(uint32_t w, float s, uint32_t& lo, uint32_t& hi) {
+  uint32_t h0, h1;
+  asm("{.reg .b16 l, h;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h;}"
+      : "=r"(h0), "=r"(h1) : "r"(w));
+  lo = f16x2_scaled_bf16x2(h0, s);
+  hi = f16x2_scaled_bf16x2(h1, s);
+}
+
+// cp.async of 4 bytes (src_bytes = 0: zero fill), and an arrival on an
+// mbarrier once this thread's earlier cp.async copies have landed (the
+// barrier's pending count is raised now and lowered then).
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+
+// 16-byte shared-memory accesses by 32-bit shared address
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
@@ -543,6 +600,11 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+__device__ __forceinline__ void tmem_st8_u32(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
 __device__ __forceinline__ void tmem_st16_u32(uint32_t taddr, const uint32_t* r) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "

@@ -32,6 +32,8 @@ struct SparseArgs {
   CUtensorMap tmap_q;   // q viewed [T*H, d_qk], 64-column x H-row box
   const uint16_t* q;    // [T, H, d_qk] bf16
   const uint16_t* kv;   // [N, ld_kv] bf16
+  const uint8_t* kv8;   // FP8 rows [N, row_bytes] (the FP8 kernel; tmap_kv is then a byte map over them)
+  int row_bytes;
   const int32_t* idx;   // [T, ld]
   uint16_t* out;        // [T, H, 512] bf16
   float* lse;           // [T, H]
@@ -131,6 +133,7 @@ inline int64_t union_build_tokbits_smem_bytes(int N, int G, int union_pad) {
 // Each returns 0 on success, -1 on a CUDA launch error, -2 if the shape has
 // no kernel instance.
 int launch_sparse_prefill(const SparseArgs& a, int num_sms, cudaStream_t stream);
+int launch_sparse_prefill_fp8(const SparseArgs& a, int num_sms, cudaStream_t stream);
 int launch_union_build(const UnionArgs& a, cudaStream_t stream);
 int launch_topk_to_key_mask(const KeyMaskArgs& a, cudaStream_t stream);
 int launch_local_to_global(const ConvertArgs& a, cudaStream_t stream);

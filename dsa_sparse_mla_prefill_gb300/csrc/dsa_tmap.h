@@ -45,6 +45,22 @@ inline bool make_row_gather_map(CUtensorMap* m, const void* base, int64_t rows, 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D byte map over `rows` rows of `row_bytes` bytes (also the row pitch, a
+// multiple of 16): box = 128 bytes x 1 row with 128-byte swizzle, so one
+// tile::gather4 load brings 4 rows of 128 bytes, as over bf16 rows.  Rows
+// outside [0, rows) read as zero bytes.  For the FP8 latent rows.
+inline bool make_row_gather_map_u8(CUtensorMap* m, const void* base, int64_t rows, int64_t row_bytes) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (fn == nullptr || rows < 1 || row_bytes < 128 || (row_bytes % 16) != 0) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  cuuint32_t box[2] = {128u, 1u};
+  cuuint32_t es[2] = {1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-D bf16 map with box = 64 columns x `box_rows` rows, 128-byte swizzle: a
 // tile of box_rows rows lands as box_rows consecutive 128-byte rows, the
 // K-major layout of one swizzle column of an MMA operand.

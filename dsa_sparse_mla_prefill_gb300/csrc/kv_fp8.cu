@@ -12,7 +12,9 @@
 //
 // The float32 steps are IEEE operations that keep subnormal values (written
 // as PTX without .ftz, since the library is otherwise built to flush them),
-// so tiny values and tiny scales follow the definition exactly.
+// so tiny values and tiny scales follow the definition exactly.  The
+// dequantize arithmetic is the shared e4m3x4_dequant_bf16x4, which the
+// attention kernels that read FP8 rows directly also use.
 //
 // One warp per 128-column block (lane l: columns 4l .. 4l+3 of the block),
 // four warps per row, rows strided over the grid.
@@ -32,23 +34,12 @@ __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
   return r;   // low byte: lo's code
 }
 
-__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint16_t v) {
-  uint32_t h;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(v));
-  return __half22float2(*reinterpret_cast<const __half2*>(&h));   // .x: low byte
-}
-
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
 
 // IEEE float32 operations that keep subnormals
 __device__ __forceinline__ float div_ieee(float a, float b) {
   float r;
   asm("div.rn.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
-  return r;
-}
-__device__ __forceinline__ float mul_ieee(float a, float b) {
-  float r;
-  asm("mul.rn.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
   return r;
 }
 __device__ __forceinline__ float max_ieee(float a, float b) {
@@ -93,11 +84,8 @@ __global__ void __launch_bounds__(NT) dequantize_kernel(Fp8KvArgs a) {
     uint16_t* dst = a.kv_out + (size_t)n * a.ld_kv;
     const uint32_t codes = *reinterpret_cast<const uint32_t*>(src + 128 * w + 4 * lane);
     const float scale = *reinterpret_cast<const float*>(src + 512 + 4 * w);
-    const float2 p = e4m3x2_to_f32x2((uint16_t)(codes & 0xffffu));
-    const float2 q = e4m3x2_to_f32x2((uint16_t)(codes >> 16));
     uint2 out;
-    out.x = pack_bf16x2(mul_ieee(p.x, scale), mul_ieee(p.y, scale));
-    out.y = pack_bf16x2(mul_ieee(q.x, scale), mul_ieee(q.y, scale));
+    e4m3x4_dequant_bf16x4(codes, scale, out.x, out.y);
     *reinterpret_cast<uint2*>(dst + 128 * w + 4 * lane) = out;
     if (w == 0 && 2 * lane < a.d_rope)
       *reinterpret_cast<uint32_t*>(dst + 512 + 2 * lane) = *reinterpret_cast<const uint32_t*>(src + 528 + 4 * lane);

@@ -32,30 +32,64 @@
 //               max grows by more than 2^8), P written bf16 to shared
 //               memory, and the epilogue (O^T lane = output column).
 //   Warps 0-3 run at 192 registers, warps 4-19 at 72.
+//
+// FP8 rows (the same kernel with F8 = true; row = 512 e4m3 codes | 4 fp32
+// block scales | bf16 RoPE): the key rows are gathered as codes, half the
+// bytes, and turned into bf16 on chip with the dequantize arithmetic
+// (e4m3x4_dequant_bf16x4), so the result is bit-for-bit that of the bf16
+// kernel on the dequantized table.  Sixteen producer warps (8-23), thread =
+// key row:
+//   warps 8-15  K stream: every 128-code block (and the RoPE columns) is
+//               gathered into a code ring (tile::gather4, 4 rows x 128 bytes),
+//               then each thread converts its row's half block and writes it
+//               with tcgen05.st into a TMEM chunk ring, which the QK MMAs
+//               read as their A operand (no bf16 K tile in shared memory).
+//   warps 16-23 V stream: the same blocks again into a second code ring,
+//               converted into the 128B-swizzled V units the P.V MMAs read.
+//   Warps 0-3 run at 176 registers, warps 4-23 at 56 (768 threads at 80).
 #include "dsa_device.cuh"
 #include "dsa_kernels.h"
 
 namespace dsa {
 namespace sparse {
 
+template <bool B>
+struct BoolConst {
+  static constexpr bool value = B;
+};
+
 constexpr int BK = 128;         // keys per tile (the MMA's M)
 constexpr int KMAX = 2048;      // longest index row the kernel compacts
-constexpr int NTHREADS = 640;   // 20 warps, launched at 96 registers each
 constexpr int REGS_SOFTMAX = 192; // warpgroup 0 after rebalancing
-constexpr int REGS_OTHER = 72;    // warpgroups 1-4 (4*32*192 + 16*32*72 = 640*96)
 constexpr float kTau = 8.0f;    // lazy-rescale threshold (log2 units)
 
-template <int H, int NC>
+template <int H, int NC, bool F8>
 struct Cfg {
+  // bf16 rows: 20 warps launched at 96 registers; the softmax warpgroup
+  // raised to 192, warpgroups 1-4 lowered to 72 (4*32*192 + 16*32*72 =
+  // 640*96).  FP8 rows: 24 warps at 80; softmax 176, the other five
+  // warpgroups 56 (128*176 + 640*56 <= 768*80).  One setmaxnreg for all the
+  // warps after the softmax warpgroup: a per-warpgroup choice behind a branch
+  // cost the bf16 kernel 12 % (ptxas then allocates those regions more
+  // conservatively), and giving the MMA warpgroup 64 did not pay here.
+  static constexpr int NTHREADS = F8 ? 768 : 640;
+  static constexpr int REGS_SMX = F8 ? 176 : REGS_SOFTMAX;
+  static constexpr int REGS_WG1 = F8 ? 56 : 72;
+  static constexpr int REGS_PROD = F8 ? 56 : 72;
+  static_assert(128 * REGS_SMX + 128 * REGS_WG1 + (NTHREADS - 256) * REGS_PROD <= NTHREADS * (F8 ? 80 : 96),
+                "registers");
   static constexpr uint32_t CHUNK_BYTES = BK * 128u;            // 128 keys x 64 columns: one swizzle column
   static constexpr uint32_t UNIT_BYTES = 2u * CHUNK_BYTES;      // 128 keys x 128 columns: one PV M-block
   static constexpr uint32_t Q_BYTES = NC * H * 128u;
   static constexpr uint32_t P_BYTES = 2u * H * 128u;            // 128 keys = 2 swizzle columns
   static constexpr uint32_t KIDX_BYTES = 2u * KMAX * 4u;
   static constexpr uint32_t RED_BYTES = 2u * 4u * H * 4u;
-  static constexpr int NBAR = 44;
+  static constexpr int NBAR = F8 ? 92 : 44;
   static constexpr uint32_t TAIL = NBAR * 8u + 64u + 1024u;     // barriers, misc words, alignment slack
   static constexpr uint32_t SMEM_LIMIT = 227u * 1024u;
+  // FP8 rows: one fp32 block scale per row of each code slot (at most 6 slots)
+  static constexpr uint32_t SCL_BYTES = F8 ? 6u * BK * 4u : 0u;
+  static constexpr uint32_t FIXED = Q_BYTES + P_BYTES + KIDX_BYTES + RED_BYTES + SCL_BYTES + TAIL;
   // V ring: 128-column units for PV; K ring: 64-column chunks for QK.
   // Every thread that waits on a ring barrier must pass through each of
   // its phases in order (a phase two ahead has the parity of one that
@@ -64,25 +98,39 @@ struct Cfg {
   // issuer m mod 2; K slot s is filled by K producer warp s and consumed
   // by the QK issuer, which takes every chunk.
   static constexpr int NVR = 2;
-  static constexpr int NKR_FIT =
-      (int)((SMEM_LIMIT - TAIL - Q_BYTES - P_BYTES - KIDX_BYTES - RED_BYTES - NVR * UNIT_BYTES) / CHUNK_BYTES);
-  static constexpr int NKR = 6;   // one slot per K-stream warp
-  static_assert(NKR_FIT >= NKR, "shared memory budget");
+  static constexpr int NFIT = (int)((SMEM_LIMIT - FIXED - NVR * UNIT_BYTES) / CHUNK_BYTES);
+  // bf16 rows: K ring of NKR chunk slots in shared memory, one per K-stream warp.
+  static constexpr int NKR = F8 ? 0 : 6;
+  // FP8 rows: code rings of 16 KB slots (128 rows x 128 bytes), NKC for the
+  // K stream and NVC for the V stream; the K chunks live in TMEM (NKT slots).
+  static constexpr int NVC = F8 ? 2 : 0;
+  static constexpr int NKC = F8 ? (NFIT - NVC < 4 ? NFIT - NVC : 4) : 0;
+  static constexpr int NKT = F8 ? 6 : 0;
+  static_assert(NFIT >= NKR + NKC + NVC, "shared memory budget");
+  static_assert(!F8 || NKC >= 2, "shared memory budget");
+  static_assert(NKC + NVC <= 6, "scale words");
   static_assert(NVR == 2, "V slot = unit mod 2 = PV issuer");
   static constexpr uint32_t OFF_KR = 0;
-  static constexpr uint32_t OFF_VR = OFF_KR + NKR * CHUNK_BYTES;
+  static constexpr uint32_t OFF_KC = 0;
+  static constexpr uint32_t OFF_VC = OFF_KC + NKC * CHUNK_BYTES;
+  static constexpr uint32_t OFF_VR = NKR * CHUNK_BYTES + (NKC + NVC) * CHUNK_BYTES;
   static constexpr uint32_t OFF_Q = OFF_VR + NVR * UNIT_BYTES;
   static constexpr uint32_t OFF_P = OFF_Q + Q_BYTES;
   static constexpr uint32_t OFF_KIDX = OFF_P + P_BYTES;
   static constexpr uint32_t OFF_RED = OFF_KIDX + KIDX_BYTES;
-  static constexpr uint32_t OFF_BAR = OFF_RED + RED_BYTES;
+  static constexpr uint32_t OFF_SCL = OFF_RED + RED_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_SCL + SCL_BYTES;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8u;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64u + 1024u;
   static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
   // TMEM columns: O^T double buffer (2 x 4H) + S^T double buffer (2 x H)
-  static constexpr uint32_t TMEM_COLS = (10 * H <= 256) ? 256u : 512u;
+  // [+ FP8 rows: NKT K chunks of 128 keys x 64 bf16 = 32 columns each]
   static constexpr uint32_t COL_O = 0;
   static constexpr uint32_t COL_S = 8u * H;
+  static constexpr uint32_t COL_KT = 10u * H;
+  static constexpr uint32_t TMEM_USED = COL_KT + 32u * NKT;
+  static constexpr uint32_t TMEM_COLS = (TMEM_USED <= 256) ? 256u : 512u;
+  static_assert(TMEM_USED <= 512, "tensor memory budget");
 };
 
 // barrier slots
@@ -103,6 +151,11 @@ enum {
   B_KR_EMPTY = 28,   // [NKR <= 8]
   B_VR_FULL = 36,    // [NVR <= 4]
   B_VR_EMPTY = 40,   // [NVR <= 4]
+  // FP8 rows only (the K ring slots above are then TMEM chunk slots)
+  B_KC_FULL = 44,    // [NKC <= 4][4 row quarters]
+  B_KC_EMPTY = 60,   // [NKC <= 4][4]
+  B_VC_FULL = 76,    // [NVC <= 2][4]
+  B_VC_EMPTY = 84,   // [NVC <= 2][4]
 };
 
 // Warp-level transposed max/sum reduction: every lane holds H values (one
@@ -134,10 +187,10 @@ __device__ __forceinline__ float warp_transpose_reduce(float* v) {
   return v[0];
 }
 
-template <int H, int NC>
-__global__ void __launch_bounds__(NTHREADS, 1)
+template <int H, int NC, bool F8>
+__global__ void __launch_bounds__(Cfg<H, NC, F8>::NTHREADS, 1)
 sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
-  using C = Cfg<H, NC>;
+  using C = Cfg<H, NC, F8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
@@ -158,8 +211,9 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
   if (threadIdx.x == 0) {
     mbar_init(&bars[B_IDX_FULL + 0], 1);
     mbar_init(&bars[B_IDX_FULL + 1], 1);
-    mbar_init(&bars[B_IDX_EMPTY + 0], 16);  // 3 MMA, softmax, 12 producer warps
-    mbar_init(&bars[B_IDX_EMPTY + 1], 16);
+    // 3 MMA, softmax, 12 (bf16) or 16 (FP8) producer warps
+    mbar_init(&bars[B_IDX_EMPTY + 0], F8 ? 20 : 16);
+    mbar_init(&bars[B_IDX_EMPTY + 1], F8 ? 20 : 16);
     mbar_init(&bars[B_Q_FULL], 1);
     mbar_init(&bars[B_Q_EMPTY], 1);
     for (int i = 0; i < 2; ++i) {
@@ -172,13 +226,26 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
     mbar_init(&bars[B_P_EMPTY], 2);
     for (int i = 0; i < 3; ++i) mbar_init(&bars[B_DRAIN + i], 1);
     mbar_init(&bars[B_SMX_SYNC], 128);
-    for (int i = 0; i < C::NKR; ++i) {
-      mbar_init(&bars[B_KR_FULL + i], 1);
+    // bf16: the chunk / unit leader's byte count; FP8: one arrival per
+    // converting warp (4 row quarters per TMEM chunk, 8 warps per V unit)
+    for (int i = 0; i < (F8 ? C::NKT : C::NKR); ++i) {
+      mbar_init(&bars[B_KR_FULL + i], F8 ? 4 : 1);
       mbar_init(&bars[B_KR_EMPTY + i], 1);
     }
     for (int i = 0; i < C::NVR; ++i) {
-      mbar_init(&bars[B_VR_FULL + i], 1);
+      mbar_init(&bars[B_VR_FULL + i], F8 ? 8 : 1);
       mbar_init(&bars[B_VR_EMPTY + i], 1);
+    }
+    if constexpr (F8) {
+      // code slots: per row quarter, the two warps that gather and read it
+      for (int i = 0; i < 4 * C::NKC; ++i) {
+        mbar_init(&bars[B_KC_FULL + i], 2);
+        mbar_init(&bars[B_KC_EMPTY + i], 2);
+      }
+      for (int i = 0; i < 4 * C::NVC; ++i) {
+        mbar_init(&bars[B_VC_FULL + i], 2);
+        mbar_init(&bars[B_VC_EMPTY + i], 2);
+      }
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -196,8 +263,15 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
   const int stride_t = gridDim.x;
 
   if (warp >= 4) {
-    // warpgroups 1-4 give registers back
-    regs_dec<REGS_OTHER>();
+    // the warpgroups after the first give registers back
+    if constexpr (C::REGS_WG1 == C::REGS_PROD) {
+      regs_dec<C::REGS_PROD>();
+    } else {
+      if (warp < 8)
+        regs_dec<C::REGS_WG1>();
+      else
+        regs_dec<C::REGS_PROD>();
+    }
     if (warp == 6) {
       // ------------------------------------------------------------------
       // index compaction
@@ -211,10 +285,11 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
         int cnt = 0, bad = 0;
         const bool vec = ((a.ld & 3) == 0) && ((reinterpret_cast<uintptr_t>(a.idx) & 15) == 0);
         if (vec) {
-          for (int base = 0; base < a.k; base += 512) {
-            int4 v[4];
+          constexpr int QD = 4;   // four 16-byte loads in flight per lane
+          for (int base = 0; base < a.k; base += 128 * QD) {
+            int4 v[QD];
 #pragma unroll
-            for (int qd = 0; qd < 4; ++qd) {
+            for (int qd = 0; qd < QD; ++qd) {
               const int e0 = base + qd * 128 + lane * 4;
               if (e0 + 3 < a.k) {
                 v[qd] = __ldg(reinterpret_cast<const int4*>(row + e0));
@@ -226,7 +301,7 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
               }
             }
 #pragma unroll
-            for (int qd = 0; qd < 4; ++qd) {
+            for (int qd = 0; qd < QD; ++qd) {
               const int vals[4] = {v[qd].x, v[qd].y, v[qd].z, v[qd].w};
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
@@ -259,108 +334,297 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
         if (lane == 0) mbar_arrive(&bars[B_IDX_FULL + buf]);
       }
     } else if (warp >= 8) {
-      // ----------------------------------------------------------------
-      // TMA producers: twelve warps in two independent streams.
-      //   warps 8-13:  q per token (warp 8), and the D_QK/64 key chunks of
-      //                every tile into the K ring; warp 8+s owns K slot s
-      //                and issues the whole chunk (lane l: rows 4l..4l+3).
-      //   warps 14-19: the four 128-column V units of every tile into the
-      //                V ring (unit m in slot m mod 2); all six warps take
-      //                part in every unit, lanes 0-10 of each sharing its
-      //                64 gather4 (a unit's refill is on the P.V critical
-      //                path twice per tile, so its issue time matters).
-      // Neither stream waits on the other, so QK of the next tile streams
-      // while this tile's softmax runs and V lands ahead of PV.  TMA issue
-      // cost is serial per warp, so many issuing warps keep many copies in
-      // flight.  The leader of a stage arms its byte count; copies from
-      // other issuers may complete first, which only drives the
-      // transaction count negative until then.
-      // ----------------------------------------------------------------
-      const bool kstream = warp < 8 + C::NKR;
-      const int kw = warp - 8;                      // K slot owned (K stream)
-      const int e = (warp - 14) * 11 + (lane < 11 ? lane : 64);   // V gather index 0..63 of a unit
-      const bool v_issuer = !kstream && e < 64;
-      const int g = kstream ? lane : (e & 31);       // row group
-      const int vcc = e >> 5;                       // V swizzle column
-      const bool leader = (lane == 0) && (kstream || warp == 14);
-      const uint32_t q_s = sbase + C::OFF_Q;
-      int lt = 0, lt_nz = 0;
-      uint32_t gt = 0, pos = 0;  // tiles and stages of this stream so far
-      int64_t last_armed = -1;   // last stage this warp's leader armed
-      bool ok = true;
-      for (int t = blockIdx.x; t < T && ok; t += stride_t, ++lt) {
-        const int buf = lt & 1;
-        if (!mbar_wait_warp(&bars[B_IDX_FULL + buf], (lt >> 1) & 1, abort_flag, err)) { ok = false; break; }
-        const int nvalid = meta[buf];
-        const int ntiles = (nvalid + BK - 1) / BK;
-        const int32_t* kl = kidx + buf * KMAX;
-        if (ntiles > 0) {
-          if (warp == 8) {
-            // q[t]: rows t*H .. t*H+H-1 of q viewed [T*H, D_QK], one box per swizzle column
-            if (!mbar_wait_warp(&bars[B_Q_EMPTY], (lt_nz & 1) ^ 1, abort_flag, err)) { ok = false; break; }
-            if (lane == 0) {
-              mbar_arrive_expect_tx(&bars[B_Q_FULL], C::Q_BYTES);
-              for (int c = 0; c < NC; ++c)
-                tma_load_2d(q_s + c * (H * 128), &a.tmap_q, c * 64, t * H, &bars[B_Q_FULL]);
-            }
-          }
-          for (int j = 0; j < ntiles && ok; ++j, ++gt) {
-            if (warp == 8 && lane == 0) DSA_TRACE(a.tr, gt, 0);
-            // this lane's 4 rows; keys past the valid count read as zeros
-            const int key = j * BK + 4 * g;
-            int4 r = *reinterpret_cast<const int4*>(kl + key);
-            if (key + 0 >= nvalid) r.x = -1;
-            if (key + 1 >= nvalid) r.y = -1;
-            if (key + 2 >= nvalid) r.z = -1;
-            if (key + 3 >= nvalid) r.w = -1;
-            if (kstream) {
-              for (int c = 0; c < NC; ++c, ++pos) {
-                if ((int)(pos % C::NKR) != kw) continue;
-                if (!mbar_wait_warp(&bars[B_KR_EMPTY + kw], ((pos / C::NKR) & 1) ^ 1, abort_flag, err)) {
-                  ok = false;
-                  break;
-                }
-                if (leader) mbar_arrive_expect_tx(&bars[B_KR_FULL + kw], C::CHUNK_BYTES);
-                tma_gather4(sbase + C::OFF_KR + kw * C::CHUNK_BYTES + g * 512, &a.tmap_kv, c * 64, r.x, r.y, r.z, r.w,
-                            &bars[B_KR_FULL + kw]);
-                last_armed = pos;
-              }
-            } else {
-              for (int m = 0; m < 4; ++m, ++pos) {
-                const int vgroup = (int)(pos % C::NVR);   // V slot of this unit
-                if (!mbar_wait_warp(&bars[B_VR_EMPTY + vgroup], ((pos / C::NVR) & 1) ^ 1, abort_flag, err)) {
-                  ok = false;
-                  break;
-                }
-                if (leader) mbar_arrive_expect_tx(&bars[B_VR_FULL + vgroup], C::UNIT_BYTES);
-                if (v_issuer)
-                  tma_gather4(sbase + C::OFF_VR + vgroup * C::UNIT_BYTES + vcc * C::CHUNK_BYTES + g * 512, &a.tmap_kv,
-                              (2 * m + vcc) * 64, r.x, r.y, r.z, r.w, &bars[B_VR_FULL + vgroup]);
-                last_armed = pos;
+      if constexpr (F8) {
+        // ----------------------------------------------------------------
+        // FP8 producers, thread = key row.  Warps 8-15 feed QK, warps 16-23
+        // P.V.  In each stream warp w converts rows 32*(w & 3) + lane of
+        // every tile (its TMEM lane quarter) and half hf of every 128-code
+        // block (codes 64*hf .. 64*hf+63: bf16 chunk 2b+hf).  An item is
+        // one 128-byte column block of the tile's 128 rows: code block b at
+        // byte 128b, and for the K stream with RoPE columns a fifth item at
+        // byte 528 (the RoPE columns, bf16, copied into TMEM unchanged).
+        // Items flow through a ring of 16 KB code slots; the two warps of a
+        // row quarter each gather 16 of its rows (lanes 0-3, 4 rows each)
+        // and both read it.  A warp issues items NS-1 ahead of the one it
+        // converts, within each token.  The row's block scale of an item
+        // comes with it: the hf = 0 warp copies it (cp.async, 4 bytes) into
+        // the slot's scale words, tracked by the slot's own barrier.
+        // ----------------------------------------------------------------
+        auto stream = [&](auto kstream_tag) {
+          constexpr bool KS = decltype(kstream_tag)::value;
+          constexpr bool ROPE = (NC == 9);
+          constexpr int IPT = (KS && ROPE) ? 5 : 4;         // items per tile
+          constexpr int NS = KS ? C::NKC : C::NVC;
+          constexpr int LAG = NS - 1;
+          const int q4 = warp & 3;
+          const int hf = ((warp - 8) >> 2) & 1;
+          const int row = 32 * q4 + lane;                          // row this thread converts
+          const int grow = 32 * q4 + 16 * hf + 4 * (lane & 3);     // rows this lane gathers (lanes 0-3)
+          const uint32_t cring = sbase + (KS ? C::OFF_KC : C::OFF_VC);
+          const int bfull = (KS ? B_KC_FULL : B_VC_FULL) + q4;     // + 4 * slot
+          const int bempty = (KS ? B_KC_EMPTY : B_VC_EMPTY) + q4;
+          const uint32_t scl = sbase + C::OFF_SCL + (KS ? 0u : (uint32_t)C::NKC * BK * 4u) + row * 4u;   // + 512 * slot
+          const uint32_t rsw = (uint32_t)(row & 7);               // 128B swizzle phase of this row
+          uint32_t cpos = 0;   // items of this stream so far
+          uint32_t opos = 0;   // TMEM chunks (K) or V units (V) so far
+          int lt = 0;
+          bool ok = true;
+          int drain_lo = 0, drain_hi = 0;   // after an abort: items of the token that may still be in flight
+          int lt_nz = 0;                            // tokens with at least one tile
+          for (int t = blockIdx.x; t < T && ok; t += stride_t, ++lt) {
+            const int buf = lt & 1;
+            if (!mbar_wait_warp(&bars[B_IDX_FULL + buf], (lt >> 1) & 1, abort_flag, err)) { ok = false; break; }
+            const int nvalid = meta[buf];
+            const int ntiles = (nvalid + BK - 1) / BK;
+            const int32_t* kl = kidx + buf * KMAX;
+            const int nitems = ntiles * IPT;
+            if (KS && warp == 8 && ntiles > 0) {
+              // q[t]: rows t*H .. t*H+H-1 of q viewed [T*H, D_QK], one box per swizzle column
+              if (!mbar_wait_warp(&bars[B_Q_EMPTY], (lt_nz & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+              if (lane == 0) {
+                mbar_arrive_expect_tx(&bars[B_Q_FULL], C::Q_BYTES);
+                for (int c = 0; c < NC; ++c)
+                  tma_load_2d(sbase + C::OFF_Q + c * (H * 128), &a.tmap_q, c * 64, t * H, &bars[B_Q_FULL]);
               }
             }
+            if (ntiles > 0) ++lt_nz;
+            for (int i = 0; i < nitems + LAG; ++i) {
+              if (i < nitems) {
+                // ---- issue item i
+                const int j = i / IPT, b = i - j * IPT;
+                const uint32_t cp = cpos + i, s = cp % NS;
+                if (!mbar_wait_warp(&bars[bempty + 4 * s], ((cp / NS) & 1) ^ 1, abort_flag, err)) {
+                  ok = false;
+                  drain_lo = i > LAG ? i - LAG : 0;
+                  drain_hi = i;
+                  break;
+                }
+                if (hf == 0 && b < 4) {
+                  // this row's scale of block b (zero for a key past the valid count); the
+                  // slot's phase cannot complete before this warp's arrival below
+                  const int key = j * BK + row;
+                  const bool v = key < nvalid;
+                  cp_async4(scl + s * (BK * 4), v ? a.kv8 + (size_t)kl[key] * a.row_bytes + 512 + 4 * b : a.kv8,
+                            v ? 4u : 0u);
+                  cp_async_mbar_arrive(&bars[bfull + 4 * s]);
+                }
+                __syncwarp();
+                if (lane < 4) {
+                  const int gk = j * BK + grow;
+                  int4 r = *reinterpret_cast<const int4*>(kl + gk);
+                  if (gk + 0 >= nvalid) r.x = -1;
+                  if (gk + 1 >= nvalid) r.y = -1;
+                  if (gk + 2 >= nvalid) r.z = -1;
+                  if (gk + 3 >= nvalid) r.w = -1;
+                  if (lane == 0) mbar_arrive_expect_tx(&bars[bfull + 4 * s], 16u * 128u);
+                  tma_gather4(cring + s * C::CHUNK_BYTES + grow * 128, &a.tmap_kv, b < 4 ? 128 * b : 528, r.x, r.y,
+                              r.z, r.w, &bars[bfull + 4 * s]);
+                }
+              }
+              if (i >= LAG) {
+                // ---- convert item i - LAG
+                const int ic = i - LAG;
+                const int j = ic / IPT, b = ic - j * IPT;
+                const uint32_t cp = cpos + ic, s = cp % NS;
+                // (on an abort from here on, items ic .. min(i, nitems - 1) may still be in flight)
+                drain_lo = ic;
+                drain_hi = i < nitems ? i + 1 : nitems;
+                if (!mbar_wait_warp(&bars[bfull + 4 * s], (cp / NS) & 1, abort_flag, err)) { ok = false; break; }
+                if (KS && warp == 8 && lane == 0 && b == 0) DSA_TRACE(a.tr, opos / NC + j, 0);
+                const uint32_t src = cring + s * C::CHUNK_BYTES + row * 128;
+                const float sc = lds_f32(scl + s * (BK * 4));   // (unused for the RoPE item)
+                if constexpr (KS) {
+                  const bool rope = ROPE && b == 4;
+                  if (!rope || hf == 0) {
+                    const uint32_t kt = opos + j * NC + (rope ? 8 : 2 * b + hf);
+                    const uint32_t ts = kt % C::NKT;
+                    if (!mbar_wait_warp(&bars[B_KR_EMPTY + ts], ((kt / C::NKT) & 1) ^ 1, abort_flag, err)) {
+                      ok = false;
+                      break;
+                    }
+                    tc_fence_after();
+                    const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16) + C::COL_KT + ts * 32;
+                    if (rope) {
+                      // bf16 RoPE columns: 8 pieces of 8 values, copied as they are
+#pragma unroll 1
+                      for (int pp = 0; pp < 8; pp += 2) {
+                        const uint4 w0 = lds128(src + ((((uint32_t)pp) ^ rsw) << 4));
+                        const uint4 w1 = lds128(src + ((((uint32_t)(pp + 1)) ^ rsw) << 4));
+                        const uint32_t v[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                        tmem_st8_u32(taddr + 4 * pp, v);
+                      }
+                    } else {
+                      // codes 64hf .. 64hf+63: pieces 4hf .. 4hf+3, 16 codes = 8 columns each
+#pragma unroll 1
+                      for (int pp = 0; pp < 4; ++pp) {
+                        const uint4 w = lds128(src + ((((uint32_t)(4 * hf + pp)) ^ rsw) << 4));
+                        uint32_t v[8];
+                        e4m3x4_dequant_bf16x4(w.x, sc, v[0], v[1]);
+                        e4m3x4_dequant_bf16x4(w.y, sc, v[2], v[3]);
+                        e4m3x4_dequant_bf16x4(w.z, sc, v[4], v[5]);
+                        e4m3x4_dequant_bf16x4(w.w, sc, v[6], v[7]);
+                        tmem_st8_u32(taddr + 8 * pp, v);
+                      }
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars[B_KR_FULL + ts]);
+                  }
+                } else {
+                  const uint32_t vp = opos + j * 4 + b;
+                  const uint32_t vs = vp % C::NVR;
+                  if (!mbar_wait_warp(&bars[B_VR_EMPTY + vs], ((vp / C::NVR) & 1) ^ 1, abort_flag, err)) {
+                    ok = false;
+                    break;
+                  }
+                  // this row of the unit's bf16 chunk hf (K-major, 128B-swizzled as the gathers lay it out)
+                  const uint32_t dst = sbase + C::OFF_VR + vs * C::UNIT_BYTES + hf * C::CHUNK_BYTES + row * 128;
+#pragma unroll 1
+                  for (int pp = 0; pp < 4; ++pp) {
+                    const uint4 w = lds128(src + ((((uint32_t)(4 * hf + pp)) ^ rsw) << 4));
+                    uint32_t v[8];
+                    e4m3x4_dequant_bf16x4(w.x, sc, v[0], v[1]);
+                    e4m3x4_dequant_bf16x4(w.y, sc, v[2], v[3]);
+                    e4m3x4_dequant_bf16x4(w.z, sc, v[4], v[5]);
+                    e4m3x4_dequant_bf16x4(w.w, sc, v[6], v[7]);
+                    sts128(dst + ((((uint32_t)(2 * pp)) ^ rsw) << 4), v[0], v[1], v[2], v[3]);
+                    sts128(dst + ((((uint32_t)(2 * pp + 1)) ^ rsw) << 4), v[4], v[5], v[6], v[7]);
+                  }
+                  fence_proxy_async_smem();
+                  __syncwarp();
+                  if (lane == 0) mbar_arrive(&bars[B_VR_FULL + vs]);
+                }
+                // every code of the slot this warp reads has been consumed
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[bempty + 4 * s]);
+              }
+            }
+            if (!ok) break;
+            cpos += nitems;
+            opos += KS ? ntiles * NC : ntiles * 4;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[B_IDX_EMPTY + buf]);
           }
-          ++lt_nz;
+          // After an abort, let the copies still in flight land before the
+          // CTA can exit (each slot's phase completes once its bytes land).
+          if (!ok && lane == 0) {
+            for (int c = drain_lo; c < drain_hi; ++c) {
+              const uint32_t cp = cpos + c, s = cp % NS;
+              mbar_wait_drain(&bars[bfull + 4 * s], (cp / NS) & 1, err);
+            }
+            if (KS && warp == 8 && lt_nz > 0) mbar_wait_drain(&bars[B_Q_FULL], (lt_nz - 1) & 1, err);
+          }
+          __syncwarp();
+        };
+        if (warp < 16)
+          stream(BoolConst<true>{});
+        else
+          stream(BoolConst<false>{});
+      } else {
+        // ----------------------------------------------------------------
+        // TMA producers: twelve warps in two independent streams.
+        //   warps 8-13:  q per token (warp 8), and the D_QK/64 key chunks of
+        //                every tile into the K ring; warp 8+s owns K slot s
+        //                and issues the whole chunk (lane l: rows 4l..4l+3).
+        //   warps 14-19: the four 128-column V units of every tile into the
+        //                V ring (unit m in slot m mod 2); all six warps take
+        //                part in every unit, lanes 0-10 of each sharing its
+        //                64 gather4 (a unit's refill is on the P.V critical
+        //                path twice per tile, so its issue time matters).
+        // Neither stream waits on the other, so QK of the next tile streams
+        // while this tile's softmax runs and V lands ahead of PV.  TMA issue
+        // cost is serial per warp, so many issuing warps keep many copies in
+        // flight.  The leader of a stage arms its byte count; copies from
+        // other issuers may complete first, which only drives the
+        // transaction count negative until then.
+        // ----------------------------------------------------------------
+        const bool kstream = warp < 8 + C::NKR;
+        const int kw = warp - 8;                      // K slot owned (K stream)
+        const int e = (warp - 14) * 11 + (lane < 11 ? lane : 64);   // V gather index 0..63 of a unit
+        const bool v_issuer = !kstream && e < 64;
+        const int g = kstream ? lane : (e & 31);       // row group
+        const int vcc = e >> 5;                       // V swizzle column
+        const bool leader = (lane == 0) && (kstream || warp == 14);
+        const uint32_t q_s = sbase + C::OFF_Q;
+        int lt = 0, lt_nz = 0;
+        uint32_t gt = 0, pos = 0;  // tiles and stages of this stream so far
+        int64_t last_armed = -1;   // last stage this warp's leader armed
+        bool ok = true;
+        for (int t = blockIdx.x; t < T && ok; t += stride_t, ++lt) {
+          const int buf = lt & 1;
+          if (!mbar_wait_warp(&bars[B_IDX_FULL + buf], (lt >> 1) & 1, abort_flag, err)) { ok = false; break; }
+          const int nvalid = meta[buf];
+          const int ntiles = (nvalid + BK - 1) / BK;
+          const int32_t* kl = kidx + buf * KMAX;
+          if (ntiles > 0) {
+            if (warp == 8) {
+              // q[t]: rows t*H .. t*H+H-1 of q viewed [T*H, D_QK], one box per swizzle column
+              if (!mbar_wait_warp(&bars[B_Q_EMPTY], (lt_nz & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+              if (lane == 0) {
+                mbar_arrive_expect_tx(&bars[B_Q_FULL], C::Q_BYTES);
+                for (int c = 0; c < NC; ++c)
+                  tma_load_2d(q_s + c * (H * 128), &a.tmap_q, c * 64, t * H, &bars[B_Q_FULL]);
+              }
+            }
+            for (int j = 0; j < ntiles && ok; ++j, ++gt) {
+              if (warp == 8 && lane == 0) DSA_TRACE(a.tr, gt, 0);
+              // this lane's 4 rows; keys past the valid count read as zeros
+              const int key = j * BK + 4 * g;
+              int4 r = *reinterpret_cast<const int4*>(kl + key);
+              if (key + 0 >= nvalid) r.x = -1;
+              if (key + 1 >= nvalid) r.y = -1;
+              if (key + 2 >= nvalid) r.z = -1;
+              if (key + 3 >= nvalid) r.w = -1;
+              if (kstream) {
+                for (int c = 0; c < NC; ++c, ++pos) {
+                  if ((int)(pos % C::NKR) != kw) continue;
+                  if (!mbar_wait_warp(&bars[B_KR_EMPTY + kw], ((pos / C::NKR) & 1) ^ 1, abort_flag, err)) {
+                    ok = false;
+                    break;
+                  }
+                  if (leader) mbar_arrive_expect_tx(&bars[B_KR_FULL + kw], C::CHUNK_BYTES);
+                  tma_gather4(sbase + C::OFF_KR + kw * C::CHUNK_BYTES + g * 512, &a.tmap_kv, c * 64, r.x, r.y, r.z, r.w,
+                              &bars[B_KR_FULL + kw]);
+                  last_armed = pos;
+                }
+              } else {
+                for (int m = 0; m < 4; ++m, ++pos) {
+                  const int vgroup = (int)(pos % C::NVR);   // V slot of this unit
+                  if (!mbar_wait_warp(&bars[B_VR_EMPTY + vgroup], ((pos / C::NVR) & 1) ^ 1, abort_flag, err)) {
+                    ok = false;
+                    break;
+                  }
+                  if (leader) mbar_arrive_expect_tx(&bars[B_VR_FULL + vgroup], C::UNIT_BYTES);
+                  if (v_issuer)
+                    tma_gather4(sbase + C::OFF_VR + vgroup * C::UNIT_BYTES + vcc * C::CHUNK_BYTES + g * 512, &a.tmap_kv,
+                                (2 * m + vcc) * 64, r.x, r.y, r.z, r.w, &bars[B_VR_FULL + vgroup]);
+                  last_armed = pos;
+                }
+              }
+            }
+            ++lt_nz;
+          }
+          if (!ok) break;
+          // this warp's copies of the token are issued (row indices were read at issue)
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[B_IDX_EMPTY + buf]);
         }
-        if (!ok) break;
-        // this warp's copies of the token are issued (row indices were read at issue)
+        // Let copies still in flight land before the CTA can exit: the last
+        // phase of the slot this warp fills completes only once every byte
+        // of it has landed.
+        if (leader) {
+          if (warp == 8 && lt_nz > 0) mbar_wait_drain(&bars[B_Q_FULL], (lt_nz - 1) & 1, err);
+          if (last_armed >= 0) {
+            if (kstream)
+              mbar_wait_drain(&bars[B_KR_FULL + kw], (uint32_t)(last_armed / C::NKR) & 1, err);
+            else
+              for (int64_t p = last_armed; p >= 0 && p > last_armed - C::NVR; --p)
+                mbar_wait_drain(&bars[B_VR_FULL + (int)(p % C::NVR)], (uint32_t)(p / C::NVR) & 1, err);
+          }
+        }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[B_IDX_EMPTY + buf]);
       }
-      // Let copies still in flight land before the CTA can exit: the last
-      // phase of the slot this warp fills completes only once every byte
-      // of it has landed.
-      if (leader) {
-        if (warp == 8 && lt_nz > 0) mbar_wait_drain(&bars[B_Q_FULL], (lt_nz - 1) & 1, err);
-        if (last_armed >= 0) {
-          if (kstream)
-            mbar_wait_drain(&bars[B_KR_FULL + kw], (uint32_t)(last_armed / C::NKR) & 1, err);
-          else
-            for (int64_t p = last_armed; p >= 0 && p > last_armed - C::NVR; --p)
-              mbar_wait_drain(&bars[B_VR_FULL + (int)(p % C::NVR)], (uint32_t)(p / C::NVR) & 1, err);
-        }
-      }
-      __syncwarp();
     } else if (warp == 4) {
       // ----------------------------------------------------------------
       // QK issuer (one thread): S^T = K q^T into the S double buffer, one
@@ -389,13 +653,20 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
             DSA_TRACE(a.tr, gt, 2);
             tc_fence_after();
             for (int c = 0; c < NC; ++c, ++kpos) {
-              const uint32_t slot = kpos % C::NKR;
-              if (!mbar_wait(&bars[B_KR_FULL + slot], (kpos / C::NKR) & 1, abort_flag, err)) { ok = false; break; }
+              constexpr uint32_t NK = F8 ? C::NKT : C::NKR;
+              const uint32_t slot = kpos % NK;
+              if (!mbar_wait(&bars[B_KR_FULL + slot], (kpos / NK) & 1, abort_flag, err)) { ok = false; break; }
               tc_fence_after();
-              const uint32_t abase = sbase + C::OFF_KR + slot * C::CHUNK_BYTES;
               const uint32_t bbase = q_s + c * (H * 128);
-              mma_bf16_ss_x4(d_s, sdesc_sw128(abase, 16, 1024), sdesc_sw128(bbase, 16, 1024), 2u, 2u, IDESC_QK,
-                             c > 0 ? 1u : 0u);
+              if constexpr (F8) {
+                // A = the chunk in TMEM (lane = key, 8 columns per 16 keys' K step)
+                mma_bf16_ts_x4(d_s, tmem + C::COL_KT + slot * 32, sdesc_sw128(bbase, 16, 1024), 8u, 2u, IDESC_QK,
+                               c > 0 ? 1u : 0u);
+              } else {
+                const uint32_t abase = sbase + C::OFF_KR + slot * C::CHUNK_BYTES;
+                mma_bf16_ss_x4(d_s, sdesc_sw128(abase, 16, 1024), sdesc_sw128(bbase, 16, 1024), 2u, 2u, IDESC_QK,
+                               c > 0 ? 1u : 0u);
+              }
               mma_commit(&bars[B_KR_EMPTY + slot]);
             }
             if (!ok) break;
@@ -469,7 +740,7 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
       __syncwarp();
     }
   } else {
-    regs_inc<REGS_SOFTMAX>();
+    regs_inc<C::REGS_SMX>();
     // ------------------------------------------------------------------
     // softmax + epilogue (warps 0-3, thread i <-> TMEM lane i)
     // ------------------------------------------------------------------
@@ -652,32 +923,41 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
   if (warp == 4) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-template <int H, int NC>
+template <int H, int NC, bool F8>
 static int launch_t(const SparseArgs& a, int num_sms, cudaStream_t stream) {
-  using C = Cfg<H, NC>;
+  using C = Cfg<H, NC, F8>;
   static int attr_set[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(sparse_prefill_kernel<H, NC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(sparse_prefill_kernel<H, NC, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES) != cudaSuccess)
       return -1;
     attr_set[dev] = 1;
   }
   const int grid = a.T < num_sms ? a.T : num_sms;
-  sparse_prefill_kernel<H, NC><<<grid, NTHREADS, C::SMEM_BYTES, stream>>>(a);
+  sparse_prefill_kernel<H, NC, F8><<<grid, C::NTHREADS, C::SMEM_BYTES, stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+template <bool F8>
+static int launch_f(const SparseArgs& a, int num_sms, cudaStream_t stream) {
+  const int nc = a.d_qk / 64;
+  if (a.H == 16 && nc == 9) return launch_t<16, 9, F8>(a, num_sms, stream);
+  if (a.H == 32 && nc == 9) return launch_t<32, 9, F8>(a, num_sms, stream);
+  if (a.H == 16 && nc == 8) return launch_t<16, 8, F8>(a, num_sms, stream);
+  if (a.H == 32 && nc == 8) return launch_t<32, 8, F8>(a, num_sms, stream);
+  return -2;
 }
 
 }  // namespace sparse
 
 int launch_sparse_prefill(const SparseArgs& a, int num_sms, cudaStream_t stream) {
-  const int nc = a.d_qk / 64;
-  if (a.H == 16 && nc == 9) return sparse::launch_t<16, 9>(a, num_sms, stream);
-  if (a.H == 32 && nc == 9) return sparse::launch_t<32, 9>(a, num_sms, stream);
-  if (a.H == 16 && nc == 8) return sparse::launch_t<16, 8>(a, num_sms, stream);
-  if (a.H == 32 && nc == 8) return sparse::launch_t<32, 8>(a, num_sms, stream);
-  return -2;
+  return sparse::launch_f<false>(a, num_sms, stream);
+}
+
+int launch_sparse_prefill_fp8(const SparseArgs& a, int num_sms, cudaStream_t stream) {
+  return sparse::launch_f<true>(a, num_sms, stream);
 }
 
 }  // namespace dsa

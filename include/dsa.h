@@ -349,6 +349,22 @@ int64_t dsa_kv_fp8_row_bytes(int d_rope);
 int dsa_kv_fp8_quantize(const uint16_t* kv, int N, int ld_kv, int d_rope, uint8_t* kv_fp8, dsa_stream_t stream);
 int dsa_kv_fp8_dequantize(const uint8_t* kv_fp8, int N, int d_rope, uint16_t* kv, int ld_kv, dsa_stream_t stream);
 
+/* Per-token sparse MLA prefill reading FP8 latent rows directly (the pages'
+ * per-token form, as dsa_sparse_prefill, over the row layout above).  Each
+ * selected row is gathered as codes + scales + RoPE (656 bytes at d_rope =
+ * 64 against 1152 in bf16) and dequantized on chip with exactly the
+ * dsa_kv_fp8_dequantize arithmetic, so out and lse are bit-for-bit those of
+ * dsa_kv_fp8_dequantize followed by dsa_sparse_prefill, without the bf16
+ * table.
+ * q      DEVICE [T, H, d_qk] bf16, 16-byte aligned; d_qk = 512 + d_rope.
+ * kv_fp8 DEVICE [N, dsa_kv_fp8_row_bytes(d_rope)], 16-byte aligned (may be
+ *        null when N = 0).
+ * idx, k, ld, out, lse, scale: as dsa_sparse_prefill.  H in {16, 32};
+ * d_rope in {0, 64}; d_v = 512; k <= 2048, else DSA_ERR_UNSUPPORTED. */
+int dsa_sparse_prefill_fp8(const uint16_t* q, const uint8_t* kv_fp8, int N, int d_rope, const int32_t* idx, int T,
+                           int H, int d_qk, int d_v, int k, int ld, float scale, uint16_t* out, float* lse,
+                           dsa_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Form choice (host only, no GPU call).  "[Perf][GLM-5.3-Flash] ...", commit
  * messages: prompts within the top-k budget run dense MHA, longer ones masked
