@@ -852,14 +852,19 @@ def run_profile_case(args):
     from synth import WORKLOADS, make_masked_inputs, make_sparse_inputs, scaled_down
     dev = torch.device("cuda", 0)
     n = args.profile_tokens
-    if args.profile in ("sparse", "union", "grouped"):
-        base = WORKLOADS[args.profile_workload or ("v32_h32_16k" if args.profile == "sparse" else "grouped_21k_of_32k")]
+    if args.profile in ("sparse", "sparse_fp8", "union", "grouped"):
+        base = WORKLOADS[args.profile_workload or
+                         ("v32_h32_16k" if args.profile.startswith("sparse") else "grouped_21k_of_32k")]
         w = scaled_down(base, (n,), (base.N,), name=f"{base.name}_last{n}")
         x = make_sparse_inputs(w)
         q, kv = to_dev(x.q, dev), to_dev(x.kv, dev)
         idx = torch.from_numpy(x.idx).to(dev)
         if args.profile == "sparse":
             fn = lambda: dsa.dsa_sparse_prefill(q, kv, idx, w.k, w.scale)
+        elif args.profile == "sparse_fp8":
+            d_rope = w.d_qk - 512
+            f8 = dsa.dsa_kv_fp8_quantize(kv, d_rope)
+            fn = lambda: dsa.dsa_sparse_prefill_fp8(q, f8, idx, w.k, w.scale, d_rope=d_rope)
         else:
             upad = dsa.dsa_union_pad(w.G, w.k, 128)
             u, ul, m = dsa.dsa_union_build(idx, w.k, w.G, w.N, cu_seqlens_q=x.cu_seqlens_q, union_pad=upad)
@@ -909,7 +914,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-chunk", type=int, default=1216, help="tokens per chunk of the host-buffer call (8 per SM)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work per core")
-    ap.add_argument("--profile", choices=["sparse", "union", "grouped", "masked"], default=None,
+    ap.add_argument("--profile", choices=["sparse", "sparse_fp8", "union", "grouped", "masked"], default=None,
                     help="run a small case of one kernel (for ncu) instead of the benchmark")
     ap.add_argument("--profile-tokens", type=int, default=2048)
     ap.add_argument("--profile-workload", default=None,
