@@ -174,15 +174,25 @@ int dsa_sparse_prefill_host(const uint16_t* q, const uint16_t* kv, int kv_on_hos
   if (!pipe_of(&p)) return DSA_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  // On an error after work was queued on the library's streams, the caller's
+  // stream still waits for all of it, so no copy into the caller's buffers is
+  // left in flight behind the caller's next work (the first error is the one
+  // returned; errors of these joins are not).
+  auto fail = [&](int st) {
+    const cudaStream_t ss[3] = {p->h2d, p->cmp, p->d2h};
+    for (cudaStream_t s : ss)
+      if (cudaEventRecord(p->exit, s) == cudaSuccess) cudaStreamWaitEvent((cudaStream_t)stream, p->exit, 0);
+    return st;
+  };
   // start after the work already queued on the caller's stream
   if (!ok(cudaEventRecord(p->entry, (cudaStream_t)stream)) || !ok(cudaStreamWaitEvent(p->h2d, p->entry, 0)) ||
       !ok(cudaStreamWaitEvent(p->cmp, p->entry, 0)) || !ok(cudaStreamWaitEvent(p->d2h, p->entry, 0)))
-    return DSA_ERR_CUDA;
+    return fail(DSA_ERR_CUDA);
   const uint16_t* kv_dev = kv;
   if (kv_host) {
     if (!ok(cudaMemcpyAsync(ws, kv, (size_t)N * ld_kv * 2, cudaMemcpyHostToDevice, p->h2d)) ||
         !ok(cudaEventRecord(p->kv_in, p->h2d)) || !ok(cudaStreamWaitEvent(p->cmp, p->kv_in, 0)))
-      return DSA_ERR_CUDA;
+      return fail(DSA_ERR_CUDA);
     kv_dev = reinterpret_cast<const uint16_t*>(ws);
   }
   const std::vector<int> plan = plan_chunks(T, chunk, p->num_sms);
@@ -197,24 +207,24 @@ int dsa_sparse_prefill_host(const uint16_t* q, const uint16_t* kv, int kv_on_hos
     uint16_t* dout = reinterpret_cast<uint16_t*>(set + L.q + L.idx);
     float* dlse = reinterpret_cast<float*>(set + L.q + L.idx + L.out);
     // inputs of chunk i, once the kernel of chunk i - NB has read set b
-    if (i >= NB && !ok(cudaStreamWaitEvent(p->h2d, p->done[b], 0))) return DSA_ERR_CUDA;
+    if (i >= NB && !ok(cudaStreamWaitEvent(p->h2d, p->done[b], 0))) return fail(DSA_ERR_CUDA);
     if (!ok(cudaMemcpyAsync(dq, q + t0 * H * d_qk, (size_t)n * H * d_qk * 2, cudaMemcpyHostToDevice, p->h2d)) ||
         !ok(cudaMemcpyAsync(didx, idx + t0 * ld, (size_t)n * ld * 4, cudaMemcpyHostToDevice, p->h2d)) ||
         !ok(cudaEventRecord(p->in[b], p->h2d)))
-      return DSA_ERR_CUDA;
+      return fail(DSA_ERR_CUDA);
     // the kernel, once its inputs are in and set b's previous outputs left
     if (!ok(cudaStreamWaitEvent(p->cmp, p->in[b], 0)) || (i >= NB && !ok(cudaStreamWaitEvent(p->cmp, p->out[b], 0))))
-      return DSA_ERR_CUDA;
+      return fail(DSA_ERR_CUDA);
     const int st = dsa_sparse_prefill(dq, kv_dev, N, ld_kv, didx, n, H, d_qk, d_v, k, ld, scale, dout, dlse,
                                       (dsa_stream_t)p->cmp);
-    if (st != DSA_OK) return st;
-    if (!ok(cudaEventRecord(p->done[b], p->cmp))) return DSA_ERR_CUDA;
+    if (st != DSA_OK) return fail(st);
+    if (!ok(cudaEventRecord(p->done[b], p->cmp))) return fail(DSA_ERR_CUDA);
     // outputs of chunk i back to the host
     if (!ok(cudaStreamWaitEvent(p->d2h, p->done[b], 0)) ||
         !ok(cudaMemcpyAsync(out + t0 * H * d_v, dout, (size_t)n * H * d_v * 2, cudaMemcpyDeviceToHost, p->d2h)) ||
         !ok(cudaMemcpyAsync(lse + t0 * H, dlse, (size_t)n * H * 4, cudaMemcpyDeviceToHost, p->d2h)) ||
         !ok(cudaEventRecord(p->out[b], p->d2h)))
-      return DSA_ERR_CUDA;
+      return fail(DSA_ERR_CUDA);
   }
   // the caller's stream continues once the last outputs are in host memory
   if (!ok(cudaEventRecord(p->exit, p->d2h)) || !ok(cudaStreamWaitEvent((cudaStream_t)stream, p->exit, 0)))
