@@ -534,7 +534,7 @@ def pin_kv_fp8_round_trip(seed=14) -> bool:
 # ----------------------------------------------------------------------------
 # the tolerance checker every parity test relies on
 # ----------------------------------------------------------------------------
-def _verdict(got_out, got_lse, ref_out, ref_lse):
+def _accepts(got_out, got_lse, ref_out, ref_lse):
     return bool(O.compare(got_out, got_lse, ref_out, ref_lse)["ok"])
 
 
@@ -551,7 +551,7 @@ def pin_compare_statistics() -> bool:
     z = O.compare(np.ones((2, 3)), np.zeros(2), np.ones((2, 3)), np.zeros(2))
     ok &= bool(z["ok"]) and z["out_max_abs"] == 0 and z["out_rel_l2"] == 0 and z["lse_max_abs"] == 0
     # empty tensors pass
-    ok &= _verdict(np.zeros((0, 4, 8)), np.zeros((0, 4)), np.zeros((0, 4, 8)), np.zeros((0, 4)))
+    ok &= _accepts(np.zeros((0, 4, 8)), np.zeros((0, 4)), np.zeros((0, 4, 8)), np.zeros((0, 4)))
     return ok
 
 
@@ -564,16 +564,16 @@ def pin_compare_out_bounds() -> bool:
     n = 10000
     ref = np.ones(n)
     lse = np.zeros(4)
-    ok = _verdict(ref * (1 + 0.0049), lse, ref, lse)
-    ok &= not _verdict(ref * (1 + 0.00502), lse, ref, lse)
+    ok = _accepts(ref * (1 + 0.0049), lse, ref, lse)
+    ok &= not _accepts(ref * (1 + 0.00502), lse, ref, lse)
     one = ref.copy()
     one[123] += 0.019
-    ok &= _verdict(one, lse, ref, lse)
+    ok &= _accepts(one, lse, ref, lse)
     one[123] += 0.002
-    ok &= not _verdict(one, lse, ref, lse)
+    ok &= not _accepts(one, lse, ref, lse)
     # all-zero reference: the plain norm of the difference is the measure
-    ok &= _verdict(np.full(4, 1e-3), lse, np.zeros(4), lse)
-    ok &= not _verdict(np.full(4, 3e-3), lse, np.zeros(4), lse)
+    ok &= _accepts(np.full(4, 1e-3), lse, np.zeros(4), lse)
+    ok &= not _accepts(np.full(4, 3e-3), lse, np.zeros(4), lse)
     return ok
 
 
@@ -585,16 +585,16 @@ def pin_compare_lse_bounds() -> bool:
     infinities must fail."""
     out = np.ones(8)
     n = 1000
-    ok = not _verdict(out, np.full(n, 0.11), out, np.full(n, 0.1))
-    ok &= _verdict(out, np.full(n, 0.1 + 1e-4), out, np.full(n, 0.1))
+    ok = not _accepts(out, np.full(n, 0.11), out, np.full(n, 0.1))
+    ok &= _accepts(out, np.full(n, 0.1 + 1e-4), out, np.full(n, 0.1))
     big = np.full(n, 100.0)
     g = big.copy()
     g[7] += 0.03
-    ok &= not _verdict(out, g, out, big)
+    ok &= not _accepts(out, g, out, big)
     g[7] = 100.0 + 0.015
-    ok &= _verdict(out, g, out, big)
+    ok &= _accepts(out, g, out, big)
     ref = np.array([-np.inf, 1.0, 2.0])
-    ok &= not _verdict(out, np.array([-np.inf, 6.0, 2.0]), out, ref)
+    ok &= not _accepts(out, np.array([-np.inf, 6.0, 2.0]), out, ref)
     return ok
 
 
@@ -604,21 +604,21 @@ def pin_compare_infinities_and_nan() -> bool:
     broadcast."""
     out = np.ones(4)
     ref = np.array([-np.inf, 1.0])
-    ok = _verdict(out, np.array([-np.inf, 1.0]), out, ref)
-    ok &= not _verdict(out, np.array([0.0, 1.0]), out, ref)            # finite where ref is -inf
-    ok &= not _verdict(out, np.array([np.inf, 1.0]), out, ref)         # wrong sign
-    ok &= not _verdict(out, np.array([-np.inf, -np.inf]), out, ref)    # -inf where ref is finite
+    ok = _accepts(out, np.array([-np.inf, 1.0]), out, ref)
+    ok &= not _accepts(out, np.array([0.0, 1.0]), out, ref)            # finite where ref is -inf
+    ok &= not _accepts(out, np.array([np.inf, 1.0]), out, ref)         # wrong sign
+    ok &= not _accepts(out, np.array([-np.inf, -np.inf]), out, ref)    # -inf where ref is finite
     # NaN beside zeros: read as zero it would pass, so only NaN detection fails it
     zo = np.zeros(4)
     bad = zo.copy()
     bad[2] = np.nan
     zl = np.array([-np.inf, 0.0])
     nl = np.array([-np.inf, np.nan])
-    ok &= _verdict(zo, zl, zo, zl)
-    ok &= not _verdict(bad, zl, zo, zl)
-    ok &= not _verdict(zo, nl, zo, zl)
-    ok &= not _verdict(zo, zl, bad, zl)
-    ok &= not _verdict(zo, zl, zo, nl)
+    ok &= _accepts(zo, zl, zo, zl)
+    ok &= not _accepts(bad, zl, zo, zl)
+    ok &= not _accepts(zo, nl, zo, zl)
+    ok &= not _accepts(zo, zl, bad, zl)
+    ok &= not _accepts(zo, zl, zo, nl)
     try:
         O.compare(np.ones((5, 1, 8)), np.zeros((5, 1)), np.ones((5, 3, 8)), np.zeros((5, 3)))
         ok = False
