@@ -52,8 +52,8 @@ int dsa_form_calibration_default(dsa_form_calibration* c) {
   c->per_token_ms0 = 0.07;
   c->union_frac = 0.20;
   c->union_ms0 = 0.009;
-  c->grouped_frac_576 = 0.497;
-  c->grouped_frac_512 = 0.473;
+  c->grouped_frac_576 = 0.515;
+  c->grouped_frac_512 = 0.504;
   c->grouped_ms0 = 0.033;
   c->masked_frac_192 = 0.568;
   c->masked_frac_256 = 0.65;

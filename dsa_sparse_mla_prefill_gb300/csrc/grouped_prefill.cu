@@ -36,6 +36,12 @@
 // of each stream waits; every MMA completion is committed to both CTAs'
 // barriers.
 //
+// O^T lives in tensor memory once (TMEM holds O^T and two S^T buffers), so a
+// group's epilogue (the pair's row sums, lse, out = O / l) is deferred until
+// the next group's first tile has stored its P: the group's last P.V then
+// runs beside that softmax instead of stalling it, and O is read, scaled and
+// packed before it is released to the next group's first P.V.
+//
 // Warp roles (24 warps): 0-7 softmax (two per TMEM lane quarter: warp w
 // holds slots 32(w%4) .. +31 and pseudo-heads 64(w/4) .. +63, as two blocks
 // of 32), 8 QK issuer (and tensor-memory allocation), 9 PV issuer (issuers
@@ -530,6 +536,79 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
       return r;
     };
 
+    // Epilogue of a group (et0: its first token, enrows: its pseudo-head
+    // rows, em / el: the reference and this warp's running sums): the
+    // pair's sums, lse, and out = O / l.  It runs once the next group's
+    // first tile has stored its P, so the group's last P.V overlaps that
+    // softmax instead of being waited for; O is released to the next
+    // group's P.V as soon as it has been read.
+    auto epilogue = [&](int et0, int enrows, const float* em, const float* el) -> bool {
+      float l[2];
+#pragma unroll
+      for (int sub = 0; sub < 2; ++sub) {
+        const uint32_t pp = post(sub, el[sub]);
+        if (!wait_x(sub, pp)) return false;
+        l[sub] = gathered(sub, pp, false);
+      }
+      float inv_l[2];
+#pragma unroll
+      for (int sub = 0; sub < 2; ++sub) {
+        inv_l[sub] = (l[sub] > 0.f) ? 1.0f / l[sub] : 0.f;
+        const int p = 64 * hb + 32 * sub + lane;
+        if (leader && qw == 0 && p < enrows)
+          a.lse[(size_t)et0 * H + p] = (l[sub] > 0.f) ? (em[sub] + log2f(l[sub])) * 0.6931471805599453f : -INFINITY;
+      }
+      // 1/l of the warp's 64 heads, read back as broadcasts (head 64hb + hl at negm[hl])
+      negm[lane] = inv_l[0];
+      negm[32 + lane] = inv_l[1];
+      __syncwarp();
+      if (!mbar_wait_cluster_warp(&bars[B_OF], lgq & 1, abort_flag, err)) return false;
+      tc_fence_after();
+      // O^T lane = output column: lanes 2i and 2i+1 hold adjacent columns; for
+      // each pair of heads (hl, hl+1) the even lane takes head hl of both
+      // columns and the odd lane head hl+1 (one exchange), so each stores one
+      // bf16 pair.  All of O is read, scaled and packed before O is released
+      // to the next group's P.V; the stores follow.
+      const uint32_t odd = (uint32_t)(lane & 1);
+      uint32_t pk[2][32];   // [M-block][head pair]: bf16 x2 of this lane's head of the pair
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+#pragma unroll
+        for (int q32 = 0; q32 < 2; ++q32) {
+          // two 16-column loads in flight per wait
+          float o[32];
+          tmem_ld16(tmem + lane_off + C::COL_O + b * HP + 64 * hb + 32 * q32, o);
+          tmem_ld16(tmem + lane_off + C::COL_O + b * HP + 64 * hb + 32 * q32 + 16, o + 16);
+          tmem_ld_wait();
+#pragma unroll
+          for (int h = 0; h < 32; h += 2) {
+            const int hl = 32 * q32 + h;   // heads 64hb + hl (even lane), + hl + 1 (odd lane)
+            const float mine = odd ? o[h + 1] : o[h];
+            const float x = __shfl_xor_sync(0xffffffffu, odd ? o[h] : o[h + 1], 1);
+            const float il = negm[hl + odd];
+            pk[b][hl / 2] = odd ? pack_bf16x2(x * il, mine * il) : pack_bf16x2(mine * il, x * il);
+          }
+        }
+      }
+      tc_fence_before();
+      warp_arrive_leader(&bars[B_OE]);
+      ++lgq;
+      uint16_t* out_g = a.out + (size_t)(et0 * H + 64 * hb) * 512 + 128 * rank + (key & ~1);
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int hl = 2 * i + (int)odd;
+          if (64 * hb + hl < enrows)
+            *reinterpret_cast<uint32_t*>(out_g + (size_t)hl * 512 + 256 * b) = pk[b][i];
+        }
+      }
+      return true;
+    };
+
+    bool pend = false;   // a group whose epilogue has not run yet
+    int pe_t0 = 0, pe_nrows = 0;
+    float pe_m[2] = {0.f, 0.f}, pe_l[2] = {0.f, 0.f};
     for (int g = cid; g < a.num_groups && ok; g += ncl) {
       int t0, n;
       group_of(a.req, G, g, t0, n);
@@ -691,48 +770,25 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
             mbar_arrive(&bars[B_PRX + pb]);
         }
         if (key == 0 && hb == 0) DSA_TRACE(a.tr, gt, 6);
-      }
-      if (!ok) break;
-      // -------- epilogue: the pair's sums, lse, O / l --------
-      float l[2];
-#pragma unroll
-      for (int sub = 0; sub < 2; ++sub) {
-        const uint32_t pp = post(sub, l_l[sub]);
-        if (!wait_x(sub, pp)) { ok = false; break; }
-        l[sub] = gathered(sub, pp, false);
-      }
-      if (!ok) break;
-      float inv_l[2];
-#pragma unroll
-      for (int sub = 0; sub < 2; ++sub) {
-        inv_l[sub] = (l[sub] > 0.f) ? 1.0f / l[sub] : 0.f;
-        const int p = 64 * hb + 32 * sub + lane;
-        if (leader && qw == 0 && p < nrows)
-          a.lse[(size_t)t0 * H + p] = (l[sub] > 0.f) ? (m_l[sub] + log2f(l[sub])) * 0.6931471805599453f : -INFINITY;
-      }
-      if (!mbar_wait_cluster_warp(&bars[B_OF], lgq & 1, abort_flag, err)) { ok = false; break; }
-      tc_fence_after();
-      uint16_t* out_g = a.out + (size_t)(t0 * H + 64 * hb) * 512 + 128 * rank + key;
-#pragma unroll 1
-      for (int b = 0; b < 2; ++b) {
-#pragma unroll 1
-        for (int q16 = 0; q16 < 4; ++q16) {
-          float o[16];
-          tmem_ld16(tmem + lane_off + C::COL_O + b * HP + 64 * hb + 16 * q16, o);
-          tmem_ld_wait();
-          const float ilv = (q16 >> 1) ? inv_l[1] : inv_l[0];
-#pragma unroll
-          for (int h = 0; h < 16; ++h) {
-            const int hl = 16 * q16 + h;   // head 64hb + hl
-            const float il = __shfl_sync(0xffffffffu, ilv, hl & 31);
-            if (64 * hb + hl < nrows) out_g[(size_t)hl * 512 + 256 * b] = f32_to_bf16_rn(o[h] * il);
+        if (j == 0 && pend) {
+          if (!epilogue(pe_t0, pe_nrows, pe_m, pe_l)) {
+            ok = false;
+            break;
           }
+          pend = false;
         }
       }
-      tc_fence_before();
-      warp_arrive_leader(&bars[B_OE]);
-      ++lgq;
+      if (!ok) break;
+      // this group's epilogue waits for the next group's first tile
+      pend = true;
+      pe_t0 = t0;
+      pe_nrows = nrows;
+      pe_m[0] = m_l[0];
+      pe_m[1] = m_l[1];
+      pe_l[0] = l_l[0];
+      pe_l[1] = l_l[1];
     }
+    if (ok && pend) epilogue(pe_t0, pe_nrows, pe_m, pe_l);
   }
 
   tc_fence_before();
