@@ -543,12 +543,15 @@ grouped_prefill_kernel(const __grid_constant__ GroupedArgs a) {
     // softmax instead of being waited for; O is released to the next
     // group's P.V as soon as it has been read.
     auto epilogue = [&](int et0, int enrows, const float* em, const float* el) -> bool {
+      // both blocks' partial sums posted before either is waited for (one round trip)
+      uint32_t pp[2];
+      pp[0] = post(0, el[0]);
+      pp[1] = post(1, el[1]);
       float l[2];
 #pragma unroll
       for (int sub = 0; sub < 2; ++sub) {
-        const uint32_t pp = post(sub, el[sub]);
-        if (!wait_x(sub, pp)) return false;
-        l[sub] = gathered(sub, pp, false);
+        if (!wait_x(sub, pp[sub])) return false;
+        l[sub] = gathered(sub, pp[sub], false);
       }
       float inv_l[2];
 #pragma unroll
