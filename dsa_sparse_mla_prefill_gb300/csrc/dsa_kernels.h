@@ -121,13 +121,14 @@ inline int union_build_smem_bytes(int N, int union_pad) {
   return 8 * Wp + union_pad;
 }
 
-// The token-bitmap variant: the mask bytes, prefix[Wp] and G bitmaps of
-// (Wp | 1) words; used when it needs at most kUnionTokbitsMaxSmem bytes.
-constexpr int kUnionTokbitsMaxSmem = 96 * 1024;
-inline int64_t union_build_tokbits_smem_bytes(int N, int G, int union_pad) {
+// The byte-map variant: one membership byte per KV position (32 Wp bytes),
+// the union words and their prefix (Wp words each); used when it needs at
+// most kUnionBytemapMaxSmem bytes (two or more CTAs per SM).
+constexpr int kUnionBytemapMaxSmem = 96 * 1024;
+inline int64_t union_build_bytemap_smem_bytes(int N) {
   const int64_t W = (N + 31) / 32;
   const int64_t Wp = (W + 3) & ~3;
-  return (int64_t)union_pad + 4 * Wp + 4 * (int64_t)G * (Wp | 1);
+  return 40 * Wp;
 }
 
 // Each returns 0 on success, -1 on a CUDA launch error, -2 if the shape has

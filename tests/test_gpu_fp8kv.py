@@ -26,20 +26,23 @@ def awkward_rows(rng, N, width):
     """bf16 rows with mixed magnitudes, an all-zero block, negative zeros and values far
     below their block's maximum (they round to zero or to subnormal codes)."""
     x = normal_bf16(rng, (N, width))
+    # the special blocks sit in rows 0, 1, 2 (as many of them as there are rows)
     x[0, 128:256] = 0
-    x[1, 0:128] = 0x8000                      # -0.0
-    x[2, 256:384] = normal_bf16(rng, (128,)) & 0x80FF   # tiny values (exponent field 1)
-    x[2, 300] = 0x4300                        # 128.0 in the same block
+    x[min(1, N - 1), 0:128] = 0x8000          # -0.0
+    r = min(2, N - 1)
+    x[r, 256:384] = normal_bf16(rng, (128,)) & 0x80FF   # tiny values (exponent field 1)
+    x[r, 300] = 0x4300                        # 128.0 in the same block
     scale = np.exp2(rng.integers(-30, 30, size=(N, 1))).astype(np.float32)
     vals = ((x.astype(np.uint32) << 16).view(np.float32) * scale).astype(np.float32)
     return (vals.view(np.uint32) >> 16).astype(np.uint16)
 
 
-@pytest.mark.parametrize("d_rope,ld", [(64, 576), (64, 584), (0, 512)])
-def test_quantize_dequantize_bit_exact(d_rope, ld):
+@pytest.mark.parametrize("d_rope,ld,N", [(64, 576, 300), (64, 584, 300), (0, 512, 300),
+                                         (64, 576, 1), (64, 576, 13), (0, 512, 8)])
+def test_quantize_dequantize_bit_exact(d_rope, ld, N):
+    """Row counts below, at and off the kernel's eight-row step (ragged tails)."""
     import dsa_sparse_mla_prefill_gb300 as dsa
-    rng = np.random.default_rng(ld + d_rope)
-    N = 300
+    rng = np.random.default_rng(ld + d_rope + N)
     kv = awkward_rows(rng, N, ld)
     want = O.kv_fp8_quantize(kv, d_rope)
     got = dsa.dsa_kv_fp8_quantize(bf(kv), d_rope)
