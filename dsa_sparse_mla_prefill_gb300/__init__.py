@@ -257,8 +257,10 @@ def dsa_sparse_prefill_host(q, kv, idx, k: int, scale: float, out, lse, workspac
     """Per-token sparse prefill from and to host memory: q [T, H, d_qk] bf16, idx [T, ld] int32,
     out [T, H, 512] bf16 and lse [T, H] fp32 are host tensors (pinned, for the copies to overlap
     the kernel), kv [N, ld_kv] bf16 a host or CUDA tensor, workspace a CUDA uint8 tensor of
-    dsa_sparse_prefill_host_workspace bytes.  Asynchronous on `stream` (synchronize before
-    reading out and lse)."""
+    dsa_sparse_prefill_host_workspace bytes.  A workspace sized with chunk_tokens >= T selects
+    the streamed form (one kernel launch, copies in chunks of at most chunk_tokens); a smaller
+    one the ring of chunk launches.  Asynchronous on `stream` (synchronize before reading out
+    and lse)."""
     import torch
     _host_tensor(q, torch.bfloat16, "q", 3)
     _host_tensor(idx, torch.int32, "idx", 2)

@@ -155,6 +155,17 @@ int dsa_union_build(const int32_t* idx, int T, int k, int ld, int G, const int32
 int dsa_sparse_prefill(const uint16_t* q, const uint16_t* kv, int N, int ld_kv, const int32_t* idx, int T,
                        int H, int d_qk, int d_v, int k, int ld, float scale, uint16_t* out, float* lse,
                        dsa_stream_t stream) {
+  return dsa::sparse_prefill_streamed(q, kv, N, ld_kv, idx, T, H, d_qk, d_v, k, ld, scale, out, lse, nullptr,
+                                      nullptr, 0, (cudaStream_t)stream);
+}
+
+}  // extern "C"
+
+namespace dsa {
+
+int sparse_prefill_streamed(const uint16_t* q, const uint16_t* kv, int N, int ld_kv, const int32_t* idx, int T,
+                            int H, int d_qk, int d_v, int k, int ld, float scale, uint16_t* out, float* lse,
+                            const uint32_t* ready, uint32_t* done, int done_blk, cudaStream_t stream) {
   if (T < 0 || N < 0 || k < 0 || ld < k || ld_kv < d_qk) return DSA_ERR_INVALID_ARG;
   if (!(H == 16 || H == 32) || !(d_qk == 576 || d_qk == 512) || d_v != 512 || k > 2048)
     return DSA_ERR_UNSUPPORTED;
@@ -184,15 +195,23 @@ int dsa_sparse_prefill(const uint16_t* q, const uint16_t* kv, int N, int ld_kv, 
   a.ld = ld;
   a.scale = scale;
   a.tr = g_trace;
+  a.ready = ready;
+  a.done = done;
+  a.done_blk = done_blk;
+  if ((ready == nullptr) != (done == nullptr) || (done != nullptr && done_blk < 1)) return DSA_ERR_INVALID_ARG;
   // With N = 0 every index is out of range, no tile is formed and the map is
   // never used: it is encoded over q so that it is well formed.
   if (!dsa::make_row_gather_map(&a.tmap_kv, N > 0 ? (const void*)kv : (const void*)q, N > 0 ? N : 1,
                                 N > 0 ? ld_kv : d_qk, N > 0 ? ld_kv : d_qk))
     return DSA_ERR_CUDA;
   if (!dsa::make_tile_map(&a.tmap_q, q, (int64_t)T * H, d_qk, d_qk, H)) return DSA_ERR_CUDA;
-  const int r = dsa::launch_sparse_prefill(a, d->num_sms, (cudaStream_t)stream);
+  const int r = dsa::launch_sparse_prefill(a, d->num_sms, stream);
   return r == 0 ? DSA_OK : (r == -2 ? DSA_ERR_UNSUPPORTED : DSA_ERR_CUDA);
 }
+
+}  // namespace dsa
+
+extern "C" {
 
 int dsa_grouped_prefill(const uint16_t* q, const uint16_t* kv, int N, int ld_kv, const int32_t* union_idx,
                         const int32_t* union_len, const uint8_t* mask, int union_pad, int G,
@@ -441,6 +460,9 @@ int dsa_sparse_prefill_fp8(const uint16_t* q, const uint8_t* kv_fp8, int N, int 
   a.kv = nullptr;
   a.kv8 = kv_fp8;
   a.row_bytes = rb;
+  a.ready = nullptr;
+  a.done = nullptr;
+  a.done_blk = 0;
   a.idx = idx;
   a.out = out;
   a.lse = lse;

@@ -504,6 +504,69 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// The same for global memory: orders what this thread has observed through
+// the generic proxy (a flag it acquired) before the TMA reads it issues next.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// flags shared with the copy engines (streamed host calls)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Loads cached in L2 only: for data another agent (a copy engine) may have
+// written while the kernel runs, which the non-coherent path must not serve.
+__device__ __forceinline__ int4 ld_cg_i4(const int4* p) {
+  int4 v;
+  asm volatile("ld.global.cg.v4.s32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ int ld_cg_i32(const int* p) {
+  int v;
+  asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+// Bounded wait (lane 0 polls, the warp follows) until *ready > t.  Returns
+// false, raising the CTA's abort flag and the timeout counter, when it ran
+// out or another thread of the CTA already gave up.
+__device__ __forceinline__ bool wait_ready_warp(const uint32_t* ready, uint32_t t, volatile int* abort_flag,
+                                                unsigned int* err) {
+  bool ok = true;
+  if (lane_id() == 0 && ld_acquire_gpu(ready) <= t) {
+    const uint64_t t0 = globaltimer();
+    while (true) {
+      __nanosleep(256);
+      if (ld_acquire_gpu(ready) > t) break;
+      if (*abort_flag) {
+        ok = false;
+        break;
+      }
+      if (globaltimer() - t0 > kWaitTimeoutNs) {
+        *abort_flag = 1;
+        atomicAdd(err + ERR_TIMEOUT, 1u);
+        ok = false;
+        break;
+      }
+    }
+  }
+  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  __syncwarp();
+  return ok;
+}
+
 // ---------------------------------------------------------------------------
 // tcgen05: TMEM allocation
 // ---------------------------------------------------------------------------

@@ -41,6 +41,15 @@ struct SparseArgs {
   int T, H, d_qk, N, ld_kv, k, ld;
   float scale;
   TraceArgs tr;
+  // Streamed from host memory (null otherwise): token t's q and index row may
+  // be read once *ready > t (a copy stream raises it after each chunk lands);
+  // once token t's out and lse are stored, done[t / done_blk] is incremented
+  // (a copy stream waits on those counters before reading a chunk back).  A
+  // CTA that gives up still counts its remaining tokens, so every counter
+  // reaches its total.
+  const uint32_t* ready;
+  uint32_t* done;
+  int done_blk;
 };
 
 struct UnionArgs {
@@ -136,11 +145,19 @@ inline int64_t union_build_bytemap_smem_bytes(int N) {
 int launch_sparse_prefill(const SparseArgs& a, int num_sms, cudaStream_t stream);
 int launch_sparse_prefill_fp8(const SparseArgs& a, int num_sms, cudaStream_t stream);
 int launch_union_build(const UnionArgs& a, cudaStream_t stream);
+
 int launch_topk_to_key_mask(const KeyMaskArgs& a, cudaStream_t stream);
 int launch_local_to_global(const ConvertArgs& a, cudaStream_t stream);
 int launch_grouped_prefill(const GroupedArgs& a, int num_sms, cudaStream_t stream);
 int launch_masked_mha(const MaskedArgs& a, int num_sms, cudaStream_t stream);
 int launch_wait_timeout(unsigned int* err, cudaStream_t stream);
 int launch_kv_fp8(const Fp8KvArgs& a, bool quantize, int num_sms, cudaStream_t stream);
+
+// dsa_sparse_prefill with the streamed-call fields of SparseArgs (ready, done,
+// done_blk; all null / 0 for an ordinary call).  Same checks and DSA_* status
+// as dsa_sparse_prefill.
+int sparse_prefill_streamed(const uint16_t* q, const uint16_t* kv, int N, int ld_kv, const int32_t* idx, int T,
+                            int H, int d_qk, int d_v, int k, int ld, float scale, uint16_t* out, float* lse,
+                            const uint32_t* ready, uint32_t* done, int done_blk, cudaStream_t stream);
 
 }  // namespace dsa

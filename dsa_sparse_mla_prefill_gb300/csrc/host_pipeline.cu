@@ -18,14 +18,28 @@
 // such multiple the workspace allows, and the first and last chunks ramp
 // (one, two, four ... tokens per SM) so that the copy before the first
 // kernel and the copy after the last are short.
+//
+// Streamed form (a workspace that holds every token's buffers): one kernel
+// launch covers all tokens and the copies flow around it.  After each chunk's
+// inputs land, the host-to-device stream raises a `ready` word to the chunk's
+// end (a stream write, ordered after the copies); the kernel reads a token's
+// inputs only once `ready` is past it.  The kernel counts finished tokens in
+// blocks of one token per CTA, and the device-to-host stream waits (stream
+// waits on those counters) before it reads a chunk back.  This removes the
+// per-chunk launch (each launch fills and drains every CTA's pipeline once).
+// Every upload is queued before the kernel and no read-back wait is queued
+// unless the kernel launched; a CTA that gives up still completes its
+// counters, so no stream waits for a value that never comes.
 #include <cstdint>
 #include <cstring>
 #include <initializer_list>
 #include <vector>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/dsa.h"
+#include "dsa_kernels.h"
 
 namespace {
 
@@ -93,6 +107,35 @@ bool pipe_of(Pipe** p) {
 
 int64_t up(int64_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
+// Stream memory operations of the driver API, found through the runtime.
+typedef CUresult (*PfnStreamValue32)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
+struct MemOps {
+  bool tried = false;
+  PfnStreamValue32 write = nullptr, wait = nullptr;
+};
+MemOps g_memops;
+
+const MemOps* mem_ops() {
+  if (!g_memops.tried) {
+    g_memops.tried = true;
+    void* pw = nullptr;
+    void* pa = nullptr;
+    cudaDriverEntryPointQueryResult qw, qa;
+    if (cudaGetDriverEntryPointByVersion("cuStreamWriteValue32", &pw, 12000, cudaEnableDefault, &qw) ==
+            cudaSuccess &&
+        qw == cudaDriverEntryPointSuccess &&
+        cudaGetDriverEntryPointByVersion("cuStreamWaitValue32", &pa, 12000, cudaEnableDefault, &qa) ==
+            cudaSuccess &&
+        qa == cudaDriverEntryPointSuccess && pw && pa) {
+      g_memops.write = reinterpret_cast<PfnStreamValue32>(pw);
+      g_memops.wait = reinterpret_cast<PfnStreamValue32>(pa);
+    } else {
+      cudaGetLastError();
+    }
+  }
+  return g_memops.write ? &g_memops : nullptr;
+}
+
 // Chunk sizes for T tokens, none above `cap`, as described at the top.
 std::vector<int> plan_chunks(int T, int cap, int unit) {
   std::vector<int> out;
@@ -131,6 +174,19 @@ Layout layout(int chunk, int N, int ld_kv, int H, int d_qk, int d_v, int ld, boo
   return l;
 }
 
+// Streamed form: the table, one buffer set for all T tokens, then the
+// `ready` word and the done counters (one word per token at most).
+int64_t streamed_bytes(int T, int N, int ld_kv, int H, int d_qk, int d_v, int ld, bool kv_host) {
+  const Layout l = layout(T, N, ld_kv, H, d_qk, d_v, ld, kv_host);
+  return l.kv + l.set + up(4 * ((int64_t)T + 1));
+}
+
+// Chunks of the streamed form: at most this many tokens per SM.  Small
+// chunks keep the uploads just ahead of the kernel (a CTA's next token is at
+// most two chunks away) and the last read-back short; their cost is a few
+// queued operations each.
+constexpr int kStreamTokensPerSm = 2;
+
 }  // namespace
 
 extern "C" {
@@ -152,8 +208,8 @@ int dsa_sparse_prefill_host_plan(int T, int chunk_tokens, int num_sms, int32_t* 
 int64_t dsa_sparse_prefill_host_workspace(int T, int N, int ld_kv, int H, int d_qk, int d_v, int ld,
                                           int chunk_tokens, int kv_on_host) {
   if (T < 0 || N < 0 || ld_kv < 1 || H < 1 || d_qk < 1 || d_v < 1 || ld < 1 || chunk_tokens < 1) return -1;
-  const int chunk = chunk_tokens < T ? chunk_tokens : (T > 0 ? T : 1);
-  return layout(chunk, N, ld_kv, H, d_qk, d_v, ld, kv_on_host != 0).total;
+  if (chunk_tokens >= T) return streamed_bytes(T, N, ld_kv, H, d_qk, d_v, ld, kv_on_host != 0 && N > 0);
+  return layout(chunk_tokens, N, ld_kv, H, d_qk, d_v, ld, kv_on_host != 0).total;
 }
 
 int dsa_sparse_prefill_host(const uint16_t* q, const uint16_t* kv, int kv_on_host, int N, int ld_kv,
@@ -169,7 +225,11 @@ int dsa_sparse_prefill_host(const uint16_t* q, const uint16_t* kv, int kv_on_hos
   const int chunk = chunk_tokens < T ? chunk_tokens : T;
   const bool kv_host = kv_on_host != 0 && N > 0;
   const Layout L = layout(chunk, N, ld_kv, H, d_qk, d_v, ld, kv_host);
-  if (workspace_bytes < L.total) return DSA_ERR_INVALID_ARG;
+  // the streamed form when the workspace holds every token (and the driver
+  // has stream memory operations), else the ring of chunk launches
+  const bool fits_all = workspace_bytes >= streamed_bytes(T, N, ld_kv, H, d_qk, d_v, ld, kv_host);
+  const bool streamed = fits_all && mem_ops() != nullptr;
+  if (!streamed && workspace_bytes < L.total) return fits_all ? DSA_ERR_UNSUPPORTED : DSA_ERR_INVALID_ARG;
   Pipe* p;
   if (!pipe_of(&p)) return DSA_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -188,6 +248,75 @@ int dsa_sparse_prefill_host(const uint16_t* q, const uint16_t* kv, int kv_on_hos
   if (!ok(cudaEventRecord(p->entry, (cudaStream_t)stream)) || !ok(cudaStreamWaitEvent(p->h2d, p->entry, 0)) ||
       !ok(cudaStreamWaitEvent(p->cmp, p->entry, 0)) || !ok(cudaStreamWaitEvent(p->d2h, p->entry, 0)))
     return fail(DSA_ERR_CUDA);
+  if (streamed) {
+    const MemOps* mo = mem_ops();
+    const Layout F = layout(T, N, ld_kv, H, d_qk, d_v, ld, kv_host);
+    uint8_t* set = ws + F.kv;
+    uint16_t* dq = reinterpret_cast<uint16_t*>(set);
+    int32_t* didx = reinterpret_cast<int32_t*>(set + F.q);
+    uint16_t* dout = reinterpret_cast<uint16_t*>(set + F.q + F.idx);
+    float* dlse = reinterpret_cast<float*>(set + F.q + F.idx + F.out);
+    uint32_t* ready = reinterpret_cast<uint32_t*>(set + F.set);
+    uint32_t* done = ready + 1;
+    const int blk = T < p->num_sms ? T : p->num_sms;   // one token per CTA (the kernel's grid)
+    const int nblk = (T + blk - 1) / blk;
+    const CUstream h2d = (CUstream)p->h2d, d2h = (CUstream)p->d2h;
+    // counters cleared before the kernel and the read-backs start
+    if (!ok(cudaMemsetAsync(ready, 0, 4 * ((size_t)nblk + 1), p->h2d)) || !ok(cudaEventRecord(p->kv_in, p->h2d)) ||
+        !ok(cudaStreamWaitEvent(p->cmp, p->kv_in, 0)) || !ok(cudaStreamWaitEvent(p->d2h, p->kv_in, 0)))
+      return fail(DSA_ERR_CUDA);
+    const uint16_t* kv_dev = kv;
+    if (kv_host) {
+      if (!ok(cudaMemcpyAsync(ws, kv, (size_t)N * ld_kv * 2, cudaMemcpyHostToDevice, p->h2d))) return fail(DSA_ERR_CUDA);
+      kv_dev = reinterpret_cast<const uint16_t*>(ws);
+    }
+    const int cap = chunk < kStreamTokensPerSm * p->num_sms ? chunk : kStreamTokensPerSm * p->num_sms;
+    const std::vector<int> plan = plan_chunks(T, cap, p->num_sms);
+    auto upload = [&](int64_t t0, int n) {
+      return ok(cudaMemcpyAsync(dq + t0 * H * d_qk, q + t0 * H * d_qk, (size_t)n * H * d_qk * 2,
+                                cudaMemcpyHostToDevice, p->h2d)) &&
+             ok(cudaMemcpyAsync(didx + t0 * ld, idx + t0 * ld, (size_t)n * ld * 4, cudaMemcpyHostToDevice, p->h2d)) &&
+             mo->write(h2d, (CUdeviceptr)ready, (cuuint32_t)(t0 + n), CU_STREAM_WRITE_VALUE_DEFAULT) == CUDA_SUCCESS;
+    };
+    // the table and the first chunk, then the kernel (so that it starts while
+    // the host queues the rest), then the other chunks' uploads
+    if (!upload(0, plan[0])) return fail(DSA_ERR_CUDA);
+    const int st = dsa::sparse_prefill_streamed(dq, kv_dev, N, ld_kv, didx, T, H, d_qk, d_v, k, ld, scale, dout,
+                                                dlse, ready, done, blk, p->cmp);
+    if (st != DSA_OK) return fail(st);
+    if (!ok(cudaEventRecord(p->done[0], p->cmp))) return fail(DSA_ERR_CUDA);
+    int64_t t0 = plan[0];
+    for (size_t i = 1; i < plan.size(); t0 += plan[i], ++i)
+      if (!upload(t0, plan[i])) {
+        // release the kernel rather than leave it waiting out its bound (the
+        // call reports the error; no read-back was queued)
+        mo->write(h2d, (CUdeviceptr)ready, (cuuint32_t)T, CU_STREAM_WRITE_VALUE_DEFAULT);
+        return fail(DSA_ERR_CUDA);
+      }
+    // each chunk back once every block of tokens it touches is counted done
+    t0 = 0;
+    int waited = -1;   // blocks already waited for
+    for (int n : plan) {
+      const int b_last = (int)((t0 + n - 1) / blk);
+      for (int b = waited + 1; b <= b_last; ++b) {
+        const int64_t cnt = (int64_t)T - (int64_t)b * blk < blk ? (int64_t)T - (int64_t)b * blk : blk;
+        if (mo->wait(d2h, (CUdeviceptr)(done + b), (cuuint32_t)cnt, CU_STREAM_WAIT_VALUE_GEQ) != CUDA_SUCCESS)
+          return fail(DSA_ERR_CUDA);
+      }
+      waited = b_last;
+      if (!ok(cudaMemcpyAsync(out + t0 * H * d_v, dout + t0 * H * d_v, (size_t)n * H * d_v * 2, cudaMemcpyDeviceToHost,
+                              p->d2h)) ||
+          !ok(cudaMemcpyAsync(lse + t0 * H, dlse + t0 * H, (size_t)n * H * 4, cudaMemcpyDeviceToHost, p->d2h)))
+        return fail(DSA_ERR_CUDA);
+      t0 += n;
+    }
+    // the caller's stream continues once the outputs are in host memory and
+    // the kernel has ended
+    if (!ok(cudaEventRecord(p->exit, p->d2h)) || !ok(cudaStreamWaitEvent((cudaStream_t)stream, p->exit, 0)) ||
+        !ok(cudaStreamWaitEvent((cudaStream_t)stream, p->done[0], 0)))
+      return DSA_ERR_CUDA;
+    return DSA_OK;
+  }
   const uint16_t* kv_dev = kv;
   if (kv_host) {
     if (!ok(cudaMemcpyAsync(ws, kv, (size_t)N * ld_kv * 2, cudaMemcpyHostToDevice, p->h2d)) ||

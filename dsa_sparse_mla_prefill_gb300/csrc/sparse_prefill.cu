@@ -14,6 +14,10 @@
 // second gather hits L2):
 //   warp 6      compacts the token's index row (valid entries only, order
 //               kept) into shared memory; out-of-range entries are counted.
+//               In the streamed instance (STREAM: q and the indices arrive
+//               from host memory while the kernel runs) it also waits for
+//               each token's chunk to land and counts the CTA's finished
+//               tokens for the copy stream that reads them back.
 //   warps 8-19  issue TMA loads: q per token (tiled boxes) and the key
 //               rows as tile::gather4 (4 rows x 128 bytes per instruction)
 //               straight into 128B-swizzled tiles of 128 keys.  Warps 8-13
@@ -147,7 +151,8 @@ enum {
   B_O_EMPTY = 14,    // [2]
   B_DRAIN = 16,      // [3] one per MMA issuer
   B_SMX_SYNC = 19,   // softmax warpgroup barrier (128)
-  B_KR_FULL = 20,    // [NKR <= 8]
+  B_KR_FULL = 20,    // [NKR <= 6]
+  B_OUT_DONE = 26,   // [2] streamed: a token without keys stored (softmax warpgroup, 128)
   B_KR_EMPTY = 28,   // [NKR <= 8]
   B_VR_FULL = 36,    // [NVR <= 4]
   B_VR_EMPTY = 40,   // [NVR <= 4]
@@ -187,10 +192,25 @@ __device__ __forceinline__ float warp_transpose_reduce(float* v) {
   return v[0];
 }
 
-template <int H, int NC, bool F8>
+// Index loads: the read-only path, or (streamed calls) L2-only loads, since a
+// streamed row was written by a copy engine while the kernel runs.
+template <bool STREAM>
+__device__ __forceinline__ int4 load_idx4(const int4* p) {
+  if constexpr (STREAM) return ld_cg_i4(p);
+  else return __ldg(p);
+}
+template <bool STREAM>
+__device__ __forceinline__ int load_idx(const int* p) {
+  if constexpr (STREAM) return ld_cg_i32(p);
+  else return __ldg(p);
+}
+
+template <int H, int NC, bool F8, bool STREAM>
 __global__ void __launch_bounds__(Cfg<H, NC, F8>::NTHREADS, 1)
 sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
   using C = Cfg<H, NC, F8>;
+  static_assert(!(F8 && STREAM), "the FP8 rows are never streamed");
+  static_assert(C::NKR <= 6 && C::NKT <= 6, "B_OUT_DONE sits in K ring slots 6 and 7");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
@@ -226,6 +246,10 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
     mbar_init(&bars[B_P_EMPTY], 2);
     for (int i = 0; i < 3; ++i) mbar_init(&bars[B_DRAIN + i], 1);
     mbar_init(&bars[B_SMX_SYNC], 128);
+    if constexpr (STREAM) {
+      mbar_init(&bars[B_OUT_DONE + 0], 128);
+      mbar_init(&bars[B_OUT_DONE + 1], 128);
+    }
     // bf16: the chunk / unit leader's byte count; FP8: one arrival per
     // converting warp (4 row quarters per TMEM chunk, 8 warps per V unit)
     for (int i = 0; i < (F8 ? C::NKT : C::NKR); ++i) {
@@ -276,10 +300,55 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
       // ------------------------------------------------------------------
       // index compaction
       // ------------------------------------------------------------------
+      // Streamed calls: this warp also counts the CTA's tokens done, in order.
+      // Once the softmax warps have stored a token (they arrive on B_O_EMPTY
+      // after the stores, or on B_OUT_DONE for a token without keys), a fence
+      // makes those stores visible device-wide and a release add counts the
+      // token; the copy stream that reads the token back waits for that
+      // count.  Token lt - 2 is counted before token lt is compacted (the
+      // softmax needs token lt's indices before it can arrive twice on one
+      // barrier).
+      int lc = 0;              // tokens counted
+      int tc = blockIdx.x;     // the next token to count
+      uint32_t nz = 0;         // of them with keys (O buffer uses)
+      uint32_t ez = 0;         // without keys, two bits: uses of B_OUT_DONE 0 and 1 so far
+      auto count_next = [&](bool wait) -> bool {
+        bool w = true;
+        if (wait) {
+          // the counted token's valid-key count (its index buffer is reused
+          // only for token lc + 2, compacted after this)
+          if (meta[lc & 1] > 0) {
+            w = mbar_wait_warp(&bars[B_O_EMPTY + (nz & 1)], (nz >> 1) & 1, abort_flag, err);
+            ++nz;
+          } else {
+            const uint32_t b = lc & 1;
+            w = mbar_wait_warp(&bars[B_OUT_DONE + b], (ez >> b) & 1, abort_flag, err);
+            ez ^= 1u << b;
+          }
+        }
+        // (counted even when the wait gave up: a count that never completes
+        // would hold the copy stream; the timeout counter reports the failure)
+        if (lane == 0) {
+          __threadfence();
+          red_release_gpu_add(a.done + tc / a.done_blk, 1u);
+        }
+        __syncwarp();
+        ++lc;
+        tc += stride_t;
+        return w;
+      };
+      bool ok = true;
       int lt = 0;
       for (int t = blockIdx.x; t < T; t += stride_t, ++lt) {
         const int buf = lt & 1;
-        if (!mbar_wait_warp(&bars[B_IDX_EMPTY + buf], ((lt >> 1) & 1) ^ 1, abort_flag, err)) break;
+        if constexpr (STREAM) {
+          if (lt >= 2 && !count_next(true)) { ok = false; break; }
+        }
+        if (!mbar_wait_warp(&bars[B_IDX_EMPTY + buf], ((lt >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+        if constexpr (STREAM) {
+          // the token's chunk must have landed
+          if (!wait_ready_warp(a.ready, (uint32_t)t, abort_flag, err)) { ok = false; break; }
+        }
         const int32_t* row = a.idx + (size_t)t * a.ld;
         int32_t* dst = kidx + buf * KMAX;
         int cnt = 0, bad = 0;
@@ -292,12 +361,12 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
             for (int qd = 0; qd < QD; ++qd) {
               const int e0 = base + qd * 128 + lane * 4;
               if (e0 + 3 < a.k) {
-                v[qd] = __ldg(reinterpret_cast<const int4*>(row + e0));
+                v[qd] = load_idx4<STREAM>(reinterpret_cast<const int4*>(row + e0));
               } else {
-                v[qd].x = (e0 + 0 < a.k) ? __ldg(row + e0 + 0) : -1;
-                v[qd].y = (e0 + 1 < a.k) ? __ldg(row + e0 + 1) : -1;
-                v[qd].z = (e0 + 2 < a.k) ? __ldg(row + e0 + 2) : -1;
-                v[qd].w = (e0 + 3 < a.k) ? __ldg(row + e0 + 3) : -1;
+                v[qd].x = (e0 + 0 < a.k) ? load_idx<STREAM>(row + e0 + 0) : -1;
+                v[qd].y = (e0 + 1 < a.k) ? load_idx<STREAM>(row + e0 + 1) : -1;
+                v[qd].z = (e0 + 2 < a.k) ? load_idx<STREAM>(row + e0 + 2) : -1;
+                v[qd].w = (e0 + 3 < a.k) ? load_idx<STREAM>(row + e0 + 3) : -1;
               }
             }
 #pragma unroll
@@ -317,7 +386,7 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
         } else {
           for (int base = 0; base < a.k; base += 32) {
             const int e = base + lane;
-            const int x = (e < a.k) ? __ldg(row + e) : -1;
+            const int x = (e < a.k) ? load_idx<STREAM>(row + e) : -1;
             const bool ok = (x >= 0) && (x < a.N);
             bad += (x < -1 || x >= a.N) ? 1 : 0;
             const uint32_t m = __ballot_sync(0xffffffffu, ok);
@@ -332,6 +401,10 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[B_IDX_FULL + buf]);
+      }
+      if constexpr (STREAM) {
+        // the tokens not counted yet (after a failure, without waiting)
+        while (tc < T) ok = count_next(ok) && ok;
       }
     } else if (warp >= 8) {
       if constexpr (F8) {
@@ -554,6 +627,7 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
         for (int t = blockIdx.x; t < T && ok; t += stride_t, ++lt) {
           const int buf = lt & 1;
           if (!mbar_wait_warp(&bars[B_IDX_FULL + buf], (lt >> 1) & 1, abort_flag, err)) { ok = false; break; }
+          if constexpr (STREAM) fence_proxy_async_global();   // q and kv were written by a copy engine
           const int nvalid = meta[buf];
           const int ntiles = (nvalid + BK - 1) / BK;
           const int32_t* kl = kidx + buf * KMAX;
@@ -752,6 +826,9 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
     uint32_t gt = 0;
     uint32_t sync_phase = 0;
     bool ok = true;
+    // Streamed calls: the index warp counts each token done once its out and
+    // lse stores are in, seeing them through B_O_EMPTY (arrived on after the
+    // stores) or, for a token without keys, B_OUT_DONE.
     for (int t = blockIdx.x; t < T && ok; t += stride_t, ++lt) {
       const int buf = lt & 1;
       if (!mbar_wait_warp(&bars[B_IDX_FULL + buf], (lt >> 1) & 1, abort_flag, err)) { ok = false; break; }
@@ -763,6 +840,7 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
       if (ntiles == 0) {
         for (int i = tid; i < H * 512; i += 128) out_t[i] = 0;
         if (tid < H) a.lse[(size_t)t * H + tid] = -INFINITY;
+        if constexpr (STREAM) mbar_arrive(&bars[B_OUT_DONE + (lt & 1)]);
         continue;
       }
       const int ob = lt_nz & 1;
@@ -923,41 +1001,44 @@ sparse_prefill_kernel(const __grid_constant__ SparseArgs a) {
   if (warp == 4) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-template <int H, int NC, bool F8>
+template <int H, int NC, bool F8, bool STREAM>
 static int launch_t(const SparseArgs& a, int num_sms, cudaStream_t stream) {
   using C = Cfg<H, NC, F8>;
   static int attr_set[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(sparse_prefill_kernel<H, NC, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(sparse_prefill_kernel<H, NC, F8, STREAM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES) != cudaSuccess)
       return -1;
     attr_set[dev] = 1;
   }
   const int grid = a.T < num_sms ? a.T : num_sms;
-  sparse_prefill_kernel<H, NC, F8><<<grid, C::NTHREADS, C::SMEM_BYTES, stream>>>(a);
+  sparse_prefill_kernel<H, NC, F8, STREAM><<<grid, C::NTHREADS, C::SMEM_BYTES, stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
-template <bool F8>
+template <bool F8, bool STREAM>
 static int launch_f(const SparseArgs& a, int num_sms, cudaStream_t stream) {
   const int nc = a.d_qk / 64;
-  if (a.H == 16 && nc == 9) return launch_t<16, 9, F8>(a, num_sms, stream);
-  if (a.H == 32 && nc == 9) return launch_t<32, 9, F8>(a, num_sms, stream);
-  if (a.H == 16 && nc == 8) return launch_t<16, 8, F8>(a, num_sms, stream);
-  if (a.H == 32 && nc == 8) return launch_t<32, 8, F8>(a, num_sms, stream);
+  if (a.H == 16 && nc == 9) return launch_t<16, 9, F8, STREAM>(a, num_sms, stream);
+  if (a.H == 32 && nc == 9) return launch_t<32, 9, F8, STREAM>(a, num_sms, stream);
+  if (a.H == 16 && nc == 8) return launch_t<16, 8, F8, STREAM>(a, num_sms, stream);
+  if (a.H == 32 && nc == 8) return launch_t<32, 8, F8, STREAM>(a, num_sms, stream);
   return -2;
 }
 
 }  // namespace sparse
 
 int launch_sparse_prefill(const SparseArgs& a, int num_sms, cudaStream_t stream) {
-  return sparse::launch_f<false>(a, num_sms, stream);
+  // the streamed instance only for streamed calls: its extra waits and
+  // counting stay out of the ordinary kernel's code
+  if (a.ready != nullptr && a.done != nullptr) return sparse::launch_f<false, true>(a, num_sms, stream);
+  return sparse::launch_f<false, false>(a, num_sms, stream);
 }
 
 int launch_sparse_prefill_fp8(const SparseArgs& a, int num_sms, cudaStream_t stream) {
-  return sparse::launch_f<true>(a, num_sms, stream);
+  return sparse::launch_f<true, false>(a, num_sms, stream);
 }
 
 }  // namespace dsa

@@ -253,11 +253,26 @@ int dsa_last_device_error(dsa_stream_t stream, uint32_t* counts);
 /* ------------------------------------------------------------------------
  * dsa_sparse_prefill from and to HOST memory, with the copies overlapped
  * with the attention (the end-to-end call: inputs that live on the host,
- * results wanted there).  The tokens go through in chunks of chunk_tokens;
- * three internal streams of the library carry the host -> device copies of
- * a chunk's q and indices, the per-token kernel of the chunk, and the device
- * -> host copies of its out and lse, so chunk i+1 arrives and chunk i-1
- * leaves while chunk i is computed (3 chunks in flight).
+ * results wanted there).  Three internal streams of the library carry the
+ * host -> device copies of q and the indices, the per-token kernel, and the
+ * device -> host copies of out and lse.  Two forms, chosen by the workspace:
+ *
+ * streamed (a workspace of dsa_sparse_prefill_host_workspace(..., chunk_tokens
+ *   >= T, ...) bytes, which holds every token): ONE kernel launch over all
+ *   tokens.  The inputs are copied in chunks (of at most chunk_tokens and at
+ *   most 2 tokens per SM); after each chunk a stream write raises a counter,
+ *   and the kernel takes up a token only once the counter is past it.  The
+ *   kernel counts finished tokens per block of one token per CTA, and each
+ *   chunk's outputs are copied back once the blocks it covers are counted
+ *   (stream waits on those counters).  Needs the driver's stream memory
+ *   operations (DSA_ERR_UNSUPPORTED without them).  A kernel that gives up
+ *   (a bounded wait ran out, counted in dsa_last_device_error) still
+ *   completes every counter, so no copy waits forever; its outputs are then
+ *   incomplete.
+ * ring (a smaller workspace, of dsa_sparse_prefill_host_workspace(...,
+ *   chunk_tokens < T, ...) bytes): the tokens go through in chunks of
+ *   chunk_tokens, one kernel launch per chunk, so that chunk i+1 arrives and
+ *   chunk i-1 leaves while chunk i is computed (3 chunks in flight).
  *
  * q, idx, out, lse: HOST pointers, laid out as for dsa_sparse_prefill;
  *   page-locked (pinned) memory is needed for the copies to overlap.
@@ -268,12 +283,15 @@ int dsa_last_device_error(dsa_stream_t stream, uint32_t* counts);
  *   ordered on one stream.
  * stream: the copies start after the work queued on it before the call, and
  *   work queued on it after the call waits for the last outputs to be back
- *   in host memory (synchronize the stream before reading out and lse).
+ *   in host memory and the kernel to end (synchronize the stream before
+ *   reading out and lse).
  * Shapes and errors as dsa_sparse_prefill; DSA_ERR_INVALID_ARG also for
  * chunk_tokens < 1 or a workspace that is too small or misaligned.  A CUDA
- * error part way returns DSA_ERR_CUDA with earlier chunks already queued.
- * The library's streams and events are per device and shared by all calls:
- * calls on one device must not run from several host threads at once.
+ * error part way returns DSA_ERR_CUDA with the work queued so far left to
+ * finish (the caller's stream waits for it).  The results are bit for bit
+ * those of dsa_sparse_prefill on device copies of the same inputs, in either
+ * form.  The library's streams and events are per device and shared by all
+ * calls: calls on one device must not run from several host threads at once.
  * ---------------------------------------------------------------------- */
 int64_t dsa_sparse_prefill_host_workspace(int T, int N, int ld_kv, int H, int d_qk, int d_v, int ld,
                                           int chunk_tokens, int kv_on_host);
