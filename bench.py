@@ -621,7 +621,7 @@ def run_ours(args):
         "clocks": clocks.summary(),
     }
     if rank == 0 and not args.no_modes:
-        del hq, hkv, hidx, hout, hlse, ws
+        del hq, hkv, hidx, hout, hlse
         try:
             modes = run_modes(dev, stream, peaks, args.steps, args.warmup, flush)
         except Exception as e:  # report, never hide the headline

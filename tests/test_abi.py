@@ -136,6 +136,16 @@ def test_argument_validation_without_gpu(lib):
     ws = lib.dsa_sparse_prefill_host_workspace(1000, 1200, 576, 16, 576, 512, 64, 300, 1)
     assert ws >= 1200 * 576 * 2 + 3 * 300 * (16 * 576 * 2 + 64 * 4 + 16 * 512 * 2 + 16 * 4)
     assert lib.dsa_sparse_prefill_host_workspace(1000, 1200, 576, 16, 576, 512, 64, 0, 1) == -1
+    # chunk_tokens >= T sizes the streamed form: the table, one buffer set for all T tokens and the
+    # counter words (one per token at most, plus `ready`), each part rounded up to 256 bytes
+    up = lambda x: (x + 255) // 256 * 256
+    per_tok = [16 * 576 * 2, 64 * 4, 16 * 512 * 2, 16 * 4]
+    streamed = up(1200 * 576 * 2) + sum(up(1000 * b) for b in per_tok) + up(4 * 1001)
+    assert lib.dsa_sparse_prefill_host_workspace(1000, 1200, 576, 16, 576, 512, 64, 1000, 1) == streamed
+    assert lib.dsa_sparse_prefill_host_workspace(1000, 1200, 576, 16, 576, 512, 64, 5000, 1) == streamed
+    assert lib.dsa_sparse_prefill_host_workspace(1000, 1200, 576, 16, 576, 512, 64, 1000, 0) == streamed - up(1200 * 576 * 2)
+    # the ring form: the table and three chunk buffer sets
+    assert ws == up(1200 * 576 * 2) + 3 * sum(up(300 * b) for b in per_tok)
 
     def hostcall(T=1000, H=16, ws_ptr=256, ws_bytes=ws, chunk=300, kv=_vp(16)):
         return lib.dsa_sparse_prefill_host(_vp(16), kv, 1, 1200, 576, _vp(16), T, H, 576, 512, 64, 64, 0.1,
