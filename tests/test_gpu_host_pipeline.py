@@ -88,6 +88,31 @@ def test_streamed_call_equals_device_call(T, chunk, kv_on_host, empty_rows):
         assert torch.equal(hl, ref_l.cpu()), rep
 
 
+@pytest.mark.parametrize("base,H", [("v32_h32_16k", 16), ("nope_2x8192", 16), ("nope_2x8192", 32)])
+def test_streamed_call_other_instances(base, H):
+    """The streamed kernel instances of the other shapes (H = 16; D_QK = 512 without RoPE
+    columns, two requests), against the device call, bit for bit."""
+    import dsa_sparse_mla_prefill_gb300 as dsa
+    w0 = WORKLOADS[base]
+    qs = (700,) if len(w0.q_lens) == 1 else (400, 500)
+    w = scaled_down(w0, qs, tuple(q + 150 for q in qs), k=256, ld=272, H=H, seed=21)
+    x = make_sparse_inputs(w)
+    q, kv, idx = bf(x.q), bf(x.kv), i32(x.idx)
+    ref_o, ref_l = dsa.dsa_sparse_prefill(q, kv, idx, w.k, w.scale)
+    hq = pinned(x.q.view(np.int16), torch.bfloat16)
+    hkv = pinned(x.kv.view(np.int16), torch.bfloat16)
+    hidx = pinned(x.idx)
+    ws = torch.empty(dsa.dsa_sparse_prefill_host_workspace(w.T, w.N, w.d_qk, w.H, w.d_qk, w.ld, w.T, True),
+                     dtype=torch.uint8, device="cuda")
+    ho = torch.full((w.T, w.H, 512), float("nan"), dtype=torch.bfloat16).pin_memory()
+    hl = torch.full((w.T, w.H), float("nan"), dtype=torch.float32).pin_memory()
+    dsa.dsa_sparse_prefill_host(hq, hkv, hidx, w.k, w.scale, ho, hl, ws, chunk_tokens=200)
+    torch.cuda.current_stream().synchronize()
+    st, counts = dsa.dsa_last_device_error()
+    assert st == 0, counts
+    assert torch.equal(ho, ref_o.cpu()) and torch.equal(hl, ref_l.cpu())
+
+
 def test_streamed_call_orders_with_the_callers_stream():
     """As below, for the streamed form: the kernel starts only after the caller's
     earlier work, and the caller's later work sees the outputs."""
